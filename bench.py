@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark: SGEMM TFLOP/s and fraction of the GB300 FP32 peak at 3072^3.
+
+One step = one C = A B call (M = N = K = 3072, row-major, U[-1,1) inputs)
+through the C ABI, inputs already resident in HBM.  Three input sets rotate
+(3 x 113 MB > 129 MB L2) so every step starts with its operands out of L2.
+Each step is timed with CUDA events on the stream the kernel is launched on;
+the timed region is bracketed by a barrier and a device synchronisation.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
+only other place this script executes the oracle), on a bounded row sample of
+the same workload.
+
+Multi-GPU: the GEMM does not need a collective; with N ranks each GPU runs
+an independent replica (weak scaling) and the value is the sum over ranks
+(total FLOPs / max time over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+WORKLOAD = "sgemm_3072x3072x3072_uniform"
+METRIC = "SGEMM TFLOP/s and % of GB300 FP32 peak at 3072³ (1 GPU), vs CPU oracle"
+FP32_LANES_PER_SM = 128          # FP32 FMA units per Blackwell SM
+SM_MAX_MHZ_DEFAULT = 2070.0
+ROTATING_SETS = 3
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open("/tmp/_sgemm_clocks_%d.csv" % os.getpid(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.out:
+            self.out.close()
+
+    def summary(self):
+        path = "/tmp/_sgemm_clocks_%d.csv" % os.getpid()
+        if self.proc is None or not os.path.exists(path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        os.unlink(path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, parts in rows:
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [r[0] for r in rows]
+        power = []
+        for _, _, parts in rows:
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "sm_mhz_min": min(loaded), "samples": len(rows),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def kernel_source_hash() -> str:
+    """Hash of the sources that make up the SIMT kernel; profiles record it so a
+    stale DRAM-traffic figure is never reported for a changed kernel."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_matrix_sgemm_gb300", "csrc")
+    for name in ["device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh", "simt_nn.cu"]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """Bytes per launch (dram read + write) from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                and parts[1] == workload and parts[2] == want:
+            return int(parts[3])
+    return None
+
+
+def cpu_baseline(case, target_s: float):
+    """Time the oracle as it stands on a bounded sample of rows of the workload."""
+    import oracle
+    M, N, K = case["M"], case["N"], case["K"]
+    threads = oracle.default_threads()
+    A = case["A"][0]
+    B = case["B"][0]
+
+    def rows_run(r):
+        sub = np.ascontiguousarray(A[:r])
+        t = time.perf_counter()
+        oracle.sgemm(sub, B, r, N, K, lda=case["lda"], ldb=case["ldb"], nthreads=threads)
+        return time.perf_counter() - t
+
+    probe = min(M, max(threads, 32))
+    t = rows_run(probe)
+    rows = int(min(M, max(probe, probe * target_s / max(t, 1e-6))))
+    t = rows_run(rows)
+    flops = 2.0 * rows * N * K
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {M} rows of the {M}x{N}x{K} product "
+                      f"({flops / 1e9:.1f} GFLOP, {t:.2f} s, fp64 accumulation)",
+            "seconds": t}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = workloads.get(args.workload)
+    case = workloads.make_case(w)
+    M, N, K = w.M, w.N, w.K
+    threads = oracle.default_threads()
+    # each step: a row slice sized to roughly 0.2 s on this host
+    A, B = case["A"][0], case["B"][0]
+    t = time.perf_counter()
+    oracle.sgemm(np.ascontiguousarray(A[:threads]), B, threads, N, K, nthreads=threads)
+    per_row = (time.perf_counter() - t) / threads
+    rows = int(max(threads, min(M, 0.2 / max(per_row, 1e-9))))
+    sub = np.ascontiguousarray(A[:rows])
+    for _ in range(args.warmup):
+        oracle.sgemm(sub, B, rows, N, K, nthreads=threads)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.sgemm(sub, B, rows, N, K, nthreads=threads)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    flops = 2.0 * rows * N * K
+    value = flops * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64-accumulate", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {M} rows per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import dense_fp32_matrix_sgemm_gb300 as sg
+
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            raise SystemExit("--gpus > 1 must be launched with torch.distributed.run")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = workloads.get(args.workload)
+    case = workloads.make_case(w)
+    M, N, K, batch = w.M, w.N, w.K, w.batch
+    lda, ldb, ldc = case["lda"], case["ldb"], case["ldc"]
+    flops = workloads.flops(M, N, K, batch)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    # CPU baseline first (rank 0, before any heavy GPU work; no fork involved)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, args.cpu_seconds)
+
+    nsets = ROTATING_SETS
+    with torch.cuda.stream(stream):
+        hA = torch.from_numpy(case["A"].reshape(-1))
+        hB = torch.from_numpy(case["B"].reshape(-1))
+        sets = []
+        for _ in range(nsets):
+            dA = hA.to(dev, non_blocking=False).clone()
+            dB = hB.to(dev, non_blocking=False).clone()
+            dC = torch.empty(batch * M * ldc, dtype=torch.float32, device=dev)
+            sets.append((dA, dB, dC))
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        dA, dB, dC = sets[i % nsets]
+        if batch == 1:
+            sg.sgemm_f32(M, N, K, dA.data_ptr(), lda, dB.data_ptr(), ldb, dC.data_ptr(), ldc,
+                         w.transA, w.transB, sp)
+        else:
+            sg.sgemm_f32_strided_batched(M, N, K, dA.data_ptr(), lda, case["A"][0].size,
+                                         dB.data_ptr(), ldb, case["B"][0].size, dC.data_ptr(),
+                                         ldc, M * ldc, batch, w.transA, w.transB, sp)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+        if world > 1:
+            dist.barrier()
+    clocks = clk.summary()
+    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms
+    total_ms = sum(durs)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the C ABI from pinned host buffers: H2D A and B,
+    # the GEMM, D2H C, every step on one stream
+    pA = torch.from_numpy(case["A"].reshape(-1)).pin_memory()
+    pB = torch.from_numpy(case["B"].reshape(-1)).pin_memory()
+    pC = torch.empty(batch * M * ldc, dtype=torch.float32).pin_memory()
+    dA, dB, dC = sets[0]
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dA.copy_(pA, non_blocking=True)
+            dB.copy_(pB, non_blocking=True)
+            step(0)
+            pC.copy_(dC, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = (case["A"].size + case["B"].size) * 4
+    d2h = batch * M * ldc * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or SM_MAX_MHZ_DEFAULT)
+    peak_max = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    per_gpu = value / world
+    sm_now = clocks.get("sm_mhz")
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "batch": batch,
+                   "transA": w.transA, "transB": w.transB, "dist": w.dist,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"{nsets} rotating input sets of {workloads.min_bytes(M, N, K, batch) / 1e6:.0f} MB "
+                         f"(> 129 MB L2 together); each step starts with its operands evicted",
+                   "kernel": "simt_fp32_128x128_ffma2"},
+        "pct_of_fp32_peak": {
+            "at_max_clock": 100.0 * per_gpu / peak_max,
+            "peak_tflops_at_max_clock": peak_max,
+            "at_sampled_clock": (100.0 * per_gpu / (peak_max * sm_now / sm_max)) if sm_now else None,
+            "sms": sms, "fp32_lanes_per_sm": FP32_LANES_PER_SM, "sm_max_mhz": sm_max,
+        },
+        "roofline": {
+            "bound": "alu",
+            "achieved": achieved,
+            "peak": peak_max,
+            "unit": "TFLOP/s",
+            "frac": achieved / peak_max,
+            "traffic": profiled_traffic("sgemm_simt_kernel", args.workload),
+            "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
+                           f"{sm_max:.0f} MHz",
+            "algorithmic_flops_per_launch": flops,
+        },
+        "clocks": clocks,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "wall_s": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,172 @@
+"""GB300-native single-precision GEMM: C = op(A) op(B) in float32.
+
+This package is a thin ctypes binding over ``libsgemm_gb300.so``, whose C ABI
+is declared in ``include/sgemm_gb300.h``.  The binding only marshals
+arguments: every step of the product runs in the library's CUDA kernels.
+There is no CPU fallback; if the library has not been built, every call
+raises ``SgemmUnavailable``.
+
+Low-level names mirror the C ABI (raw device pointers as Python ints, stream
+as a ``cudaStream_t`` int or 0).  ``matmul`` is a convenience for torch CUDA
+tensors that computes the pointers and leading dimensions and calls
+``sgemm_f32`` / ``sgemm_f32_strided_batched``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
+           "sgemm_f32", "sgemm_f32_strided_batched",
+           "status_string", "last_error", "version", "matmul", "SGEMM_OK"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
+
+SGEMM_OK = 0
+STATUS_NAMES = {
+    0: "SGEMM_OK", 1: "SGEMM_EINVAL_DIM", 2: "SGEMM_EINVAL_LD", 3: "SGEMM_EINVAL_PTR",
+    4: "SGEMM_EINVAL_TRANS", 5: "SGEMM_EINVAL_BATCH", 6: "SGEMM_ELAUNCH", 7: "SGEMM_EDEVICE",
+}
+
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_vp = ctypes.c_void_p
+
+# Exported symbol -> (restype, argtypes).  Kept in step with include/sgemm_gb300.h.
+SIGNATURES = {
+    "sgemm_f32": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int, _vp]),
+    "sgemm_f32_strided_batched": (_int, [_i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
+                                         _vp, _i64, _i64, _i64, _int, _int, _vp]),
+    "sgemm_status_string": (ctypes.c_char_p, [_int]),
+    "sgemm_last_error": (ctypes.c_char_p, []),
+    "sgemm_version": (_int, []),
+}
+
+
+class SgemmUnavailable(RuntimeError):
+    """The CUDA library is missing or cannot be loaded (no fallback exists)."""
+
+
+class SgemmError(RuntimeError):
+    """A call returned a nonzero sgemm_status."""
+
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        self.detail = detail
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {detail}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libsgemm_gb300.so once and declare its symbols."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise SgemmUnavailable(
+                f"{_LIB_PATH} is not built; run __graft_entry__.build() or "
+                "python -m dense_fp32_matrix_sgemm_gb300._build")
+        try:
+            lib = ctypes.CDLL(_LIB_PATH)
+        except OSError as e:
+            raise SgemmUnavailable(f"cannot load {_LIB_PATH}: {e}") from e
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().sgemm_status_string(status).decode()
+
+
+def last_error() -> str:
+    return load_library().sgemm_last_error().decode()
+
+
+def version() -> int:
+    return load_library().sgemm_version()
+
+
+def _check(status: int) -> int:
+    if status != SGEMM_OK:
+        raise SgemmError(status, last_error())
+    return status
+
+
+def sgemm_f32(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, stream=0, *, check=True):
+    """C = op(A) op(B); A, B, C are device pointers (ints).  Returns the status."""
+    st = load_library().sgemm_f32(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
+                                  transA, transB, stream or None)
+    return _check(st) if check else st
+
+
+def sgemm_f32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                              batch, transA=0, transB=0, stream=0, *, check=True):
+    """Strided-batched C_z = op(A_z) op(B_z).  Returns the status."""
+    st = load_library().sgemm_f32_strided_batched(
+        M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
+        batch, transA, transB, stream or None)
+    return _check(st) if check else st
+
+
+def _operand(t, name):
+    """Return (rows, cols, ld, trans) for a 2-D/3-D CUDA float32 view: row-major
+    storage (unit column stride) is taken as is; a transposed view (unit row
+    stride) is passed as the stored matrix with trans = 1."""
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+    r, c = t.shape[-2], t.shape[-1]
+    sr, sc = t.stride(-2), t.stride(-1)
+    if sc == 1 and (sr >= max(1, c) or r <= 1):
+        return r, c, max(sr, c, 1), 0
+    if sr == 1 and (sc >= max(1, r) or c <= 1):
+        return r, c, max(sc, r, 1), 1
+    raise ValueError(f"{name} must have one unit stride among its last two dimensions")
+
+
+def matmul(A, B, out=None, stream=None):
+    """out = A @ B for float32 CUDA tensors of shape (M, K) x (K, N), or batched
+    (b, M, K) x (b, K, N).  Transposed views are handled through the trans flags
+    without copies.  Runs on ``stream`` (default: torch's current stream)."""
+    import torch
+    if A.dim() != B.dim() or A.dim() not in (2, 3):
+        raise ValueError("A and B must both be 2-D or both 3-D")
+    M, K, lda, tA = _operand(A, "A")
+    K2, N, ldb, tB = _operand(B, "B")
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    batched = A.dim() == 3
+    batch = A.shape[0] if batched else 1
+    if batched and B.shape[0] != batch:
+        raise ValueError("batch sizes differ")
+    shape = (batch, M, N) if batched else (M, N)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=A.device)
+    elif tuple(out.shape) != shape or out.dtype != torch.float32 or out.stride(-1) != 1:
+        raise ValueError("out has the wrong shape, dtype or layout")
+    ldc = max(out.stride(-2), N, 1)
+    s = stream if stream is not None else torch.cuda.current_stream(A.device)
+    sp = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+    if batched:
+        sgemm_f32_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb,
+                                  B.stride(0), out.data_ptr(), ldc, out.stride(0), batch,
+                                  tA, tB, sp)
+    else:
+        sgemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA, tB, sp)
+    return out

@@ -1,0 +1,224 @@
+// C ABI of the SGEMM library: argument validation, kernel selection, launch.
+// The public contract (layout, ownership, errors) is documented in
+// include/sgemm_gb300.h.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "gemm_args.h"
+#include "sgemm_gb300.h"
+
+namespace sgemm {
+
+cudaError_t launch_simt_nn(const GemmArgs &a, bool vec, cudaStream_t s);
+cudaError_t launch_simt_nt(const GemmArgs &a, bool vec, cudaStream_t s);
+cudaError_t launch_simt_tn(const GemmArgs &a, bool vec, cudaStream_t s);
+cudaError_t launch_simt_tt(const GemmArgs &a, bool vec, cudaStream_t s);
+
+cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, cudaStream_t s) {
+    if (!transA && !transB) return launch_simt_nn(a, vec, s);
+    if (!transA && transB) return launch_simt_nt(a, vec, s);
+    if (transA && !transB) return launch_simt_tn(a, vec, s);
+    return launch_simt_tt(a, vec, s);
+}
+
+namespace {
+
+__global__ void zero_fill_kernel(float *C, int64_t ldc, int64_t strideC, int M, int N, int batch) {
+    const int64_t total = (int64_t)batch * M * N;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t z = t / ((int64_t)M * N);
+        const int64_t r = t - z * (int64_t)M * N;
+        const int64_t i = r / N, j = r - i * N;
+        C[z * strideC + i * ldc + j] = 0.f;
+    }
+}
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;    // kernels index within a problem in int32
+constexpr int64_t kMaxLd = (int64_t)1 << 40;
+constexpr int64_t kMaxStride = (int64_t)1 << 60;
+constexpr int64_t kMaxBlocks = ((int64_t)1 << 31) - 1;
+
+bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// Is the current device an sm_103 part?  Cached per device ordinal.
+int check_device() {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0)
+        return fail(SGEMM_EDEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    static int cc_cache[64];   // 0 = unknown, else 10*major + minor
+    int cc = dev < 64 ? cc_cache[dev] : 0;
+    if (cc == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cc = 10 * major + minor;
+        if (dev < 64) cc_cache[dev] = cc;
+    }
+    if (cc != 103)
+        return fail(SGEMM_EDEVICE, "device %d has compute capability %d.%d; this library is built "
+                    "for sm_103a (GB300) only", dev, cc / 10, cc % 10);
+    return SGEMM_OK;
+}
+
+// Validates a strided-batched problem.  Returns SGEMM_OK and fills `a` when
+// there is work to do; `nothing` is set when the call is a no-op.
+int validate(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
+             const float *B, int64_t ldb, int64_t strideB, float *C, int64_t ldc,
+             int64_t strideC, int64_t batch, int transA, int transB, GemmArgs &a,
+             bool &nothing) {
+    nothing = false;
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return fail(SGEMM_EINVAL_TRANS, "transA=%d transB=%d: each must be 0 or 1", transA, transB);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(SGEMM_EINVAL_DIM, "negative size M=%lld N=%lld K=%lld", (long long)M,
+                    (long long)N, (long long)K);
+    if (batch < 0) return fail(SGEMM_EINVAL_BATCH, "batch=%lld is negative", (long long)batch);
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return fail(SGEMM_EINVAL_DIM, "a size exceeds 2^30 (M=%lld N=%lld K=%lld)", (long long)M,
+                    (long long)N, (long long)K);
+    const int64_t min_lda = transA ? (M > 1 ? M : 1) : (K > 1 ? K : 1);
+    const int64_t min_ldb = transB ? (K > 1 ? K : 1) : (N > 1 ? N : 1);
+    const int64_t min_ldc = N > 1 ? N : 1;
+    if (lda < min_lda || ldb < min_ldb || ldc < min_ldc)
+        return fail(SGEMM_EINVAL_LD, "leading dimension too small: lda=%lld (min %lld) ldb=%lld "
+                    "(min %lld) ldc=%lld (min %lld)", (long long)lda, (long long)min_lda,
+                    (long long)ldb, (long long)min_ldb, (long long)ldc, (long long)min_ldc);
+    if (lda > kMaxLd || ldb > kMaxLd || ldc > kMaxLd)
+        return fail(SGEMM_EINVAL_LD, "leading dimension above 2^40");
+    if (M == 0 || N == 0 || batch == 0) {
+        nothing = true;
+        return SGEMM_OK;
+    }
+    if (batch > 1) {
+        if (strideA < 0 || strideB < 0 || strideC < 0 || strideA > kMaxStride ||
+            strideB > kMaxStride || strideC > kMaxStride)
+            return fail(SGEMM_EINVAL_BATCH, "batch strides must be non-negative");
+        const int64_t c_extent = (M - 1) * ldc + N;
+        if (strideC < c_extent)
+            return fail(SGEMM_EINVAL_BATCH, "strideC=%lld lets the C matrices of two batches "
+                        "overlap (need >= %lld)", (long long)strideC, (long long)c_extent);
+    }
+    if (C == nullptr) return fail(SGEMM_EINVAL_PTR, "C is NULL");
+    if (!aligned(C, 4)) return fail(SGEMM_EINVAL_PTR, "C is not 4-byte aligned");
+    if (K > 0) {
+        if (A == nullptr || B == nullptr) return fail(SGEMM_EINVAL_PTR, "A or B is NULL");
+        if (!aligned(A, 4) || !aligned(B, 4))
+            return fail(SGEMM_EINVAL_PTR, "A or B is not 4-byte aligned");
+    }
+    const int64_t tiles_m = (M + kSimtTileM - 1) / kSimtTileM;
+    const int64_t tiles_n = (N + kSimtTileN - 1) / kSimtTileN;
+    if (batch * tiles_m * tiles_n > kMaxBlocks)
+        return fail(SGEMM_EINVAL_DIM, "problem needs more than 2^31-1 thread blocks");
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.lda = lda;
+    a.ldb = ldb;
+    a.ldc = ldc;
+    a.strideA = batch > 1 ? strideA : 0;
+    a.strideB = batch > 1 ? strideB : 0;
+    a.strideC = batch > 1 ? strideC : 0;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.batch = (int)batch;
+    a.tiles_m = (int)tiles_m;
+    a.tiles_n = (int)tiles_n;
+    a.group_m = 8;
+    return SGEMM_OK;
+}
+
+// 16-byte accesses are legal when every base, leading dimension and batch
+// stride keeps float4 groups aligned.
+bool vector_ok(const GemmArgs &a) {
+    return aligned(a.A, 16) && aligned(a.B, 16) && aligned(a.C, 16) && a.lda % 4 == 0 &&
+           a.ldb % 4 == 0 && a.ldc % 4 == 0 && a.strideA % 4 == 0 && a.strideB % 4 == 0 &&
+           a.strideC % 4 == 0;
+}
+
+int run(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
+        const float *B, int64_t ldb, int64_t strideB, float *C, int64_t ldc, int64_t strideC,
+        int64_t batch, int transA, int transB, void *stream) {
+    g_last_error[0] = '\0';
+    GemmArgs a;
+    bool nothing = false;
+    int st = validate(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, transA,
+                      transB, a, nothing);
+    if (st != SGEMM_OK || nothing) return st;
+    st = check_device();
+    if (st != SGEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0) {
+        e = launch_zero_fill(a, s);
+    } else {
+        e = launch_simt(a, transA != 0, transB != 0, vector_ok(a), s);
+    }
+    if (e != cudaSuccess)
+        return fail(SGEMM_ELAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
+    return SGEMM_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s) {
+    const int64_t total = (int64_t)a.batch * a.M * a.N;
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    zero_fill_kernel<<<blocks, 256, 0, s>>>(a.C, a.ldc, a.strideC, a.M, a.N, a.batch);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm
+
+extern "C" {
+
+int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+              int64_t ldb, float *C, int64_t ldc, int transA, int transB, void *stream) {
+    return sgemm::run(M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA, transB, stream);
+}
+
+int sgemm_f32_strided_batched(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                              int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
+                              float *C, int64_t ldc, int64_t strideC, int64_t batch, int transA,
+                              int transB, void *stream) {
+    return sgemm::run(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, transA,
+                      transB, stream);
+}
+
+const char *sgemm_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK: return "SGEMM_OK";
+        case SGEMM_EINVAL_DIM: return "SGEMM_EINVAL_DIM: invalid size";
+        case SGEMM_EINVAL_LD: return "SGEMM_EINVAL_LD: invalid leading dimension";
+        case SGEMM_EINVAL_PTR: return "SGEMM_EINVAL_PTR: invalid pointer";
+        case SGEMM_EINVAL_TRANS: return "SGEMM_EINVAL_TRANS: invalid transpose flag";
+        case SGEMM_EINVAL_BATCH: return "SGEMM_EINVAL_BATCH: invalid batch or stride";
+        case SGEMM_ELAUNCH: return "SGEMM_ELAUNCH: kernel launch failed";
+        case SGEMM_EDEVICE: return "SGEMM_EDEVICE: no usable sm_103 device";
+        default: return "unknown sgemm status";
+    }
+}
+
+const char *sgemm_last_error(void) { return sgemm::g_last_error; }
+
+int sgemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,34 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel
+// translation units.  Not part of the public header.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sgemm {
+
+// One (possibly batched) problem after host-side validation.  All pointers are
+// device pointers; strides and leading dimensions are in elements.
+struct GemmArgs {
+    const float *A;
+    const float *B;
+    float *C;
+    int64_t lda, ldb, ldc;
+    int64_t strideA, strideB, strideC;
+    int M, N, K;
+    int batch;
+    int tiles_m, tiles_n;   // output tiles per problem
+    int group_m;            // tile rows per raster group (L2 reuse)
+};
+
+// SIMT FP32 kernel family (CUDA cores).  vec: every base pointer, leading
+// dimension and batch stride allows 16-byte accesses.
+cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, cudaStream_t s);
+
+// C[0:M, 0:N] = 0 for every batch (the K == 0 case).
+cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s);
+
+constexpr int kSimtTileM = 128;
+constexpr int kSimtTileN = 128;
+
+}  // namespace sgemm

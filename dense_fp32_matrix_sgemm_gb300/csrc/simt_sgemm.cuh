@@ -1,0 +1,304 @@
+// SIMT FP32 SGEMM for sm_103a: C = op(A) op(B) on the CUDA cores.
+//
+// Design, after "CUDA GEMM operator performance optimization" (sections 4-10)
+// and re-tuned for Blackwell:
+//   * block tile 128 x 128, K sliced in steps of BK (section 4);
+//   * 256 threads, each owning an 8 x 8 register tile split into four 4 x 4
+//     sub-blocks 64 rows/columns apart (section 8.5, option 3), so every
+//     fragment read is one 16-byte shared-memory load;
+//   * warps of 4 x 8 threads laid out in Z order (section 8.5, option 4) so a
+//     quarter-warp touches two A and four B float4s: broadcast, no conflicts;
+//   * both operand tiles are stored K-major in shared memory ([BK][128],
+//     "A transposed", section 7.3).  Operands that are contiguous along M/N
+//     (A^T storage, row-major B) are copied with 16-byte cp.async; operands
+//     contiguous along K (row-major A, B^T storage) are corner-turned: 128-bit
+//     global loads into registers, then four scalar stores (section 7.3; the
+//     corner turning of the PMPP tiled kernel);
+//   * float4 groups of tile row kk are XOR-swizzled by a function of kk>>2
+//     (section 8.5, option 2, at float4 granularity) which makes the
+//     corner-turn stores conflict-free while reads stay 16-byte aligned;
+//   * STAGES-deep pipeline: cp.async groups for the asynchronous operand, the
+//     register-staged operand loaded one tile ahead, one barrier per K tile
+//     (sections 9-10);
+//   * packed two-wide FP32 FMA (fma.rn.f32x2, sm_100+) halves the issue slots
+//     of the outer product, leaving room for the shared-memory loads;
+//   * tiles are rasterised in groups of `group_m` tile rows so that a wave of
+//     CTAs shares A and B panels in L2 (section 2.3);
+//   * edge tiles are zero-padded on load and stores are guarded (DD2360
+//     workbook, section 14.3).
+// Each output's K terms are accumulated by one thread, in ascending k, with
+// fp32 FMAs: the result is deterministic.
+#pragma once
+
+#include "device_utils.cuh"
+#include "gemm_args.h"
+
+namespace sgemm {
+namespace simt {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int THREADS = 256;
+
+// Element offset of float4 group 0 of tile row kk after swizzling: the group
+// index is XORed with a multiple of (128/BK)/4 chosen so that the rows a warp
+// writes during a corner turn land in 32 distinct banks.  Always a multiple of
+// 4 and below 32, so a float4 stays whole and within its 32-float segment.
+template <int BK>
+__device__ __forceinline__ int swz(int kk) {
+    return (128 / BK) * (kk >> 2);
+}
+
+// Loads one BK x 128 slice of an operand into a K-major shared tile.
+// Element (mn, k) of the operand lives at base[mn*ld + k] when KCONTIG, else
+// at base[k*ld + mn].  Out-of-range elements are stored as zero.
+template <int BK, bool KCONTIG, bool VEC>
+struct TileLoader {
+    static constexpr int ELEMS = BK * 128 / THREADS;   // per thread per slice
+    static constexpr int VECS = ELEMS / 4;
+    static constexpr int KQ = BK / 4;                  // float4 groups along k per row
+
+    const float *base;
+    int64_t ld;
+    int mn0, mn_ext, K;
+    float4 rv[(KCONTIG && VEC) ? VECS : 1];
+    float rs[(KCONTIG && !VEC) ? ELEMS : 1];
+
+    // Start moving slice k0.  Asynchronous operands go straight to `tile`
+    // (cp.async, committed by the caller); staged operands land in registers.
+    __device__ __forceinline__ void fetch(int k0, float *tile) {
+        const int tid = threadIdx.x;
+        if constexpr (!KCONTIG && VEC) {
+#pragma unroll
+            for (int r = 0; r < VECS; ++r) {
+                const int g = tid + r * THREADS;
+                const int kk = g >> 5, mq = g & 31;
+                const int mn = mn0 + 4 * mq, k = k0 + kk;
+                int nv = mn_ext - mn;
+                nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
+                if (k >= K) nv = 0;
+                const float *src = nv ? base + (int64_t)k * ld + mn : base;
+                cp_async_16(smem_u32(tile + kk * 128 + ((4 * mq) ^ swz<BK>(kk))), src, nv * 4);
+            }
+        } else if constexpr (!KCONTIG && !VEC) {
+#pragma unroll
+            for (int r = 0; r < ELEMS; ++r) {
+                const int e = tid + r * THREADS;
+                const int kk = e >> 7, mm = e & 127;
+                const int mn = mn0 + mm, k = k0 + kk;
+                const bool ok = (mn < mn_ext) && (k < K);
+                const float *src = ok ? base + (int64_t)k * ld + mn : base;
+                cp_async_4(smem_u32(tile + kk * 128 + (mm ^ swz<BK>(kk))), src, ok ? 4 : 0);
+            }
+        } else if constexpr (KCONTIG && VEC) {
+#pragma unroll
+            for (int r = 0; r < VECS; ++r) {
+                const int g = tid + r * THREADS;
+                const int row = g / KQ, kq = g % KQ;
+                const int mn = mn0 + row, k = k0 + 4 * kq;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (mn < mn_ext) {
+                    const float *p = base + (int64_t)mn * ld + k;
+                    if (k + 3 < K) {
+                        v = ldg_f4(p);
+                    } else {
+                        if (k + 0 < K) v.x = __ldg(p + 0);
+                        if (k + 1 < K) v.y = __ldg(p + 1);
+                        if (k + 2 < K) v.z = __ldg(p + 2);
+                    }
+                }
+                rv[r] = v;
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < ELEMS; ++r) {
+                const int e = tid + r * THREADS;
+                const int row = e / BK, kk = e % BK;
+                const int mn = mn0 + row, k = k0 + kk;
+                rs[r] = (mn < mn_ext && k < K) ? __ldg(base + (int64_t)mn * ld + k) : 0.f;
+            }
+        }
+    }
+
+    // Write a staged slice (corner turn) into `tile`; no-op for cp.async operands.
+    __device__ __forceinline__ void commit(float *tile) {
+        const int tid = threadIdx.x;
+        if constexpr (KCONTIG && VEC) {
+#pragma unroll
+            for (int r = 0; r < VECS; ++r) {
+                const int g = tid + r * THREADS;
+                const int row = g / KQ, kq = g % KQ;
+                const int kk = 4 * kq;
+                const int col = row ^ swz<BK>(kk);   // same swizzle for kk..kk+3
+                tile[(kk + 0) * 128 + col] = rv[r].x;
+                tile[(kk + 1) * 128 + col] = rv[r].y;
+                tile[(kk + 2) * 128 + col] = rv[r].z;
+                tile[(kk + 3) * 128 + col] = rv[r].w;
+            }
+        } else if constexpr (KCONTIG && !VEC) {
+#pragma unroll
+            for (int r = 0; r < ELEMS; ++r) {
+                const int e = tid + r * THREADS;
+                const int row = e / BK, kk = e % BK;
+                tile[kk * 128 + (row ^ swz<BK>(kk))] = rs[r];
+            }
+        }
+    }
+};
+
+template <int BK, int STAGES>
+constexpr int smem_bytes() {
+    return 2 * STAGES * BK * 128 * (int)sizeof(float);
+}
+
+// Maps the linear CTA index to (batch, tile row, tile column), walking
+// `group_m` tile rows down a column before moving right.
+__device__ __forceinline__ void raster(const GemmArgs &p, int &z, int &tm, int &tn) {
+    const int per_batch = p.tiles_m * p.tiles_n;
+    const int bid = blockIdx.x;
+    z = bid / per_batch;
+    const int t = bid - z * per_batch;
+    const int group = p.group_m * p.tiles_n;
+    const int g = t / group;
+    const int first = g * p.group_m;
+    const int rows = min(p.tiles_m - first, p.group_m);
+    const int r = t - g * group;
+    tm = first + r % rows;
+    tn = r / rows;
+}
+
+template <int BK, int STAGES, bool TA, bool TB, bool VEC, bool FFMA2, int MINB = 2>
+__global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArgs p) {
+    static_assert(BK == 8 || BK == 16 || BK == 32, "BK must be 8, 16 or 32");
+    static_assert(STAGES >= 2, "need at least two stages");
+    constexpr int TILE = BK * 128;
+    extern __shared__ __align__(16) float smem[];
+    float *As = smem;
+    float *Bs = smem + STAGES * TILE;
+
+    int z, tm, tn;
+    raster(p, z, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+
+    // A is contiguous along K unless stored transposed; B the other way round.
+    TileLoader<BK, !TA, VEC> la;
+    la.base = p.A + (int64_t)z * p.strideA;
+    la.ld = p.lda;
+    la.mn0 = m0;
+    la.mn_ext = p.M;
+    la.K = p.K;
+    TileLoader<BK, TB, VEC> lb;
+    lb.base = p.B + (int64_t)z * p.strideB;
+    lb.ld = p.ldb;
+    lb.mn0 = n0;
+    lb.mn_ext = p.N;
+    lb.K = p.K;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int lane_row = (lane & 1) | ((lane >> 4) << 1);   // Z-order 4 x 8
+    const int lane_col = (lane >> 1) & 7;
+    const int ty = (warp >> 1) * 4 + lane_row;               // 0..15
+    const int tx = (warp & 1) * 8 + lane_col;                // 0..15
+    const int a_col = 4 * ty;
+    const int b_col = 4 * tx;
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    const int ktiles = (p.K + BK - 1) / BK;
+
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < ktiles) {
+            la.fetch(s * BK, As + s * TILE);
+            lb.fetch(s * BK, Bs + s * TILE);
+            la.commit(As + s * TILE);
+            lb.commit(Bs + s * TILE);
+        }
+        cp_async_commit();
+    }
+
+    int rstage = 0;            // stage holding tile kt
+    int wstage = STAGES - 1;   // stage receiving tile kt + STAGES - 1
+    for (int kt = 0; kt < ktiles; ++kt) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+
+        const int nt = kt + STAGES - 1;
+        if (nt < ktiles) {
+            la.fetch(nt * BK, As + wstage * TILE);
+            lb.fetch(nt * BK, Bs + wstage * TILE);
+        }
+        cp_async_commit();
+
+        const float *at = As + rstage * TILE;
+        const float *bt = Bs + rstage * TILE;
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            const int sw = swz<BK>(kk);
+            const float *ar = at + kk * 128;
+            const float *br = bt + kk * 128;
+            const float4 a0 = *reinterpret_cast<const float4 *>(ar + (a_col ^ sw));
+            const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + (a_col ^ sw));
+            const float4 b0 = *reinterpret_cast<const float4 *>(br + (b_col ^ sw));
+            const float4 b1 = *reinterpret_cast<const float4 *>(br + 64 + (b_col ^ sw));
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            if constexpr (FFMA2) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {
+                        float2 c = make_float2(acc[i][j], acc[i][j + 1]);
+                        c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
+                        acc[i][j] = c.x;
+                        acc[i][j + 1] = c.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+        }
+
+        if (nt < ktiles) {
+            la.commit(As + wstage * TILE);
+            lb.commit(Bs + wstage * TILE);
+        }
+        rstage = (rstage + 1 == STAGES) ? 0 : rstage + 1;
+        wstage = (wstage + 1 == STAGES) ? 0 : wstage + 1;
+    }
+    cp_async_wait<0>();
+
+    float *Cz = p.C + (int64_t)z * p.strideC;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + (i < 4 ? a_col + i : 64 + a_col + (i - 4));
+        if (row >= p.M) continue;
+        float *crow = Cz + (int64_t)row * p.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = n0 + h * 64 + b_col;
+            const float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                         acc[i][4 * h + 3]);
+            if (VEC && col + 3 < p.N) {
+                *reinterpret_cast<float4 *>(crow + col) = v;
+            } else {
+                if (col + 0 < p.N) crow[col + 0] = v.x;
+                if (col + 1 < p.N) crow[col + 1] = v.y;
+                if (col + 2 < p.N) crow[col + 2] = v.z;
+                if (col + 3 < p.N) crow[col + 3] = v.w;
+            }
+        }
+    }
+}
+
+}  // namespace simt
+}  // namespace sgemm

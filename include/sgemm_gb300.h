@@ -1,0 +1,112 @@
+/*
+ * sgemm_gb300.h -- single-precision GEMM on NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the GEMM of "CUDA GEMM operator performance optimization",
+ * section 1.1: C = A x B with A of size M x K, B of size K x N and C of size
+ * M x N, all float32, 2*M*N*K floating-point operations.  The batched form
+ * ("Batched GEMM: batched matmul in multi-head attention", same page, section
+ * 1.2) applies it to independent problems at fixed strides, e.g. Q K^T.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  All matrices are ROW-MAJOR, as in the page's kernels
+ *   (element (r, c) of an R x C matrix with leading dimension ld at X[r*ld + c]).
+ *   op(X) = X when trans == 0 and X^T when trans == 1, where trans describes
+ *   how the operand is STORED:
+ *     A, transA == 0: stored M x K, opA(i,k) = A[i*lda + k], lda >= max(1, K)
+ *     A, transA == 1: stored K x M, opA(i,k) = A[k*lda + i], lda >= max(1, M)
+ *     B, transB == 0: stored K x N, opB(k,j) = B[k*ldb + j], ldb >= max(1, N)
+ *     B, transB == 1: stored N x K, opB(k,j) = B[j*ldb + k], ldb >= max(1, K)
+ *     C:              stored M x N, C(i,j)   = C[i*ldc + j], ldc >= max(1, N)
+ *   The result OVERWRITES C[0:M, 0:N]: C = op(A) op(B).  There is no alpha or
+ *   beta (the operation on the pages has none).  Padding columns
+ *   (c >= N of C, and likewise for A and B) are never read or written.
+ *
+ * Pointers and ownership.  A, B and C are DEVICE pointers (cudaMalloc, torch
+ *   tensors, ...) owned by the caller, 4-byte aligned.  A and C, or B and C,
+ *   must not overlap.  The library keeps no pointer after the call returns
+ *   and allocates no device memory per call.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream).  Work is enqueued on it and the call returns without
+ *   synchronising; the result is visible to later work on that stream.
+ *
+ * Precision.  sgemm_f32*: every product and sum is an fp32 FMA on the CUDA
+ *   cores, each output's terms accumulated in ascending k by one thread; the
+ *   result is deterministic (bit-identical across calls).  sgemm_f32_tf32x3*:
+ *   tensor cores with the three-term TF32 split (see below).
+ *
+ * Errors.  Arguments are validated on the host before anything is enqueued;
+ *   on a violation the call returns a nonzero sgemm_status, enqueues nothing,
+ *   and sgemm_last_error() describes it.  Launch failures return
+ *   SGEMM_ELAUNCH.  Errors of the asynchronous execution itself surface, as
+ *   usual in CUDA, at the caller's next synchronisation.  The library never
+ *   exits or aborts the process.
+ *
+ * Degenerate sizes.  M == 0, N == 0 or batch == 0: nothing is done, SGEMM_OK
+ *   (pointers may then be NULL).  K == 0: C[0:M,0:N] is set to zero (the
+ *   empty sum); A and B are not read and may be NULL.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_EINVAL_DIM = 1,    /* M, N or K negative, or too large for the grid */
+    SGEMM_EINVAL_LD = 2,     /* a leading dimension below its minimum */
+    SGEMM_EINVAL_PTR = 3,    /* NULL where data is needed, or not 4-byte aligned */
+    SGEMM_EINVAL_TRANS = 4,  /* transA/transB not 0 or 1 */
+    SGEMM_EINVAL_BATCH = 5,  /* batch < 0, or strideC lets two problems' C overlap */
+    SGEMM_ELAUNCH = 6,       /* the kernel launch itself failed */
+    SGEMM_EDEVICE = 7        /* no usable device, or the device is not sm_103 */
+} sgemm_status;
+
+/*
+ * C = op(A) op(B), fp32 on the CUDA cores.
+ * Defined by: "CUDA GEMM operator performance optimization", section 1.1
+ * (GEMM), built as in sections 4-10 of that page (block, warp and thread
+ * tiling, float4 access, transposed/swizzled shared-memory tiles, multi-stage
+ * asynchronous copies); edge tiles are zero-padded as in the DD2360 workbook,
+ * section 14.3.
+ */
+int sgemm_f32(int64_t M, int64_t N, int64_t K,
+              const float *A, int64_t lda,
+              const float *B, int64_t ldb,
+              float *C, int64_t ldc,
+              int transA, int transB, void *stream);
+
+/*
+ * For z in [0, batch): C_z = op(A_z) op(B_z) with X_z = X + z*strideX
+ * (strides in elements).  strideA and strideB may be 0 (broadcast one
+ * operand).  strideC must keep the batches' C regions disjoint:
+ * strideC >= (M-1)*ldc + N when batch > 1 (else SGEMM_EINVAL_BATCH).
+ * Defined by: "CUDA GEMM operator performance optimization", section 1.2
+ * (batched matmul, Q K^T in attention), each problem as in sgemm_f32.
+ */
+int sgemm_f32_strided_batched(int64_t M, int64_t N, int64_t K,
+                              const float *A, int64_t lda, int64_t strideA,
+                              const float *B, int64_t ldb, int64_t strideB,
+                              float *C, int64_t ldc, int64_t strideC,
+                              int64_t batch, int transA, int transB, void *stream);
+
+/* Text for a status code (static storage). */
+const char *sgemm_status_string(int status);
+
+/* Detail of the last failed call on the calling host thread ("" if none).
+ * The pointer stays valid until the next call on this thread. */
+const char *sgemm_last_error(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

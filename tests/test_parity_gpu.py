@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path against the CPU oracle, element by element.
+
+Acceptance (fp32 path): |C - C_ref| <= 1e-5 * sum_k |a_ik||b_kj| + 1e-6 for
+every output, and bit-exact equality whenever the inputs are small integers
+(every partial sum is then an exact float, so any summation order gives the
+same bits).  Every case runs through the C ABI with NaN guard bands around all
+buffers and NaN in the padding columns of C; those must survive untouched.
+"""
+import numpy as np
+import pytest
+
+import dense_fp32_matrix_sgemm_gb300 as sg
+import oracle
+import workloads
+
+from gpu_util import run
+
+pytestmark = pytest.mark.gpu
+
+ENTRY = "sgemm_f32"
+
+
+def _oracle_full(case):
+    if case["batch"] == 1:
+        C, S = oracle.sgemm(case["A"][0], case["B"][0], case["M"], case["N"], case["K"],
+                            transA=case["transA"], transB=case["transB"], lda=case["lda"],
+                            ldb=case["ldb"], with_scale=True)
+        return C[None], S[None]
+    return oracle.sgemm_strided_batched(case["A"], case["B"], case["M"], case["N"], case["K"],
+                                        case["batch"], transA=case["transA"],
+                                        transB=case["transB"], lda=case["lda"], ldb=case["ldb"],
+                                        with_scale=True)
+
+
+def check_full(case, got, exact=False, label=""):
+    ref, S = _oracle_full(case)
+    assert np.isfinite(got).all(), f"{label}: non-finite outputs"
+    if exact:
+        bad = got != ref
+        assert not bad.any(), f"{label}: {int(bad.sum())} outputs differ from the exact result"
+    ok = oracle.within_tolerance(got, ref, S)
+    if not ok.all():
+        idx = np.argwhere(~ok)[:5]
+        raise AssertionError(f"{label}: {int((~ok).sum())} outputs outside the bound, first "
+                             f"{idx.tolist()} got {got[~ok][:5]} want {ref[~ok][:5]}")
+    return oracle.rrmse(got, ref)
+
+
+def check_sampled(case, got, nrows=16, nent=1024, seed=0, exact=False, label=""):
+    """Full rows (row-major A only) plus random single entries."""
+    M, N, K = case["M"], case["N"], case["K"]
+    rng = np.random.default_rng(seed)
+    z = 0
+    if not case["transA"]:
+        rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, nrows)]))
+        sub = np.ascontiguousarray(case["A"][z][rows])
+        ref, S = oracle.sgemm(sub, case["B"][z], len(rows), N, K, transB=case["transB"],
+                              lda=case["lda"], ldb=case["ldb"], with_scale=True)
+        g = got[z][rows]
+        ok = oracle.within_tolerance(g, ref, S)
+        assert ok.all(), f"{label}: {int((~ok).sum())} sampled-row outputs outside the bound"
+        if exact:
+            assert np.array_equal(g, ref), f"{label}: sampled rows not bit-exact"
+    r = rng.integers(0, M, nent)
+    c = rng.integers(0, N, nent)
+    r[:4] = [0, M - 1, 0, M - 1]
+    c[:4] = [0, N - 1, N - 1, 0]
+    out, sab = oracle.sgemm_entries(case["A"][z], case["B"][z], M, N, K, r, c,
+                                    transA=case["transA"], transB=case["transB"],
+                                    lda=case["lda"], ldb=case["ldb"])
+    g = got[z][r, c]
+    ok = np.abs(g.astype(np.float64) - out) <= oracle.REL_TOL * sab + oracle.ABS_TOL
+    assert ok.all(), f"{label}: {int((~ok).sum())} sampled entries outside the bound"
+    if exact:
+        assert np.array_equal(g, out)
+
+
+# ---------------------------------------------------------------- named workloads
+
+SMALL = ["sgemm_256x256x256_uniform", "sgemm_256x256x256_int",
+         "sgemm_2049x3071x1537_tA_normal", "sgemm_2049x3071x1537_tA_int",
+         "sgemm_3072x3072x3072_uniform", "sgemm_3072x3072x3072_int"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_parity(name):
+    case = workloads.make_case(name)
+    got = run(case, entry=ENTRY)
+    err = check_full(case, got, exact=case["A"].dtype == np.float32 and "int" in name, label=name)
+    print(f"{name}: RRMSE {err:.3e}")
+
+
+def test_batched_qkT_full_parity():
+    name = "sgemm_batched96_512x512x64_qkT_normal"
+    case = workloads.make_case(name)
+    got = run(case, entry=ENTRY + "_strided_batched")
+    err = check_full(case, got, label=name)
+    print(f"{name}: RRMSE {err:.3e}")
+
+
+@pytest.mark.parametrize("name", ["sgemm_8192x8192x4096_uniform", "sgemm_4096x4096x8192_uniform",
+                                  "sgemm_8192x8192x8192_uniform"])
+def test_large_workload_sampled_parity(name):
+    case = workloads.make_case(name)
+    got = run(case, entry=ENTRY)
+    check_sampled(case, got, label=name)
+
+
+# ---------------------------------------------------------------- shapes and layouts
+
+LAB = [(64, 64, 64), (100, 70, 50), (513, 1023, 8192)]   # (M, N, K): DD2360 section 14.3 lab sizes
+
+
+@pytest.mark.parametrize("M,N,K", LAB)
+def test_lab_shapes(M, N, K):
+    case = workloads.make_operands(M, N, K, dist="uniform", seed=1, key=200)
+    check_full(case, run(case, entry=ENTRY), label=f"{M}x{N}x{K}")
+
+
+EDGE = [(1, 1, 1), (1, 129, 7), (129, 1, 15), (127, 129, 17), (129, 127, 33), (255, 257, 1),
+        (130, 250, 16), (128, 128, 8), (257, 131, 77), (3, 300, 400)]
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", EDGE)
+def test_edges_all_layouts(M, N, K, tA, tB):
+    # padded leading dimensions (multiples of 4) with NaN in the padding
+    lda = ((M if tA else K) + 4) // 4 * 4 + 4
+    ldb = ((K if tB else N) + 4) // 4 * 4
+    ldc = (N + 4) // 4 * 4
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=ldc,
+                                   dist="normal", poison=True, seed=2, key=201)
+    check_full(case, run(case, entry=ENTRY), label=f"{M}x{N}x{K} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("offset,M,N,K", [(1, 130, 67, 45), (2, 64, 64, 64), (3, 257, 33, 129)])
+def test_unaligned_scalar_path(offset, M, N, K, tA, tB):
+    # odd leading dimensions and base addresses that are not 16-byte aligned
+    lda = (M if tA else K) + 1
+    ldb = (K if tB else N) + 3
+    ldc = N + 1
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=ldc,
+                                   dist="int", poison=True, seed=3, key=202)
+    check_full(case, run(case, entry=ENTRY, offset=offset), exact=True,
+               label=f"offset {offset} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1)])
+def test_integer_ragged_bit_exact(tA, tB):
+    M, N, K = 333, 517, 1000
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, dist="int", seed=4, key=203)
+    check_full(case, run(case, entry=ENTRY), exact=True, label="int ragged")
+
+
+def test_batched_broadcast_and_layouts():
+    for tA, tB in [(0, 0), (1, 0), (0, 1), (1, 1)]:
+        case = workloads.make_operands(70, 90, 33, batch=5, transA=tA, transB=tB,
+                                       dist="normal", sigma=0.125, seed=5, key=204)
+        got = run(case, entry=ENTRY + "_strided_batched")
+        check_full(case, got, label=f"batched tA={tA} tB={tB}")
+    # stride 0 on B: every batch multiplies by the same B
+    case = workloads.make_operands(40, 50, 60, batch=4, dist="int", seed=6, key=205)
+    got = run(case, entry=ENTRY + "_strided_batched", strideB=0)
+    for z in range(4):
+        ref = oracle.sgemm(case["A"][z], case["B"][0], 40, 50, 60)
+        assert np.array_equal(got[z], ref)
+
+
+# ---------------------------------------------------------------- semantics
+
+def test_k_zero_writes_zeros():
+    import torch
+    M, N = 70, 45
+    C = torch.full((M, 48), float("nan"), device="cuda")
+    sg.sgemm_f32(M, N, 0, 0, 1, 0, N, C.data_ptr(), 48, 0, 0, 0)
+    torch.cuda.synchronize()
+    out = C.cpu().numpy()
+    assert (out[:, :N] == 0).all() and np.isnan(out[:, N:]).all()
+
+
+def test_empty_problem_leaves_c_untouched():
+    import torch
+    C = torch.full((8, 8), 7.0, device="cuda")
+    sg.sgemm_f32(0, 8, 8, 0, 8, 0, 8, C.data_ptr(), 8, 0, 0, 0)
+    sg.sgemm_f32(8, 0, 8, 0, 8, 0, 1, C.data_ptr(), 8, 0, 0, 0)
+    torch.cuda.synchronize()
+    assert (C == 7).all()
+
+
+def test_deterministic_bits():
+    case = workloads.make_operands(300, 200, 500, dist="normal", seed=7, key=206)
+    a = run(case, entry=ENTRY)
+    b = run(case, entry=ENTRY)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_runs_on_a_side_stream():
+    import torch
+    s = torch.cuda.Stream()
+    case = workloads.make_operands(200, 300, 100, dist="int", seed=8, key=207)
+    with torch.cuda.stream(s):
+        got = run(case, entry=ENTRY, stream=s.cuda_stream)
+    check_full(case, got, exact=True, label="side stream")
+
+
+def test_matmul_convenience_handles_views():
+    import torch
+    torch.manual_seed(0)
+    A = torch.randn(300, 200, device="cuda")
+    B = torch.randn(150, 200, device="cuda")
+    out = sg.matmul(A, B.t())          # B^T view: passed with transB = 1, no copy
+    ref, S = oracle.sgemm(A.cpu().numpy(), B.cpu().numpy(), 300, 150, 200, transB=1,
+                          with_scale=True)
+    assert oracle.within_tolerance(out.cpu().numpy(), ref, S).all()
+    Ab = torch.randn(3, 64, 32, device="cuda")
+    Bb = torch.randn(3, 32, 48, device="cuda")
+    outb = sg.matmul(Ab, Bb)
+    for z in range(3):
+        ref, S = oracle.sgemm(Ab[z].cpu().numpy(), Bb[z].cpu().numpy(), 64, 48, 32,
+                              with_scale=True)
+        assert oracle.within_tolerance(outb[z].cpu().numpy(), ref, S).all()
