@@ -19,7 +19,8 @@ import threading
 
 __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32", "sgemm_f32_strided_batched",
-           "status_string", "last_error", "version", "matmul", "SGEMM_OK"]
+           "status_string", "last_error", "version", "matmul", "SGEMM_OK",
+           "probe_fp32_fma", "probe_out_elems"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -42,6 +43,8 @@ SIGNATURES = {
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_last_error": (ctypes.c_char_p, []),
     "sgemm_version": (_int, []),
+    "sgemm_probe_fp32_fma": (_int, [_int, _i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
+    "sgemm_probe_out_elems": (_i64, []),
 }
 
 
@@ -122,6 +125,18 @@ def sgemm_f32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
         M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
         batch, transA, transB, stream or None)
     return _check(st) if check else st
+
+
+def probe_fp32_fma(packed: int, iterations: int, out_ptr: int, stream=0) -> float:
+    """Launch the FP32 FMA probe; returns the FLOPs of the launch."""
+    flops = ctypes.c_double(0.0)
+    _check(load_library().sgemm_probe_fp32_fma(packed, iterations, out_ptr or None,
+                                               ctypes.byref(flops), stream or None))
+    return flops.value
+
+
+def probe_out_elems() -> int:
+    return load_library().sgemm_probe_out_elems()
 
 
 def _operand(t, name):

@@ -17,7 +17,7 @@ struct GemmArgs {
     int64_t strideA, strideB, strideC;
     int M, N, K;
     int batch;
-    int tiles_m, tiles_n;   // output tiles per problem
+    int tiles_m, tiles_n;   // output tiles per problem (each launcher sets its own)
     int group_m;            // tile rows per raster group (L2 reuse)
 };
 
@@ -28,6 +28,7 @@ cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, c
 // C[0:M, 0:N] = 0 for every batch (the K == 0 case).
 cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s);
 
+// Smallest block tile of any kernel: bounds the grid size during validation.
 constexpr int kSimtTileM = 128;
 constexpr int kSimtTileN = 128;
 

@@ -1,0 +1,68 @@
+// FP32 FMA throughput probe: the measured denominator of "% of FP32 peak".
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "sgemm_gb300.h"
+#include "sgemm_gb300_probe.h"
+
+namespace sgemm {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 8;
+constexpr int kChains = 16;   // independent float2 chains per thread
+
+template <bool PACKED>
+__global__ void __launch_bounds__(kThreads) fp32_probe_kernel(float *out, long long iters) {
+    // x <- x * m + c converges to c / (1 - m) = 1; values stay normal.
+    const float m = 0.9990234375f, c = 1.0f - m;
+    float2 x[kChains];
+#pragma unroll
+    for (int j = 0; j < kChains; ++j)
+        x[j] = make_float2(0.5f + 0.01f * j + 1e-6f * threadIdx.x, 0.25f + 0.01f * j);
+    const float2 m2 = make_float2(m, m), c2 = make_float2(c, c);
+    for (long long i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int j = 0; j < kChains; ++j) {
+            if constexpr (PACKED) {
+                x[j] = __ffma2_rn(x[j], m2, c2);
+            } else {
+                x[j].x = fmaf(x[j].x, m, c);
+                x[j].y = fmaf(x[j].y, m, c);
+            }
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kChains; ++j) s += x[j].x + x[j].y;
+    out[blockIdx.x * (int64_t)blockDim.x + threadIdx.x] = s / (2 * kChains);
+}
+
+int64_t probe_ctas() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return (int64_t)sms * kCtasPerSm;
+}
+
+}  // namespace
+}  // namespace sgemm
+
+extern "C" int64_t sgemm_probe_out_elems(void) { return sgemm::probe_ctas() * sgemm::kThreads; }
+
+extern "C" int sgemm_probe_fp32_fma(int packed, int64_t iterations, float *out, double *flops_out,
+                                    void *stream) {
+    if ((packed != 0 && packed != 1) || iterations <= 0) return SGEMM_EINVAL_DIM;
+    if (out == nullptr || flops_out == nullptr) return SGEMM_EINVAL_PTR;
+    const int64_t ctas = sgemm::probe_ctas();
+    if (ctas <= 0) return SGEMM_EDEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (packed)
+        sgemm::fp32_probe_kernel<true><<<(unsigned)ctas, sgemm::kThreads, 0, s>>>(out, iterations);
+    else
+        sgemm::fp32_probe_kernel<false><<<(unsigned)ctas, sgemm::kThreads, 0, s>>>(out, iterations);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ELAUNCH;
+    *flops_out = 2.0 * 2.0 * sgemm::kChains * (double)iterations * (double)ctas * sgemm::kThreads;
+    return SGEMM_OK;
+}

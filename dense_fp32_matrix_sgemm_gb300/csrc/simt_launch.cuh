@@ -11,14 +11,16 @@ namespace sgemm {
 namespace simt {
 
 // Tuned configuration for GB300: K slice, pipeline depth, packed FMA.
-constexpr int kBK = 16;
+constexpr int kBK = 32;
 constexpr int kStages = 3;
 constexpr bool kFfma2 = true;
+constexpr int kBN = 128;
+constexpr int kMinBlocks = 1;   // one 96 KB CTA per SM, up to 255 registers per thread
 
 template <bool TA, bool TB, bool VEC>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t s) {
-    auto kern = sgemm_simt_kernel<kBK, kStages, TA, TB, VEC, kFfma2>;
-    constexpr int smem = smem_bytes<kBK, kStages>();
+    auto kern = sgemm_simt_kernel<kBK, kStages, kBN, TA, TB, VEC, kFfma2, kMinBlocks>;
+    constexpr int smem = smem_bytes<kBK, kStages, kBN>();
     if (smem > 48 * 1024) {
         // The opt-in shared-memory limit is a per-device function attribute.
         static std::atomic<unsigned long long> configured{0};
@@ -32,8 +34,11 @@ cudaError_t launch_variant(const GemmArgs &a, cudaStream_t s) {
             configured.fetch_or(bit);
         }
     }
-    const long long blocks = (long long)a.batch * a.tiles_m * a.tiles_n;
-    kern<<<(unsigned)blocks, THREADS, smem, s>>>(a);
+    GemmArgs g = a;
+    g.tiles_m = (a.M + BM - 1) / BM;
+    g.tiles_n = (a.N + kBN - 1) / kBN;
+    const long long blocks = (long long)g.batch * g.tiles_m * g.tiles_n;
+    kern<<<(unsigned)blocks, THREADS, smem, s>>>(g);
     return cudaGetLastError();
 }
 

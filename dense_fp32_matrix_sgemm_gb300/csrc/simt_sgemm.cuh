@@ -2,7 +2,7 @@
 //
 // Design, after "CUDA GEMM operator performance optimization" (sections 4-10)
 // and re-tuned for Blackwell:
-//   * block tile 128 x 128, K sliced in steps of BK (section 4);
+//   * block tile 128 x BN (BN = 128 or 256), K sliced in steps of BK (section 4);
 //   * 256 threads, each owning an 8 x 8 register tile split into four 4 x 4
 //     sub-blocks 64 rows/columns apart (section 8.5, option 3), so every
 //     fragment read is one 16-byte shared-memory load;
@@ -37,7 +37,6 @@ namespace sgemm {
 namespace simt {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
 constexpr int THREADS = 256;
 
 // Element offset of float4 group 0 of tile row kk after swizzling: the group
@@ -49,14 +48,16 @@ __device__ __forceinline__ int swz(int kk) {
     return (128 / BK) * (kk >> 2);
 }
 
-// Loads one BK x 128 slice of an operand into a K-major shared tile.
-// Element (mn, k) of the operand lives at base[mn*ld + k] when KCONTIG, else
-// at base[k*ld + mn].  Out-of-range elements are stored as zero.
-template <int BK, bool KCONTIG, bool VEC>
+// Loads one BK x ROWS slice of an operand into a K-major shared tile
+// ([BK][ROWS] floats).  Element (mn, k) of the operand lives at
+// base[mn*ld + k] when KCONTIG, else at base[k*ld + mn].  Out-of-range
+// elements are stored as zero.
+template <int BK, int ROWS, bool KCONTIG, bool VEC>
 struct TileLoader {
-    static constexpr int ELEMS = BK * 128 / THREADS;   // per thread per slice
+    static constexpr int ELEMS = BK * ROWS / THREADS;  // per thread per slice
     static constexpr int VECS = ELEMS / 4;
     static constexpr int KQ = BK / 4;                  // float4 groups along k per row
+    static constexpr int GROUPS = ROWS / 4;            // float4 groups along mn per k row
 
     const float *base;
     int64_t ld;
@@ -72,23 +73,23 @@ struct TileLoader {
 #pragma unroll
             for (int r = 0; r < VECS; ++r) {
                 const int g = tid + r * THREADS;
-                const int kk = g >> 5, mq = g & 31;
+                const int kk = g / GROUPS, mq = g % GROUPS;
                 const int mn = mn0 + 4 * mq, k = k0 + kk;
                 int nv = mn_ext - mn;
                 nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
                 if (k >= K) nv = 0;
                 const float *src = nv ? base + (int64_t)k * ld + mn : base;
-                cp_async_16(smem_u32(tile + kk * 128 + ((4 * mq) ^ swz<BK>(kk))), src, nv * 4);
+                cp_async_16(smem_u32(tile + kk * ROWS + ((4 * mq) ^ swz<BK>(kk))), src, nv * 4);
             }
         } else if constexpr (!KCONTIG && !VEC) {
 #pragma unroll
             for (int r = 0; r < ELEMS; ++r) {
                 const int e = tid + r * THREADS;
-                const int kk = e >> 7, mm = e & 127;
+                const int kk = e / ROWS, mm = e % ROWS;
                 const int mn = mn0 + mm, k = k0 + kk;
                 const bool ok = (mn < mn_ext) && (k < K);
                 const float *src = ok ? base + (int64_t)k * ld + mn : base;
-                cp_async_4(smem_u32(tile + kk * 128 + (mm ^ swz<BK>(kk))), src, ok ? 4 : 0);
+                cp_async_4(smem_u32(tile + kk * ROWS + (mm ^ swz<BK>(kk))), src, ok ? 4 : 0);
             }
         } else if constexpr (KCONTIG && VEC) {
 #pragma unroll
@@ -130,25 +131,25 @@ struct TileLoader {
                 const int row = g / KQ, kq = g % KQ;
                 const int kk = 4 * kq;
                 const int col = row ^ swz<BK>(kk);   // same swizzle for kk..kk+3
-                tile[(kk + 0) * 128 + col] = rv[r].x;
-                tile[(kk + 1) * 128 + col] = rv[r].y;
-                tile[(kk + 2) * 128 + col] = rv[r].z;
-                tile[(kk + 3) * 128 + col] = rv[r].w;
+                tile[(kk + 0) * ROWS + col] = rv[r].x;
+                tile[(kk + 1) * ROWS + col] = rv[r].y;
+                tile[(kk + 2) * ROWS + col] = rv[r].z;
+                tile[(kk + 3) * ROWS + col] = rv[r].w;
             }
         } else if constexpr (KCONTIG && !VEC) {
 #pragma unroll
             for (int r = 0; r < ELEMS; ++r) {
                 const int e = tid + r * THREADS;
                 const int row = e / BK, kk = e % BK;
-                tile[kk * 128 + (row ^ swz<BK>(kk))] = rs[r];
+                tile[kk * ROWS + (row ^ swz<BK>(kk))] = rs[r];
             }
         }
     }
 };
 
-template <int BK, int STAGES>
+template <int BK, int STAGES, int BN_>
 constexpr int smem_bytes() {
-    return 2 * STAGES * BK * 128 * (int)sizeof(float);
+    return STAGES * BK * (BM + BN_) * (int)sizeof(float);
 }
 
 // Maps the linear CTA index to (batch, tile row, tile column), walking
@@ -167,27 +168,33 @@ __device__ __forceinline__ void raster(const GemmArgs &p, int &z, int &tm, int &
     tn = r / rows;
 }
 
-template <int BK, int STAGES, bool TA, bool TB, bool VEC, bool FFMA2, int MINB = 2>
+// Block tile 128 x BN_ (BN_ = 128 or 256); each thread owns an 8 x (BN_/16)
+// register tile made of 4 x 4 sub-blocks spaced 64 rows / 64 columns apart.
+template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int MINB>
 __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArgs p) {
     static_assert(BK == 8 || BK == 16 || BK == 32, "BK must be 8, 16 or 32");
+    static_assert(BN_ == 128 || BN_ == 256, "BN must be 128 or 256");
     static_assert(STAGES >= 2, "need at least two stages");
-    constexpr int TILE = BK * 128;
+    constexpr int TN = BN_ / 16;         // columns per thread
+    constexpr int NSB = BN_ / 64;        // 4-wide column sub-blocks per thread
+    constexpr int ATILE = BK * BM;
+    constexpr int BTILE = BK * BN_;
     extern __shared__ __align__(16) float smem[];
     float *As = smem;
-    float *Bs = smem + STAGES * TILE;
+    float *Bs = smem + STAGES * ATILE;
 
     int z, tm, tn;
     raster(p, z, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
+    const int m0 = tm * BM, n0 = tn * BN_;
 
     // A is contiguous along K unless stored transposed; B the other way round.
-    TileLoader<BK, !TA, VEC> la;
+    TileLoader<BK, BM, !TA, VEC> la;
     la.base = p.A + (int64_t)z * p.strideA;
     la.ld = p.lda;
     la.mn0 = m0;
     la.mn_ext = p.M;
     la.K = p.K;
-    TileLoader<BK, TB, VEC> lb;
+    TileLoader<BK, BN_, TB, VEC> lb;
     lb.base = p.B + (int64_t)z * p.strideB;
     lb.ld = p.ldb;
     lb.mn0 = n0;
@@ -203,21 +210,21 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     const int a_col = 4 * ty;
     const int b_col = 4 * tx;
 
-    float acc[8][8];
+    float acc[8][TN];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
     const int ktiles = (p.K + BK - 1) / BK;
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
         if (s < ktiles) {
-            la.fetch(s * BK, As + s * TILE);
-            lb.fetch(s * BK, Bs + s * TILE);
-            la.commit(As + s * TILE);
-            lb.commit(Bs + s * TILE);
+            la.fetch(s * BK, As + s * ATILE);
+            lb.fetch(s * BK, Bs + s * BTILE);
+            la.commit(As + s * ATILE);
+            lb.commit(Bs + s * BTILE);
         }
         cp_async_commit();
     }
@@ -230,30 +237,36 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
 
         const int nt = kt + STAGES - 1;
         if (nt < ktiles) {
-            la.fetch(nt * BK, As + wstage * TILE);
-            lb.fetch(nt * BK, Bs + wstage * TILE);
+            la.fetch(nt * BK, As + wstage * ATILE);
+            lb.fetch(nt * BK, Bs + wstage * BTILE);
         }
         cp_async_commit();
 
-        const float *at = As + rstage * TILE;
-        const float *bt = Bs + rstage * TILE;
+        const float *at = As + rstage * ATILE;
+        const float *bt = Bs + rstage * BTILE;
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             const int sw = swz<BK>(kk);
-            const float *ar = at + kk * 128;
-            const float *br = bt + kk * 128;
+            const float *ar = at + kk * BM;
+            const float *br = bt + kk * BN_;
             const float4 a0 = *reinterpret_cast<const float4 *>(ar + (a_col ^ sw));
             const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + (a_col ^ sw));
-            const float4 b0 = *reinterpret_cast<const float4 *>(br + (b_col ^ sw));
-            const float4 b1 = *reinterpret_cast<const float4 *>(br + 64 + (b_col ^ sw));
             const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float b[TN];
+#pragma unroll
+            for (int h = 0; h < NSB; ++h) {
+                const float4 bv = *reinterpret_cast<const float4 *>(br + 64 * h + (b_col ^ sw));
+                b[4 * h + 0] = bv.x;
+                b[4 * h + 1] = bv.y;
+                b[4 * h + 2] = bv.z;
+                b[4 * h + 3] = bv.w;
+            }
             if constexpr (FFMA2) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float2 ai = make_float2(a[i], a[i]);
 #pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
+                    for (int j = 0; j < TN; j += 2) {
                         float2 c = make_float2(acc[i][j], acc[i][j + 1]);
                         c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
                         acc[i][j] = c.x;
@@ -264,13 +277,13 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
             }
         }
 
         if (nt < ktiles) {
-            la.commit(As + wstage * TILE);
-            lb.commit(Bs + wstage * TILE);
+            la.commit(As + wstage * ATILE);
+            lb.commit(Bs + wstage * BTILE);
         }
         rstage = (rstage + 1 == STAGES) ? 0 : rstage + 1;
         wstage = (wstage + 1 == STAGES) ? 0 : wstage + 1;
@@ -284,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
         if (row >= p.M) continue;
         float *crow = Cz + (int64_t)row * p.ldc;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NSB; ++h) {
             const int col = n0 + h * 64 + b_col;
             const float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
                                          acc[i][4 * h + 3]);

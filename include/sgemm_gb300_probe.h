@@ -1,0 +1,42 @@
+/*
+ * sgemm_gb300_probe.h -- measuring the FP32 peak that SGEMM is judged against.
+ *
+ * The peak of a GPU's FP32 units is cores x 2 FLOP (one FMA) x clock
+ * (DD2360 workbook, section 3, worked example on the T4's FP32 peak).  This
+ * probe measures it instead of assuming it: every thread runs 16 independent
+ * FMA chains held in registers, no memory traffic, on a grid of 8 CTAs of 256
+ * threads per SM.  The caller times the launch (e.g. with CUDA events on
+ * `stream`) and divides *flops_out by the time.
+ */
+#ifndef SGEMM_GB300_PROBE_H
+#define SGEMM_GB300_PROBE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Launch the FP32 FMA probe on `stream` (cudaStream_t as void*).
+ *   packed      0: scalar fma.rn.f32;  1: packed fma.rn.f32x2 (two FMAs per
+ *               instruction, sm_100 and newer).
+ *   iterations  loop trips per thread (> 0); each trip does 32 FMAs per thread.
+ *   out         device buffer of at least sgemm_probe_out_elems() floats,
+ *               owned by the caller; receives one value per thread (the
+ *               chains converge to 1.0, a check that the work was done).
+ *   flops_out   host pointer; receives the FLOPs of one launch (2 per FMA).
+ * Returns an sgemm_status (SGEMM_EINVAL_* on bad arguments, SGEMM_ELAUNCH,
+ * SGEMM_EDEVICE); asynchronous like every call of the library.
+ */
+int sgemm_probe_fp32_fma(int packed, int64_t iterations, float *out, double *flops_out,
+                         void *stream);
+
+/* Number of floats `out` must hold on the current device. */
+int64_t sgemm_probe_out_elems(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_PROBE_H */
