@@ -1,0 +1,362 @@
+// FP32 GEMM on the tensor cores with the three-term TF32 split (3xTF32).
+//
+// TF32 keeps 10 explicit mantissa bits, so one TF32 product loses about 750x
+// in accuracy against FP32 FMA (the RRMSE comparison of 1.03e-6 vs 7.78e-4 on
+// the ChetanC28/cuda-kernels page).  Writing every input as x = hi + lo with
+// hi = tf32(x) and lo = tf32(x - hi), the product a*b is recovered to about
+// 2^-21 relative by hi_a*hi_b + hi_a*lo_b + lo_a*hi_b (the lo*lo term is
+// below that and dropped), each term a TF32 MMA accumulated in fp32 in TMEM.
+//
+// Stage 1 (split kernels): op(A) and op(B) are rewritten into a caller-owned
+//   workspace as K-major planes [batch][hi|lo][rows][Kp] (Kp = K rounded up
+//   to 4 so rows are 16-byte aligned for TMA).  M- or N-major operands are
+//   corner-turned through a padded shared tile on the way.
+// Stage 2 (GEMM kernel, one 128 x 256 output tile per CTA, 128 threads):
+//   warp 0 / lane 0 issues TMA loads of the four 128-byte-swizzled K slices
+//   (A hi/lo 128 x 32, B hi/lo 256 x 32) into a 2-stage ring; warp 1 owns the
+//   TMEM accumulator (256 columns) and lane 0 issues 3 MMAs (M128 N256 K8)
+//   per 8-wide K step, releasing each stage with tcgen05.commit; after the
+//   last commit all four warps read their 32 TMEM lanes (= tile rows) and
+//   store guarded rows of C.  Every mbarrier wait is bounded; a wait that runs
+//   out flags the CTA, the roles drain and the error word is raised.
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "gemm_args.h"
+#include "tc_utils.cuh"
+
+namespace sgemm {
+namespace tf32x3 {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 32;          // one 128-byte swizzle row of fp32
+constexpr int STAGES = 2;
+constexpr int THREADS = 128;
+constexpr int TMEM_COLS = 256;
+constexpr int A_TILE_BYTES = BM * BK * 4;   // 16 KB
+constexpr int B_TILE_BYTES = BN * BK * 4;   // 32 KB
+constexpr int STAGE_BYTES = 2 * A_TILE_BYTES + 2 * B_TILE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+__device__ unsigned int g_tf32x3_error = 0;   // bit 0: a pipeline wait ran out
+
+// ------------------------------------------------------------------ split
+
+// KCONTIG operand: element (r, k) at X[z*sX + r*ld + k].
+__global__ void split_kcontig_kernel(const float *__restrict__ X, int64_t ld, int64_t sX, int R,
+                                     int K, int Kp, int batch, float *__restrict__ ws) {
+    const int64_t plane = (int64_t)R * Kp;
+    for (int64_t row = blockIdx.y * (int64_t)blockDim.y + threadIdx.y; row < (int64_t)batch * R;
+         row += (int64_t)gridDim.y * blockDim.y) {
+        const int64_t z = row / R, r = row - z * R;
+        const float *src = X + z * sX + r * ld;
+        float *hi = ws + (2 * z) * plane + r * Kp;
+        float *lo = hi + plane;
+        for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) {
+            const float x = src[k];
+            const float h = tc::to_tf32(x);
+            hi[k] = h;
+            lo[k] = tc::to_tf32(x - h);
+        }
+    }
+}
+
+// M/N-major operand: element (r, k) at X[z*sX + k*ld + r]; transposed through
+// a 32 x 33 shared tile so both the read and the write are coalesced.
+__global__ void split_transpose_kernel(const float *__restrict__ X, int64_t ld, int64_t sX, int R,
+                                       int K, int Kp, int batch, float *__restrict__ ws) {
+    __shared__ float tile[32][33];
+    const int64_t plane = (int64_t)R * Kp;
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+    for (int z = blockIdx.z; z < batch; z += gridDim.z) {
+        const float *src = X + (int64_t)z * sX;
+        float *hi = ws + (2 * (int64_t)z) * plane;
+        float *lo = hi + plane;
+        for (int kt = blockIdx.y; kt * 32 < K; kt += gridDim.y) {
+            for (int rt = blockIdx.x; rt * 32 < R; rt += gridDim.x) {
+                const int k0 = kt * 32, r0 = rt * 32;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    const int k = k0 + ty + i, r = r0 + tx;
+                    tile[ty + i][tx] = (k < K && r < R) ? src[(int64_t)k * ld + r] : 0.f;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    const int r = r0 + ty + i, k = k0 + tx;
+                    if (r < R && k < K) {
+                        const float x = tile[tx][ty + i];
+                        const float h = tc::to_tf32(x);
+                        hi[(int64_t)r * Kp + k] = h;
+                        lo[(int64_t)r * Kp + k] = tc::to_tf32(x - h);
+                    }
+                }
+                __syncthreads();
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ GEMM
+
+struct Tf32x3Params {
+    float *C;
+    int64_t ldc, strideC;
+    int M, N, K;
+    int tiles_m, tiles_n, group_m;
+    int vec_c;   // C rows allow 16-byte stores
+};
+
+__device__ __forceinline__ void raster(const Tf32x3Params &p, int &z, int &tm, int &tn) {
+    const int per_batch = p.tiles_m * p.tiles_n;
+    const int bid = blockIdx.x;
+    z = bid / per_batch;
+    const int t = bid - z * per_batch;
+    const int group = p.group_m * p.tiles_n;
+    const int g = t / group;
+    const int first = g * p.group_m;
+    const int rows = min(p.tiles_m - first, p.group_m);
+    const int r = t - g * group;
+    tm = first + r % rows;
+    tn = r / rows;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Tf32x3Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
+    const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t tiles = tc::smem_u32_generic(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    const uint32_t full0 = tc::smem_u32_generic(bars);           // full[s]  = full0 + 8 s
+    const uint32_t empty0 = full0 + 8 * STAGES;                    // empty[s] = empty0 + 8 s
+    const uint32_t done_bar = empty0 + 8 * STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int z, tm, tn;
+    raster(p, z, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int kblocks = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
+        }
+        tc::mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        int issued = 0;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % STAGES;
+            if (kb >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((kb / STAGES) & 1) ^ 1, abort_flag))
+                break;
+            const uint32_t st = tiles + s * STAGE_BYTES;
+            const uint32_t fb = full0 + 8 * s;
+            tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const int k0 = kb * BK;
+            tc::tma_load_3d(st, &tmA, fb, k0, m0, 2 * z);
+            tc::tma_load_3d(st + A_TILE_BYTES, &tmA, fb, k0, m0, 2 * z + 1);
+            tc::tma_load_3d(st + 2 * A_TILE_BYTES, &tmB, fb, k0, n0, 2 * z);
+            tc::tma_load_3d(st + 2 * A_TILE_BYTES + B_TILE_BYTES, &tmB, fb, k0, n0, 2 * z + 1);
+            issued = kb + 1;
+        }
+        if (*abort_flag) {
+            // let this thread's copies in flight land before the CTA exits
+            for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb) {
+                const int s = kb % STAGES;
+                const long long t0 = clock64();
+                while (!tc::mbar_try_wait(full0 + 8 * s, (kb / STAGES) & 1) &&
+                       clock64() - t0 < tc::kWaitLimitCycles) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = tc::tf32_idesc<BM, BN>();
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % STAGES;
+            if (!tc::mbar_wait(full0 + 8 * s, (kb / STAGES) & 1, abort_flag)) break;
+            tc::fence_after_sync();
+            const uint32_t st = tiles + s * STAGE_BYTES;
+            const uint64_t ahi = tc::sw128_kmajor_desc(st);
+            const uint64_t alo = tc::sw128_kmajor_desc(st + A_TILE_BYTES);
+            const uint64_t bhi = tc::sw128_kmajor_desc(st + 2 * A_TILE_BYTES);
+            const uint64_t blo = tc::sw128_kmajor_desc(st + 2 * A_TILE_BYTES + B_TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 8; ++kk) {
+                const uint64_t step = (uint64_t)(kk * 32) >> 4;   // 8 tf32 = 32 bytes along K
+                const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                tc::mma_tf32(tmem, alo + step, bhi + step, idesc, first);
+                tc::mma_tf32(tmem, ahi + step, blo + step, idesc, 1u);
+                tc::mma_tf32(tmem, ahi + step, bhi + step, idesc, 1u);
+            }
+            tc::mma_commit(empty0 + 8 * s);
+        }
+        tc::mma_commit(done_bar);   // tracks every MMA issued above, also on abort
+    }
+    __syncwarp();
+
+    // ---------------- epilogue: TMEM lane (32*warp + lane) holds tile row m0 + 32*warp + lane
+    const bool ok = tc::mbar_wait(done_bar, 0, abort_flag);
+    tc::fence_after_sync();
+    if (ok && !*abort_flag) {
+        const int row = m0 + 32 * warp + lane;
+        float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tc::tmem_ld_32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c), v);
+            if (row < p.M) {
+                const int col0 = n0 + 32 * c;
+                if (p.vec_c && col0 + 31 < p.N) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(crow + col0 + j) =
+                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j < p.N) crow[col0 + j] = v[j];
+                }
+            }
+        }
+    }
+    if (*abort_flag && threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Planes [2*batch][rows][Kp] of fp32, box 32 (K) x box_rows x 1, 128B swizzle.
+bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp, int batch,
+                    int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)(2 * batch)};
+    const cuuint64_t strides[2] = {(cuuint64_t)Kp * 4, (cuuint64_t)rows * Kp * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace tf32x3
+
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
+    const size_t Kp = (size_t)((K + 3) / 4 * 4);
+    const size_t a = tf32x3::align_up(2 * (size_t)batch * (size_t)M * Kp * 4, 256);
+    const size_t b = tf32x3::align_up(2 * (size_t)batch * (size_t)N * Kp * 4, 256);
+    return a + b;
+}
+
+cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
+                          cudaStream_t s) {
+    using namespace tf32x3;
+    const int Kp = (a.K + 3) / 4 * 4;
+    float *wsA = static_cast<float *>(ws);
+    float *wsB = wsA + tf32x3::align_up(2 * (size_t)a.batch * a.M * Kp * 4, 256) / 4;
+
+    // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major hi/lo planes
+    auto split = [&](const float *X, int64_t ld, int64_t sX, int R, bool kcontig, float *out) {
+        if (kcontig) {
+            dim3 block(32, 8);
+            const int64_t rows = (int64_t)a.batch * R;
+            dim3 grid((unsigned)((a.K + 31) / 32 < 64 ? (a.K + 31) / 32 : 64),
+                      (unsigned)((rows + 7) / 8 < 65535 ? (rows + 7) / 8 : 65535));
+            split_kcontig_kernel<<<grid, block, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch, out);
+        } else {
+            dim3 block(32, 8);
+            dim3 grid((unsigned)((R + 31) / 32 < 65535 ? (R + 31) / 32 : 65535),
+                      (unsigned)((a.K + 31) / 32 < 65535 ? (a.K + 31) / 32 : 65535),
+                      (unsigned)(a.batch < 65535 ? a.batch : 65535));
+            split_transpose_kernel<<<grid, block, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch, out);
+        }
+    };
+    split(a.A, a.lda, a.strideA, a.M, !transA, wsA);
+    split(a.B, a.ldb, a.strideB, a.N, transB, wsB);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // stage 2: the tensor-core GEMM
+    CUtensorMap tmA, tmB;
+    if (!make_plane_map(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
+        !make_plane_map(&tmB, wsB, a.N, a.K, Kp, a.batch, BN))
+        return cudaErrorInvalidValue;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(tf32x3_gemm_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    Tf32x3Params p;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.strideC = a.strideC;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.tiles_m = (a.M + BM - 1) / BM;
+    p.tiles_n = (a.N + BN - 1) / BN;
+    p.group_m = 8;
+    p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && a.ldc % 4 == 0 && a.strideC % 4 == 0;
+    const long long blocks = (long long)a.batch * p.tiles_m * p.tiles_n;
+    tf32x3_gemm_kernel<<<(unsigned)blocks, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+cudaError_t tf32x3_read_error(unsigned int *flags, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, tf32x3::g_tf32x3_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(tf32x3::g_tf32x3_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace sgemm
