@@ -20,7 +20,8 @@ import threading
 __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32", "sgemm_f32_strided_batched",
            "status_string", "last_error", "version", "matmul", "SGEMM_OK",
-           "probe_fp32_fma", "probe_out_elems"]
+           "probe_fp32_fma", "probe_out_elems", "sgemm_f32_tf32x3",
+           "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -29,6 +30,7 @@ SGEMM_OK = 0
 STATUS_NAMES = {
     0: "SGEMM_OK", 1: "SGEMM_EINVAL_DIM", 2: "SGEMM_EINVAL_LD", 3: "SGEMM_EINVAL_PTR",
     4: "SGEMM_EINVAL_TRANS", 5: "SGEMM_EINVAL_BATCH", 6: "SGEMM_ELAUNCH", 7: "SGEMM_EDEVICE",
+    8: "SGEMM_EWORKSPACE",
 }
 
 _i64 = ctypes.c_int64
@@ -43,6 +45,13 @@ SIGNATURES = {
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_last_error": (ctypes.c_char_p, []),
     "sgemm_version": (_int, []),
+    "sgemm_f32_tf32x3": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
+                                _vp, ctypes.c_uint64, _vp]),
+    "sgemm_f32_tf32x3_strided_batched": (_int, [_i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
+                                                _i64, _vp, _i64, _i64, _i64, _int, _int, _vp,
+                                                ctypes.c_uint64, _vp]),
+    "sgemm_f32_tf32x3_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _i64]),
+    "sgemm_device_status": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
     "sgemm_probe_fp32_fma": (_int, [_int, _i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_probe_out_elems": (_i64, []),
 }
@@ -127,6 +136,37 @@ def sgemm_f32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
     return _check(st) if check else st
 
 
+def sgemm_f32_tf32x3(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,
+                     workspace_bytes=0, stream=0, *, check=True):
+    """C = op(A) op(B) on the tensor cores (3xTF32); ``workspace`` is a device
+    pointer of at least tf32x3_workspace_size(M, N, K, 1) bytes."""
+    st = load_library().sgemm_f32_tf32x3(M, N, K, A or None, lda, B or None, ldb, C or None,
+                                         ldc, transA, transB, workspace or None, workspace_bytes,
+                                         stream or None)
+    return _check(st) if check else st
+
+
+def sgemm_f32_tf32x3_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                                     batch, transA=0, transB=0, workspace=0, workspace_bytes=0,
+                                     stream=0, *, check=True):
+    """Strided-batched 3xTF32 product."""
+    st = load_library().sgemm_f32_tf32x3_strided_batched(
+        M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
+        batch, transA, transB, workspace or None, workspace_bytes, stream or None)
+    return _check(st) if check else st
+
+
+def tf32x3_workspace_size(M, N, K, batch=1) -> int:
+    return load_library().sgemm_f32_tf32x3_workspace_size(M, N, K, batch)
+
+
+def device_status(reset: bool = False) -> int:
+    """The library's device status word (bit 0: a tensor-core pipeline wait ran out)."""
+    flags = ctypes.c_uint(0)
+    _check(load_library().sgemm_device_status(ctypes.byref(flags), 1 if reset else 0))
+    return flags.value
+
+
 def probe_fp32_fma(packed: int, iterations: int, out_ptr: int, stream=0) -> float:
     """Launch the FP32 FMA probe; returns the FLOPs of the launch."""
     flops = ctypes.c_double(0.0)
@@ -155,11 +195,17 @@ def _operand(t, name):
     raise ValueError(f"{name} must have one unit stride among its last two dimensions")
 
 
-def matmul(A, B, out=None, stream=None):
+def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None):
     """out = A @ B for float32 CUDA tensors of shape (M, K) x (K, N), or batched
     (b, M, K) x (b, K, N).  Transposed views are handled through the trans flags
-    without copies.  Runs on ``stream`` (default: torch's current stream)."""
+    without copies.  Runs on ``stream`` (default: torch's current stream).
+
+    precision="fp32": CUDA-core FMA (sgemm_f32*); "tf32x3": tensor cores with
+    the three-term TF32 split (sgemm_f32_tf32x3*), using ``workspace`` (a CUDA
+    uint8 tensor) or a fresh one from torch's allocator."""
     import torch
+    if precision not in ("fp32", "tf32x3"):
+        raise ValueError("precision must be 'fp32' or 'tf32x3'")
     if A.dim() != B.dim() or A.dim() not in (2, 3):
         raise ValueError("A and B must both be 2-D or both 3-D")
     M, K, lda, tA = _operand(A, "A")
@@ -178,7 +224,19 @@ def matmul(A, B, out=None, stream=None):
     ldc = max(out.stride(-2), N, 1)
     s = stream if stream is not None else torch.cuda.current_stream(A.device)
     sp = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
-    if batched:
+    if precision == "tf32x3":
+        need = tf32x3_workspace_size(M, N, K, batch)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
+        ws, wsb = workspace.data_ptr(), workspace.numel()
+        if batched:
+            sgemm_f32_tf32x3_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0),
+                                             B.data_ptr(), ldb, B.stride(0), out.data_ptr(), ldc,
+                                             out.stride(0), batch, tA, tB, ws, wsb, sp)
+        else:
+            sgemm_f32_tf32x3(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                             tA, tB, ws, wsb, sp)
+    elif batched:
         sgemm_f32_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb,
                                   B.stride(0), out.data_ptr(), ldc, out.stride(0), batch,
                                   tA, tB, sp)

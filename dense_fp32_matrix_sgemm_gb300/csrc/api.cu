@@ -152,21 +152,33 @@ bool vector_ok(const GemmArgs &a) {
            a.strideC % 4 == 0;
 }
 
-int run(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
+enum class Path { Simt, Tf32x3 };
+
+int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
         const float *B, int64_t ldb, int64_t strideB, float *C, int64_t ldc, int64_t strideC,
-        int64_t batch, int transA, int transB, void *stream) {
+        int64_t batch, int transA, int transB, void *workspace, uint64_t workspace_bytes,
+        void *stream) {
     g_last_error[0] = '\0';
     GemmArgs a;
     bool nothing = false;
     int st = validate(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, transA,
                       transB, a, nothing);
     if (st != SGEMM_OK || nothing) return st;
+    if (path == Path::Tf32x3 && K > 0) {
+        const uint64_t need = tf32x3_workspace_bytes(M, N, K, batch);
+        if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+            return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: need %llu bytes, 256-byte "
+                        "aligned", workspace, (unsigned long long)workspace_bytes,
+                        (unsigned long long)need);
+    }
     st = check_device();
     if (st != SGEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (K == 0) {
         e = launch_zero_fill(a, s);
+    } else if (path == Path::Tf32x3) {
+        e = launch_tf32x3(a, transA != 0, transB != 0, workspace, s);
     } else {
         e = launch_simt(a, transA != 0, transB != 0, vector_ok(a), s);
     }
@@ -192,15 +204,48 @@ extern "C" {
 
 int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
               int64_t ldb, float *C, int64_t ldc, int transA, int transB, void *stream) {
-    return sgemm::run(M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA, transB, stream);
+    return sgemm::run(sgemm::Path::Simt, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA,
+                      transB, nullptr, 0, stream);
 }
 
 int sgemm_f32_strided_batched(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                               int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
                               float *C, int64_t ldc, int64_t strideC, int64_t batch, int transA,
                               int transB, void *stream) {
-    return sgemm::run(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, transA,
-                      transB, stream);
+    return sgemm::run(sgemm::Path::Simt, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                      strideC, batch, transA, transB, nullptr, 0, stream);
+}
+
+int sgemm_f32_tf32x3(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                     int64_t ldb, float *C, int64_t ldc, int transA, int transB, void *workspace,
+                     uint64_t workspace_bytes, void *stream) {
+    return sgemm::run(sgemm::Path::Tf32x3, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA,
+                      transB, workspace, workspace_bytes, stream);
+}
+
+int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                     int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
+                                     float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                     int transA, int transB, void *workspace,
+                                     uint64_t workspace_bytes, void *stream) {
+    return sgemm::run(sgemm::Path::Tf32x3, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                      strideC, batch, transA, transB, workspace, workspace_bytes, stream);
+}
+
+uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch) {
+    if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+    return sgemm::tf32x3_workspace_bytes(M, N, K, batch);
+}
+
+int sgemm_device_status(unsigned int *flags, int reset) {
+    if (flags == nullptr) return SGEMM_EINVAL_PTR;
+    int st = sgemm::check_device();
+    if (st != SGEMM_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = sgemm::tf32x3_read_error(flags, reset != 0);
+    if (e != cudaSuccess)
+        return sgemm::fail(SGEMM_ELAUNCH, "device status read failed: %s", cudaGetErrorString(e));
+    return SGEMM_OK;
 }
 
 const char *sgemm_status_string(int status) {
@@ -213,12 +258,13 @@ const char *sgemm_status_string(int status) {
         case SGEMM_EINVAL_BATCH: return "SGEMM_EINVAL_BATCH: invalid batch or stride";
         case SGEMM_ELAUNCH: return "SGEMM_ELAUNCH: kernel launch failed";
         case SGEMM_EDEVICE: return "SGEMM_EDEVICE: no usable sm_103 device";
+        case SGEMM_EWORKSPACE: return "SGEMM_EWORKSPACE: workspace missing, misaligned or too small";
         default: return "unknown sgemm status";
     }
 }
 
 const char *sgemm_last_error(void) { return sgemm::g_last_error; }
 
-int sgemm_version(void) { return 100; }
+int sgemm_version(void) { return 200; }
 
 }  // extern "C"

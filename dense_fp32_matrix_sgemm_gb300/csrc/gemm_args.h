@@ -25,6 +25,11 @@ struct GemmArgs {
 // dimension and batch stride allows 16-byte accesses.
 cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, cudaStream_t s);
 
+// Tensor-core 3xTF32 path: split kernels into `ws`, then the tcgen05 GEMM.
+cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s);
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
+cudaError_t tf32x3_read_error(unsigned int *flags, bool reset);
+
 // C[0:M, 0:N] = 0 for every batch (the K == 0 case).
 cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s);
 

@@ -11,6 +11,10 @@
 namespace sgemm {
 namespace tc {
 
+__device__ __forceinline__ uint32_t smem_u32_generic(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -221,8 +221,9 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     // ---------------- epilogue: TMEM lane (32*warp + lane) holds tile row m0 + 32*warp + lane
     const bool ok = tc::mbar_wait(done_bar, 0, abort_flag);
+    __syncwarp();   // reconverge before the warp-collective TMEM loads
     tc::fence_after_sync();
-    if (ok && !*abort_flag) {
+    if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
         const int row = m0 + 32 * warp + lane;
         float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
 #pragma unroll 1

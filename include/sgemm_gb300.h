@@ -64,7 +64,8 @@ typedef enum {
     SGEMM_EINVAL_TRANS = 4,  /* transA/transB not 0 or 1 */
     SGEMM_EINVAL_BATCH = 5,  /* batch < 0, or strideC lets two problems' C overlap */
     SGEMM_ELAUNCH = 6,       /* the kernel launch itself failed */
-    SGEMM_EDEVICE = 7        /* no usable device, or the device is not sm_103 */
+    SGEMM_EDEVICE = 7,       /* no usable device, or the device is not sm_103 */
+    SGEMM_EWORKSPACE = 8     /* workspace NULL, misaligned or smaller than required */
 } sgemm_status;
 
 /*
@@ -94,6 +95,54 @@ int sgemm_f32_strided_batched(int64_t M, int64_t N, int64_t K,
                               const float *B, int64_t ldb, int64_t strideB,
                               float *C, int64_t ldc, int64_t strideC,
                               int64_t batch, int transA, int transB, void *stream);
+
+/*
+ * C = op(A) op(B) on the tensor cores with FP32 accuracy: every input is split
+ * as x = hi + lo with hi = tf32(x), lo = tf32(x - hi), and the product is
+ * formed as lo_a*hi_b + hi_a*lo_b + hi_a*hi_b (three TF32 MMAs per K step,
+ * tcgen05 with the accumulator in tensor memory, fp32 accumulation).  The
+ * dropped lo_a*lo_b term and the TF32 rounding of lo are below 2^-20 of
+ * |a||b| per product, so results meet the same elementwise bound as
+ * sgemm_f32; small-integer inputs are exact.  Not bit-identical to
+ * sgemm_f32 (different summation order), deterministic across calls.
+ * Defined by: "CUDA GEMM operator performance optimization", section 1.1
+ * (GEMM); the TF32 accuracy trade-off it removes is the FMA vs TF32 RRMSE
+ * comparison (1.03e-6 vs 7.78e-4) on the ChetanC28/cuda-kernels page.
+ *
+ * Arguments as sgemm_f32, plus a caller-owned DEVICE workspace of at least
+ * sgemm_f32_tf32x3_workspace_size(M, N, K, 1) bytes, 256-byte aligned, not
+ * overlapping A, B or C, and not used by other work while this call's
+ * kernels run on `stream` (it holds the split operands).
+ * SGEMM_EWORKSPACE if it is NULL, misaligned or too small.
+ */
+int sgemm_f32_tf32x3(int64_t M, int64_t N, int64_t K,
+                     const float *A, int64_t lda,
+                     const float *B, int64_t ldb,
+                     float *C, int64_t ldc,
+                     int transA, int transB,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* Strided-batched form of sgemm_f32_tf32x3 (arguments as
+ * sgemm_f32_strided_batched plus the workspace, sized for `batch`). */
+int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K,
+                                     const float *A, int64_t lda, int64_t strideA,
+                                     const float *B, int64_t ldb, int64_t strideB,
+                                     float *C, int64_t ldc, int64_t strideC,
+                                     int64_t batch, int transA, int transB,
+                                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* Workspace bytes the tf32x3 entry points need: the hi and lo TF32 planes of
+ * op(A) and op(B), 2 * batch * (M + N) * round_up(K, 4) floats plus padding.
+ * 0 for empty problems or negative sizes. */
+uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
+
+/*
+ * Reads (and with reset != 0 clears) the library's device status word on the
+ * current device.  Bit 0 set: a tensor-core kernel gave up on a pipeline wait
+ * that exceeded its time limit (about 2 s); that call's C is not valid.
+ * Synchronises the device.  Returns an sgemm_status.
+ */
+int sgemm_device_status(unsigned int *flags, int reset);
 
 /* Text for a status code (static storage). */
 const char *sgemm_status_string(int status);

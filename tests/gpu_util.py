@@ -39,12 +39,17 @@ def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
     sC = M * ldc
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     fn = getattr(sg, entry)
+    extra = ()
+    if "tf32x3" in entry:
+        need = sg.tf32x3_workspace_size(M, N, K, batch)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        extra = (ws.data_ptr(), need)
     if entry.endswith("strided_batched"):
         fn(M, N, K, pA, lda, sA, pB, ldb, sB, pC, ldc, sC, batch, case["transA"],
-           case["transB"], s)
+           case["transB"], *extra, s)
     else:
         assert batch == 1
-        fn(M, N, K, pA, lda, pB, ldb, pC, ldc, case["transA"], case["transB"], s)
+        fn(M, N, K, pA, lda, pB, ldb, pC, ldc, case["transA"], case["transB"], *extra, s)
     torch.cuda.synchronize()
     out = Cbuf.cpu().numpy()
     assert np.isnan(out[:GUARD + offset]).all(), "write before the start of C"

@@ -17,7 +17,13 @@ from gpu_util import run
 
 pytestmark = pytest.mark.gpu
 
-ENTRY = "sgemm_f32"
+# Both product paths meet the same acceptance bound and are exact on small integers.
+PATHS = {"simt": "sgemm_f32", "tf32x3": "sgemm_f32_tf32x3"}
+
+
+@pytest.fixture(params=sorted(PATHS))
+def entry(request):
+    return PATHS[request.param]
 
 
 def _oracle_full(case):
@@ -83,26 +89,26 @@ SMALL = ["sgemm_256x256x256_uniform", "sgemm_256x256x256_int",
 
 
 @pytest.mark.parametrize("name", SMALL)
-def test_workload_full_parity(name):
+def test_workload_full_parity(name, entry):
     case = workloads.make_case(name)
-    got = run(case, entry=ENTRY)
+    got = run(case, entry=entry)
     err = check_full(case, got, exact=case["A"].dtype == np.float32 and "int" in name, label=name)
-    print(f"{name}: RRMSE {err:.3e}")
+    print(f"{entry} {name}: RRMSE {err:.3e}")
 
 
-def test_batched_qkT_full_parity():
+def test_batched_qkT_full_parity(entry):
     name = "sgemm_batched96_512x512x64_qkT_normal"
     case = workloads.make_case(name)
-    got = run(case, entry=ENTRY + "_strided_batched")
+    got = run(case, entry=entry + "_strided_batched")
     err = check_full(case, got, label=name)
-    print(f"{name}: RRMSE {err:.3e}")
+    print(f"{entry} {name}: RRMSE {err:.3e}")
 
 
 @pytest.mark.parametrize("name", ["sgemm_8192x8192x4096_uniform", "sgemm_4096x4096x8192_uniform",
                                   "sgemm_8192x8192x8192_uniform"])
-def test_large_workload_sampled_parity(name):
+def test_large_workload_sampled_parity(name, entry):
     case = workloads.make_case(name)
-    got = run(case, entry=ENTRY)
+    got = run(case, entry=entry)
     check_sampled(case, got, label=name)
 
 
@@ -112,9 +118,9 @@ LAB = [(64, 64, 64), (100, 70, 50), (513, 1023, 8192)]   # (M, N, K): DD2360 sec
 
 
 @pytest.mark.parametrize("M,N,K", LAB)
-def test_lab_shapes(M, N, K):
+def test_lab_shapes(M, N, K, entry):
     case = workloads.make_operands(M, N, K, dist="uniform", seed=1, key=200)
-    check_full(case, run(case, entry=ENTRY), label=f"{M}x{N}x{K}")
+    check_full(case, run(case, entry=entry), label=f"{M}x{N}x{K}")
 
 
 EDGE = [(1, 1, 1), (1, 129, 7), (129, 1, 15), (127, 129, 17), (129, 127, 33), (255, 257, 1),
@@ -123,45 +129,45 @@ EDGE = [(1, 1, 1), (1, 129, 7), (129, 1, 15), (127, 129, 17), (129, 127, 33), (2
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", EDGE)
-def test_edges_all_layouts(M, N, K, tA, tB):
+def test_edges_all_layouts(M, N, K, tA, tB, entry):
     # padded leading dimensions (multiples of 4) with NaN in the padding
     lda = ((M if tA else K) + 4) // 4 * 4 + 4
     ldb = ((K if tB else N) + 4) // 4 * 4
     ldc = (N + 4) // 4 * 4
     case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=ldc,
                                    dist="normal", poison=True, seed=2, key=201)
-    check_full(case, run(case, entry=ENTRY), label=f"{M}x{N}x{K} tA={tA} tB={tB}")
+    check_full(case, run(case, entry=entry), label=f"{M}x{N}x{K} tA={tA} tB={tB}")
 
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("offset,M,N,K", [(1, 130, 67, 45), (2, 64, 64, 64), (3, 257, 33, 129)])
-def test_unaligned_scalar_path(offset, M, N, K, tA, tB):
+def test_unaligned_scalar_path(offset, M, N, K, tA, tB, entry):
     # odd leading dimensions and base addresses that are not 16-byte aligned
     lda = (M if tA else K) + 1
     ldb = (K if tB else N) + 3
     ldc = N + 1
     case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=ldc,
                                    dist="int", poison=True, seed=3, key=202)
-    check_full(case, run(case, entry=ENTRY, offset=offset), exact=True,
+    check_full(case, run(case, entry=entry, offset=offset), exact=True,
                label=f"offset {offset} tA={tA} tB={tB}")
 
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1)])
-def test_integer_ragged_bit_exact(tA, tB):
+def test_integer_ragged_bit_exact(tA, tB, entry):
     M, N, K = 333, 517, 1000
     case = workloads.make_operands(M, N, K, transA=tA, transB=tB, dist="int", seed=4, key=203)
-    check_full(case, run(case, entry=ENTRY), exact=True, label="int ragged")
+    check_full(case, run(case, entry=entry), exact=True, label="int ragged")
 
 
-def test_batched_broadcast_and_layouts():
+def test_batched_broadcast_and_layouts(entry):
     for tA, tB in [(0, 0), (1, 0), (0, 1), (1, 1)]:
         case = workloads.make_operands(70, 90, 33, batch=5, transA=tA, transB=tB,
                                        dist="normal", sigma=0.125, seed=5, key=204)
-        got = run(case, entry=ENTRY + "_strided_batched")
+        got = run(case, entry=entry + "_strided_batched")
         check_full(case, got, label=f"batched tA={tA} tB={tB}")
     # stride 0 on B: every batch multiplies by the same B
     case = workloads.make_operands(40, 50, 60, batch=4, dist="int", seed=6, key=205)
-    got = run(case, entry=ENTRY + "_strided_batched", strideB=0)
+    got = run(case, entry=entry + "_strided_batched", strideB=0)
     for z in range(4):
         ref = oracle.sgemm(case["A"][z], case["B"][0], 40, 50, 60)
         assert np.array_equal(got[z], ref)
@@ -174,6 +180,7 @@ def test_k_zero_writes_zeros():
     M, N = 70, 45
     C = torch.full((M, 48), float("nan"), device="cuda")
     sg.sgemm_f32(M, N, 0, 0, 1, 0, N, C.data_ptr(), 48, 0, 0, 0)
+    sg.sgemm_f32_tf32x3(M, N, 0, 0, 1, 0, N, C.data_ptr(), 48, 0, 0, 0, 0, 0)
     torch.cuda.synchronize()
     out = C.cpu().numpy()
     assert (out[:, :N] == 0).all() and np.isnan(out[:, N:]).all()
@@ -188,35 +195,69 @@ def test_empty_problem_leaves_c_untouched():
     assert (C == 7).all()
 
 
-def test_deterministic_bits():
+def test_deterministic_bits(entry):
     case = workloads.make_operands(300, 200, 500, dist="normal", seed=7, key=206)
-    a = run(case, entry=ENTRY)
-    b = run(case, entry=ENTRY)
+    a = run(case, entry=entry)
+    b = run(case, entry=entry)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
-def test_runs_on_a_side_stream():
+def test_runs_on_a_side_stream(entry):
     import torch
     s = torch.cuda.Stream()
     case = workloads.make_operands(200, 300, 100, dist="int", seed=8, key=207)
     with torch.cuda.stream(s):
-        got = run(case, entry=ENTRY, stream=s.cuda_stream)
+        got = run(case, entry=entry, stream=s.cuda_stream)
     check_full(case, got, exact=True, label="side stream")
 
 
-def test_matmul_convenience_handles_views():
+@pytest.mark.parametrize("precision", ["fp32", "tf32x3"])
+def test_matmul_convenience_handles_views(precision):
     import torch
     torch.manual_seed(0)
     A = torch.randn(300, 200, device="cuda")
     B = torch.randn(150, 200, device="cuda")
-    out = sg.matmul(A, B.t())          # B^T view: passed with transB = 1, no copy
+    out = sg.matmul(A, B.t(), precision=precision)   # B^T view: transB = 1, no copy
     ref, S = oracle.sgemm(A.cpu().numpy(), B.cpu().numpy(), 300, 150, 200, transB=1,
                           with_scale=True)
     assert oracle.within_tolerance(out.cpu().numpy(), ref, S).all()
     Ab = torch.randn(3, 64, 32, device="cuda")
     Bb = torch.randn(3, 32, 48, device="cuda")
-    outb = sg.matmul(Ab, Bb)
+    outb = sg.matmul(Ab, Bb, precision=precision)
     for z in range(3):
         ref, S = oracle.sgemm(Ab[z].cpu().numpy(), Bb[z].cpu().numpy(), 64, 48, 32,
                               with_scale=True)
         assert oracle.within_tolerance(outb[z].cpu().numpy(), ref, S).all()
+
+
+def test_tf32x3_workspace_checked_on_host():
+    import torch
+    M, N, K = 64, 64, 64
+    A = torch.zeros(M, K, device="cuda")
+    B = torch.zeros(K, N, device="cuda")
+    C = torch.zeros(M, N, device="cuda")
+    need = sg.tf32x3_workspace_size(M, N, K, 1)
+    assert need >= 2 * (M + N) * K * 4
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    st = sg.sgemm_f32_tf32x3(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, 0, 0,
+                             ws.data_ptr(), need - 4, 0, check=False)
+    assert st == 8
+    st = sg.sgemm_f32_tf32x3(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, 0, 0,
+                             ws.data_ptr() + 16, need, 0, check=False)
+    assert st == 8
+    st = sg.sgemm_f32_tf32x3(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, 0, 0,
+                             0, need, 0, check=False)
+    assert st == 8
+    assert sg.device_status(reset=True) == 0
+
+
+def test_tf32x3_beats_single_tf32_accuracy():
+    """3xTF32 must land near FP32 FMA accuracy (RRMSE ~1e-6 on the
+    ChetanC28/cuda-kernels page), far below a single TF32 pass (~7.8e-4)."""
+    case = workloads.make_case("sgemm_3072x3072x3072_uniform")
+    got = run(case, entry="sgemm_f32_tf32x3")
+    ref, S = _oracle_full(case)
+    err = oracle.rrmse(got, ref)
+    print(f"tf32x3 RRMSE at 3072^3: {err:.3e}")
+    assert err < 5e-6
+    assert sg.device_status(reset=True) == 0
