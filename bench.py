@@ -37,6 +37,7 @@ import workloads  # noqa: E402
 WORKLOAD = "sgemm_3072x3072x3072_uniform"
 METRIC = "SGEMM TFLOP/s and % of GB300 FP32 peak at 3072³ (1 GPU), vs CPU oracle"
 FP32_LANES_PER_SM = 128          # FP32 FMA units per Blackwell SM
+TF32_PER_BF16 = 1.1 / 2.25       # nominal dense TF32 / BF16 tensor rates of GB300
 SM_MAX_MHZ_DEFAULT = 2070.0
 ROTATING_SETS = 3
 
@@ -51,6 +52,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-tf32x3", action="store_true", help="skip the tensor-core path report")
     return p.parse_args()
 
 
@@ -141,12 +143,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ helpers
 
-def kernel_source_hash() -> str:
-    """Hash of the sources that make up the SIMT kernel; profiles record it so a
-    stale DRAM-traffic figure is never reported for a changed kernel."""
+KERNEL_SOURCES = {
+    "sgemm_simt_kernel": ["device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh", "simt_nn.cu"],
+    "tf32x3_gemm_kernel": ["tc_utils.cuh", "tf32x3.cu"],
+}
+
+
+def kernel_source_hash(kernel: str = "sgemm_simt_kernel") -> str:
+    """Hash of the sources that make up a kernel; profiles record it so a stale
+    DRAM-traffic figure is never reported for a changed kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_matrix_sgemm_gb300", "csrc")
-    for name in ["device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh", "simt_nn.cu"]:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -158,7 +166,7 @@ def profiled_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
@@ -350,6 +358,65 @@ def main():
     h2d = (case["A"].size + case["B"].size) * 4
     d2h = batch * M * ldc * 4
 
+    # the tensor-core 3xTF32 path, reported separately on the same inputs
+    tc = None
+    if not args.no_tf32x3:
+        need = sg.tf32x3_workspace_size(M, N, K, batch)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+        def tc_step(i):
+            dA, dB, dC = sets[i % nsets]
+            if batch == 1:
+                sg.sgemm_f32_tf32x3(M, N, K, dA.data_ptr(), lda, dB.data_ptr(), ldb, dC.data_ptr(),
+                                    ldc, w.transA, w.transB, ws.data_ptr(), need, sp)
+            else:
+                sg.sgemm_f32_tf32x3_strided_batched(
+                    M, N, K, dA.data_ptr(), lda, case["A"][0].size, dB.data_ptr(), ldb,
+                    case["B"][0].size, dC.data_ptr(), ldc, M * ldc, batch, w.transA, w.transB,
+                    ws.data_ptr(), need, sp)
+
+        for i in range(args.warmup):
+            tc_step(i)
+        torch.cuda.synchronize(dev)
+        t0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        t1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            t0[i].record(stream)
+            tc_step(i)
+            t1[i].record(stream)
+        torch.cuda.synchronize(dev)
+        tc_ms = sum(a.elapsed_time(b) for a, b in zip(t0, t1)) / args.steps
+        status = sg.device_status(reset=True)
+        # accuracy of the last result (set (steps-1) % nsets) against the oracle on sampled rows
+        tc_rrmse = None
+        if rank == 0 and batch == 1 and not w.transA:
+            import oracle
+            dC = sets[(args.steps - 1) % nsets][2]
+            rows = np.arange(0, M, max(1, M // 64))
+            got = dC.view(M, ldc)[rows, :N].cpu().numpy()
+            ref = oracle.sgemm(np.ascontiguousarray(case["A"][0][rows]), case["B"][0], len(rows),
+                               N, K, lda=lda, ldb=ldb)
+            tc_rrmse = oracle.rrmse(got, ref)
+        peaks = measured_peaks()
+        bf16 = peaks.get("bf16_tflops")
+        tf32_peak = bf16 * TF32_PER_BF16 if bf16 else 1100.0
+        tc_alg = flops / (tc_ms * 1e-3) / 1e12
+        tc = {
+            "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
+            "kernels": "split (2 launches) + tf32x3_gemm_kernel (128x256 tile, tcgen05 kind::tf32)",
+            "gpu_launches_per_step": 3,
+            "pct_of_fp32_peak_at_max_clock": None,
+            "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_peak,
+                         "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_peak,
+                         "traffic": profiled_traffic("tf32x3_gemm_kernel", args.workload),
+                         "peak_source": ("measured bf16 burst x nominal TF32/BF16 ratio 1.1/2.25"
+                                         if bf16 else "nominal dense TF32"),
+                         "note": "achieved = tensor-pipe work (3 TF32 MMAs per product) / time of "
+                                 "the whole call, split kernels included"},
+            "rrmse_vs_oracle": tc_rrmse,
+            "device_status": status,
+        }
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -405,6 +472,9 @@ def main():
         "gpu_launches": args.steps,
         "wall_s": wall,
     }
+    if tc is not None:
+        tc["pct_of_fp32_peak_at_max_clock"] = 100.0 * tc["value"] / world / peak_max
+        line["tf32x3"] = tc
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     print(json.dumps(line), flush=True)

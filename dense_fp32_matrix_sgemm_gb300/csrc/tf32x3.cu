@@ -13,11 +13,17 @@
 //   corner-turned through a padded shared tile on the way.
 // Stage 2 (GEMM kernel, one 128 x 256 output tile per CTA, 128 threads):
 //   warp 0 / lane 0 issues TMA loads of the four 128-byte-swizzled K slices
-//   (A hi/lo 128 x 32, B hi/lo 256 x 32) into a 2-stage ring; warp 1 owns the
-//   TMEM accumulator (256 columns) and lane 0 issues 3 MMAs (M128 N256 K8)
+//   (A hi/lo 128 x 32, B hi/lo 256 x 32) into a 2-stage ring; warp 1 owns two
+//   TMEM accumulators of 256 columns and lane 0 issues 3 MMAs (M128 N256 K8)
 //   per 8-wide K step, releasing each stage with tcgen05.commit; after the
-//   last commit all four warps read their 32 TMEM lanes (= tile rows) and
-//   store guarded rows of C.  Every mbarrier wait is bounded; a wait that runs
+//   last commit all four warps read their 32 TMEM lanes (= tile rows) of both
+//   accumulators, add them and store guarded rows of C.
+// The tensor cores add each MMA's partial sum into its fp32 accumulator with
+// a rounding that is biased towards zero, so the error of a long K grows with
+// the number of updates.  hi*hi therefore has an accumulator of its own (K/8
+// updates) and the two small terms share the second one, whose values are
+// 2^-10 smaller, so their rounding is negligible; one round-to-nearest add
+// combines the two in the epilogue.  Every mbarrier wait is bounded; a wait that runs
 //   out flags the CTA, the roles drain and the error word is raised.
 #include <cstdint>
 #include <cstdio>
@@ -38,7 +44,8 @@ constexpr int BN = 256;
 constexpr int BK = 32;          // one 128-byte swizzle row of fp32
 constexpr int STAGES = 2;
 constexpr int THREADS = 128;
-constexpr int TMEM_COLS = 256;
+constexpr int ACC_COLS = BN;        // one fp32 accumulator column per output column
+constexpr int TMEM_COLS = 2 * ACC_COLS;   // [hi*hi | lo*hi + hi*lo]
 constexpr int A_TILE_BYTES = BM * BK * 4;   // 16 KB
 constexpr int B_TILE_BYTES = BN * BK * 4;   // 32 KB
 constexpr int STAGE_BYTES = 2 * A_TILE_BYTES + 2 * B_TILE_BYTES;
@@ -208,10 +215,10 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < BK / 8; ++kk) {
                 const uint64_t step = (uint64_t)(kk * 32) >> 4;   // 8 tf32 = 32 bytes along K
-                const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
-                tc::mma_tf32(tmem, alo + step, bhi + step, idesc, first);
-                tc::mma_tf32(tmem, ahi + step, blo + step, idesc, 1u);
-                tc::mma_tf32(tmem, ahi + step, bhi + step, idesc, 1u);
+                const uint32_t acc = (kb == 0 && kk == 0) ? 0u : 1u;
+                tc::mma_tf32(tmem + ACC_COLS, alo + step, bhi + step, idesc, acc);
+                tc::mma_tf32(tmem + ACC_COLS, ahi + step, blo + step, idesc, 1u);
+                tc::mma_tf32(tmem, ahi + step, bhi + step, idesc, acc);
             }
             tc::mma_commit(empty0 + 8 * s);
         }
@@ -228,8 +235,12 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tc::tmem_ld_32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c), v);
+            float v[32], w[32];
+            const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c);
+            tc::tmem_ld_32(ta, v);
+            tc::tmem_ld_32(ta + ACC_COLS, w);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += w[j];
             if (row < p.M) {
                 const int col0 = n0 + 32 * c;
                 if (p.vec_c && col0 + 31 < p.N) {
