@@ -21,7 +21,8 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32", "sgemm_f32_strided_batched",
            "status_string", "last_error", "version", "matmul", "SGEMM_OK",
            "probe_fp32_fma", "probe_out_elems", "sgemm_f32_tf32x3",
-           "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status"]
+           "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status",
+           "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -52,6 +53,9 @@ SIGNATURES = {
                                                 ctypes.c_uint64, _vp]),
     "sgemm_f32_tf32x3_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _i64]),
     "sgemm_device_status": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
+    "sgemm_f32_tf32x3_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int,
+                                        _int, _vp]),
+    "sgemm_f32_tf32x3_noalloc_max_bytes": (ctypes.c_uint64, []),
     "sgemm_probe_fp32_fma": (_int, [_int, _i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_probe_out_elems": (_i64, []),
 }
@@ -154,6 +158,20 @@ def sgemm_f32_tf32x3_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, 
         M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
         batch, transA, transB, workspace or None, workspace_bytes, stream or None)
     return _check(st) if check else st
+
+
+def sgemm_f32_tf32x3_noalloc(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, stream=0, *,
+                             check=True):
+    """3xTF32 product that allocates nothing: its scratch is the library's
+    built-in device array (see include/sgemm_gb300.h for the size limit and
+    the rule that overlapping calls race)."""
+    st = load_library().sgemm_f32_tf32x3_noalloc(M, N, K, A or None, lda, B or None, ldb,
+                                                 C or None, ldc, transA, transB, stream or None)
+    return _check(st) if check else st
+
+
+def tf32x3_noalloc_max_bytes() -> int:
+    return load_library().sgemm_f32_tf32x3_noalloc_max_bytes()
 
 
 def tf32x3_workspace_size(M, N, K, batch=1) -> int:

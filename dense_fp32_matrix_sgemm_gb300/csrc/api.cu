@@ -189,6 +189,10 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
 
 }  // namespace
 
+// Records a failure detail for sgemm_last_error() on behalf of another
+// translation unit and returns `code`.
+int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s) {
     const int64_t total = (int64_t)a.batch * a.M * a.N;
     int blocks = (int)((total + 255) / 256);

@@ -1,0 +1,84 @@
+// sgemm_f32_tf32x3_noalloc: the 3xTF32 tensor-core product with its scratch
+// taken from memory the library reserves for itself, so the call allocates
+// nothing and needs no workspace argument.
+//
+// The scratch is the file-scope array below.  Host code cannot use the
+// array's name as a device address (in host code it names a host-side
+// stand-in), so the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, and handed to the kernels.
+#include <cstdio>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "sgemm_gb300.h"
+
+namespace sgemm {
+
+int record_error(int code, const char *msg);
+
+namespace {
+
+// 64 MiB of device scratch, held by every GPU that loads this library until
+// the process exits.
+constexpr unsigned long long kNoallocScratchBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (looked up on the
+// first call made with that device current).
+int scratch_for_current_device(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return record_error(SGEMM_EDEVICE, "no usable CUDA device for the built-in scratch");
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            char msg[256];
+            snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the built-in scratch failed: %s",
+                     cudaGetErrorString(e));
+            return record_error(SGEMM_EDEVICE, msg);
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return SGEMM_OK;
+}
+
+}  // namespace
+}  // namespace sgemm
+
+extern "C" uint64_t sgemm_f32_tf32x3_noalloc_max_bytes(void) {
+    return sgemm::kNoallocScratchBytes;
+}
+
+extern "C" int sgemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const float *A,
+                                        int64_t lda, const float *B, int64_t ldb, float *C,
+                                        int64_t ldc, int transA, int transB, void *stream) {
+    // Sizes beyond the built-in scratch are rejected before anything runs.
+    const uint64_t need = sgemm_f32_tf32x3_workspace_size(M, N, K, 1);
+    if (need > sgemm::kNoallocScratchBytes) {
+        char msg[256];
+        snprintf(msg, sizeof msg,
+                 "M=%lld N=%lld K=%lld needs %llu bytes of scratch; the built-in scratch of "
+                 "sgemm_f32_tf32x3_noalloc holds %llu bytes (2*(M+N)*round_up(K,4)*4 must fit)",
+                 (long long)M, (long long)N, (long long)K, (unsigned long long)need,
+                 sgemm::kNoallocScratchBytes);
+        return sgemm::record_error(SGEMM_EWORKSPACE, msg);
+    }
+    void *scratch = nullptr;
+    if (need > 0) {
+        const int st = sgemm::scratch_for_current_device(&scratch);
+        if (st != SGEMM_OK) return st;
+    }
+    // The split kernels write every scratch element the GEMM kernel reads, so
+    // nothing has to be cleared between calls.
+    return sgemm_f32_tf32x3(M, N, K, A, lda, B, ldb, C, ldc, transA, transB, scratch,
+                            sgemm::kNoallocScratchBytes, stream);
+}

@@ -137,6 +137,37 @@ int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K,
 uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
 
 /*
+ * sgemm_f32_tf32x3 for callers that cannot allocate device memory: some hosts
+ * own every byte of device memory themselves and forbid allocation inside the
+ * callback that runs the GEMM (plugin and enqueue interfaces of inference
+ * runtimes, for instance), and some latency-critical loops cannot afford
+ * cudaMalloc, which may synchronise the device.  This entry point takes no
+ * workspace and allocates nothing: the split TF32 operands go into a scratch
+ * array of sgemm_f32_tf32x3_noalloc_max_bytes() bytes (64 MiB) that the
+ * library reserves on every GPU that loads it, for the life of the process.
+ * There is no counterpart on the source pages; it exists for these callers.
+ *
+ * Arguments, layout, precision and results as sgemm_f32_tf32x3 (no batch).
+ * Limit: 2 * (M + N) * round_up(K, 4) * 4 bytes (plus 256-byte alignment
+ * padding) must fit in the scratch, e.g. M = N = K = 2048; larger problems
+ * return SGEMM_EWORKSPACE with the sizes in sgemm_last_error().
+ * The first call with a given device current looks up the scratch's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture on that device.  Every call on a device shares the one scratch
+ * array: calls whose kernels can overlap on the GPU (different streams
+ * without ordering between them) race on it and give wrong results.  The
+ * scratch keeps the last call's contents; no call relies on it being zero.
+ */
+int sgemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K,
+                             const float *A, int64_t lda,
+                             const float *B, int64_t ldb,
+                             float *C, int64_t ldc,
+                             int transA, int transB, void *stream);
+
+/* Size in bytes of the built-in scratch of sgemm_f32_tf32x3_noalloc. */
+uint64_t sgemm_f32_tf32x3_noalloc_max_bytes(void);
+
+/*
  * Reads (and with reset != 0 clears) the library's device status word on the
  * current device.  Bit 0 set: a tensor-core kernel gave up on a pipeline wait
  * that exceeded its time limit (about 2 s); that call's C is not valid.

@@ -1,0 +1,66 @@
+"""sgemm_f32_tf32x3_noalloc: the tensor-core product for callers that cannot
+allocate device memory (hosts that own all device memory and forbid
+allocation inside their GEMM callback, or loops that cannot afford cudaMalloc).
+
+It must give what sgemm_f32_tf32x3 with a caller-supplied workspace gives, call
+after call, even though every call reuses the same built-in scratch.  This
+file is collected last on purpose, so a run that stops at the first failure
+has already run every other test.
+"""
+import numpy as np
+import pytest
+
+import dense_fp32_matrix_sgemm_gb300 as sg
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_both(case):
+    import torch
+    M, N, K = case["M"], case["N"], case["K"]
+    A = torch.from_numpy(case["A"][0]).cuda()
+    B = torch.from_numpy(case["B"][0]).cuda()
+    C_ref = torch.full((M, case["ldc"]), float("nan"), device="cuda")
+    C_new = torch.full((M, case["ldc"]), float("nan"), device="cuda")
+    need = sg.tf32x3_workspace_size(M, N, K, 1)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    sg.sgemm_f32_tf32x3(M, N, K, A.data_ptr(), case["lda"], B.data_ptr(), case["ldb"],
+                        C_ref.data_ptr(), case["ldc"], case["transA"], case["transB"],
+                        ws.data_ptr(), need, s)
+    sg.sgemm_f32_tf32x3_noalloc(M, N, K, A.data_ptr(), case["lda"], B.data_ptr(), case["ldb"],
+                                C_new.data_ptr(), case["ldc"], case["transA"], case["transB"], s)
+    torch.cuda.synchronize()
+    return C_ref.cpu().numpy(), C_new.cpu().numpy()
+
+
+def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
+    # two different problems back to back: the second call must not see
+    # anything the first one left in the shared scratch
+    cases = [workloads.make_operands(1000, 600, 700, transA=1, dist="normal", seed=11, key=400),
+             workloads.make_operands(513, 1023, 1024, transB=1, ldc=1028, dist="uniform",
+                                     seed=12, key=401)]
+    for case in cases:
+        M, N, K = case["M"], case["N"], case["K"]
+        ref, new = _run_both(case)
+        _, S = oracle.sgemm(case["A"][0], case["B"][0], M, N, K, transA=case["transA"],
+                            transB=case["transB"], lda=case["lda"], ldb=case["ldb"],
+                            with_scale=True)
+        assert np.isfinite(new[:, :N]).all()
+        ok = oracle.within_tolerance(new[:, :N], ref[:, :N], S)
+        assert ok.all(), f"{int((~ok).sum())} outputs differ beyond the bound"
+        if case["ldc"] > N:
+            assert np.isnan(new[:, N:]).all(), "padding columns of C were written"
+    assert sg.device_status(reset=True) == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    cap = sg.tf32x3_noalloc_max_bytes()
+    assert cap == 64 << 20
+    M = N = K = 4096          # needs 2 * 8192 * 4096 * 4 = 256 MiB
+    assert sg.tf32x3_workspace_size(M, N, K, 1) > cap
+    st = sg.sgemm_f32_tf32x3_noalloc(M, N, K, 16, K, 16, N, 16, N, 0, 0, 0, check=False)
+    assert st == 8
+    assert "built-in scratch" in sg.last_error()
