@@ -152,6 +152,18 @@ def test_unaligned_scalar_path(offset, M, N, K, tA, tB, entry):
                label=f"offset {offset} tA={tA} tB={tB}")
 
 
+@pytest.mark.parametrize("tA", [0, 1])
+def test_wide_tile_ragged_edges(tA, entry):
+    # 576 narrow tiles (4 waves on 152 SMs) against 288 wide ones (2 waves): the
+    # launcher picks the 128 x 256 tile here, with ragged M, N and K tails
+    M, N, K = 3001, 2999, 777
+    lda = (M if tA else K) + 3
+    lda -= lda % 4
+    case = workloads.make_operands(M, N, K, transA=tA, lda=lda + 4, ldb=3000, ldc=3004,
+                                   dist="normal", poison=True, seed=9, key=208)
+    check_full(case, run(case, entry=entry), label=f"wide tile tA={tA}")
+
+
 @pytest.mark.parametrize("tA,tB", [(0, 0), (1, 1)])
 def test_integer_ragged_bit_exact(tA, tB, entry):
     M, N, K = 333, 517, 1000
