@@ -175,6 +175,18 @@ def profiled_traffic(kernel: str, workload: str):
     return None
 
 
+def simt_kernel_label(M, N, batch, transB, sms):
+    """The tile the library's launcher picks (same wave model as
+    csrc/simt_launch.cuh: waves of one CTA per SM, a 128x256 tile costing 1.95
+    128x128 tiles; the wide tile only for row-major B)."""
+    tm = -(-M // 128)
+    narrow = batch * tm * -(-N // 128)
+    wide = batch * tm * -(-N // 256)
+    if not transB and 1.95 * -(-wide // sms) < -(-narrow // sms):
+        return "sgemm_simt_kernel 128x256 tile, BK 32, 2 stages, fma.rn.f32x2"
+    return "sgemm_simt_kernel 128x128 tile, BK 32, 3 stages, fma.rn.f32x2"
+
+
 def cpu_baseline(case, target_s: float):
     """Time the oracle as it stands on a bounded sample of rows of the workload."""
     import oracle
@@ -424,6 +436,7 @@ def main():
 
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
+    sms_for_label = sms
     peaks = measured_peaks()
     sm_max = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or SM_MAX_MHZ_DEFAULT)
     peak_max = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
@@ -448,7 +461,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"{nsets} rotating input sets of {workloads.min_bytes(M, N, K, batch) / 1e6:.0f} MB "
                          f"(> 129 MB L2 together); each step starts with its operands evicted",
-                   "kernel": "simt_fp32_128x128_ffma2"},
+                   "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label)},
         "pct_of_fp32_peak": {
             "at_max_clock": 100.0 * per_gpu / peak_max,
             "peak_tflops_at_max_clock": peak_max,
