@@ -22,7 +22,8 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "status_string", "last_error", "version", "matmul", "SGEMM_OK",
            "probe_fp32_fma", "probe_out_elems", "sgemm_f32_tf32x3",
            "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status",
-           "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes"]
+           "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes", "sgemm_f32_tf32",
+           "sgemm_f32_tf32_strided_batched", "tf32_workspace_size"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -52,6 +53,12 @@ SIGNATURES = {
                                                 _i64, _vp, _i64, _i64, _i64, _int, _int, _vp,
                                                 ctypes.c_uint64, _vp]),
     "sgemm_f32_tf32x3_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _i64]),
+    "sgemm_f32_tf32": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
+                              _vp, ctypes.c_uint64, _vp]),
+    "sgemm_f32_tf32_strided_batched": (_int, [_i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
+                                              _i64, _vp, _i64, _i64, _i64, _int, _int, _vp,
+                                              ctypes.c_uint64, _vp]),
+    "sgemm_f32_tf32_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _i64]),
     "sgemm_device_status": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
     "sgemm_f32_tf32x3_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int,
                                         _int, _vp]),
@@ -174,6 +181,28 @@ def tf32x3_noalloc_max_bytes() -> int:
     return load_library().sgemm_f32_tf32x3_noalloc_max_bytes()
 
 
+def sgemm_f32_tf32(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,
+                   workspace_bytes=0, stream=0, *, check=True):
+    """Plain single-TF32 tensor-core product (reduced precision, see the header)."""
+    st = load_library().sgemm_f32_tf32(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
+                                       transA, transB, workspace or None, workspace_bytes,
+                                       stream or None)
+    return _check(st) if check else st
+
+
+def sgemm_f32_tf32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                                   batch, transA=0, transB=0, workspace=0, workspace_bytes=0,
+                                   stream=0, *, check=True):
+    st = load_library().sgemm_f32_tf32_strided_batched(
+        M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
+        batch, transA, transB, workspace or None, workspace_bytes, stream or None)
+    return _check(st) if check else st
+
+
+def tf32_workspace_size(M, N, K, batch=1) -> int:
+    return load_library().sgemm_f32_tf32_workspace_size(M, N, K, batch)
+
+
 def tf32x3_workspace_size(M, N, K, batch=1) -> int:
     return load_library().sgemm_f32_tf32x3_workspace_size(M, N, K, batch)
 
@@ -219,11 +248,12 @@ def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None):
     without copies.  Runs on ``stream`` (default: torch's current stream).
 
     precision="fp32": CUDA-core FMA (sgemm_f32*); "tf32x3": tensor cores with
-    the three-term TF32 split (sgemm_f32_tf32x3*), using ``workspace`` (a CUDA
-    uint8 tensor) or a fresh one from torch's allocator."""
+    the three-term TF32 split (sgemm_f32_tf32x3*); "tf32": one TF32 product
+    (sgemm_f32_tf32*, reduced precision).  The tensor-core modes use
+    ``workspace`` (a CUDA uint8 tensor) or a fresh one from torch's allocator."""
     import torch
-    if precision not in ("fp32", "tf32x3"):
-        raise ValueError("precision must be 'fp32' or 'tf32x3'")
+    if precision not in ("fp32", "tf32x3", "tf32"):
+        raise ValueError("precision must be 'fp32', 'tf32x3' or 'tf32'")
     if A.dim() != B.dim() or A.dim() not in (2, 3):
         raise ValueError("A and B must both be 2-D or both 3-D")
     M, K, lda, tA = _operand(A, "A")
@@ -242,18 +272,20 @@ def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None):
     ldc = max(out.stride(-2), N, 1)
     s = stream if stream is not None else torch.cuda.current_stream(A.device)
     sp = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
-    if precision == "tf32x3":
-        need = tf32x3_workspace_size(M, N, K, batch)
+    if precision in ("tf32x3", "tf32"):
+        x3 = precision == "tf32x3"
+        need = (tf32x3_workspace_size if x3 else tf32_workspace_size)(M, N, K, batch)
         if workspace is None or workspace.numel() < need:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
         ws, wsb = workspace.data_ptr(), workspace.numel()
         if batched:
-            sgemm_f32_tf32x3_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0),
-                                             B.data_ptr(), ldb, B.stride(0), out.data_ptr(), ldc,
-                                             out.stride(0), batch, tA, tB, ws, wsb, sp)
+            fn = sgemm_f32_tf32x3_strided_batched if x3 else sgemm_f32_tf32_strided_batched
+            fn(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb, B.stride(0),
+               out.data_ptr(), ldc, out.stride(0), batch, tA, tB, ws, wsb, sp)
         else:
-            sgemm_f32_tf32x3(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
-                             tA, tB, ws, wsb, sp)
+            fn = sgemm_f32_tf32x3 if x3 else sgemm_f32_tf32
+            fn(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA, tB, ws,
+               wsb, sp)
     elif batched:
         sgemm_f32_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb,
                                   B.stride(0), out.data_ptr(), ldc, out.stride(0), batch,

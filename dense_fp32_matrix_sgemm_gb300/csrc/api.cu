@@ -152,7 +152,7 @@ bool vector_ok(const GemmArgs &a) {
            a.strideC % 4 == 0;
 }
 
-enum class Path { Simt, Tf32x3 };
+enum class Path { Simt, Tf32x3, Tf32 };
 
 int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
         const float *B, int64_t ldb, int64_t strideB, float *C, int64_t ldc, int64_t strideC,
@@ -164,8 +164,9 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     int st = validate(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, transA,
                       transB, a, nothing);
     if (st != SGEMM_OK || nothing) return st;
-    if (path == Path::Tf32x3 && K > 0) {
-        const uint64_t need = tf32x3_workspace_bytes(M, N, K, batch);
+    if (path != Path::Simt && K > 0) {
+        const uint64_t need = path == Path::Tf32x3 ? tf32x3_workspace_bytes(M, N, K, batch)
+                                                   : tf32_workspace_bytes(M, N, K, batch);
         if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
             return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: need %llu bytes, 256-byte "
                         "aligned", workspace, (unsigned long long)workspace_bytes,
@@ -179,6 +180,8 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
         e = launch_zero_fill(a, s);
     } else if (path == Path::Tf32x3) {
         e = launch_tf32x3(a, transA != 0, transB != 0, workspace, s);
+    } else if (path == Path::Tf32) {
+        e = launch_tf32(a, transA != 0, transB != 0, workspace, s);
     } else {
         e = launch_simt(a, transA != 0, transB != 0, vector_ok(a), s);
     }
@@ -234,6 +237,27 @@ int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K, const floa
                                      uint64_t workspace_bytes, void *stream) {
     return sgemm::run(sgemm::Path::Tf32x3, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
                       strideC, batch, transA, transB, workspace, workspace_bytes, stream);
+}
+
+int sgemm_f32_tf32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                   int64_t ldb, float *C, int64_t ldc, int transA, int transB, void *workspace,
+                   uint64_t workspace_bytes, void *stream) {
+    return sgemm::run(sgemm::Path::Tf32, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA,
+                      transB, workspace, workspace_bytes, stream);
+}
+
+int sgemm_f32_tf32_strided_batched(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                   int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
+                                   float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                   int transA, int transB, void *workspace,
+                                   uint64_t workspace_bytes, void *stream) {
+    return sgemm::run(sgemm::Path::Tf32, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                      strideC, batch, transA, transB, workspace, workspace_bytes, stream);
+}
+
+uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch) {
+    if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+    return sgemm::tf32_workspace_bytes(M, N, K, batch);
 }
 
 uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch) {

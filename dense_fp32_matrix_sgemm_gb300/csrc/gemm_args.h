@@ -30,6 +30,10 @@ cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset);
 
+// Plain single-term TF32 tensor-core product (hi only), same workspace scheme.
+cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s);
+size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
+
 // C[0:M, 0:N] = 0 for every batch (the K == 0 case).
 cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s);
 

@@ -121,17 +121,21 @@ __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, float (&v)[32]) {
 // ---------------------------------------------------------------- MMA
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
-// with 128-byte swizzling: rows of 128 bytes, 8-row swizzle atoms 1024 bytes
-// apart (stride byte offset), tile base 1024-byte aligned.  Advancing along
-// K inside the 128-byte row is done by adding the byte offset / 16 to the
-// start-address field.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
+// with the swizzle that matches its row length: rows of ROW_BYTES (128, 64 or
+// 32 bytes, i.e. 32, 16 or 8 fp32 of K), swizzle atoms of 8 rows, atoms
+// 8 * ROW_BYTES apart (stride byte offset), tile base 1024-byte aligned.
+// Advancing along K inside a row is done by adding the byte offset / 16 to
+// the start-address field.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t smem_addr) {
+    static_assert(ROW_BYTES == 128 || ROW_BYTES == 64 || ROW_BYTES == 32, "unsupported row length");
+    constexpr uint64_t layout = ROW_BYTES == 128 ? 2 : ROW_BYTES == 64 ? 4 : 6;
     uint64_t d = 0;
     d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);   // start address, bits 0-13
     d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: 1024 B
+    d |= (uint64_t)((8 * ROW_BYTES) >> 4) << 32;     // stride byte offset: one 8-row atom
     d |= (uint64_t)1 << 46;                          // descriptor version for sm_100 family
-    d |= (uint64_t)2 << 61;                          // layout: 128-byte swizzle
+    d |= layout << 61;                               // swizzle mode
     return d;
 }
 

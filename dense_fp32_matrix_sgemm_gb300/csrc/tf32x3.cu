@@ -1,4 +1,5 @@
-// FP32 GEMM on the tensor cores with the three-term TF32 split (3xTF32).
+// FP32 GEMM on the tensor cores with the three-term TF32 split (3xTF32), and
+// the plain single-term TF32 product.
 //
 // TF32 keeps 10 explicit mantissa bits, so one TF32 product loses about 750x
 // in accuracy against FP32 FMA (the RRMSE comparison of 1.03e-6 vs 7.78e-4 on
@@ -6,25 +7,29 @@
 // hi = tf32(x) and lo = tf32(x - hi), the product a*b is recovered to about
 // 2^-21 relative by hi_a*hi_b + hi_a*lo_b + lo_a*hi_b (the lo*lo term is
 // below that and dropped), each term a TF32 MMA accumulated in fp32 in TMEM.
+// With TERMS = 1 only hi_a*hi_b is formed: the plain TF32 product.
 //
 // Stage 1 (split kernels): op(A) and op(B) are rewritten into a caller-owned
-//   workspace as K-major planes [batch][hi|lo][rows][Kp] (Kp = K rounded up
-//   to 4 so rows are 16-byte aligned for TMA).  M- or N-major operands are
-//   corner-turned through a padded shared tile on the way.
+//   workspace as K-major planes [batch][TERMS == 3 ? hi|lo : hi][rows][Kp]
+//   (Kp = K rounded up to 4 so rows are 16-byte aligned for TMA).  M- or
+//   N-major operands are corner-turned through a padded shared tile.
 // Stage 2 (GEMM kernel, one 128 x 256 output tile per CTA, 128 threads):
-//   warp 0 / lane 0 issues TMA loads of the four 128-byte-swizzled K slices
-//   (A hi/lo 128 x 32, B hi/lo 256 x 32) into a 2-stage ring; warp 1 owns two
-//   TMEM accumulators of 256 columns and lane 0 issues 3 MMAs (M128 N256 K8)
+//   warp 0 / lane 0 issues TMA loads of the swizzled K slices (BK fp32 of K,
+//   swizzle span = BK * 4 bytes:
+//   A planes 128 rows, B planes 256 rows) into a STAGES-deep ring; warp 1
+//   owns the TMEM accumulators and lane 0 issues TERMS MMAs (M128 N256 K8)
 //   per 8-wide K step, releasing each stage with tcgen05.commit; after the
-//   last commit all four warps read their 32 TMEM lanes (= tile rows) of both
-//   accumulators, add them and store guarded rows of C.
+//   last commit all four warps read their 32 TMEM lanes (= tile rows), add
+//   the accumulators and store guarded rows of C.
 // The tensor cores add each MMA's partial sum into its fp32 accumulator with
 // a rounding that is biased towards zero, so the error of a long K grows with
 // the number of updates.  hi*hi therefore has an accumulator of its own (K/8
 // updates) and the two small terms share the second one, whose values are
 // 2^-10 smaller, so their rounding is negligible; one round-to-nearest add
-// combines the two in the epilogue.  Every mbarrier wait is bounded; a wait that runs
-//   out flags the CTA, the roles drain and the error word is raised.
+// combines the two in the epilogue.
+// Every mbarrier wait is bounded; a wait that runs out flags the CTA, the
+// roles drain (copies in flight land, MMAs complete, TMEM is freed) and the
+// library's device error word is raised.
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -41,41 +46,67 @@ namespace tf32x3 {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 32;          // one 128-byte swizzle row of fp32
-constexpr int STAGES = 2;
 constexpr int THREADS = 128;
-constexpr int ACC_COLS = BN;        // one fp32 accumulator column per output column
-constexpr int TMEM_COLS = 2 * ACC_COLS;   // [hi*hi | lo*hi + hi*lo]
-constexpr int A_TILE_BYTES = BM * BK * 4;   // 16 KB
-constexpr int B_TILE_BYTES = BN * BK * 4;   // 32 KB
-constexpr int STAGE_BYTES = 2 * A_TILE_BYTES + 2 * B_TILE_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int ACC_COLS = BN;   // one fp32 accumulator column per output column
+
+template <int BK_, int STAGES_, int TERMS_>
+struct Config {
+    static constexpr int BK = BK_;             // fp32 of K per stage (one swizzled row)
+    static constexpr int STAGES = STAGES_;
+    static constexpr int TERMS = TERMS_;       // 3: hi/lo split; 1: plain TF32
+    static constexpr int PLANES = TERMS == 3 ? 2 : 1;
+    static constexpr int ROW_BYTES = BK * 4;
+    static constexpr int A_TILE = BM * ROW_BYTES;
+    static constexpr int B_TILE = BN * ROW_BYTES;
+    static constexpr int STAGE_BYTES = PLANES * (A_TILE + B_TILE);
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int TMEM_COLS = TERMS == 3 ? 2 * ACC_COLS : ACC_COLS;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
 
 __device__ unsigned int g_tf32x3_error = 0;   // bit 0: a pipeline wait ran out
 
 // ------------------------------------------------------------------ split
 
-// KCONTIG operand: element (r, k) at X[z*sX + r*ld + k].
+// K-contiguous operand, element (r, k) at X[z*sX + r*ld + k].  One thread per
+// four consecutive k of a row; 16-byte loads where the row allows, 16-byte
+// stores always (rows of the planes are Kp long; the padding gets zeros).
+template <int PLANES>
 __global__ void split_kcontig_kernel(const float *__restrict__ X, int64_t ld, int64_t sX, int R,
-                                     int K, int Kp, int batch, float *__restrict__ ws) {
+                                     int K, int Kp, int batch, int vec, float *__restrict__ ws) {
     const int64_t plane = (int64_t)R * Kp;
-    for (int64_t row = blockIdx.y * (int64_t)blockDim.y + threadIdx.y; row < (int64_t)batch * R;
-         row += (int64_t)gridDim.y * blockDim.y) {
+    const int quads = Kp / 4;
+    const int64_t total = (int64_t)batch * R * quads;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = t / quads;
+        const int k = (int)(t - row * quads) * 4;
         const int64_t z = row / R, r = row - z * R;
-        const float *src = X + z * sX + r * ld;
-        float *hi = ws + (2 * z) * plane + r * Kp;
-        float *lo = hi + plane;
-        for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) {
-            const float x = src[k];
-            const float h = tc::to_tf32(x);
-            hi[k] = h;
-            lo[k] = tc::to_tf32(x - h);
+        const float *src = X + z * sX + r * ld + k;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vec && k + 3 < K) {
+            x = __ldg(reinterpret_cast<const float4 *>(src));
+        } else {
+            if (k + 0 < K) x.x = __ldg(src + 0);
+            if (k + 1 < K) x.y = __ldg(src + 1);
+            if (k + 2 < K) x.z = __ldg(src + 2);
+            if (k + 3 < K) x.w = __ldg(src + 3);
+        }
+        const float4 h = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
+                                     tc::to_tf32(x.w));
+        float *hi = ws + (PLANES * z) * plane + r * Kp + k;
+        *reinterpret_cast<float4 *>(hi) = h;
+        if constexpr (PLANES == 2) {
+            *reinterpret_cast<float4 *>(hi + plane) =
+                make_float4(tc::to_tf32(x.x - h.x), tc::to_tf32(x.y - h.y),
+                            tc::to_tf32(x.z - h.z), tc::to_tf32(x.w - h.w));
         }
     }
 }
 
 // M/N-major operand: element (r, k) at X[z*sX + k*ld + r]; transposed through
 // a 32 x 33 shared tile so both the read and the write are coalesced.
+template <int PLANES>
 __global__ void split_transpose_kernel(const float *__restrict__ X, int64_t ld, int64_t sX, int R,
                                        int K, int Kp, int batch, float *__restrict__ ws) {
     __shared__ float tile[32][33];
@@ -83,8 +114,7 @@ __global__ void split_transpose_kernel(const float *__restrict__ X, int64_t ld, 
     const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
     for (int z = blockIdx.z; z < batch; z += gridDim.z) {
         const float *src = X + (int64_t)z * sX;
-        float *hi = ws + (2 * (int64_t)z) * plane;
-        float *lo = hi + plane;
+        float *hi = ws + (PLANES * (int64_t)z) * plane;
         for (int kt = blockIdx.y; kt * 32 < K; kt += gridDim.y) {
             for (int rt = blockIdx.x; rt * 32 < R; rt += gridDim.x) {
                 const int k0 = kt * 32, r0 = rt * 32;
@@ -101,7 +131,7 @@ __global__ void split_transpose_kernel(const float *__restrict__ X, int64_t ld, 
                         const float x = tile[tx][ty + i];
                         const float h = tc::to_tf32(x);
                         hi[(int64_t)r * Kp + k] = h;
-                        lo[(int64_t)r * Kp + k] = tc::to_tf32(x - h);
+                        if constexpr (PLANES == 2) hi[plane + (int64_t)r * Kp + k] = tc::to_tf32(x - h);
                     }
                 }
                 __syncthreads();
@@ -134,9 +164,12 @@ __device__ __forceinline__ void raster(const Tf32x3Params &p, int &z, int &tm, i
     tn = r / rows;
 }
 
+template <class CFG>
 __global__ void __launch_bounds__(THREADS, 1)
 tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Tf32x3Params p) {
+    constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
+    constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
@@ -167,12 +200,13 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         tc::tma_prefetch_desc(&tmA);
         tc::tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), TMEM_COLS);
+    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), CFG::TMEM_COLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
+    // stage layout: A planes (hi[, lo]) then B planes (hi[, lo])
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
         int issued = 0;
@@ -184,10 +218,12 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             const uint32_t fb = full0 + 8 * s;
             tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
             const int k0 = kb * BK;
-            tc::tma_load_3d(st, &tmA, fb, k0, m0, 2 * z);
-            tc::tma_load_3d(st + A_TILE_BYTES, &tmA, fb, k0, m0, 2 * z + 1);
-            tc::tma_load_3d(st + 2 * A_TILE_BYTES, &tmB, fb, k0, n0, 2 * z);
-            tc::tma_load_3d(st + 2 * A_TILE_BYTES + B_TILE_BYTES, &tmB, fb, k0, n0, 2 * z + 1);
+#pragma unroll
+            for (int pl = 0; pl < PLANES; ++pl) {
+                tc::tma_load_3d(st + pl * A_TILE, &tmA, fb, k0, m0, PLANES * z + pl);
+                tc::tma_load_3d(st + PLANES * A_TILE + pl * B_TILE, &tmB, fb, k0, n0,
+                                PLANES * z + pl);
+            }
             issued = kb + 1;
         }
         if (*abort_flag) {
@@ -208,16 +244,18 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             if (!tc::mbar_wait(full0 + 8 * s, (kb / STAGES) & 1, abort_flag)) break;
             tc::fence_after_sync();
             const uint32_t st = tiles + s * STAGE_BYTES;
-            const uint64_t ahi = tc::sw128_kmajor_desc(st);
-            const uint64_t alo = tc::sw128_kmajor_desc(st + A_TILE_BYTES);
-            const uint64_t bhi = tc::sw128_kmajor_desc(st + 2 * A_TILE_BYTES);
-            const uint64_t blo = tc::sw128_kmajor_desc(st + 2 * A_TILE_BYTES + B_TILE_BYTES);
+            const uint64_t ahi = tc::kmajor_desc<CFG::ROW_BYTES>(st);
+            const uint64_t bhi = tc::kmajor_desc<CFG::ROW_BYTES>(st + PLANES * A_TILE);
 #pragma unroll
             for (int kk = 0; kk < BK / 8; ++kk) {
                 const uint64_t step = (uint64_t)(kk * 32) >> 4;   // 8 tf32 = 32 bytes along K
                 const uint32_t acc = (kb == 0 && kk == 0) ? 0u : 1u;
-                tc::mma_tf32(tmem + ACC_COLS, alo + step, bhi + step, idesc, acc);
-                tc::mma_tf32(tmem + ACC_COLS, ahi + step, blo + step, idesc, 1u);
+                if constexpr (CFG::TERMS == 3) {
+                    const uint64_t alo = tc::kmajor_desc<CFG::ROW_BYTES>(st + A_TILE);
+                    const uint64_t blo = tc::kmajor_desc<CFG::ROW_BYTES>(st + 2 * A_TILE + B_TILE);
+                    tc::mma_tf32(tmem + ACC_COLS, alo + step, bhi + step, idesc, acc);
+                    tc::mma_tf32(tmem + ACC_COLS, ahi + step, blo + step, idesc, 1u);
+                }
                 tc::mma_tf32(tmem, ahi + step, bhi + step, idesc, acc);
             }
             tc::mma_commit(empty0 + 8 * s);
@@ -235,12 +273,15 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-            float v[32], w[32];
+            float v[32];
             const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c);
             tc::tmem_ld_32(ta, v);
-            tc::tmem_ld_32(ta + ACC_COLS, w);
+            if constexpr (CFG::TERMS == 3) {
+                float w[32];
+                tc::tmem_ld_32(ta + ACC_COLS, w);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] += w[j];
+                for (int j = 0; j < 32; ++j) v[j] += w[j];
+            }
             if (row < p.M) {
                 const int col0 = n0 + 32 * c;
                 if (p.vec_c && col0 + 31 < p.N) {
@@ -262,7 +303,7 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, TMEM_COLS);
+        tc::tmem_dealloc(tmem, CFG::TMEM_COLS);
     }
 }
 
@@ -282,53 +323,57 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Planes [2*batch][rows][Kp] of fp32, box 32 (K) x box_rows x 1, 128B swizzle.
+// Planes [planes*batch][rows][Kp] of fp32, box BK (K) x box_rows x 1, with
+// the swizzle whose span equals the BK-float row.
+template <class CFG>
 bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp, int batch,
                     int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)(2 * batch)};
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows,
+                                (cuuint64_t)(CFG::PLANES * batch)};
     const cuuint64_t strides[2] = {(cuuint64_t)Kp * 4, (cuuint64_t)rows * Kp * 4};
-    const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)CFG::BK, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = CFG::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : CFG::ROW_BYTES == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                         : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-}  // namespace tf32x3
-
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
+size_t plane_bytes(int64_t rows, int64_t K, int64_t batch, int planes) {
     const size_t Kp = (size_t)((K + 3) / 4 * 4);
-    const size_t a = tf32x3::align_up(2 * (size_t)batch * (size_t)M * Kp * 4, 256);
-    const size_t b = tf32x3::align_up(2 * (size_t)batch * (size_t)N * Kp * 4, 256);
-    return a + b;
+    return align_up((size_t)planes * (size_t)batch * (size_t)rows * Kp * 4, 256);
 }
 
-cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
-                          cudaStream_t s) {
-    using namespace tf32x3;
+template <class CFG>
+cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+    constexpr int PLANES = CFG::PLANES;
     const int Kp = (a.K + 3) / 4 * 4;
     float *wsA = static_cast<float *>(ws);
-    float *wsB = wsA + tf32x3::align_up(2 * (size_t)a.batch * a.M * Kp * 4, 256) / 4;
+    float *wsB = wsA + plane_bytes(a.M, a.K, a.batch, PLANES) / 4;
 
-    // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major hi/lo planes
+    // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes
     auto split = [&](const float *X, int64_t ld, int64_t sX, int R, bool kcontig, float *out) {
         if (kcontig) {
-            dim3 block(32, 8);
-            const int64_t rows = (int64_t)a.batch * R;
-            dim3 grid((unsigned)((a.K + 31) / 32 < 64 ? (a.K + 31) / 32 : 64),
-                      (unsigned)((rows + 7) / 8 < 65535 ? (rows + 7) / 8 : 65535));
-            split_kcontig_kernel<<<grid, block, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch, out);
+            const int vec = (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 && sX % 4 == 0;
+            const int64_t total = (int64_t)a.batch * R * (Kp / 4);
+            const int64_t want = (total + 255) / 256;
+            const int blocks = (int)(want < 152 * 32 ? want : 152 * 32);
+            split_kcontig_kernel<PLANES><<<blocks, 256, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch,
+                                                                vec, out);
         } else {
             dim3 block(32, 8);
             dim3 grid((unsigned)((R + 31) / 32 < 65535 ? (R + 31) / 32 : 65535),
                       (unsigned)((a.K + 31) / 32 < 65535 ? (a.K + 31) / 32 : 65535),
                       (unsigned)(a.batch < 65535 ? a.batch : 65535));
-            split_transpose_kernel<<<grid, block, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch, out);
+            split_transpose_kernel<PLANES><<<grid, block, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch,
+                                                                  out);
         }
     };
     split(a.A, a.lda, a.strideA, a.M, !transA, wsA);
@@ -338,14 +383,15 @@ cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
 
     // stage 2: the tensor-core GEMM
     CUtensorMap tmA, tmB;
-    if (!make_plane_map(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
-        !make_plane_map(&tmB, wsB, a.N, a.K, Kp, a.batch, BN))
+    if (!make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
+        !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, BN))
         return cudaErrorInvalidValue;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tf32x3_gemm_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(tf32x3_gemm_kernel<CFG>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        CFG::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     Tf32x3Params p;
@@ -360,8 +406,33 @@ cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
     p.group_m = 8;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && a.ldc % 4 == 0 && a.strideC % 4 == 0;
     const long long blocks = (long long)a.batch * p.tiles_m * p.tiles_n;
-    tf32x3_gemm_kernel<<<(unsigned)blocks, THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+    tf32x3_gemm_kernel<CFG><<<(unsigned)blocks, THREADS, CFG::SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();
+}
+
+}  // namespace tf32x3
+
+// Tuned configurations (K slice, stages, terms), both 192 KB of ring.  The
+// pipeline is latency-bound, so what counts is the bytes in flight: 3 of 4
+// stages of 48 KB for the split product (64-byte swizzle) beat 1 of 2 stages
+// of 96 KB by 13-16 %; the single-term product takes 32-float slices.
+using Tf32x3Cfg = tf32x3::Config<16, 4, 3>;
+using Tf32Cfg = tf32x3::Config<32, 4, 1>;
+
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
+    return tf32x3::plane_bytes(M, K, batch, 2) + tf32x3::plane_bytes(N, K, batch, 2);
+}
+
+size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
+    return tf32x3::plane_bytes(M, K, batch, 1) + tf32x3::plane_bytes(N, K, batch, 1);
+}
+
+cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+    return tf32x3::launch<Tf32x3Cfg>(a, transA, transB, ws, s);
+}
+
+cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+    return tf32x3::launch<Tf32Cfg>(a, transA, transB, ws, s);
 }
 
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset) {

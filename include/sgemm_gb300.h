@@ -137,6 +137,39 @@ int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K,
 uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
 
 /*
+ * C = op(A) op(B) as ONE TF32 product per term: inputs rounded to TF32
+ * (10 explicit mantissa bits, round to nearest), products summed in fp32 on
+ * the tensor cores.  The fast, reduced-precision mode: each product carries a
+ * relative error up to about 2^-10, so results are NOT held to the FP32
+ * bound of the other entry points; the tests hold them to
+ * |C - C_ref| <= 2e-3 * sum_k |a||b| + 1e-6 and report the RRMSE.  Inputs
+ * that are exact in TF32 (e.g. small integers) give exact results.
+ * Defined by: the TF32 tensor-core stage of the ChetanC28/cuda-kernels page
+ * (19.12 TFLOP/s and RRMSE 7.78e-4 against 1.03e-6 for FMA on an RTX 4000
+ * Ada), re-built on tcgen05.
+ * Arguments as sgemm_f32_tf32x3; workspace of
+ * sgemm_f32_tf32_workspace_size(M, N, K, batch) bytes (half of the split
+ * product's).
+ */
+int sgemm_f32_tf32(int64_t M, int64_t N, int64_t K,
+                   const float *A, int64_t lda,
+                   const float *B, int64_t ldb,
+                   float *C, int64_t ldc,
+                   int transA, int transB,
+                   void *workspace, uint64_t workspace_bytes, void *stream);
+
+int sgemm_f32_tf32_strided_batched(int64_t M, int64_t N, int64_t K,
+                                   const float *A, int64_t lda, int64_t strideA,
+                                   const float *B, int64_t ldb, int64_t strideB,
+                                   float *C, int64_t ldc, int64_t strideC,
+                                   int64_t batch, int transA, int transB,
+                                   void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* Workspace bytes of the sgemm_f32_tf32 entry points: batch * (M + N) *
+ * round_up(K, 4) floats plus padding.  0 for empty problems. */
+uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
+
+/*
  * sgemm_f32_tf32x3 for callers that cannot allocate device memory: some hosts
  * own every byte of device memory themselves and forbid allocation inside the
  * callback that runs the GEMM (plugin and enqueue interfaces of inference

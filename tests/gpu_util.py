@@ -40,8 +40,9 @@ def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     fn = getattr(sg, entry)
     extra = ()
-    if "tf32x3" in entry:
-        need = sg.tf32x3_workspace_size(M, N, K, batch)
+    if "tf32" in entry:
+        size = sg.tf32x3_workspace_size if "tf32x3" in entry else sg.tf32_workspace_size
+        need = size(M, N, K, batch)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
         extra = (ws.data_ptr(), need)
     if entry.endswith("strided_batched"):

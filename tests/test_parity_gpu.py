@@ -225,6 +225,7 @@ def test_runs_on_a_side_stream(entry):
 
 @pytest.mark.parametrize("precision", ["fp32", "tf32x3"])
 def test_matmul_convenience_handles_views(precision):
+    """(the plain TF32 mode is checked on its own bound below)"""
     import torch
     torch.manual_seed(0)
     A = torch.randn(300, 200, device="cuda")
@@ -278,4 +279,52 @@ def test_tf32x3_beats_single_tf32_accuracy():
     bias = float(np.mean((got.astype(np.float64) - ref) * np.sign(ref)))
     print(f"tf32x3 RRMSE at 3072^3: {err:.3e}, mean signed error {bias:.3e}")
     assert err < 1e-5
+    assert sg.device_status(reset=True) == 0
+
+
+# ---------------------------------------------------------------- plain TF32 mode
+
+TF32_REL = 2e-3   # one TF32 rounding (2^-11) on each factor of every product, plus margin
+
+
+def _check_tf32(case, got, label):
+    ref, S = _oracle_full(case)
+    assert np.isfinite(got).all(), label
+    ok = oracle.within_tolerance(got, ref, S, rel=TF32_REL)
+    assert ok.all(), f"{label}: {int((~ok).sum())} outputs outside the TF32 bound"
+    return oracle.rrmse(got, ref)
+
+
+@pytest.mark.parametrize("name", ["sgemm_256x256x256_uniform", "sgemm_3072x3072x3072_uniform",
+                                  "sgemm_2049x3071x1537_tA_normal"])
+def test_tf32_plain_within_tf32_bound(name):
+    case = workloads.make_case(name)
+    err = _check_tf32(case, run(case, entry="sgemm_f32_tf32"), name)
+    print(f"sgemm_f32_tf32 {name}: RRMSE {err:.3e}")
+    # a real TF32 product: far above FP32 FMA (1e-6), at most the page's 7.78e-4 scale
+    assert 1e-5 < err < 1.5e-3
+
+
+@pytest.mark.parametrize("name", ["sgemm_256x256x256_int", "sgemm_2049x3071x1537_tA_int"])
+def test_tf32_plain_exact_on_small_integers(name):
+    case = workloads.make_case(name)
+    got = run(case, entry="sgemm_f32_tf32")
+    ref, _ = _oracle_full(case)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 257, 33), (300, 200, 77)])
+def test_tf32_plain_edges(M, N, K, tA, tB):
+    lda = ((M if tA else K) + 4) // 4 * 4
+    ldb = ((K if tB else N) + 4) // 4 * 4
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=N + 3,
+                                   dist="normal", poison=True, seed=21, key=209)
+    _check_tf32(case, run(case, entry="sgemm_f32_tf32"), f"tf32 {M}x{N}x{K} tA={tA} tB={tB}")
+
+
+def test_tf32_plain_batched_qkT():
+    case = workloads.make_case("sgemm_batched96_512x512x64_qkT_normal")
+    err = _check_tf32(case, run(case, entry="sgemm_f32_tf32_strided_batched"), "tf32 batched")
+    print(f"sgemm_f32_tf32 batched qkT: RRMSE {err:.3e}")
     assert sg.device_status(reset=True) == 0
