@@ -429,6 +429,42 @@ def main():
             "device_status": status,
         }
 
+    # split-K on the pages' one-tile case (128 x 128 x 32768): plain vs split
+    sk = None
+    if not args.no_tf32x3 and rank == 0:
+        sm_, sn_, sk_ = 128, 128, 32768
+        gA = torch.rand(sm_, sk_, device=dev) * 2 - 1
+        gB = torch.rand(sk_, sn_, device=dev) * 2 - 1
+        gC = torch.empty(sm_, sn_, device=dev)
+        splits = sg.splitk_auto_splits(sm_, sn_, sk_)
+        need_sk = sg.splitk_workspace_size(sm_, sn_, sk_, splits)
+        wsk = torch.empty(max(need_sk, 1), dtype=torch.uint8, device=dev)
+
+        def plain():
+            sg.sgemm_f32(sm_, sn_, sk_, gA.data_ptr(), sk_, gB.data_ptr(), sn_, gC.data_ptr(), sn_,
+                         0, 0, sp)
+
+        def split():
+            sg.sgemm_f32_splitk(sm_, sn_, sk_, gA.data_ptr(), sk_, gB.data_ptr(), sn_,
+                                gC.data_ptr(), sn_, 0, 0, splits, wsk.data_ptr(), need_sk, sp)
+
+        def timed(fn, reps=10):
+            for _ in range(2):
+                fn()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(reps):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            return a0.elapsed_time(a1) / reps
+
+        t_plain, t_split = timed(plain), timed(split)
+        fl = 2.0 * sm_ * sn_ * sk_
+        sk = {"shape": [sm_, sn_, sk_], "splits": splits, "plain_ms": t_plain,
+              "splitk_ms": t_split, "speedup": t_plain / t_split,
+              "splitk_tflops": fl / (t_split * 1e-3) / 1e12}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -488,6 +524,8 @@ def main():
     if tc is not None:
         tc["pct_of_fp32_peak_at_max_clock"] = 100.0 * tc["value"] / world / peak_max
         line["tf32x3"] = tc
+    if sk is not None:
+        line["splitk_one_tile"] = sk
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     print(json.dumps(line), flush=True)

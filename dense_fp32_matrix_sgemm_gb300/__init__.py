@@ -23,7 +23,8 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "probe_fp32_fma", "probe_out_elems", "sgemm_f32_tf32x3",
            "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status",
            "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes", "sgemm_f32_tf32",
-           "sgemm_f32_tf32_strided_batched", "tf32_workspace_size"]
+           "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
+           "splitk_auto_splits", "splitk_workspace_size"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -47,6 +48,10 @@ SIGNATURES = {
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_last_error": (ctypes.c_char_p, []),
     "sgemm_version": (_int, []),
+    "sgemm_f32_splitk": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
+                                _int, _vp, ctypes.c_uint64, _vp]),
+    "sgemm_f32_splitk_auto_splits": (_int, [_i64, _i64, _i64]),
+    "sgemm_f32_splitk_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _int]),
     "sgemm_f32_tf32x3": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
                                 _vp, ctypes.c_uint64, _vp]),
     "sgemm_f32_tf32x3_strided_batched": (_int, [_i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
@@ -145,6 +150,23 @@ def sgemm_f32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
         M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
         batch, transA, transB, stream or None)
     return _check(st) if check else st
+
+
+def sgemm_f32_splitk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, splits=0, workspace=0,
+                     workspace_bytes=0, stream=0, *, check=True):
+    """sgemm_f32 with K split into chunks summed in a fixed order (deterministic)."""
+    st = load_library().sgemm_f32_splitk(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
+                                         transA, transB, splits, workspace or None,
+                                         workspace_bytes, stream or None)
+    return _check(st) if check else st
+
+
+def splitk_auto_splits(M, N, K) -> int:
+    return load_library().sgemm_f32_splitk_auto_splits(M, N, K)
+
+
+def splitk_workspace_size(M, N, K, splits=0) -> int:
+    return load_library().sgemm_f32_splitk_workspace_size(M, N, K, splits)
 
 
 def sgemm_f32_tf32x3(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,

@@ -141,6 +141,7 @@ int validate(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64
     a.tiles_m = (int)tiles_m;
     a.tiles_n = (int)tiles_n;
     a.group_m = 8;
+    a.kchunk = 0;
     return SGEMM_OK;
 }
 
@@ -192,9 +193,51 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
 
 }  // namespace
 
+int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+               int64_t ldb, float *C, int64_t ldc, int transA, int transB, int splits,
+               void *workspace, uint64_t workspace_bytes, void *stream);
+
 // Records a failure detail for sgemm_last_error() on behalf of another
 // translation unit and returns `code`.
 int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+               int64_t ldb, float *C, int64_t ldc, int transA, int transB, int splits,
+               void *workspace, uint64_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    if (splits < 0 || splits > 4096)
+        return fail(SGEMM_EINVAL_DIM, "splits=%d: must be 0 (automatic) or 1..4096", splits);
+    GemmArgs a;
+    bool nothing = false;
+    int st = validate(M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA, transB, a, nothing);
+    if (st != SGEMM_OK || nothing) return st;
+    if (K > 0 && splits == 0) splits = splitk_auto_splits(M, N, K);
+    // the number of K-chunks actually used (chunks are whole 32-wide slices)
+    const int64_t chunk = K > 0 ? ((K + splits - 1) / splits + 31) / 32 * 32 : 0;
+    const int used = K > 0 ? (int)((K + chunk - 1) / chunk) : 1;
+    if (K > 0 && used > 1) {
+        const uint64_t need = splitk_workspace_bytes(M, N, K, splits);
+        if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+            return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: split-K needs %llu bytes, "
+                        "256-byte aligned", workspace, (unsigned long long)workspace_bytes,
+                        (unsigned long long)need);
+    }
+    st = check_device();
+    if (st != SGEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0)
+        e = launch_zero_fill(a, s);
+    else if (used <= 1)
+        e = launch_simt(a, transA != 0, transB != 0, vector_ok(a), s);
+    else {
+        const bool vec = aligned(A, 16) && aligned(B, 16) && lda % 4 == 0 && ldb % 4 == 0;
+        e = launch_simt_splitk(a, transA != 0, transB != 0, vec, splits, workspace, s);
+    }
+    if (e != cudaSuccess)
+        return fail(SGEMM_ELAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
+    return SGEMM_OK;
+}
 
 cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s) {
     const int64_t total = (int64_t)a.batch * a.M * a.N;
@@ -253,6 +296,24 @@ int sgemm_f32_tf32_strided_batched(int64_t M, int64_t N, int64_t K, const float 
                                    uint64_t workspace_bytes, void *stream) {
     return sgemm::run(sgemm::Path::Tf32, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
                       strideC, batch, transA, transB, workspace, workspace_bytes, stream);
+}
+
+int sgemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                     int64_t ldb, float *C, int64_t ldc, int transA, int transB, int splits,
+                     void *workspace, uint64_t workspace_bytes, void *stream) {
+    return sgemm::run_splitk(M, N, K, A, lda, B, ldb, C, ldc, transA, transB, splits, workspace,
+                             workspace_bytes, stream);
+}
+
+int sgemm_f32_splitk_auto_splits(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return 1;
+    return sgemm::splitk_auto_splits(M, N, K);
+}
+
+uint64_t sgemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits) {
+    if (M <= 0 || N <= 0 || K <= 0 || splits < 0) return 0;
+    if (splits == 0) splits = sgemm_f32_splitk_auto_splits(M, N, K);
+    return sgemm::splitk_workspace_bytes(M, N, K, splits);
 }
 
 uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch) {

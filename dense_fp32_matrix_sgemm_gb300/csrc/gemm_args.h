@@ -19,6 +19,8 @@ struct GemmArgs {
     int batch;
     int tiles_m, tiles_n;   // output tiles per problem (each launcher sets its own)
     int group_m;            // tile rows per raster group (L2 reuse)
+    int kchunk;             // split-K: > 0 means problem z covers k in [z*kchunk, (z+1)*kchunk)
+                            // (A/B strides step by one chunk, C by one partial plane)
 };
 
 // SIMT FP32 kernel family (CUDA cores).  vec: every base pointer, leading
@@ -33,6 +35,13 @@ cudaError_t tf32x3_read_error(unsigned int *flags, bool reset);
 // Plain single-term TF32 tensor-core product (hi only), same workspace scheme.
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s);
 size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
+
+// Split-K on the SIMT kernel: `splits` K-chunks into partial planes in `ws`,
+// then a fixed-order sum into C.  batch must be 1.
+cudaError_t launch_simt_splitk(const GemmArgs &a, bool transA, bool transB, bool vec, int splits,
+                               void *ws, cudaStream_t s);
+size_t splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
+int splitk_auto_splits(int64_t M, int64_t N, int64_t K);
 
 // C[0:M, 0:N] = 0 for every batch (the K == 0 case).
 cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s);

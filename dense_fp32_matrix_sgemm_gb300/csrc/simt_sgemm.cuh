@@ -224,6 +224,8 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     int z, tm, tn;
     raster(p, z, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN_;
+    // split-K: problem z is the K-chunk [z*kchunk, min(K, (z+1)*kchunk))
+    const int Kz = p.kchunk > 0 ? min(p.kchunk, p.K - z * p.kchunk) : p.K;
 
     // A is contiguous along K unless stored transposed; B the other way round.
     using ALoader = typename std::conditional<AK, KMajorATileLoader<BK>,
@@ -233,13 +235,13 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     la.ld = p.lda;
     la.mn0 = m0;
     la.mn_ext = p.M;
-    la.K = p.K;
+    la.K = Kz;
     TileLoader<BK, BN_, TB, VEC> lb;
     lb.base = p.B + (int64_t)z * p.strideB;
     lb.ld = p.ldb;
     lb.mn0 = n0;
     lb.mn_ext = p.N;
-    lb.K = p.K;
+    lb.K = Kz;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-    const int ktiles = (p.K + BK - 1) / BK;
+    const int ktiles = (Kz + BK - 1) / BK;
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {

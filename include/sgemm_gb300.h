@@ -97,6 +97,43 @@ int sgemm_f32_strided_batched(int64_t M, int64_t N, int64_t K,
                               int64_t batch, int transA, int transB, void *stream);
 
 /*
+ * sgemm_f32 with K split into `splits` chunks for problems whose output tiles
+ * cannot fill the GPU (e.g. 256 x 256 x 256 is four 128 x 128 tiles, and
+ * 128 x 128 x 32768 is one).  Each chunk computes a partial product into the
+ * workspace; one more pass sums the partials in chunk order into C, so the
+ * result is deterministic (not bit-identical to sgemm_f32: the sum is grouped
+ * differently), meets the same FP32 bound, and is exact on small integers.
+ * Defined by: the split-K stage of the ChetanC28/cuda-kernels page
+ * ("splitting the K dimension across blocks for small problems", 28.87x on a
+ * 128 x 128 x 32768 product), each chunk as in sgemm_f32.
+ *   splits     0: choose automatically (sgemm_f32_splitk_auto_splits), else
+ *              1..4096; chunks are whole multiples of 32 in K, so fewer
+ *              chunks than asked may be used.  One chunk = plain sgemm_f32
+ *              (no workspace needed).
+ *   workspace  caller-owned device memory of at least
+ *              sgemm_f32_splitk_workspace_size(M, N, K, splits) bytes,
+ *              256-byte aligned, not overlapping A, B or C, not used by other
+ *              work while this call runs on `stream`.  SGEMM_EWORKSPACE if
+ *              missing or too small.
+ * Not batched.  Arguments otherwise as sgemm_f32.
+ */
+int sgemm_f32_splitk(int64_t M, int64_t N, int64_t K,
+                     const float *A, int64_t lda,
+                     const float *B, int64_t ldb,
+                     float *C, int64_t ldc,
+                     int transA, int transB, int splits,
+                     void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* Number of K chunks chosen for splits = 0: enough 128 x 128 tiles to put one
+ * CTA on every SM of the current device, each chunk at least 256 deep, at
+ * most 64; 1 when the tiles already fill the device. */
+int sgemm_f32_splitk_auto_splits(int64_t M, int64_t N, int64_t K);
+
+/* Workspace bytes for sgemm_f32_splitk (splits = 0: the automatic choice):
+ * chunks * M * round_up(N, 4) floats plus padding; 0 when one chunk is used. */
+uint64_t sgemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits);
+
+/*
  * C = op(A) op(B) on the tensor cores with FP32 accuracy: every input is split
  * as x = hi + lo with hi = tf32(x), lo = tf32(x - hi), and the product is
  * formed as lo_a*hi_b + hi_a*lo_b + hi_a*hi_b (three TF32 MMAs per K step,

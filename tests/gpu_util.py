@@ -20,7 +20,7 @@ def _upload(arr: np.ndarray, offset: int):
 
 
 def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
-        stream=None) -> np.ndarray:
+        stream=None, splits: int = 0) -> np.ndarray:
     """Run the case on the GPU; returns C (batch, M, N).
 
     ``offset`` shifts every buffer by that many floats (4-byte aligned only when
@@ -40,6 +40,10 @@ def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     fn = getattr(sg, entry)
     extra = ()
+    if entry == "sgemm_f32_splitk":
+        need = sg.splitk_workspace_size(M, N, K, splits)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        extra = (splits, ws.data_ptr(), need)
     if "tf32" in entry:
         size = sg.tf32x3_workspace_size if "tf32x3" in entry else sg.tf32_workspace_size
         need = size(M, N, K, batch)

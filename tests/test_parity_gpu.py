@@ -328,3 +328,54 @@ def test_tf32_plain_batched_qkT():
     err = _check_tf32(case, run(case, entry="sgemm_f32_tf32_strided_batched"), "tf32 batched")
     print(f"sgemm_f32_tf32 batched qkT: RRMSE {err:.3e}")
     assert sg.device_status(reset=True) == 0
+
+
+# ---------------------------------------------------------------- split-K
+
+@pytest.mark.parametrize("M,N,K,splits", [(128, 128, 32768, 0), (256, 256, 256, 0),
+                                          (256, 256, 256, 3), (100, 70, 5000, 7),
+                                          (129, 255, 1000, 0), (64, 64, 31, 4)])
+def test_splitk_parity(M, N, K, splits):
+    case = workloads.make_operands(M, N, K, dist="uniform", seed=30, key=210)
+    got = run(case, entry="sgemm_f32_splitk", splits=splits)
+    err = check_full(case, got, label=f"splitk {M}x{N}x{K} splits={splits}")
+    print(f"splitk {M}x{N}x{K} splits={splits} (auto {sg.splitk_auto_splits(M, N, K)}): RRMSE {err:.3e}")
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_splitk_layouts_integer_exact(tA, tB):
+    M, N, K = 150, 90, 3000
+    lda = ((M if tA else K) + 4) // 4 * 4
+    ldb = ((K if tB else N) + 4) // 4 * 4
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=N + 2,
+                                   dist="int", poison=True, seed=31, key=211)
+    got = run(case, entry="sgemm_f32_splitk", splits=5)
+    check_full(case, got, exact=True, label=f"splitk int tA={tA} tB={tB}")
+
+
+def test_splitk_unaligned_and_deterministic():
+    M, N, K = 77, 133, 2048
+    case = workloads.make_operands(M, N, K, lda=K + 1, ldb=N + 1, ldc=N + 1, dist="normal",
+                                   poison=True, seed=32, key=212)
+    a = run(case, entry="sgemm_f32_splitk", offset=1, splits=8)
+    b = run(case, entry="sgemm_f32_splitk", offset=1, splits=8)
+    check_full(case, a, label="splitk unaligned")
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_splitk_workspace_and_auto_choice():
+    import torch
+    assert sg.splitk_auto_splits(128, 128, 32768) > 1      # one tile: split to fill the GPU
+    assert sg.splitk_auto_splits(8192, 8192, 4096) == 1    # thousands of tiles: no split
+    assert sg.splitk_workspace_size(8192, 8192, 4096, 0) == 0
+    need = sg.splitk_workspace_size(128, 128, 32768, 0)
+    assert need > 0
+    A = torch.zeros(128, 32768, device="cuda")
+    B = torch.zeros(32768, 128, device="cuda")
+    C = torch.zeros(128, 128, device="cuda")
+    st = sg.sgemm_f32_splitk(128, 128, 32768, A.data_ptr(), 32768, B.data_ptr(), 128,
+                             C.data_ptr(), 128, 0, 0, 0, 0, 0, 0, check=False)
+    assert st == 8
+    st = sg.sgemm_f32_splitk(128, 128, 32768, A.data_ptr(), 32768, B.data_ptr(), 128,
+                             C.data_ptr(), 128, 0, 0, -1, 0, 0, 0, check=False)
+    assert st == 1
