@@ -63,6 +63,23 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tflops(flops_per_step: float, steps: int, max_total_ms: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas: every rank ran `steps` steps of
+    `flops_per_step`, the job took as long as the slowest rank."""
+    return world * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -333,13 +350,9 @@ def main():
             dist.barrier()
     clocks = clk.summary()
     durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms
-    total_ms = sum(durs)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_over_ranks(sum(durs), dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = weak_scaling_tflops(flops, args.steps, total_ms, world)
 
     # end to end through the C ABI from pinned host buffers: H2D A and B,
     # the GEMM, D2H C, every step on one stream
