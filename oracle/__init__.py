@@ -65,6 +65,9 @@ def load(path: str = LIB, *, rebuild: bool = False):
     lib.oracle_sgemm_entries.restype = _int
     lib.oracle_sgemm_entries.argtypes = [_i64, _i64, _i64, _fp, _i64, _int, _fp, _i64, _int,
                                          _i64, _lp, _lp, _fp, _dp]
+    lib.oracle_sgemm_ex.restype = _int
+    lib.oracle_sgemm_ex.argtypes = [_i64, _i64, _i64, ctypes.c_double, _fp, _i64, _int, _fp, _i64,
+                                    _int, ctypes.c_double, _fp, _i64, _fp, _fp, _i64, _dp, _i64]
     if path == LIB:
         _lib = lib
     return lib
@@ -153,6 +156,36 @@ def sgemm_entries(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, rows, co
     if st:
         raise RuntimeError(f"oracle_sgemm_entries failed with status {st}")
     return out, sab
+
+
+def sgemm_ex(A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, *, alpha: float = 1.0,
+             beta: float = 0.0, C_in: Optional[np.ndarray] = None, bias: Optional[np.ndarray] = None,
+             transA: int = 0, transB: int = 0, lda: Optional[int] = None,
+             ldb: Optional[int] = None, lib=None):
+    """C = alpha op(A) op(B) + beta C_in + bias (bias per column), formed in fp64
+    and rounded once; returns (C, S) with the tolerance scale S.  One dot
+    product per output (single thread): for small and medium problems."""
+    lib = lib or load()
+    A = _f32(np.ascontiguousarray(A))
+    B = _f32(np.ascontiguousarray(B))
+    lda = lda if lda is not None else (M if transA else K)
+    ldb = ldb if ldb is not None else (K if transB else N)
+    if beta != 0.0:
+        C_in = _f32(np.ascontiguousarray(C_in))
+        ldc_in = C_in.shape[-1]
+    else:
+        ldc_in = N
+    if bias is not None:
+        bias = _f32(np.ascontiguousarray(bias))
+    C = np.zeros((M, N), dtype=np.float32)
+    S = np.zeros((M, N), dtype=np.float64)
+    st = lib.oracle_sgemm_ex(M, N, K, alpha, _ptr(A, _fp), lda, transA, _ptr(B, _fp), ldb, transB,
+                             beta, _ptr(C_in, _fp) if beta != 0.0 else None, ldc_in,
+                             _ptr(bias, _fp) if bias is not None else None,
+                             _ptr(C, _fp), N, _ptr(S, _dp), N)
+    if st:
+        raise RuntimeError(f"oracle_sgemm_ex failed with status {st}")
+    return C, S
 
 
 # Acceptance bound for fp32 results against the oracle, elementwise:

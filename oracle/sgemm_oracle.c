@@ -173,3 +173,51 @@ int oracle_sgemm_entries(int64_t M, int64_t N, int64_t K,
     }
     return 0;
 }
+
+/* The general form: C_out = alpha * op(A) op(B) + beta * C_in + bias (bias
+ * broadcast along rows, one value per output column).  Everything is formed
+ * in fp64 (the product sum in ascending k as above) and rounded once to fp32.
+ * beta == 0 means C_in is not read (it may hold anything); bias may be NULL.
+ * S (nullable) receives the tolerance scale
+ * |alpha| * sum_k |a||b| + |beta| * |C_in| + |bias|.
+ * This is the fully connected layer Y = XW + b that "CUDA GEMM operator
+ * performance optimization" section 1.2 names, with the BLAS-style scaling. */
+int oracle_sgemm_ex(int64_t M, int64_t N, int64_t K, double alpha,
+                    const float *A, int64_t lda, int transA,
+                    const float *B, int64_t ldb, int transB,
+                    double beta, const float *C_in, int64_t ldc_in,
+                    const float *bias, float *C_out, int64_t ldc_out,
+                    double *S, int64_t lds) {
+    if (M < 0 || N < 0 || K < 0) return 2;
+    if (M == 0 || N == 0) return 0;
+    /* one dot product per output, in ascending k, kept in fp64 until the end */
+    oracle_job j;
+    memset(&j, 0, sizeof j);
+    j.M = M; j.N = N; j.K = K;
+    j.A = A; j.lda = lda; j.transA = transA;
+    j.B = B; j.ldb = ldb; j.transB = transB;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t c = 0; c < N; ++c) {
+            double acc = 0.0, s = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = op_a(&j, i, k), b = op_b(&j, k, c);
+                acc += a * b;
+                s += fabs(a) * fabs(b);
+            }
+            double v = alpha * acc;
+            double scale = fabs(alpha) * s;
+            if (beta != 0.0) {
+                const double cin = (double)C_in[i * ldc_in + c];
+                v += beta * cin;
+                scale += fabs(beta) * fabs(cin);
+            }
+            if (bias) {
+                v += (double)bias[c];
+                scale += fabs((double)bias[c]);
+            }
+            C_out[i * ldc_out + c] = (float)v;
+            if (S) S[i * lds + c] = scale;
+        }
+    }
+    return 0;
+}

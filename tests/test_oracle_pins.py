@@ -228,9 +228,79 @@ def pin_degenerate(lib):
     assert oracle.sgemm(A, B, 0, 4, 1, lib=lib).shape == (0, 4)
 
 
+def pin_ex_reduces_to_plain(lib):
+    """alpha = 1, beta = 0, no bias is the plain product bit for bit; alpha = -1
+    negates it exactly."""
+    M, N, K = 23, 17, 91
+    for tA, tB in [(0, 0), (1, 1)]:
+        c = workloads.make_operands(M, N, K, transA=tA, transB=tB, dist="normal", seed=16,
+                                    key=109)
+        plain = oracle.sgemm(c["A"], c["B"], M, N, K, transA=tA, transB=tB, lib=lib)
+        ex, _ = oracle.sgemm_ex(c["A"], c["B"], M, N, K, transA=tA, transB=tB, lib=lib)
+        assert np.array_equal(ex, plain)
+        neg, _ = oracle.sgemm_ex(c["A"], c["B"], M, N, K, alpha=-1.0, transA=tA, transB=tB,
+                                 lib=lib)
+        assert np.array_equal(neg, -plain)
+
+
+def pin_ex_integer_closed_form(lib):
+    """Integer inputs and integer alpha, beta: alpha*(A@B) + beta*C_in + bias is
+    exact, against int64 arithmetic."""
+    M, N, K = 31, 29, 57
+    c = workloads.make_operands(M, N, K, dist="int", seed=17, key=110)
+    a, b = ops(c)
+    rng = np.random.default_rng(18)
+    C_in = rng.integers(-50, 51, size=(M, N)).astype(np.float32)
+    bias = rng.integers(-9, 10, size=N).astype(np.float32)
+    for alpha, beta, use_bias in [(3.0, -2.0, True), (0.0, 1.0, True), (-1.0, 0.0, False),
+                                  (2.0, 5.0, False), (0.0, 0.0, True)]:
+        got, S = oracle.sgemm_ex(c["A"], c["B"], M, N, K, alpha=alpha, beta=beta, C_in=C_in,
+                                 bias=bias if use_bias else None, lib=lib)
+        want = (int(alpha) * (a.astype(np.int64) @ b.astype(np.int64))
+                + int(beta) * C_in.astype(np.int64)
+                + (bias.astype(np.int64) if use_bias else 0))
+        assert np.array_equal(got, want.astype(np.float32)), (alpha, beta, use_bias)
+        scale = (abs(alpha) * (np.abs(a).astype(np.int64) @ np.abs(b).astype(np.int64))
+                 + abs(beta) * np.abs(C_in) + (np.abs(bias) if use_bias else 0))
+        assert np.array_equal(S, scale.astype(np.float64)), (alpha, beta, use_bias)
+
+
+def pin_ex_beta_zero_ignores_c_in(lib):
+    """beta = 0 never reads C_in: NaN there cannot reach the result."""
+    M, N, K = 8, 9, 10
+    c = workloads.make_operands(M, N, K, dist="normal", seed=19, key=111)
+    nan_c = np.full((M, N), np.nan, np.float32)
+    got, _ = oracle.sgemm_ex(c["A"], c["B"], M, N, K, alpha=0.5, beta=0.0, C_in=nan_c,
+                             bias=np.ones(N, np.float32), lib=lib)
+    assert np.isfinite(got).all()
+
+
+def pin_ex_rational_bruteforce(lib):
+    """Non-dyadic alpha and beta on tiny inputs: the exact rational value,
+    correctly rounded."""
+    M, N, K = 3, 4, 5
+    c = workloads.make_operands(M, N, K, dist="uniform", seed=20, key=112)
+    a, b = ops(c)
+    rng = np.random.default_rng(21)
+    C_in = rng.standard_normal((M, N)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32)
+    alpha, beta = 0.7, -1.3
+    got, _ = oracle.sgemm_ex(c["A"], c["B"], M, N, K, alpha=alpha, beta=beta, C_in=C_in,
+                             bias=bias, lib=lib)
+    for i in range(M):
+        for j in range(N):
+            dot = sum((Fraction(float(a[i, k])) * Fraction(float(b[k, j])) for k in range(K)),
+                      Fraction(0))
+            q = Fraction(alpha) * dot + Fraction(beta) * Fraction(float(C_in[i, j])) + \
+                Fraction(float(bias[j]))
+            assert got[i, j] == f32_round(q), (i, j)
+
+
 PINS = [pin_rational_bruteforce, pin_hand_2x2_3x3, pin_identity, pin_all_ones,
         pin_unit_selector, pin_integer_exact, pin_numpy_float64, pin_transpose_storage,
-        pin_scale_pm1, pin_batched_slices, pin_entries, pin_degenerate]
+        pin_scale_pm1, pin_batched_slices, pin_entries, pin_degenerate,
+        pin_ex_reduces_to_plain, pin_ex_integer_closed_form, pin_ex_beta_zero_ignores_c_in,
+        pin_ex_rational_bruteforce]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -259,6 +329,9 @@ MUTANTS = {
                            "for (int64_t k = 1; k < K; ++k) {\n            const double a = op_a(&j, i, k), b"),
     "row_offset_in_store": ("j->C[i * j->ldc + c] = (float)acc[c];",
                             "j->C[i * j->ldc + (c + 1) % N] = (float)acc[c];"),
+    "ex_drops_bias": ("v += (double)bias[c];", "v += 0.0 * (double)bias[c];"),
+    "ex_beta_scales_product": ("v += beta * cin;", "v += beta * acc;"),
+    "ex_alpha_ignored": ("double v = alpha * acc;", "double v = acc;"),
 }
 
 
