@@ -24,7 +24,8 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status",
            "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes", "sgemm_f32_tf32",
            "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
-           "splitk_auto_splits", "splitk_workspace_size"]
+           "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex",
+           "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -48,6 +49,14 @@ SIGNATURES = {
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_last_error": (ctypes.c_char_p, []),
     "sgemm_version": (_int, []),
+    "sgemm_f32_ex": (_int, [_i64, _i64, _i64, ctypes.c_float, _vp, _i64, _vp, _i64,
+                            ctypes.c_float, _vp, _i64, _vp, _int, _int, _vp]),
+    "sgemm_f32_ex_strided_batched": (_int, [_i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64,
+                                            _vp, _i64, _i64, ctypes.c_float, _vp, _i64, _i64,
+                                            _vp, _i64, _int, _int, _vp]),
+    "sgemm_f32_tf32x3_ex": (_int, [_i64, _i64, _i64, ctypes.c_float, _vp, _i64, _vp, _i64,
+                                   ctypes.c_float, _vp, _i64, _vp, _int, _int, _vp,
+                                   ctypes.c_uint64, _vp]),
     "sgemm_f32_splitk": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
                                 _int, _vp, ctypes.c_uint64, _vp]),
     "sgemm_f32_splitk_auto_splits": (_int, [_i64, _i64, _i64]),
@@ -149,6 +158,31 @@ def sgemm_f32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
     st = load_library().sgemm_f32_strided_batched(
         M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
         batch, transA, transB, stream or None)
+    return _check(st) if check else st
+
+
+def sgemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=0, transA=0, transB=0,
+                 stream=0, *, check=True):
+    """C = alpha op(A) op(B) + beta C + bias (bias: device pointer to N floats or 0)."""
+    st = load_library().sgemm_f32_ex(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                     C or None, ldc, bias or None, transA, transB, stream or None)
+    return _check(st) if check else st
+
+
+def sgemm_f32_ex_strided_batched(M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                                 strideC, bias, batch, transA=0, transB=0, stream=0, *,
+                                 check=True):
+    st = load_library().sgemm_f32_ex_strided_batched(
+        M, N, K, alpha, A or None, lda, strideA, B or None, ldb, strideB, beta, C or None, ldc,
+        strideC, bias or None, batch, transA, transB, stream or None)
+    return _check(st) if check else st
+
+
+def sgemm_f32_tf32x3_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=0, transA=0, transB=0,
+                        workspace=0, workspace_bytes=0, stream=0, *, check=True):
+    st = load_library().sgemm_f32_tf32x3_ex(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
+                                            C or None, ldc, bias or None, transA, transB,
+                                            workspace or None, workspace_bytes, stream or None)
     return _check(st) if check else st
 
 

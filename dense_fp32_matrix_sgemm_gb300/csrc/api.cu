@@ -27,14 +27,18 @@ cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, c
 
 namespace {
 
-__global__ void zero_fill_kernel(float *C, int64_t ldc, int64_t strideC, int M, int N, int batch) {
+__global__ void epilogue_only_kernel(float *C, int64_t ldc, int64_t strideC, int M, int N,
+                                     int batch, float beta, const float *bias) {
     const int64_t total = (int64_t)batch * M * N;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
         const int64_t z = t / ((int64_t)M * N);
         const int64_t r = t - z * (int64_t)M * N;
         const int64_t i = r / N, j = r - i * N;
-        C[z * strideC + i * ldc + j] = 0.f;
+        float *c = C + z * strideC + i * ldc + j;
+        float v = beta != 0.f ? beta * *c : 0.f;
+        if (bias) v += bias[j];
+        *c = v;
     }
 }
 
@@ -142,6 +146,9 @@ int validate(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64
     a.tiles_n = (int)tiles_n;
     a.group_m = 8;
     a.kchunk = 0;
+    a.alpha = 1.f;
+    a.beta = 0.f;
+    a.bias = nullptr;
     return SGEMM_OK;
 }
 
@@ -155,16 +162,27 @@ bool vector_ok(const GemmArgs &a) {
 
 enum class Path { Simt, Tf32x3, Tf32 };
 
+struct Epi {
+    float alpha = 1.f, beta = 0.f;
+    const float *bias = nullptr;
+};
+
 int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
         const float *B, int64_t ldb, int64_t strideB, float *C, int64_t ldc, int64_t strideC,
         int64_t batch, int transA, int transB, void *workspace, uint64_t workspace_bytes,
-        void *stream) {
+        void *stream, const Epi &epi = Epi()) {
     g_last_error[0] = '\0';
     GemmArgs a;
     bool nothing = false;
     int st = validate(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, transA,
                       transB, a, nothing);
     if (st != SGEMM_OK || nothing) return st;
+    if (epi.bias != nullptr && !aligned(epi.bias, 4))
+        return fail(SGEMM_EINVAL_PTR, "bias is not 4-byte aligned");
+    a.alpha = epi.alpha;
+    a.beta = epi.beta;
+    a.bias = epi.bias;
+    if (a.alpha == 0.f) K = 0;   // the product term vanishes: A and B are not read
     if (path != Path::Simt && K > 0) {
         const uint64_t need = path == Path::Tf32x3 ? tf32x3_workspace_bytes(M, N, K, batch)
                                                    : tf32_workspace_bytes(M, N, K, batch);
@@ -178,7 +196,7 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (K == 0) {
-        e = launch_zero_fill(a, s);
+        e = launch_epilogue_only(a, s);
     } else if (path == Path::Tf32x3) {
         e = launch_tf32x3(a, transA != 0, transB != 0, workspace, s);
     } else if (path == Path::Tf32) {
@@ -227,7 +245,7 @@ int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (K == 0)
-        e = launch_zero_fill(a, s);
+        e = launch_epilogue_only(a, s);
     else if (used <= 1)
         e = launch_simt(a, transA != 0, transB != 0, vector_ok(a), s);
     else {
@@ -239,12 +257,13 @@ int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, con
     return SGEMM_OK;
 }
 
-cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s) {
+cudaError_t launch_epilogue_only(const GemmArgs &a, cudaStream_t s) {
     const int64_t total = (int64_t)a.batch * a.M * a.N;
     int blocks = (int)((total + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    zero_fill_kernel<<<blocks, 256, 0, s>>>(a.C, a.ldc, a.strideC, a.M, a.N, a.batch);
+    epilogue_only_kernel<<<blocks, 256, 0, s>>>(a.C, a.ldc, a.strideC, a.M, a.N, a.batch, a.beta,
+                                                a.bias);
     return cudaGetLastError();
 }
 
@@ -296,6 +315,42 @@ int sgemm_f32_tf32_strided_batched(int64_t M, int64_t N, int64_t K, const float 
                                    uint64_t workspace_bytes, void *stream) {
     return sgemm::run(sgemm::Path::Tf32, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
                       strideC, batch, transA, transB, workspace, workspace_bytes, stream);
+}
+
+int sgemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                 const float *B, int64_t ldb, float beta, float *C, int64_t ldc, const float *bias,
+                 int transA, int transB, void *stream) {
+    sgemm::Epi e;
+    e.alpha = alpha;
+    e.beta = beta;
+    e.bias = bias;
+    return sgemm::run(sgemm::Path::Simt, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA,
+                      transB, nullptr, 0, stream, e);
+}
+
+int sgemm_f32_ex_strided_batched(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                 int64_t lda, int64_t strideA, const float *B, int64_t ldb,
+                                 int64_t strideB, float beta, float *C, int64_t ldc,
+                                 int64_t strideC, const float *bias, int64_t batch, int transA,
+                                 int transB, void *stream) {
+    sgemm::Epi e;
+    e.alpha = alpha;
+    e.beta = beta;
+    e.bias = bias;
+    return sgemm::run(sgemm::Path::Simt, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc,
+                      strideC, batch, transA, transB, nullptr, 0, stream, e);
+}
+
+int sgemm_f32_tf32x3_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                        const float *bias, int transA, int transB, void *workspace,
+                        uint64_t workspace_bytes, void *stream) {
+    sgemm::Epi e;
+    e.alpha = alpha;
+    e.beta = beta;
+    e.bias = bias;
+    return sgemm::run(sgemm::Path::Tf32x3, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA,
+                      transB, workspace, workspace_bytes, stream, e);
 }
 
 int sgemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,

@@ -21,7 +21,16 @@ struct GemmArgs {
     int group_m;            // tile rows per raster group (L2 reuse)
     int kchunk;             // split-K: > 0 means problem z covers k in [z*kchunk, (z+1)*kchunk)
                             // (A/B strides step by one chunk, C by one partial plane)
+    // epilogue: C = alpha * op(A) op(B) + beta * C + bias[col]; beta == 0 never
+    // reads C, bias may be null.  alpha = 1, beta = 0, bias = null is the plain
+    // product and stores the accumulators unchanged.
+    float alpha, beta;
+    const float *bias;
 };
+
+__host__ __device__ inline bool plain_epilogue(const GemmArgs &a) {
+    return a.alpha == 1.f && a.beta == 0.f && a.bias == nullptr;
+}
 
 // SIMT FP32 kernel family (CUDA cores).  vec: every base pointer, leading
 // dimension and batch stride allows 16-byte accesses.
@@ -43,8 +52,9 @@ cudaError_t launch_simt_splitk(const GemmArgs &a, bool transA, bool transB, bool
 size_t splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 int splitk_auto_splits(int64_t M, int64_t N, int64_t K);
 
-// C[0:M, 0:N] = 0 for every batch (the K == 0 case).
-cudaError_t launch_zero_fill(const GemmArgs &a, cudaStream_t s);
+// C[0:M, 0:N] = beta * C + bias for every batch: the whole result when the
+// product term vanishes (K == 0 or alpha == 0); zeros for the plain epilogue.
+cudaError_t launch_epilogue_only(const GemmArgs &a, cudaStream_t s);
 
 // Smallest block tile of any kernel: bounds the grid size during validation.
 constexpr int kSimtTileM = 128;

@@ -201,6 +201,47 @@ __device__ __forceinline__ void raster(const GemmArgs &p, int &z, int &tm, int &
     tn = r / rows;
 }
 
+// Stores four consecutive outputs of a row, applying the epilogue
+// C = alpha * acc + beta * C + bias[col] unless it is the plain one.  Columns
+// at or past N are neither read nor written; 16-byte accesses when `vec`
+// allows and the four columns are all in range.
+__device__ __forceinline__ void store_c4(const GemmArgs &p, float *crow, int col, float4 v,
+                                         bool vec, bool plain) {
+    const bool full = vec && col + 3 < p.N;
+    if (!plain) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.beta != 0.f) {
+            if (full) {
+                o = *reinterpret_cast<const float4 *>(crow + col);
+            } else {
+                if (col + 0 < p.N) o.x = crow[col + 0];
+                if (col + 1 < p.N) o.y = crow[col + 1];
+                if (col + 2 < p.N) o.z = crow[col + 2];
+                if (col + 3 < p.N) o.w = crow[col + 3];
+            }
+        }
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.bias != nullptr) {
+            if (col + 0 < p.N) b.x = p.bias[col + 0];
+            if (col + 1 < p.N) b.y = p.bias[col + 1];
+            if (col + 2 < p.N) b.z = p.bias[col + 2];
+            if (col + 3 < p.N) b.w = p.bias[col + 3];
+        }
+        v.x = fmaf(p.beta, o.x, p.alpha * v.x) + b.x;
+        v.y = fmaf(p.beta, o.y, p.alpha * v.y) + b.y;
+        v.z = fmaf(p.beta, o.z, p.alpha * v.z) + b.z;
+        v.w = fmaf(p.beta, o.w, p.alpha * v.w) + b.w;
+    }
+    if (full) {
+        *reinterpret_cast<float4 *>(crow + col) = v;
+    } else {
+        if (col + 0 < p.N) crow[col + 0] = v.x;
+        if (col + 1 < p.N) crow[col + 1] = v.y;
+        if (col + 2 < p.N) crow[col + 2] = v.z;
+        if (col + 3 < p.N) crow[col + 3] = v.w;
+    }
+}
+
 // Block tile 128 x BN_ (BN_ = 128 or 256); each thread owns an 8 x (BN_/16)
 // register tile made of 4 x 4 sub-blocks spaced 64 rows / 64 columns apart.
 // AK (K-contiguous A only, 16-byte access): A stays in its own [128][BK]
@@ -353,6 +394,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     cp_async_wait<0>();
 
     float *Cz = p.C + (int64_t)z * p.strideC;
+    const bool plain = plain_epilogue(p);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = m0 + (i < 4 ? a_col + i : 64 + a_col + (i - 4));
@@ -363,14 +405,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
             const int col = n0 + h * 64 + b_col;
             const float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
                                          acc[i][4 * h + 3]);
-            if (VEC && col + 3 < p.N) {
-                *reinterpret_cast<float4 *>(crow + col) = v;
-            } else {
-                if (col + 0 < p.N) crow[col + 0] = v.x;
-                if (col + 1 < p.N) crow[col + 1] = v.y;
-                if (col + 2 < p.N) crow[col + 2] = v.z;
-                if (col + 3 < p.N) crow[col + 3] = v.w;
-            }
+            store_c4(p, crow, col, v, VEC, plain);
         }
     }
 }

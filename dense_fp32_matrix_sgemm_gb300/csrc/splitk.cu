@@ -45,7 +45,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ P, int S, int M, 
             acc.w += v.w;
         }
         float *c = C + i * ldc + j;
-        if (vec && j + 3 < N) {
+        const bool full = vec && j + 3 < N;
+        if (full) {
             *reinterpret_cast<float4 *>(c) = acc;
         } else {
             if (j + 0 < N) c[0] = acc.x;

@@ -148,6 +148,8 @@ struct Tf32x3Params {
     int M, N, K;
     int tiles_m, tiles_n, group_m;
     int vec_c;   // C rows allow 16-byte stores
+    float alpha, beta;      // epilogue C = alpha * acc + beta * C + bias[col]
+    const float *bias;
 };
 
 __device__ __forceinline__ void raster(const Tf32x3Params &p, int &z, int &tm, int &tn) {
@@ -284,6 +286,15 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             }
             if (row < p.M) {
                 const int col0 = n0 + 32 * c;
+                if (!(p.alpha == 1.f && p.beta == 0.f && p.bias == nullptr)) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = col0 + j;
+                        const float old = (p.beta != 0.f && col < p.N) ? crow[col] : 0.f;
+                        const float b = (p.bias != nullptr && col < p.N) ? p.bias[col] : 0.f;
+                        v[j] = fmaf(p.beta, old, p.alpha * v[j]) + b;
+                    }
+                }
                 if (p.vec_c && col0 + 31 < p.N) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
@@ -405,6 +416,9 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     p.tiles_n = (a.N + BN - 1) / BN;
     p.group_m = 8;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && a.ldc % 4 == 0 && a.strideC % 4 == 0;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.bias = a.bias;
     const long long blocks = (long long)a.batch * p.tiles_m * p.tiles_n;
     tf32x3_gemm_kernel<CFG><<<(unsigned)blocks, THREADS, CFG::SMEM_BYTES, s>>>(tmA, tmB, p);
     return cudaGetLastError();

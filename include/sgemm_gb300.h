@@ -97,6 +97,33 @@ int sgemm_f32_strided_batched(int64_t M, int64_t N, int64_t K,
                               int64_t batch, int transA, int transB, void *stream);
 
 /*
+ * C = alpha * op(A) op(B) + beta * C + bias, fp32 on the CUDA cores: the
+ * fully connected layer Y = XW + b ("CUDA GEMM operator performance
+ * optimization", section 1.2) with BLAS-style scaling, fused into the store
+ * of sgemm_f32's kernel (each output: alpha * acc, then fma with beta * C,
+ * then + bias[j], fp32).
+ *   bias   NULL, or a device array of N floats added to every row.
+ *   beta   0 means C is not read (it may hold anything, NaN included).
+ *   alpha  0 means A and B are not read; C = beta * C + bias.
+ * Results meet |C - C_ref| <= 1e-5 * (|alpha| sum_k |a||b| + |beta||C| +
+ * |bias|) + 1e-6 against the same expression formed exactly.
+ * Arguments otherwise as sgemm_f32.
+ */
+int sgemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                 const float *A, int64_t lda,
+                 const float *B, int64_t ldb,
+                 float beta, float *C, int64_t ldc,
+                 const float *bias, int transA, int transB, void *stream);
+
+/* Strided-batched form of sgemm_f32_ex; the same bias row for every batch. */
+int sgemm_f32_ex_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                 const float *A, int64_t lda, int64_t strideA,
+                                 const float *B, int64_t ldb, int64_t strideB,
+                                 float beta, float *C, int64_t ldc, int64_t strideC,
+                                 const float *bias, int64_t batch, int transA, int transB,
+                                 void *stream);
+
+/*
  * sgemm_f32 with K split into `splits` chunks for problems whose output tiles
  * cannot fill the GPU (e.g. 256 x 256 x 256 is four 128 x 128 tiles, and
  * 128 x 128 x 32768 is one).  Each chunk computes a partial product into the
@@ -158,6 +185,14 @@ int sgemm_f32_tf32x3(int64_t M, int64_t N, int64_t K,
                      float *C, int64_t ldc,
                      int transA, int transB,
                      void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* sgemm_f32_tf32x3 with the epilogue of sgemm_f32_ex (alpha, beta, bias). */
+int sgemm_f32_tf32x3_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda,
+                        const float *B, int64_t ldb,
+                        float beta, float *C, int64_t ldc,
+                        const float *bias, int transA, int transB,
+                        void *workspace, uint64_t workspace_bytes, void *stream);
 
 /* Strided-batched form of sgemm_f32_tf32x3 (arguments as
  * sgemm_f32_strided_batched plus the workspace, sized for `batch`). */

@@ -335,9 +335,25 @@ MUTANTS = {
 }
 
 
+def run_pins_against(lib_path: str) -> list:
+    """Names of the pins that fail against the oracle library at lib_path."""
+    lib = oracle.load(lib_path)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except (AssertionError, RuntimeError):
+            caught.append(pin.__name__)
+    return caught
+
+
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="gcc not available")
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_planted_mistakes_are_caught(name):
+    # Each mutant runs in a child process: an index mistake can read outside
+    # the input buffers, and a crash of the child also counts as caught.
+    import subprocess
+    import sys
     src = open(oracle.SRC).read()
     old, new = MUTANTS[name]
     assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
@@ -347,16 +363,14 @@ def test_planted_mistakes_are_caught(name):
             f.write(src.replace(old, new))
         so = os.path.join(d, f"mut_{name}.so")
         oracle.compile_oracle(path, so)
-        lib = oracle.load(so)
-        caught = []
-        for pin in PINS:
-            try:
-                pin(lib)
-            except AssertionError:
-                caught.append(pin.__name__)
-            except RuntimeError:
-                caught.append(pin.__name__)
-        assert caught, f"no pin catches the planted mistake {name}"
+        code = ("import sys; sys.path[:0] = [%r, %r]; import test_oracle_pins as t; "
+                "c = t.run_pins_against(%r); print(c); sys.exit(0 if c else 3)"
+                % (os.path.dirname(os.path.dirname(__file__)), os.path.dirname(__file__), so))
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                           timeout=300)
+        assert r.returncode != 3, f"no pin catches the planted mistake {name}: {r.stdout}"
+        # 0: some pin failed; < 0: the mutant crashed the child (caught too)
+        assert r.returncode == 0 or r.returncode < 0, f"mutant runner failed: {r.stderr[-2000:]}"
 
 
 # --------------------------------------------------------------------------

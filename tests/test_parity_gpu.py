@@ -379,3 +379,89 @@ def test_splitk_workspace_and_auto_choice():
     st = sg.sgemm_f32_splitk(128, 128, 32768, A.data_ptr(), 32768, B.data_ptr(), 128,
                              C.data_ptr(), 128, 0, 0, -1, 0, 0, 0, check=False)
     assert st == 1
+
+
+# ---------------------------------------------------------------- alpha, beta, bias epilogue
+
+def _run_ex(case, alpha, beta, C_in, bias, entry):
+    import torch
+    M, N, K = case["M"], case["N"], case["K"]
+    ldc = case["ldc"]
+    A = torch.from_numpy(case["A"][0]).cuda()
+    B = torch.from_numpy(case["B"][0]).cuda()
+    Cbuf = torch.full((M, ldc), float("nan"), device="cuda")
+    if C_in is not None:
+        Cbuf[:, :N] = torch.from_numpy(C_in).cuda()
+    bias_t = torch.from_numpy(bias).cuda() if bias is not None else None
+    bp = bias_t.data_ptr() if bias_t is not None else 0
+    s = torch.cuda.current_stream().cuda_stream
+    if entry == "sgemm_f32_ex":
+        sg.sgemm_f32_ex(M, N, K, alpha, A.data_ptr(), case["lda"], B.data_ptr(), case["ldb"], beta,
+                        Cbuf.data_ptr(), ldc, bp, case["transA"], case["transB"], s)
+    else:
+        need = sg.tf32x3_workspace_size(M, N, K, 1)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        sg.sgemm_f32_tf32x3_ex(M, N, K, alpha, A.data_ptr(), case["lda"], B.data_ptr(),
+                               case["ldb"], beta, Cbuf.data_ptr(), ldc, bp, case["transA"],
+                               case["transB"], ws.data_ptr(), need, s)
+    torch.cuda.synchronize()
+    out = Cbuf.cpu().numpy()
+    assert np.isnan(out[:, N:]).all()
+    return out[:, :N]
+
+
+@pytest.mark.parametrize("ex_entry", ["sgemm_f32_ex", "sgemm_f32_tf32x3_ex"])
+@pytest.mark.parametrize("alpha,beta,with_bias", [(0.7, -1.3, True), (1.0, 0.0, True),
+                                                  (-2.0, 0.5, False), (0.0, 2.0, True),
+                                                  (1.0, 0.0, False)])
+def test_epilogue_alpha_beta_bias(ex_entry, alpha, beta, with_bias):
+    M, N, K = 300, 270, 333
+    case = workloads.make_operands(M, N, K, transA=1, ldc=N + 2, dist="normal", seed=40, key=213)
+    rng = np.random.default_rng(41)
+    C_in = rng.standard_normal((M, N)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32) if with_bias else None
+    got = _run_ex(case, alpha, beta, C_in if beta != 0.0 else None, bias, ex_entry)
+    ref, S = oracle.sgemm_ex(case["A"][0], case["B"][0], M, N, K, alpha=alpha, beta=beta,
+                             C_in=C_in, bias=bias, transA=1, lda=case["lda"])
+    ok = oracle.within_tolerance(got, ref, S)
+    assert ok.all(), f"{int((~ok).sum())} outputs outside the bound"
+
+
+def test_epilogue_integer_exact_and_batched():
+    import torch
+    M, N, K, batch = 64, 96, 50, 3
+    case = workloads.make_operands(M, N, K, batch=batch, dist="int", seed=42, key=214)
+    rng = np.random.default_rng(43)
+    C_in = rng.integers(-20, 21, size=(batch, M, N)).astype(np.float32)
+    bias = rng.integers(-5, 6, size=N).astype(np.float32)
+    A = torch.from_numpy(case["A"]).cuda()
+    B = torch.from_numpy(case["B"]).cuda()
+    C = torch.from_numpy(C_in.copy()).cuda()
+    bt = torch.from_numpy(bias).cuda()
+    sg.sgemm_f32_ex_strided_batched(M, N, K, 3.0, A.data_ptr(), K, M * K, B.data_ptr(), N, K * N,
+                                    -2.0, C.data_ptr(), N, M * N, bt.data_ptr(), batch, 0, 0,
+                                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy()
+    for z in range(batch):
+        want = (3 * (case["opA"][z].astype(np.int64) @ case["opB"][z].astype(np.int64))
+                - 2 * C_in[z].astype(np.int64) + bias.astype(np.int64))
+        assert np.array_equal(got[z], want.astype(np.float32))
+
+
+def test_epilogue_k_zero_and_alpha_zero():
+    import torch
+    M, N = 40, 30
+    C = torch.full((M, N), 2.0, device="cuda")
+    bias = torch.arange(N, dtype=torch.float32, device="cuda")
+    A = torch.full((M, 8), float("nan"), device="cuda")
+    B = torch.full((8, N), float("nan"), device="cuda")
+    # alpha = 0: A and B (NaN here) are not read
+    sg.sgemm_f32_ex(M, N, 8, 0.0, A.data_ptr(), 8, B.data_ptr(), N, 3.0, C.data_ptr(), N,
+                    bias.data_ptr(), 0, 0, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(C, 6.0 + bias.expand(M, N))
+    # K = 0: the empty product, C = beta * C + bias
+    sg.sgemm_f32_ex(M, N, 0, 1.0, 0, 1, 0, N, 0.5, C.data_ptr(), N, bias.data_ptr(), 0, 0, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(C, 3.0 + 1.5 * bias.expand(M, N))
