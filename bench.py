@@ -444,6 +444,7 @@ def main():
 
     # split-K on the pages' one-tile case (128 x 128 x 32768): plain vs split
     sk = None
+    gemv_line = None
     if not args.no_tf32x3 and rank == 0:
         sm_, sn_, sk_ = 128, 128, 32768
         gA = torch.rand(sm_, sk_, device=dev) * 2 - 1
@@ -477,6 +478,24 @@ def main():
         sk = {"shape": [sm_, sn_, sk_], "splits": splits, "plain_ms": t_plain,
               "splitk_ms": t_split, "speedup": t_plain / t_split,
               "splitk_tflops": fl / (t_split * 1e-3) / 1e12}
+        del gA, gB, gC, wsk
+
+        # matrix-vector shape (N = 1): bound by reading A once from HBM
+        gm, gk = 8192, 8192
+        vA = torch.rand(gm, gk, device=dev) * 2 - 1      # 256 MB, larger than L2
+        vx = torch.rand(gk, 1, device=dev) * 2 - 1
+        vy = torch.empty(gm, 1, device=dev)
+
+        def gemv():
+            sg.sgemm_f32(gm, 1, gk, vA.data_ptr(), gk, vx.data_ptr(), 1, vy.data_ptr(), 1, 0, 0, sp)
+
+        t_gemv = timed(gemv)
+        gbytes = 4.0 * (gm * gk + gk + gm)
+        hbm = float(measured_peaks().get("hbm_gbs") or 6787.0)
+        gemv_line = {"shape": [gm, 1, gk], "ms": t_gemv, "gbs": gbytes / (t_gemv * 1e-3) / 1e9,
+                     "frac_of_hbm": gbytes / (t_gemv * 1e-3) / 1e9 / hbm,
+                     "hbm_peak_gbs": hbm, "bound": "hbm"}
+        del vA, vx, vy
 
     if rank != 0:
         if world > 1:
@@ -539,6 +558,7 @@ def main():
         line["tf32x3"] = tc
     if sk is not None:
         line["splitk_one_tile"] = sk
+        line["gemv"] = gemv_line
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     print(json.dumps(line), flush=True)

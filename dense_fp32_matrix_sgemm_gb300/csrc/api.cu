@@ -201,6 +201,8 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
         e = launch_tf32x3(a, transA != 0, transB != 0, workspace, s);
     } else if (path == Path::Tf32) {
         e = launch_tf32(a, transA != 0, transB != 0, workspace, s);
+    } else if (gemv_shape(a)) {
+        e = launch_gemv(a, transA != 0, transB != 0, s);
     } else {
         e = launch_simt(a, transA != 0, transB != 0, vector_ok(a), s);
     }

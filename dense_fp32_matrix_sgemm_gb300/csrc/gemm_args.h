@@ -52,6 +52,10 @@ cudaError_t launch_simt_splitk(const GemmArgs &a, bool transA, bool transB, bool
 size_t splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 int splitk_auto_splits(int64_t M, int64_t N, int64_t K);
 
+// Matrix-vector shapes (N == 1 or M == 1): bandwidth-bound kernels.
+bool gemv_shape(const GemmArgs &a);
+cudaError_t launch_gemv(const GemmArgs &a, bool transA, bool transB, cudaStream_t s);
+
 // C[0:M, 0:N] = beta * C + bias for every batch: the whole result when the
 // product term vanishes (K == 0 or alpha == 0); zeros for the plain epilogue.
 cudaError_t launch_epilogue_only(const GemmArgs &a, cudaStream_t s);

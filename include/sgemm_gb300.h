@@ -74,7 +74,10 @@ typedef enum {
  * (GEMM), built as in sections 4-10 of that page (block, warp and thread
  * tiling, float4 access, transposed/swizzled shared-memory tiles, multi-stage
  * asynchronous copies); edge tiles are zero-padded as in the DD2360 workbook,
- * section 14.3.
+ * section 14.3.  Matrix-vector shapes (N == 1 or M == 1) go to bandwidth-bound
+ * kernels instead (warp-per-output dot products or thread-per-output column
+ * sums, DD2360 workbook section 15.2); their sums run in a different but
+ * fixed order, so they are deterministic too.
  */
 int sgemm_f32(int64_t M, int64_t N, int64_t K,
               const float *A, int64_t lda,

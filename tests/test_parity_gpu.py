@@ -465,3 +465,36 @@ def test_epilogue_k_zero_and_alpha_zero():
     sg.sgemm_f32_ex(M, N, 0, 1.0, 0, 1, 0, N, 0.5, C.data_ptr(), N, bias.data_ptr(), 0, 0, 0)
     torch.cuda.synchronize()
     assert torch.equal(C, 3.0 + 1.5 * bias.expand(M, N))
+
+
+# ---------------------------------------------------------------- matrix-vector shapes
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(4099, 1, 3001), (1, 4099, 3001), (1, 1, 777), (513, 1, 8),
+                                   (1, 255, 1)])
+def test_gemv_shapes(M, N, K, tA, tB):
+    lda = ((M if tA else K) + 4) // 4 * 4
+    ldb = ((K if tB else N) + 4) // 4 * 4
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, lda=lda, ldb=ldb, ldc=N + 3,
+                                   dist="normal", poison=True, seed=50, key=215)
+    check_full(case, run(case, entry="sgemm_f32"), label=f"gemv {M}x{N}x{K} tA={tA} tB={tB}")
+
+
+def test_gemv_integer_exact_batched_and_unaligned():
+    case = workloads.make_operands(300, 1, 1000, batch=4, transA=1, dist="int", seed=51, key=216)
+    check_full(case, run(case, entry="sgemm_f32_strided_batched"), exact=True, label="gemv batch")
+    case = workloads.make_operands(1, 517, 999, lda=1000, ldb=518, ldc=518, dist="int",
+                                   poison=True, seed=52, key=217)
+    check_full(case, run(case, entry="sgemm_f32", offset=1), exact=True, label="gemv unaligned")
+
+
+def test_gemv_epilogue():
+    M, N, K = 1000, 1, 640
+    case = workloads.make_operands(M, N, K, dist="normal", seed=53, key=218)
+    rng = np.random.default_rng(54)
+    C_in = rng.standard_normal((M, N)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32)
+    got = _run_ex(case, 0.5, -1.5, C_in, bias, "sgemm_f32_ex")
+    ref, S = oracle.sgemm_ex(case["A"][0], case["B"][0], M, N, K, alpha=0.5, beta=-1.5,
+                             C_in=C_in, bias=bias)
+    assert oracle.within_tolerance(got, ref, S).all()
