@@ -161,8 +161,9 @@ class ClockSampler:
 # ------------------------------------------------------------------ helpers
 
 KERNEL_SOURCES = {
-    "sgemm_simt_kernel": ["device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh", "simt_nn.cu"],
-    "tf32x3_gemm_kernel": ["tc_utils.cuh", "tf32x3.cu"],
+    "sgemm_simt_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh",
+                          "simt_nn.cu"],
+    "tf32x3_gemm_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
 }
 
 

@@ -56,6 +56,7 @@ __global__ void gemv_dot_kernel(const GemvArgs a) {
         float acc = 0.f;
         if constexpr (VEC) {
             int k = 4 * lane;
+#pragma unroll 4
             for (; k + 3 < a.K; k += 128) {
                 const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + k));
                 const float4 vv = __ldg(reinterpret_cast<const float4 *>(v + k));
@@ -95,6 +96,7 @@ gemv_colsum_kernel(const GemvArgs a) {
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     // warp wp takes k = wp, wp + 8, ...
     if (r0 < a.R) {
+#pragma unroll 4
         for (int k = wp; k < a.K; k += kColsumSplit) {
             const float vk = __ldg(v + k * a.incv);
             const float *row = X + (int64_t)k * a.ldx + r0;
