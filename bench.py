@@ -53,6 +53,8 @@ def parse():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-tf32x3", action="store_true", help="skip the tensor-core path report")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the per-workload table (every named workload, both FP32 paths)")
     return p.parse_args()
 
 
@@ -203,6 +205,54 @@ def simt_kernel_label(M, N, batch, transB, sms):
     if not transB and 1.95 * -(-wide // sms) < -(-narrow // sms):
         return "sgemm_simt_kernel 128x256 tile, BK 32, 2 stages, fma.rn.f32x2"
     return "sgemm_simt_kernel 128x128 tile, BK 32, 3 stages, fma.rn.f32x2"
+
+
+def workload_table(torch, sg, dev, stream, sp, reps=5):
+    """ms and TFLOP/s of sgemm_f32 and sgemm_f32_tf32x3 on every named workload
+    (operands resident on the device, median of `reps` after two warm-ups)."""
+    out = {}
+    for name, w in workloads.WORKLOADS.items():
+        case = workloads.make_case(w)
+        lda, ldb, ldc = case["lda"], case["ldb"], case["ldc"]
+        dA = torch.from_numpy(case["A"].reshape(-1)).to(dev)
+        dB = torch.from_numpy(case["B"].reshape(-1)).to(dev)
+        dC = torch.empty(w.batch * w.M * ldc, dtype=torch.float32, device=dev)
+        need = sg.tf32x3_workspace_size(w.M, w.N, w.K, w.batch)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        sA, sB, sC = case["A"][0].size, case["B"][0].size, w.M * ldc
+        row = {"M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "transA": w.transA,
+               "transB": w.transB}
+
+        def simt():
+            sg.sgemm_f32_strided_batched(w.M, w.N, w.K, dA.data_ptr(), lda, sA, dB.data_ptr(), ldb,
+                                         sB, dC.data_ptr(), ldc, sC, w.batch, w.transA, w.transB,
+                                         sp)
+
+        def tc():
+            sg.sgemm_f32_tf32x3_strided_batched(w.M, w.N, w.K, dA.data_ptr(), lda, sA,
+                                                dB.data_ptr(), ldb, sB, dC.data_ptr(), ldc, sC,
+                                                w.batch, w.transA, w.transB, ws.data_ptr(), need,
+                                                sp)
+
+        for label, fn in (("simt", simt), ("tf32x3", tc)):
+            for _ in range(2):
+                fn()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            ms = sorted(ts)[len(ts) // 2]
+            row[label + "_ms"] = ms
+            row[label + "_tflops"] = workloads.flops(w.M, w.N, w.K, w.batch) / (ms * 1e-3) / 1e12
+        out[name] = row
+        del dA, dB, dC, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(case, target_s: float):
@@ -498,6 +548,11 @@ def main():
                      "hbm_peak_gbs": hbm, "bound": "hbm"}
         del vA, vx, vy
 
+    # every named workload on both FP32-accuracy paths (not the timed step)
+    table = None
+    if not args.no_workloads and rank == 0:
+        table = workload_table(torch, sg, dev, stream, sp)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -560,6 +615,8 @@ def main():
     if sk is not None:
         line["splitk_one_tile"] = sk
         line["gemv"] = gemv_line
+    if table is not None:
+        line["workloads"] = table
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     print(json.dumps(line), flush=True)

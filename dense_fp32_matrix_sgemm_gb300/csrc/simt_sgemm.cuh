@@ -30,8 +30,6 @@
 // fp32 FMAs: the result is deterministic.
 #pragma once
 
-#include <type_traits>
-
 #include "device_utils.cuh"
 #include "gemm_args.h"
 
@@ -149,37 +147,6 @@ struct TileLoader {
     }
 };
 
-// Loads a BK x 128 slice of a K-contiguous A (element (m, k) at base[m*ld + k])
-// WITHOUT a corner turn: the shared tile keeps A's own order, [128][BK], and
-// 16-byte chunk c of row m is stored at chunk c ^ ((m >> 2) & (BK/4 - 1)).
-// Every chunk travels by 16-byte cp.async (zero-filled past M and K), and
-// the compute loop reads four consecutive k of one row with one 16-byte load.
-template <int BK>
-struct KMajorATileLoader {
-    static constexpr int KQ = BK / 4;                   // 16-byte chunks per row
-    static constexpr int VECS = BK * BM / THREADS / 4;
-    const float *base;
-    int64_t ld;
-    int mn0, mn_ext, K;
-
-    __device__ __forceinline__ void fetch(int k0, float *tile) {
-        const int tid = threadIdx.x;
-#pragma unroll
-        for (int r = 0; r < VECS; ++r) {
-            const int g = tid + r * THREADS;
-            const int row = g / KQ, kq = g % KQ;
-            const int mn = mn0 + row, k = k0 + 4 * kq;
-            int nv = K - k;
-            nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
-            if (mn >= mn_ext) nv = 0;
-            const float *src = nv ? base + (int64_t)mn * ld + k : base;
-            const int pc = kq ^ ((row >> 2) & (KQ - 1));
-            cp_async_16(smem_u32(tile + row * BK + 4 * pc), src, nv * 4);
-        }
-    }
-    __device__ __forceinline__ void commit(float *) {}
-};
-
 template <int BK, int STAGES, int BN_>
 constexpr int smem_bytes() {
     return STAGES * BK * (BM + BN_) * (int)sizeof(float);
@@ -244,13 +211,12 @@ __device__ __forceinline__ void store_c4(const GemmArgs &p, float *crow, int col
 
 // Block tile 128 x BN_ (BN_ = 128 or 256); each thread owns an 8 x (BN_/16)
 // register tile made of 4 x 4 sub-blocks spaced 64 rows / 64 columns apart.
-// AK (K-contiguous A only, 16-byte access): A stays in its own [128][BK]
-// order in shared memory (KMajorATileLoader) and each thread reads its A
-// fragments as four consecutive k per 16-byte load, held over four k steps.
+// CK: the k step of the tile loop at which register-staged (corner-turned)
+// slices are written to shared memory; BK means after the last step.
 template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int MINB,
-          bool AK = false>
+          int CK = BK>
 __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArgs p) {
-    static_assert(!AK || (VEC && !TA), "the K-major A tile needs row-major A and 16-byte access");
+    static_assert(CK >= 0 && CK <= BK, "commit step out of range");
     static_assert(BK == 8 || BK == 16 || BK == 32, "BK must be 8, 16 or 32");
     static_assert(BN_ == 128 || BN_ == 256, "BN must be 128 or 256");
     static_assert(STAGES >= 2, "need at least two stages");
@@ -269,9 +235,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     const int Kz = p.kchunk > 0 ? min(p.kchunk, p.K - z * p.kchunk) : p.K;
 
     // A is contiguous along K unless stored transposed; B the other way round.
-    using ALoader = typename std::conditional<AK, KMajorATileLoader<BK>,
-                                              TileLoader<BK, BM, !TA, VEC>>::type;
-    ALoader la;
+    TileLoader<BK, BM, !TA, VEC> la;
     la.base = p.A + (int64_t)z * p.strideA;
     la.ld = p.lda;
     la.mn0 = m0;
@@ -327,34 +291,20 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
 
         const float *at = As + rstage * ATILE;
         const float *bt = Bs + rstage * BTILE;
-        float4 af[AK ? 8 : 1];   // A fragments of four k steps (AK only)
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             const int sw = swz<BK>(kk);
             const float *br = bt + kk * BN_;
-            float a[8];
-            if constexpr (AK) {
-                // rows 4ty + i and 64 + 4ty + i, chunk kk/4: loaded at kk % 4 == 0
-                if ((kk & 3) == 0) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int row = (i < 4 ? a_col + i : 64 + a_col + (i - 4));
-                        const int pc = (kk >> 2) ^ ((row >> 2) & (BK / 4 - 1));
-                        af[i] = *reinterpret_cast<const float4 *>(at + row * BK + 4 * pc);
-                    }
+            if constexpr (CK < BK) {
+                if (kk == CK && nt < ktiles) {
+                    la.commit(As + wstage * ATILE);
+                    lb.commit(Bs + wstage * BTILE);
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int q = kk & 3;
-                    a[i] = q == 0 ? af[i].x : q == 1 ? af[i].y : q == 2 ? af[i].z : af[i].w;
-                }
-            } else {
-                const float *ar = at + kk * BM;
-                const float4 a0 = *reinterpret_cast<const float4 *>(ar + (a_col ^ sw));
-                const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + (a_col ^ sw));
-                a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-                a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
             }
+            const float *ar = at + kk * BM;
+            const float4 a0 = *reinterpret_cast<const float4 *>(ar + (a_col ^ sw));
+            const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + (a_col ^ sw));
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             float b[TN];
 #pragma unroll
             for (int h = 0; h < NSB; ++h) {
@@ -384,7 +334,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
             }
         }
 
-        if (nt < ktiles) {
+        if (CK >= BK && nt < ktiles) {
             la.commit(As + wstage * ATILE);
             lb.commit(Bs + wstage * BTILE);
         }
