@@ -479,7 +479,7 @@ def main():
         tc_alg = flops / (tc_ms * 1e-3) / 1e12
         tc = {
             "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
-            "kernels": "split (2 launches) + tf32x3_gemm_kernel (128x256 tile, tcgen05 kind::tf32)",
+            "kernels": "split (2 launches) + tf32x3_gemm_kernel (128x256 or 128x128 tile by wave count, tcgen05 kind::tf32)",
             "gpu_launches_per_step": 3,
             "pct_of_fp32_peak_at_max_clock": None,
             "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_peak,

@@ -13,11 +13,12 @@
 //   workspace as K-major planes [batch][TERMS == 3 ? hi|lo : hi][rows][Kp]
 //   (Kp = K rounded up to 4 so rows are 16-byte aligned for TMA).  M- or
 //   N-major operands are corner-turned through a padded shared tile.
-// Stage 2 (GEMM kernel, one 128 x 256 output tile per CTA, 128 threads):
+// Stage 2 (GEMM kernel, one 128 x BN output tile per CTA, BN = 256 or 128
+//   picked per problem by counting waves, 128 threads):
 //   warp 0 / lane 0 issues TMA loads of the swizzled K slices (BK fp32 of K,
 //   swizzle span = BK * 4 bytes:
-//   A planes 128 rows, B planes 256 rows) into a STAGES-deep ring; warp 1
-//   owns the TMEM accumulators and lane 0 issues TERMS MMAs (M128 N256 K8)
+//   A planes 128 rows, B planes BN rows) into a STAGES-deep ring; warp 1
+//   owns the TMEM accumulators and lane 0 issues TERMS MMAs (M128 N=BN K8)
 //   per 8-wide K step, releasing each stage with tcgen05.commit; after the
 //   last commit all four warps read their 32 TMEM lanes (= tile rows), add
 //   the accumulators and store guarded rows of C.
@@ -45,15 +46,15 @@ namespace sgemm {
 namespace tf32x3 {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int THREADS = 128;
-constexpr int ACC_COLS = BN;   // one fp32 accumulator column per output column
 
-template <int BK_, int STAGES_, int TERMS_>
+template <int BK_, int STAGES_, int TERMS_, int BN_ = 256>
 struct Config {
     static constexpr int BK = BK_;             // fp32 of K per stage (one swizzled row)
     static constexpr int STAGES = STAGES_;
     static constexpr int TERMS = TERMS_;       // 3: hi/lo split; 1: plain TF32
+    static constexpr int BN = BN_;             // output tile width (MMA N): 128 or 256
+    static constexpr int ACC_COLS = BN;        // one fp32 accumulator column per output column
     static constexpr int PLANES = TERMS == 3 ? 2 : 1;
     static constexpr int ROW_BYTES = BK * 4;
     static constexpr int A_TILE = BM * ROW_BYTES;
@@ -61,6 +62,7 @@ struct Config {
     static constexpr int STAGE_BYTES = PLANES * (A_TILE + B_TILE);
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr int TMEM_COLS = TERMS == 3 ? 2 * ACC_COLS : ACC_COLS;
+    static_assert(BN == 128 || BN == 256, "tile width");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Tf32x3Params p) {
     constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
+    constexpr int BN = CFG::BN, ACC_COLS = CFG::ACC_COLS;
     constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
@@ -369,6 +372,21 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     float *wsA = static_cast<float *>(ws);
     float *wsB = wsA + plane_bytes(a.M, a.K, a.batch, PLANES) / 4;
 
+    // tensor maps first (they depend only on the workspace and the sizes), so
+    // no host work separates the split launches from the GEMM launch
+    CUtensorMap tmA, tmB;
+    if (!make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
+        !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN))
+        return cudaErrorInvalidValue;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(tf32x3_gemm_kernel<CFG>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        CFG::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
     // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes
     auto split = [&](const float *X, int64_t ld, int64_t sX, int R, bool kcontig, float *out) {
         if (kcontig) {
@@ -393,18 +411,6 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     if (e != cudaSuccess) return e;
 
     // stage 2: the tensor-core GEMM
-    CUtensorMap tmA, tmB;
-    if (!make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
-        !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, BN))
-        return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tf32x3_gemm_kernel<CFG>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        CFG::SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
     Tf32x3Params p;
     p.C = a.C;
     p.ldc = a.ldc;
@@ -413,7 +419,7 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     p.N = a.N;
     p.K = a.K;
     p.tiles_m = (a.M + BM - 1) / BM;
-    p.tiles_n = (a.N + BN - 1) / BN;
+    p.tiles_n = (a.N + CFG::BN - 1) / CFG::BN;
     p.group_m = 8;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && a.ldc % 4 == 0 && a.strideC % 4 == 0;
     p.alpha = a.alpha;
@@ -426,12 +432,34 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
 
 }  // namespace tf32x3
 
-// Tuned configurations (K slice, stages, terms), both 192 KB of ring.  The
-// pipeline is latency-bound, so what counts is the bytes in flight: 3 of 4
-// stages of 48 KB for the split product (64-byte swizzle) beat 1 of 2 stages
-// of 96 KB by 13-16 %; the single-term product takes 32-float slices.
-using Tf32x3Cfg = tf32x3::Config<16, 4, 3>;
-using Tf32Cfg = tf32x3::Config<32, 4, 1>;
+// Tuned configurations (K slice, stages, terms, tile width).  The ring is
+// latency-bound, so what counts is the bytes in flight: for the 128 x 256
+// tile, 3 of 4 stages of 48 KB (64-byte swizzle) beat 1 of 2 stages of 96 KB
+// by 13-16 %; the 128 x 128 tile does best with 32-float slices.
+using Tf32x3Wide = tf32x3::Config<16, 4, 3, 256>;
+using Tf32x3Narrow = tf32x3::Config<32, 3, 3, 128>;
+using Tf32Wide = tf32x3::Config<32, 4, 1, 256>;
+using Tf32Narrow = tf32x3::Config<32, 6, 1, 128>;
+
+namespace {
+
+// A 128 x 256 tile costs about 1.75 128 x 128 tiles (8192 x 8192 x 4096,
+// where the wave tail is negligible); count waves of one CTA per SM and take
+// the cheaper tiling, the wide one on ties.
+bool tc_wide_tile(const GemmArgs &a) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 1;
+    const long long tm = (a.M + tf32x3::BM - 1) / tf32x3::BM;
+    const long long wide = (long long)a.batch * tm * ((a.N + 255) / 256);
+    const long long narrow = (long long)a.batch * tm * ((a.N + 127) / 128);
+    const double cost_wide = 1.75 * (double)((wide + sms - 1) / sms);
+    const double cost_narrow = (double)((narrow + sms - 1) / sms);
+    return cost_wide <= cost_narrow;
+}
+
+}  // namespace
 
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
     return tf32x3::plane_bytes(M, K, batch, 2) + tf32x3::plane_bytes(N, K, batch, 2);
@@ -442,11 +470,13 @@ size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
 }
 
 cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
-    return tf32x3::launch<Tf32x3Cfg>(a, transA, transB, ws, s);
+    return tc_wide_tile(a) ? tf32x3::launch<Tf32x3Wide>(a, transA, transB, ws, s)
+                           : tf32x3::launch<Tf32x3Narrow>(a, transA, transB, ws, s);
 }
 
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
-    return tf32x3::launch<Tf32Cfg>(a, transA, transB, ws, s);
+    return tc_wide_tile(a) ? tf32x3::launch<Tf32Wide>(a, transA, transB, ws, s)
+                           : tf32x3::launch<Tf32Narrow>(a, transA, transB, ws, s);
 }
 
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset) {
