@@ -24,7 +24,7 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status",
            "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes", "sgemm_f32_tf32",
            "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
-           "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex",
+           "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex", "selftest_wait_timeout",
            "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +79,7 @@ SIGNATURES = {
     "sgemm_f32_tf32x3_noalloc_max_bytes": (ctypes.c_uint64, []),
     "sgemm_probe_fp32_fma": (_int, [_int, _i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_probe_out_elems": (_i64, []),
+    "sgemm_selftest_wait_timeout": (_int, [_i64, _vp]),
 }
 
 
@@ -280,6 +281,11 @@ def probe_fp32_fma(packed: int, iterations: int, out_ptr: int, stream=0) -> floa
 
 def probe_out_elems() -> int:
     return load_library().sgemm_probe_out_elems()
+
+
+def selftest_wait_timeout(limit_cycles: int = 10_000_000, stream=0) -> int:
+    """Run the bounded-wait self-test (see include/sgemm_gb300_probe.h)."""
+    return _check(load_library().sgemm_selftest_wait_timeout(limit_cycles, stream or None))
 
 
 def _operand(t, name):

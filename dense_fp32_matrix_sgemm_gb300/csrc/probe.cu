@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include "sgemm_gb300.h"
+#include "gemm_args.h"
 #include "sgemm_gb300_probe.h"
 
 namespace sgemm {
@@ -64,5 +65,15 @@ extern "C" int sgemm_probe_fp32_fma(int packed, int64_t iterations, float *out, 
         sgemm::fp32_probe_kernel<false><<<(unsigned)ctas, sgemm::kThreads, 0, s>>>(out, iterations);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ELAUNCH;
     *flops_out = 2.0 * 2.0 * sgemm::kChains * (double)iterations * (double)ctas * sgemm::kThreads;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_selftest_wait_timeout(int64_t limit_cycles, void *stream) {
+    if (limit_cycles < 1000 || limit_cycles > 4000000000LL) return SGEMM_EINVAL_DIM;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_EDEVICE;
+    if (sgemm::launch_wait_timeout_selftest(limit_cycles, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return SGEMM_ELAUNCH;
     return SGEMM_OK;
 }

@@ -48,12 +48,13 @@ constexpr long long kWaitLimitCycles = 4000000000LL;
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns false when the CTA aborted or this wait ran out (it then sets
 // *abort).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          long long limit = kWaitLimitCycles) {
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             return false;
         }

@@ -321,6 +321,27 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 }
 
+// ------------------------------------------------------------------ self-test
+
+// Exercises the failure path of the pipeline waits: one CTA waits, with the
+// same bounded wait the GEMM kernel uses, on an mbarrier that nothing ever
+// arrives on.  The wait gives up after `limit` cycles, the CTA raises the
+// library's device status word and exits normally.
+__global__ void wait_timeout_selftest_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_word;
+    const uint32_t b = tc::smem_u32_generic(&bar);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(b, 1);
+        abort_word = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    const bool ok = tc::mbar_wait(b, 0, &abort_word, limit);
+    __syncthreads();
+    if (threadIdx.x == 0 && (!ok || abort_word)) atomicOr(&g_tf32x3_error, 1u);
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -477,6 +498,11 @@ cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
     return tc_wide_tile(a) ? tf32x3::launch<Tf32Wide>(a, transA, transB, ws, s)
                            : tf32x3::launch<Tf32Narrow>(a, transA, transB, ws, s);
+}
+
+cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t s) {
+    tf32x3::wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(limit_cycles);
+    return cudaGetLastError();
 }
 
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset) {

@@ -35,6 +35,16 @@ int sgemm_probe_fp32_fma(int packed, int64_t iterations, float *out, double *flo
 /* Number of floats `out` must hold on the current device. */
 int64_t sgemm_probe_out_elems(void);
 
+/*
+ * Self-test of the library's failure path (no counterpart on the source
+ * pages): launches one CTA that waits, with the bounded wait of the tensor-core
+ * pipeline, on a barrier nothing ever arrives on.  After about `limit_cycles`
+ * SM cycles (1e3 .. 4e9) the wait gives up, the CTA sets bit 0 of the device
+ * status word (read it with sgemm_device_status) and exits normally; the CUDA
+ * context stays usable.  Nothing faults, traps or hangs.
+ */
+int sgemm_selftest_wait_timeout(int64_t limit_cycles, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

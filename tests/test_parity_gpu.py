@@ -498,3 +498,20 @@ def test_gemv_epilogue():
     ref, S = oracle.sgemm_ex(case["A"][0], case["B"][0], M, N, K, alpha=0.5, beta=-1.5,
                              C_in=C_in, bias=bias)
     assert oracle.within_tolerance(got, ref, S).all()
+
+
+# ---------------------------------------------------------------- failure path of the pipeline waits
+
+def test_bounded_wait_gives_up_and_reports():
+    """A pipeline wait on a barrier nothing arrives on gives up after its limit,
+    raises the device status bit, and the context keeps working."""
+    import time
+    assert sg.device_status(reset=True) == 0
+    t = time.time()
+    sg.selftest_wait_timeout(20_000_000)            # ~10 ms at 2 GHz
+    assert sg.device_status(reset=True) & 1
+    assert time.time() - t < 30
+    assert sg.device_status() == 0                   # reset worked
+    case = workloads.make_operands(200, 300, 100, dist="int", seed=60, key=219)
+    check_full(case, run(case, entry="sgemm_f32_tf32x3"), exact=True, label="after self-test")
+    assert sg.device_status() == 0
