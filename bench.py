@@ -195,10 +195,13 @@ def profiled_traffic(kernel: str, workload: str):
     return None
 
 
-def simt_kernel_label(M, N, batch, transB, sms):
-    """The tile the library's launcher picks (same wave model as
-    csrc/simt_launch.cuh: waves of one CTA per SM, a 128x256 tile costing 1.95
-    128x128 tiles; the wide tile only for row-major B)."""
+def simt_kernel_label(M, N, batch, transB, sms, K=3072):
+    """The tile the library's launcher picks (same rules as
+    csrc/simt_launch.cuh: K <= 256 takes two CTAs per SM; otherwise waves of
+    one CTA per SM, a 128x256 tile costing 1.95 128x128 tiles, the wide tile
+    only for row-major B)."""
+    if K <= 256:
+        return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
     tm = -(-M // 128)
     narrow = batch * tm * -(-N // 128)
     wide = batch * tm * -(-N // 256)
@@ -585,7 +588,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"{nsets} rotating input sets of {workloads.min_bytes(M, N, K, batch) / 1e6:.0f} MB "
                          f"(> 129 MB L2 together); each step starts with its operands evicted",
-                   "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label)},
+                   "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label, K)},
         "pct_of_fp32_peak": {
             "at_max_clock": 100.0 * per_gpu / peak_max,
             "peak_tflops_at_max_clock": peak_max,
