@@ -304,15 +304,20 @@ def _operand(t, name):
     raise ValueError(f"{name} must have one unit stride among its last two dimensions")
 
 
-def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None):
-    """out = A @ B for float32 CUDA tensors of shape (M, K) x (K, N), or batched
-    (b, M, K) x (b, K, N).  Transposed views are handled through the trans flags
-    without copies.  Runs on ``stream`` (default: torch's current stream).
+def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None, alpha=1.0, beta=0.0,
+           bias=None, splits=None):
+    """out = alpha * A @ B + beta * out + bias for float32 CUDA tensors of shape
+    (M, K) x (K, N), or batched (b, M, K) x (b, K, N); bias has N elements.
+    Transposed views are handled through the trans flags without copies.
+    Runs on ``stream`` (default: torch's current stream).
 
-    precision="fp32": CUDA-core FMA (sgemm_f32*); "tf32x3": tensor cores with
-    the three-term TF32 split (sgemm_f32_tf32x3*); "tf32": one TF32 product
-    (sgemm_f32_tf32*, reduced precision).  The tensor-core modes use
-    ``workspace`` (a CUDA uint8 tensor) or a fresh one from torch's allocator."""
+    precision="fp32": CUDA-core FMA (sgemm_f32*, or sgemm_f32_ex* with an
+    epilogue, or sgemm_f32_splitk when ``splits`` is given: 0 = automatic);
+    "tf32x3": tensor cores with the three-term TF32 split (sgemm_f32_tf32x3*);
+    "tf32": one TF32 product (sgemm_f32_tf32*, reduced precision).  The
+    tensor-core modes and split-K use ``workspace`` (a CUDA uint8 tensor) or a
+    fresh one from torch's allocator.  beta != 0 needs ``out`` (its values are
+    read)."""
     import torch
     if precision not in ("fp32", "tf32x3", "tf32"):
         raise ValueError("precision must be 'fp32', 'tf32x3' or 'tf32'")
@@ -327,20 +332,59 @@ def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None):
     if batched and B.shape[0] != batch:
         raise ValueError("batch sizes differ")
     shape = (batch, M, N) if batched else (M, N)
+    plain = alpha == 1.0 and beta == 0.0 and bias is None
     if out is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 reads out: pass it")
         out = torch.empty(shape, dtype=torch.float32, device=A.device)
     elif tuple(out.shape) != shape or out.dtype != torch.float32 or out.stride(-1) != 1:
         raise ValueError("out has the wrong shape, dtype or layout")
+    bp = 0
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda or bias.numel() != N or \
+                (bias.dim() > 0 and bias.stride(-1) != 1):
+            raise ValueError("bias must be a contiguous float32 CUDA tensor of N elements")
+        bp = bias.data_ptr()
     ldc = max(out.stride(-2), N, 1)
     s = stream if stream is not None else torch.cuda.current_stream(A.device)
     sp = s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
-    if precision in ("tf32x3", "tf32"):
-        x3 = precision == "tf32x3"
-        need = (tf32x3_workspace_size if x3 else tf32_workspace_size)(M, N, K, batch)
+
+    def scratch(need):
+        nonlocal workspace
         if workspace is None or workspace.numel() < need:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
-        ws, wsb = workspace.data_ptr(), workspace.numel()
-        if batched:
+        return workspace.data_ptr(), workspace.numel()
+
+    if splits is not None:
+        if precision != "fp32" or batched or not plain:
+            raise ValueError("split-K is for single fp32 products without an epilogue")
+        ws, wsb = scratch(splitk_workspace_size(M, N, K, splits))
+        sgemm_f32_splitk(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA,
+                         tB, splits, ws, wsb, sp)
+    elif precision == "fp32":
+        if plain and batched:
+            sgemm_f32_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb,
+                                      B.stride(0), out.data_ptr(), ldc, out.stride(0), batch,
+                                      tA, tB, sp)
+        elif plain:
+            sgemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA, tB,
+                      sp)
+        elif batched:
+            sgemm_f32_ex_strided_batched(M, N, K, alpha, A.data_ptr(), lda, A.stride(0),
+                                         B.data_ptr(), ldb, B.stride(0), beta, out.data_ptr(), ldc,
+                                         out.stride(0), bp, batch, tA, tB, sp)
+        else:
+            sgemm_f32_ex(M, N, K, alpha, A.data_ptr(), lda, B.data_ptr(), ldb, beta,
+                         out.data_ptr(), ldc, bp, tA, tB, sp)
+    else:
+        x3 = precision == "tf32x3"
+        ws, wsb = scratch((tf32x3_workspace_size if x3 else tf32_workspace_size)(M, N, K, batch))
+        if not plain:
+            if not x3 or batched:
+                raise ValueError("the epilogue is available for single tf32x3 products")
+            sgemm_f32_tf32x3_ex(M, N, K, alpha, A.data_ptr(), lda, B.data_ptr(), ldb, beta,
+                                out.data_ptr(), ldc, bp, tA, tB, ws, wsb, sp)
+        elif batched:
             fn = sgemm_f32_tf32x3_strided_batched if x3 else sgemm_f32_tf32_strided_batched
             fn(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb, B.stride(0),
                out.data_ptr(), ldc, out.stride(0), batch, tA, tB, ws, wsb, sp)
@@ -348,10 +392,4 @@ def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None):
             fn = sgemm_f32_tf32x3 if x3 else sgemm_f32_tf32
             fn(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA, tB, ws,
                wsb, sp)
-    elif batched:
-        sgemm_f32_strided_batched(M, N, K, A.data_ptr(), lda, A.stride(0), B.data_ptr(), ldb,
-                                  B.stride(0), out.data_ptr(), ldc, out.stride(0), batch,
-                                  tA, tB, sp)
-    else:
-        sgemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA, tB, sp)
     return out

@@ -31,6 +31,7 @@
 // Every mbarrier wait is bounded; a wait that runs out flags the CTA, the
 // roles drain (copies in flight land, MMAs complete, TMEM is freed) and the
 // library's device error word is raised.
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -399,14 +400,20 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     if (!make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
         !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN))
         return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tf32x3_gemm_kernel<CFG>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        CFG::SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        // the opt-in shared-memory size is a per-device function attribute
+        static std::atomic<unsigned long long> configured{0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const unsigned long long bit = 1ull << (dev & 63);
+        if (!(configured.load() & bit)) {
+            e = cudaFuncSetAttribute(tf32x3_gemm_kernel<CFG>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, CFG::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            configured.fetch_or(bit);
+        }
+    }
 
     // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes
     auto split = [&](const float *X, int64_t ld, int64_t sX, int R, bool kcontig, float *out) {

@@ -515,3 +515,24 @@ def test_bounded_wait_gives_up_and_reports():
     case = workloads.make_operands(200, 300, 100, dist="int", seed=60, key=219)
     check_full(case, run(case, entry="sgemm_f32_tf32x3"), exact=True, label="after self-test")
     assert sg.device_status() == 0
+
+
+def test_matmul_convenience_epilogue_and_splitk():
+    import torch
+    torch.manual_seed(1)
+    A = torch.randn(200, 300, device="cuda")
+    B = torch.randn(300, 150, device="cuda")
+    bias = torch.randn(150, device="cuda")
+    C0 = torch.randn(200, 150, device="cuda")
+    an, bn = A.cpu().numpy(), B.cpu().numpy()
+    for prec in ("fp32", "tf32x3"):
+        out = C0.clone()
+        sg.matmul(A, B, out=out, precision=prec, alpha=0.5, beta=2.0, bias=bias)
+        ref, S = oracle.sgemm_ex(an, bn, 200, 150, 300, alpha=0.5, beta=2.0,
+                                 C_in=C0.cpu().numpy(), bias=bias.cpu().numpy())
+        assert oracle.within_tolerance(out.cpu().numpy(), ref, S).all(), prec
+    out = sg.matmul(A, B, splits=0)
+    ref, S = oracle.sgemm(an, bn, 200, 150, 300, with_scale=True)
+    assert oracle.within_tolerance(out.cpu().numpy(), ref, S).all()
+    with pytest.raises(ValueError):
+        sg.matmul(A, B, beta=1.0)          # beta reads out, which was not given
