@@ -1,5 +1,6 @@
 // Small device-side helpers shared by the SGEMM kernels: asynchronous
-// global->shared copies (cp.async, sm_80+) and shared-memory addresses.
+// global->shared copies (cp.async, sm_80+), shared-memory addresses, and
+// thread-block-cluster primitives (rank, barrier, distributed shared memory).
 #pragma once
 
 #include <cstdint>
@@ -36,6 +37,39 @@ __device__ __forceinline__ void cp_async_wait() {
 
 __device__ __forceinline__ float4 ldg_f4(const float *p) {
     return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+// Rank of this CTA within its cluster, and the number of CTAs in the cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(n));
+    return n;
+}
+
+// Cluster-wide barrier: every thread of every CTA in the cluster arrives; the
+// release/acquire pair makes shared-memory writes made before it visible to
+// distributed-shared-memory reads after it.  Not the .aligned form, so
+// threads need not be converged when they reach it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n"
+                 "barrier.cluster.wait.acquire;\n" ::: "memory");
+}
+
+// 16-byte load from the shared memory of CTA `rank` of this cluster, at the
+// offset that `local` (a shared::cta address) has in this CTA.
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(local), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+    return v;
 }
 
 }  // namespace sgemm

@@ -31,6 +31,10 @@ constexpr int kCommitWide = 8;
 // FMAs; 32 % faster on 96 x 512 x 512 x 64 although the register cap spills a
 // little.
 constexpr int kShortK = 256;
+// Cluster split-K: problems whose 128 x 128 tiles (all batches) cover at most
+// half the SMs split K over the S CTAs of a cluster, S in {2, 4, 8} (8 is the
+// portable cluster limit), each CTA taking whole 32-deep slices.
+constexpr int kMaxClusterSplit = 8;
 
 inline int sm_count() {
     static std::atomic<int> cached[64];
@@ -57,24 +61,30 @@ inline bool pick_wide_tile(const GemmArgs &a) {
     return cost_wide < cost_narrow;
 }
 
+// Sets the opt-in dynamic shared-memory size of `kern` once per device.
+template <typename Kern>
+cudaError_t ensure_smem_attribute(Kern kern, int smem, std::atomic<unsigned long long> &configured) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    return cudaSuccess;
+}
+
 template <int STAGES, int BN_, bool TA, bool TB, bool VEC, int MINB = kMinBlocks>
 cudaError_t launch_config(const GemmArgs &a, cudaStream_t s) {
     constexpr int commit = BN_ == 256 ? kCommitWide : (STAGES == 2 ? kBK : kCommitNarrow);
     auto kern = sgemm_simt_kernel<kBK, STAGES, BN_, TA, TB, VEC, kFfma2, MINB, commit>;
     constexpr int smem = smem_bytes<kBK, STAGES, BN_>();
-    if (smem > 48 * 1024) {
-        // The opt-in shared-memory limit is a per-device function attribute.
-        static std::atomic<unsigned long long> configured{0};
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        const unsigned long long bit = 1ull << (dev & 63);
-        if (!(configured.load() & bit)) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return e;
-            configured.fetch_or(bit);
-        }
-    }
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = ensure_smem_attribute(kern, smem, configured);
+    if (e != cudaSuccess) return e;
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + BN_ - 1) / BN_;
@@ -83,11 +93,88 @@ cudaError_t launch_config(const GemmArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The cluster split for one (transA, transB, vec) variant.  Returns false
+// (launching nothing) when the problem has enough tiles to fill the GPU, K is
+// too short to split, or no cluster size lets every cluster be resident at
+// once; else launches and stores the launch status in `err`.
+template <bool TA, bool TB, bool VEC>
+bool launch_cluster_split(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
+    constexpr int kStages = kStagesNarrow;
+    auto kern = sgemm_simt_kernel<kBK, kStages, 128, TA, TB, VEC, kFfma2, kMinBlocks, kCommitNarrow,
+                                  true>;
+    constexpr int smem = smem_bytes<kBK, kStages, 128, true>();
+    const long long sms = sm_count();
+    const long long tm = (a.M + BM - 1) / BM, tn = (a.N + 127) / 128;
+    const long long tiles = (long long)a.batch * tm * tn;
+    if (a.kchunk != 0 || tiles * 2 > sms) return false;
+    const long long slices = (a.K + kBK - 1) / kBK;
+    if (slices < 2) return false;
+
+    static std::atomic<unsigned long long> configured{0};
+    err = ensure_smem_attribute(kern, smem, configured);
+    if (err != cudaSuccess) return true;
+    int dev = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return true;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+
+    // Clusters of each size that fit on the device at once (0: not asked yet,
+    // -1: that size cannot run); a split that needs a second wave loses.
+    static std::atomic<int> resident[64][4];
+    auto fits = [&](int c) {
+        std::atomic<int> &slot = resident[dev & 63][c == 2 ? 0 : (c == 4 ? 1 : 2)];
+        int n = slot.load();
+        if (n == 0) {
+            attr[0].val.clusterDim.x = (unsigned)c;
+            cfg.gridDim = dim3((unsigned)c);
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+                (void)cudaGetLastError();   // the unsplit kernels still serve the call
+                n = -1;
+            }
+            slot.store(n);
+        }
+        return n >= tiles;
+    };
+    // the fewest 32-deep slices per CTA; the smallest cluster among equals
+    int S = 1;
+    long long best = slices;
+    for (int c = 2; c <= kMaxClusterSplit; c *= 2) {
+        if (tiles * c > sms || c > slices) break;
+        const long long per = (slices + c - 1) / c;
+        if (per < best && fits(c)) {
+            best = per;
+            S = c;
+        }
+    }
+    if (S < 2) return false;
+
+    GemmArgs g = a;
+    g.tiles_m = (int)tm;
+    g.tiles_n = (int)tn;
+    g.kchunk = (int)(best * kBK);
+    attr[0].val.clusterDim.x = (unsigned)S;
+    cfg.gridDim = dim3((unsigned)(tiles * S));
+    err = cudaLaunchKernelEx(&cfg, kern, g);
+    return true;
+}
+
 // The wide tile is used only where B arrives by cp.async (row-major B) and
 // with 16-byte access: corner-turning a 256-wide B slice needs 32 more
 // staging registers than the 255-register budget leaves.
 template <bool TA, bool TB, bool VEC>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t s) {
+    cudaError_t err = cudaSuccess;
+    if (launch_cluster_split<TA, TB, VEC>(a, s, err)) return err;
     if constexpr (VEC) {
         if (a.K <= kShortK) return launch_config<2, 128, TA, TB, VEC, 2>(a, s);
     }

@@ -25,9 +25,17 @@
 //   * tiles are rasterised in groups of `group_m` tile rows so that a wave of
 //     CTAs shares A and B panels in L2 (section 2.3);
 //   * edge tiles are zero-padded on load and stores are guarded (DD2360
-//     workbook, section 14.3).
+//     workbook, section 14.3);
+//   * problems with too few tiles to fill the GPU split K across the CTAs of
+//     a thread-block cluster (CSPLIT): each CTA accumulates one K chunk of the
+//     same tile, parks its partial tile in its own shared memory, and after a
+//     cluster barrier every CTA sums a band of rows over all the cluster's
+//     partials, read through distributed shared memory in rank order.  This
+//     is the split-K of the ChetanC28/cuda-kernels page (splitting K across
+//     blocks for small problems) with the reduction kept on chip.
 // Each output's K terms are accumulated by one thread, in ascending k, with
-// fp32 FMAs: the result is deterministic.
+// fp32 FMAs (under CSPLIT: per chunk, and the chunk sums are then added in
+// chunk order): the result is deterministic.
 #pragma once
 
 #include "device_utils.cuh"
@@ -147,16 +155,22 @@ struct TileLoader {
     }
 };
 
-template <int BK, int STAGES, int BN_>
+// Row stride (floats) of the partial tile a CSPLIT CTA parks in shared
+// memory: 4 floats of padding put the two rows a quarter-warp writes in
+// different banks.
+constexpr int kPartialLd = 128 + 4;
+
+template <int BK, int STAGES, int BN_, bool CSPLIT = false>
 constexpr int smem_bytes() {
-    return STAGES * BK * (BM + BN_) * (int)sizeof(float);
+    constexpr int pipe = STAGES * BK * (BM + BN_) * (int)sizeof(float);
+    constexpr int part = CSPLIT ? BM * kPartialLd * (int)sizeof(float) : 0;
+    return pipe > part ? pipe : part;
 }
 
-// Maps the linear CTA index to (batch, tile row, tile column), walking
+// Maps a linear tile index to (batch, tile row, tile column), walking
 // `group_m` tile rows down a column before moving right.
-__device__ __forceinline__ void raster(const GemmArgs &p, int &z, int &tm, int &tn) {
+__device__ __forceinline__ void raster(const GemmArgs &p, int bid, int &z, int &tm, int &tn) {
     const int per_batch = p.tiles_m * p.tiles_n;
-    const int bid = blockIdx.x;
     z = bid / per_batch;
     const int t = bid - z * per_batch;
     const int group = p.group_m * p.tiles_n;
@@ -213,10 +227,13 @@ __device__ __forceinline__ void store_c4(const GemmArgs &p, float *crow, int col
 // register tile made of 4 x 4 sub-blocks spaced 64 rows / 64 columns apart.
 // CK: the k step of the tile loop at which register-staged (corner-turned)
 // slices are written to shared memory; BK means after the last step.
+// CSPLIT: launched in 1-D clusters of S CTAs (S divides 128); CTA q of the
+// cluster covers k in [q*kchunk, min(K, (q+1)*kchunk)) of tile blockIdx.x / S.
 template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int MINB,
-          int CK = BK>
+          int CK = BK, bool CSPLIT = false>
 __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArgs p) {
     static_assert(CK >= 0 && CK <= BK, "commit step out of range");
+    static_assert(!CSPLIT || BN_ == 128, "the cluster split uses 128 x 128 tiles");
     static_assert(BK == 8 || BK == 16 || BK == 32, "BK must be 8, 16 or 32");
     static_assert(BN_ == 128 || BN_ == 256, "BN must be 128 or 256");
     static_assert(STAGES >= 2, "need at least two stages");
@@ -229,10 +246,14 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     float *Bs = smem + STAGES * ATILE;
 
     int z, tm, tn;
-    raster(p, z, tm, tn);
+    raster(p, CSPLIT ? (int)(blockIdx.x / cluster_size()) : (int)blockIdx.x, z, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN_;
-    // split-K: problem z is the K-chunk [z*kchunk, min(K, (z+1)*kchunk))
-    const int Kz = p.kchunk > 0 ? min(p.kchunk, p.K - z * p.kchunk) : p.K;
+    // split-K: the K-chunk [kq*kchunk, min(K, (kq+1)*kchunk)), where kq is the
+    // problem index z (partial planes; the strides step by one chunk) or,
+    // under CSPLIT, the rank in the cluster.  Ranks past the last chunk get
+    // Kz <= 0 and load nothing.
+    const int kq = CSPLIT ? (int)cluster_rank() : z;
+    const int Kz = (CSPLIT || p.kchunk > 0) ? min(p.kchunk, p.K - kq * p.kchunk) : p.K;
 
     // A is contiguous along K unless stored transposed; B the other way round.
     TileLoader<BK, BM, !TA, VEC> la;
@@ -247,6 +268,11 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
     lb.mn0 = n0;
     lb.mn_ext = p.N;
     lb.K = Kz;
+    if constexpr (CSPLIT) {
+        const int64_t kbeg = (int64_t)kq * p.kchunk;
+        la.base += TA ? kbeg * p.lda : kbeg;
+        lb.base += TB ? kbeg : kbeg * p.ldb;
+    }
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -263,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-    const int ktiles = (Kz + BK - 1) / BK;
+    const int ktiles = (Kz + BK - 1) / BK;   // <= 0: nothing to load
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
@@ -345,17 +371,55 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
 
     float *Cz = p.C + (int64_t)z * p.strideC;
     const bool plain = plain_epilogue(p);
+    if constexpr (CSPLIT) {
+        // Park the partial tile (row-major, kPartialLd floats per row) over the
+        // pipeline buffers once every warp is done reading them.
+        __syncthreads();
+        float *part = smem;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = m0 + (i < 4 ? a_col + i : 64 + a_col + (i - 4));
-        if (row >= p.M) continue;
-        float *crow = Cz + (int64_t)row * p.ldc;
+        for (int i = 0; i < 8; ++i) {
+            const int r = i < 4 ? a_col + i : 64 + a_col + (i - 4);
 #pragma unroll
-        for (int h = 0; h < NSB; ++h) {
-            const int col = n0 + h * 64 + b_col;
-            const float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
-                                         acc[i][4 * h + 3]);
-            store_c4(p, crow, col, v, VEC, plain);
+            for (int h = 0; h < NSB; ++h)
+                *reinterpret_cast<float4 *>(part + r * kPartialLd + h * 64 + b_col) =
+                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                acc[i][4 * h + 3]);
+        }
+        cluster_sync();
+        // CTA q finishes rows [q*128/S, (q+1)*128/S) of the tile: the sum over
+        // ranks 0..S-1 of the partials, in that order, then the epilogue.
+        const uint32_t crank = (uint32_t)kq, csize = cluster_size();
+        const int r0 = (int)(crank * BM / csize), r1 = (int)((crank + 1) * BM / csize);
+        constexpr int G = BN_ / 4;   // float4 groups per row
+        for (int g = tid; g < (r1 - r0) * G; g += THREADS) {
+            const int r = r0 + g / G, c = 4 * (g % G);
+            const uint32_t at = smem_u32(part + r * kPartialLd + c);
+            float4 sum = ld_cluster_f4(at, 0);
+            for (uint32_t q = 1; q < csize; ++q) {
+                const float4 v = ld_cluster_f4(at, q);
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            const int row = m0 + r;
+            if (row < p.M) store_c4(p, Cz + (int64_t)row * p.ldc, n0 + c, sum, VEC, plain);
+        }
+        // No CTA may leave (releasing its shared memory) while a peer still reads it.
+        cluster_sync();
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = m0 + (i < 4 ? a_col + i : 64 + a_col + (i - 4));
+            if (row >= p.M) continue;
+            float *crow = Cz + (int64_t)row * p.ldc;
+#pragma unroll
+            for (int h = 0; h < NSB; ++h) {
+                const int col = n0 + h * 64 + b_col;
+                const float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                             acc[i][4 * h + 3]);
+                store_c4(p, crow, col, v, VEC, plain);
+            }
         }
     }
 }

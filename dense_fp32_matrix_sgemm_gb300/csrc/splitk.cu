@@ -16,7 +16,10 @@ namespace sgemm {
 namespace {
 
 constexpr int kChunkAlign = 32;       // whole K slices of the SIMT kernel
-constexpr int kMinChunk = 256;        // keep each chunk long enough to amortise its tile load
+// One 32-deep slice per chunk at least: on GB300 the reduction pass is cheap
+// next to an idle SM (256 x 256 x 256: 8 chunks 12.4 us against 20.6 us for 2;
+// 256 x 256 x 4096: 32 chunks 22.7 us against 31.8 us for 16).
+constexpr int kMinChunk = 32;
 constexpr int kMaxAutoSplits = 64;
 
 int64_t padded_n(int64_t N) { return (N + 3) / 4 * 4; }

@@ -32,7 +32,9 @@
  *   synchronising; the result is visible to later work on that stream.
  *
  * Precision.  sgemm_f32*: every product and sum is an fp32 FMA on the CUDA
- *   cores, each output's terms accumulated in ascending k by one thread; the
+ *   cores, each output's terms accumulated in ascending k by one thread (when
+ *   the problem is too small to fill the GPU, K is first cut into chunks, each
+ *   chunk accumulated that way and the chunk sums added in chunk order); the
  *   result is deterministic (bit-identical across calls).  sgemm_f32_tf32x3*:
  *   tensor cores with the three-term TF32 split (see below).
  *
@@ -77,7 +79,11 @@ typedef enum {
  * section 14.3.  Matrix-vector shapes (N == 1 or M == 1) go to bandwidth-bound
  * kernels instead (warp-per-output dot products or thread-per-output column
  * sums, DD2360 workbook section 15.2); their sums run in a different but
- * fixed order, so they are deterministic too.
+ * fixed order, so they are deterministic too.  Problems whose 128 x 128
+ * output tiles cover at most half the SMs (e.g. 256 x 256 x 256: four tiles)
+ * split K over the 2, 4 or 8 CTAs of a thread-block cluster and add the
+ * partial tiles on chip through distributed shared memory, in chunk order:
+ * the split-K of the ChetanC28/cuda-kernels page without a workspace.
  */
 int sgemm_f32(int64_t M, int64_t N, int64_t K,
               const float *A, int64_t lda,
@@ -155,8 +161,8 @@ int sgemm_f32_splitk(int64_t M, int64_t N, int64_t K,
                      void *workspace, uint64_t workspace_bytes, void *stream);
 
 /* Number of K chunks chosen for splits = 0: enough 128 x 128 tiles to put one
- * CTA on every SM of the current device, each chunk at least 256 deep, at
- * most 64; 1 when the tiles already fill the device. */
+ * CTA on every SM of the current device, each chunk at least 32 deep (one K
+ * slice), at most 64; 1 when the tiles already fill the device. */
 int sgemm_f32_splitk_auto_splits(int64_t M, int64_t N, int64_t K);
 
 /* Workspace bytes for sgemm_f32_splitk (splits = 0: the automatic choice):

@@ -536,3 +536,48 @@ def test_matmul_convenience_epilogue_and_splitk():
     assert oracle.within_tolerance(out.cpu().numpy(), ref, S).all()
     with pytest.raises(ValueError):
         sg.matmul(A, B, beta=1.0)          # beta reads out, which was not given
+
+
+# sgemm_f32 on problems whose 128 x 128 tiles cover at most half the SMs:
+# K is split over the CTAs of a cluster (2, 4 or 8) and the partial tiles are
+# added through distributed shared memory.  Shapes pick each cluster size,
+# chunks of one slice, a last chunk holding a single k, and more ranks than
+# non-empty chunks.
+CLUSTER = [(256, 256, 256), (130, 129, 77), (200, 70, 33), (300, 260, 4096),
+           (128, 128, 32768), (1000, 1000, 300), (100, 100, 264), (64, 384, 96)]
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", CLUSTER)
+def test_cluster_split_shapes(M, N, K, tA, tB):
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, ldc=N + 3, dist="uniform",
+                                   seed=50, key=300 + M + N + K)
+    check_full(case, run(case), label=f"cluster {M}x{N}x{K} tA={tA} tB={tB}")
+    icase = workloads.make_operands(M, N, K, transA=tA, transB=tB, dist="int", seed=51,
+                                    key=400 + M + N + K)
+    check_full(icase, run(icase), exact=True, label=f"cluster int {M}x{N}x{K} tA={tA} tB={tB}")
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_cluster_split_unaligned_batched_deterministic(offset):
+    case = workloads.make_operands(150, 90, 700, batch=3, transA=1, lda=153, ldb=91,
+                                   dist="normal", seed=52, key=500)
+    first = run(case, entry="sgemm_f32_strided_batched", offset=offset)
+    check_full(case, first, label=f"cluster batched offset={offset}")
+    again = run(case, entry="sgemm_f32_strided_batched", offset=offset)
+    assert np.array_equal(first, again), "cluster split is not deterministic"
+
+
+@pytest.mark.parametrize("alpha,beta,with_bias", [(0.7, -1.3, True), (1.0, 0.0, True),
+                                                  (-2.0, 0.5, False)])
+def test_cluster_split_epilogue(alpha, beta, with_bias):
+    M, N, K = 200, 190, 1500
+    case = workloads.make_operands(M, N, K, transB=1, ldc=N + 2, dist="normal", seed=53, key=501)
+    rng = np.random.default_rng(54)
+    C_in = rng.standard_normal((M, N)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32) if with_bias else None
+    got = _run_ex(case, alpha, beta, C_in if beta != 0.0 else None, bias, "sgemm_f32_ex")
+    ref, S = oracle.sgemm_ex(case["A"][0], case["B"][0], M, N, K, alpha=alpha, beta=beta,
+                             C_in=C_in, bias=bias, transB=1, ldb=case["ldb"])
+    ok = oracle.within_tolerance(got, ref, S)
+    assert ok.all(), f"{int((~ok).sum())} outputs outside the bound"
