@@ -1,5 +1,5 @@
 // Inline-PTX wrappers for the Blackwell tensor-core path (sm_100a family,
-// built for sm_103a): mbarriers with bounded waits, TMA tile loads, tensor
+// built for sm_103a): mbarriers with bounded waits, TMA tile loads and stores, tensor
 // memory (TMEM) allocation and loads, tcgen05.mma of kind tf32, and the
 // shared-memory / instruction descriptors those MMAs take.
 #pragma once
@@ -77,6 +77,45 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         " [%0], [%1, {%3, %4, %5}], [%2];"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// 3-D tiled store of the box at (c0, c1, c2) from shared memory at `src`,
+// tracked by the issuing thread's bulk async-group.  Elements outside the
+// tensor's extents are not written.  c0 (innermost) must be a multiple of 16
+// bytes' worth of elements, and no coordinate may be negative.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1,
+                                             int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+        :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
+
+// Until at most N of this thread's bulk groups are incomplete (writes done).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // ---------------------------------------------------------------- TMEM

@@ -20,8 +20,13 @@
 //   A planes 128 rows, B planes BN rows) into a STAGES-deep ring; warp 1
 //   owns the TMEM accumulators and lane 0 issues TERMS MMAs (M128 N=BN K8)
 //   per 8-wide K step, releasing each stage with tcgen05.commit; after the
-//   last commit all four warps read their 32 TMEM lanes (= tile rows), add
-//   the accumulators and store guarded rows of C.
+//   last commit all four warps read their 32 TMEM lanes (= tile rows) 32
+//   columns at a time and add the accumulators.  For the plain product into
+//   a 16-byte-aligned C with N a multiple of 4, each warp writes its 32 x 32
+//   block into shared memory (the now idle operand ring; 128-byte swizzle,
+//   two buffers per warp) and one lane stores it with a TMA tensor store,
+//   which writes whole rows and clips the ragged edges; otherwise the threads
+//   store their own rows.
 // The tensor cores add each MMA's partial sum into its fp32 accumulator with
 // a rounding that is biased towards zero, so the error of a long K grows with
 // the number of updates.  hi*hi therefore has an accumulator of its own (K/8
@@ -151,6 +156,7 @@ struct Tf32x3Params {
     int M, N, K;
     int tiles_m, tiles_n, group_m;
     int vec_c;   // C rows allow 16-byte stores
+    int tma_c;   // store C through the tmC tensor map (plain epilogue, aligned C)
     float alpha, beta;      // epilogue C = alpha * acc + beta * C + bias[col]
     const float *bias;
 };
@@ -172,7 +178,7 @@ __device__ __forceinline__ void raster(const Tf32x3Params &p, int &z, int &tm, i
 template <class CFG>
 __global__ void __launch_bounds__(THREADS, 1)
 tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const Tf32x3Params p) {
+                   const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
     constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
     constexpr int BN = CFG::BN, ACC_COLS = CFG::ACC_COLS;
     constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
@@ -274,7 +280,46 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const bool ok = tc::mbar_wait(done_bar, 0, abort_flag);
     __syncwarp();   // reconverge before the warp-collective TMEM loads
     tc::fence_after_sync();
-    if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
+    // one warp-uniform decision: the TMEM loads below are warp-collective
+    const bool go = __all_sync(0xffffffffu, ok && !*abort_flag);
+    if (go && p.tma_c) {
+        // Warp w stages rows 32w..32w+31 of the tile, 32 columns at a time, in
+        // two 4 KB buffers at ring offset 8 KB * w (1024-byte aligned: the
+        // 128-byte swizzle puts 16-byte chunk j of row r at chunk j ^ (r & 7),
+        // so the eight rows a quarter-warp writes hit distinct banks).
+        const uint32_t stage = tiles + (uint32_t)warp * 8192u;
+        const int row0 = m0 + 32 * warp;
+        int c = 0;
+        for (; row0 < p.M && c < BN / 32 && n0 + 32 * c < p.N; ++c) {
+            float v[32];
+            const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c);
+            tc::tmem_ld_32(ta, v);
+            if constexpr (CFG::TERMS == 3) {
+                float w[32];
+                tc::tmem_ld_32(ta + ACC_COLS, w);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += w[j];
+            }
+            const uint32_t buf = stage + (uint32_t)(c & 1) * 4096u;
+            if (c >= 2) {
+                if (lane == 0) tc::bulk_wait_group_read<1>();   // the store of chunk c-2 has read it
+                __syncwarp();
+            }
+            const uint32_t rbase = buf + (uint32_t)lane * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                tc::st_shared_v4(rbase + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
+                                 v[4 * j + 2], v[4 * j + 3]);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::tma_store_3d(&tmC, buf, n0 + 32 * c, row0, z);
+                tc::bulk_commit_group();
+            }
+        }
+        if (lane == 0 && c > 0) tc::bulk_wait_group<0>();
+        __syncwarp();
+    } else if (go) {
         const int row = m0 + 32 * warp + lane;
         float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
 #pragma unroll 1
@@ -380,6 +425,23 @@ bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp
     return r == CUDA_SUCCESS;
 }
 
+// C as a [batch][M][N] tensor (row stride ldc, batch stride strideC), box
+// 32 x 32 x 1 with the 128-byte swizzle the epilogue writes in.
+bool make_c_map(CUtensorMap *map, float *C, int M, int N, int64_t ldc, int64_t strideC,
+                int batch) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batch};
+    const int64_t zstride = batch > 1 ? strideC : (int64_t)M * ldc;
+    const cuuint64_t strides[2] = {(cuuint64_t)ldc * 4, (cuuint64_t)zstride * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, C, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t plane_bytes(int64_t rows, int64_t K, int64_t batch, int planes) {
@@ -453,8 +515,16 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     p.alpha = a.alpha;
     p.beta = a.beta;
     p.bias = a.bias;
+    // The TMA store takes the plain product into a C whose base, rows and
+    // batches are 16-byte aligned and whose width is a whole number of
+    // 16-byte granules: with N not a multiple of 4 the store was seen to
+    // write the padding column next to column N-1, so such widths keep the
+    // threads' own guarded stores.  The map is only read when tma_c is set.
+    CUtensorMap tmC = {};
+    p.tma_c = p.vec_c && a.N % 4 == 0 && plain_epilogue(a) &&
+              make_c_map(&tmC, a.C, a.M, a.N, a.ldc, a.strideC, a.batch);
     const long long blocks = (long long)a.batch * p.tiles_m * p.tiles_n;
-    tf32x3_gemm_kernel<CFG><<<(unsigned)blocks, THREADS, CFG::SMEM_BYTES, s>>>(tmA, tmB, p);
+    tf32x3_gemm_kernel<CFG><<<(unsigned)blocks, THREADS, CFG::SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
     return cudaGetLastError();
 }
 
