@@ -22,8 +22,11 @@ BUILD = os.path.join(ROOT, "_build", "sgemm_gb300")
 LIB = os.path.join(PKG, "libsgemm_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Hidden visibility: the library exports only the C ABI that the public
+# headers declare, so its kernels and host stubs cannot bind to, or be bound
+# by, same-named symbols of another library in the process.
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-              "-Xptxas", "-O3", "--expt-relaxed-constexpr"]
+              "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-O3", "--expt-relaxed-constexpr"]
 
 
 def nvcc() -> str:

@@ -58,6 +58,12 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden symbol visibility; only the entry points
+ * declared here are exported. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 typedef enum {
     SGEMM_OK = 0,
     SGEMM_EINVAL_DIM = 1,    /* M, N or K negative, or too large for the grid */
@@ -298,6 +304,10 @@ const char *sgemm_last_error(void);
 
 /* Library version as 10000*major + 100*minor + patch. */
 int sgemm_version(void);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 
 #ifdef __cplusplus
 }

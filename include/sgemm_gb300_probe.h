@@ -17,6 +17,12 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden symbol visibility; only the entry points
+ * declared here are exported. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 /*
  * Launch the FP32 FMA probe on `stream` (cudaStream_t as void*).
  *   packed      0: scalar fma.rn.f32;  1: packed fma.rn.f32x2 (two FMAs per
@@ -44,6 +50,10 @@ int64_t sgemm_probe_out_elems(void);
  * context stays usable.  Nothing faults, traps or hangs.
  */
 int sgemm_selftest_wait_timeout(int64_t limit_cycles, void *stream);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 
 #ifdef __cplusplus
 }

@@ -1,7 +1,7 @@
 """Host-side checks of the C ABI that need no GPU.
 
 * The shared library builds, loads and exports every function that
-  include/*.h declares, with the binding's signatures.
+  include/*.h declares, with the binding's signatures, and nothing else.
 * Invalid arguments are rejected with the documented status code before
   anything touches a device (so these calls are safe without a GPU), and
   no-op sizes succeed without a device.
@@ -47,6 +47,19 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in include/ but not exported"
         assert name in sg.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_library_exports_nothing_else(lib):
+    # built with hidden visibility: the kernels and helpers stay internal
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", sg.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    extra = sorted(exported - set(declared_functions()))
+    assert not extra, f"exported but not declared in include/: {extra[:10]}"
 
 
 def test_library_links_no_cublas(lib):
