@@ -258,6 +258,25 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
     return out
 
 
+def tf32_probe_tflops(torch, sg, dev, stream, iters=16384, reps=5):
+    """Measured TF32 tensor-pipe peak: the library's tcgen05.mma probe (one CTA
+    per SM, operands in shared memory), CUDA events, median of `reps`."""
+    out = torch.empty(sg.probe_out_elems(), dtype=torch.float32, device=dev)
+    sp = stream.cuda_stream
+    sg.probe_tf32_mma(256, out.data_ptr(), sp)
+    ts, flops = [], 0.0
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        flops = sg.probe_tf32_mma(iters, out.data_ptr(), sp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    ms = sorted(ts)[len(ts) // 2]
+    return flops / (ms * 1e-3) / 1e12
+
+
 def cpu_baseline(case, target_s: float):
     """Time the oracle as it stands on a bounded sample of rows of the workload."""
     import oracle
@@ -281,6 +300,43 @@ def cpu_baseline(case, target_s: float):
             "sample": f"{rows} of {M} rows of the {M}x{N}x{K} product "
                       f"({flops / 1e9:.1f} GFLOP, {t:.2f} s, fp64 accumulation)",
             "seconds": t}
+
+
+def cpu_baseline_workloads(target_s: float):
+    """The oracle as it stands on every named workload: the whole product when
+    it takes under about `target_s`, else its first rows (op(A) rows of any
+    layout), the rate then standing for the full product ("extrapolated")."""
+    import oracle
+    threads = oracle.default_threads()
+    out = {}
+    for name, w in workloads.WORKLOADS.items():
+        case = workloads.make_case(w)
+        M, N, K, batch = w.M, w.N, w.K, w.batch
+        A, B = case["A"], case["B"]
+
+        def run(rows):
+            t = time.perf_counter()
+            if batch == 1:
+                oracle.sgemm(A[0], B[0], rows, N, K, transA=w.transA, transB=w.transB,
+                             lda=case["lda"], ldb=case["ldb"], nthreads=threads)
+            else:
+                oracle.sgemm_strided_batched(A, B, rows, N, K, batch, transA=w.transA,
+                                             transB=w.transB, lda=case["lda"], ldb=case["ldb"],
+                                             strideA=A[0].size, strideB=B[0].size,
+                                             nthreads=threads)
+            return time.perf_counter() - t
+
+        probe = min(M, max(threads, 32))
+        t = run(probe)
+        rows = int(min(M, max(probe, probe * target_s / max(t, 1e-6))))
+        if rows != probe:
+            t = run(rows)
+        flops = 2.0 * rows * N * K * batch
+        out[name] = {"gflops": flops / t / 1e9, "rows": rows, "of_rows": M, "seconds": t,
+                     "extrapolated": rows < M,
+                     "full_product_s": workloads.flops(M, N, K, batch) / (flops / t)}
+        del case, A, B
+    return out
 
 
 # ------------------------------------------------------------------ reference arm
@@ -360,6 +416,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case, args.cpu_seconds)
+        if not args.no_workloads:
+            cpu["per_workload"] = cpu_baseline_workloads(0.3)
 
     nsets = ROTATING_SETS
     with torch.cuda.stream(stream):
@@ -500,6 +558,7 @@ def main():
         bf16 = peaks.get("bf16_tflops")
         tf32_peak = bf16 * TF32_PER_BF16 if bf16 else 1100.0
         tc_alg = flops / (tc_ms * 1e-3) / 1e12
+        tf32_probe = tf32_probe_tflops(torch, sg, dev, stream)
         tc = {
             "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
             "kernels": "split (2 launches) + tf32x3_gemm_kernel (128x256 or 128x128 tile by wave count, tcgen05 kind::tf32)",
@@ -511,7 +570,11 @@ def main():
                          "peak_source": ("measured bf16 burst x nominal TF32/BF16 ratio 1.1/2.25"
                                          if bf16 else "nominal dense TF32"),
                          "note": "achieved = tensor-pipe work (3 TF32 MMAs per product) / time of "
-                                 "the whole call, split kernels included"},
+                                 "the whole call, split kernels included",
+                         "peak_tf32_probe": tf32_probe,
+                         "frac_of_tf32_probe": 3 * tc_alg / tf32_probe,
+                         "tf32_probe": "sgemm_probe_tf32_mma: back-to-back tcgen05.mma.kind::tf32 "
+                                       "M128 N256 K8 from shared memory, one CTA per SM"},
             "rrmse_vs_oracle": tc_rrmse,
             "device_status": status,
         }
@@ -644,7 +707,8 @@ def main():
     if table is not None:
         line["workloads"] = table
     if cpu is not None:
-        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                    "per_workload") if k in cpu}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -20,7 +20,7 @@ import threading
 __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32", "sgemm_f32_strided_batched",
            "status_string", "last_error", "version", "matmul", "SGEMM_OK",
-           "probe_fp32_fma", "probe_out_elems", "sgemm_f32_tf32x3",
+           "probe_fp32_fma", "probe_tf32_mma", "probe_out_elems", "sgemm_f32_tf32x3",
            "sgemm_f32_tf32x3_strided_batched", "tf32x3_workspace_size", "device_status",
            "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes", "sgemm_f32_tf32",
            "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
@@ -79,6 +79,7 @@ SIGNATURES = {
     "sgemm_f32_tf32x3_noalloc_max_bytes": (ctypes.c_uint64, []),
     "sgemm_probe_fp32_fma": (_int, [_int, _i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_probe_out_elems": (_i64, []),
+    "sgemm_probe_tf32_mma": (_int, [_i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_selftest_wait_timeout": (_int, [_i64, _vp]),
 }
 
@@ -276,6 +277,14 @@ def probe_fp32_fma(packed: int, iterations: int, out_ptr: int, stream=0) -> floa
     flops = ctypes.c_double(0.0)
     _check(load_library().sgemm_probe_fp32_fma(packed, iterations, out_ptr or None,
                                                ctypes.byref(flops), stream or None))
+    return flops.value
+
+
+def probe_tf32_mma(iterations: int, out_ptr: int, stream=0) -> float:
+    """Launch the TF32 tensor-pipe probe; returns the FLOPs of the launch."""
+    flops = ctypes.c_double(0.0)
+    _check(load_library().sgemm_probe_tf32_mma(iterations, out_ptr or None, ctypes.byref(flops),
+                                               stream or None))
     return flops.value
 
 

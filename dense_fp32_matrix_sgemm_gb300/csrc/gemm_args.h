@@ -41,6 +41,9 @@ cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset);
 cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t s);
+// TF32 tensor-pipe probe: `ctas` CTAs (one per SM), `iters` rounds each.
+cudaError_t launch_tf32_mma_probe(long long iters, float *out, int ctas, cudaStream_t s);
+double tf32_mma_probe_flops_per_iteration();
 
 // Plain single-term TF32 tensor-core product (hi only), same workspace scheme.
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s);

@@ -1,4 +1,5 @@
-// FP32 FMA throughput probe: the measured denominator of "% of FP32 peak".
+// Peak probes: FP32 FMA throughput (the measured denominator of "% of FP32
+// peak") and the TF32 tensor-pipe throughput of tcgen05.mma.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -65,6 +66,24 @@ extern "C" int sgemm_probe_fp32_fma(int packed, int64_t iterations, float *out, 
         sgemm::fp32_probe_kernel<false><<<(unsigned)ctas, sgemm::kThreads, 0, s>>>(out, iterations);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ELAUNCH;
     *flops_out = 2.0 * 2.0 * sgemm::kChains * (double)iterations * (double)ctas * sgemm::kThreads;
+    return SGEMM_OK;
+}
+
+extern "C" int sgemm_probe_tf32_mma(int64_t iterations, float *out, double *flops_out,
+                                    void *stream) {
+    if (iterations <= 0 || iterations > (1 << 20)) return SGEMM_EINVAL_DIM;
+    if (out == nullptr || flops_out == nullptr) return SGEMM_EINVAL_PTR;
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        sms <= 0 || major * 10 + minor != 103)
+        return SGEMM_EDEVICE;
+    if (sgemm::launch_tf32_mma_probe(iterations, out, sms, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return SGEMM_ELAUNCH;
+    *flops_out = sgemm::tf32_mma_probe_flops_per_iteration() * (double)iterations * (double)sms;
     return SGEMM_OK;
 }
 

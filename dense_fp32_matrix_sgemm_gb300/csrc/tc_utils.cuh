@@ -101,12 +101,6 @@ __device__ __forceinline__ void bulk_wait_group_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
 }
 
-// Until at most N of this thread's bulk groups are incomplete (writes done).
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-    asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -317,7 +317,9 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 tc::bulk_commit_group();
             }
         }
-        if (lane == 0 && c > 0) tc::bulk_wait_group<0>();
+        // the staging buffers must be read before the CTA's shared memory is
+        // released; the global writes complete with the kernel
+        if (lane == 0 && c > 0) tc::bulk_wait_group_read<0>();
         __syncwarp();
     } else if (go) {
         const int row = m0 + 32 * warp + lane;
@@ -386,6 +388,83 @@ __global__ void wait_timeout_selftest_kernel(long long limit) {
     const bool ok = tc::mbar_wait(b, 0, &abort_word, limit);
     __syncthreads();
     if (threadIdx.x == 0 && (!ok || abort_word)) atomicOr(&g_tf32x3_error, 1u);
+}
+
+// ------------------------------------------------------------------ TF32 probe
+
+// Tensor-pipe throughput probe for kind::tf32: every CTA (one per SM) issues
+// `iters` rounds of four M128 N256 K8 MMAs on operand tiles that stay in
+// shared memory (128-byte swizzle, as the GEMM's 32-float slices), all
+// accumulating into one 256-column TMEM accumulator; no global traffic.  The
+// single issuing thread is held back by the MMA queue, not by a spin.  The
+// completion wait is bounded; if it runs out the CTA raises the status word
+// and waits once more before freeing TMEM.
+constexpr int kProbeA = BM * 128;          // 128 rows x 32 fp32
+constexpr int kProbeB = 256 * 128;         // 256 rows x 32 fp32
+constexpr int kProbeSmem = kProbeA + kProbeB + 1024 + 64;
+
+__global__ void __launch_bounds__(THREADS, 1) tf32_mma_probe_kernel(long long iters, float *out) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
+    const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
+    uint8_t *smem = smem_raw + pad;
+    float *ops = reinterpret_cast<float *>(smem);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kProbeA + kProbeB);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 1);
+    const uint32_t bar_addr = tc::smem_u32_generic(bar);
+    const int warp = threadIdx.x >> 5;
+
+    // small TF32 values (low 13 bits zero), so the accumulator stays finite
+    for (int i = threadIdx.x; i < (kProbeA + kProbeB) / 4; i += blockDim.x)
+        ops[i] = (float)((i * 7) % 17 - 8) * 0.0078125f;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar_addr, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), 256);
+    // the operand tiles were written by the generic proxy; the MMAs read them
+    // through the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t base = tc::smem_u32_generic(smem);
+
+    if (warp == 1 && (threadIdx.x & 31) == 0) {
+        constexpr uint32_t idesc = tc::tf32_idesc<BM, 256>();
+        const uint64_t adesc = tc::kmajor_desc<128>(base);
+        const uint64_t bdesc = tc::kmajor_desc<128>(base + kProbeA);
+        for (long long it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t step = (uint64_t)(kk * 32) >> 4;
+                tc::mma_tf32(tmem, adesc + step, bdesc + step, idesc, (it | kk) ? 1u : 0u);
+            }
+        }
+        tc::mma_commit(bar_addr);
+    }
+    __syncwarp();
+    // every thread waits for the MMAs (bounded); nothing sets an abort word here
+    int never = 0;
+    bool done = tc::mbar_wait(bar_addr, 0, &never);
+    if (!done) {
+        if (threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
+        never = 0;
+        done = tc::mbar_wait(bar_addr, 0, &never);
+    }
+    tc::fence_after_sync();
+    if (warp == 0 && __all_sync(0xffffffffu, done)) {
+        float v[32];
+        tc::tmem_ld_32(tmem, v);   // lanes 0-31, columns 0-31
+        if ((threadIdx.x & 31) == 0) out[blockIdx.x] = v[0];
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 256);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -576,6 +655,24 @@ cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, c
     return tc_wide_tile(a) ? tf32x3::launch<Tf32Wide>(a, transA, transB, ws, s)
                            : tf32x3::launch<Tf32Narrow>(a, transA, transB, ws, s);
 }
+
+cudaError_t launch_tf32_mma_probe(long long iters, float *out, int ctas, cudaStream_t s) {
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(tf32x3::tf32_mma_probe_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tf32x3::kProbeSmem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    tf32x3::tf32_mma_probe_kernel<<<ctas, tf32x3::THREADS, tf32x3::kProbeSmem, s>>>(iters, out);
+    return cudaGetLastError();
+}
+
+double tf32_mma_probe_flops_per_iteration() { return 4.0 * 2.0 * tf32x3::BM * 256 * 8; }
 
 cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t s) {
     tf32x3::wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(limit_cycles);

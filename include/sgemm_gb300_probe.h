@@ -1,5 +1,6 @@
 /*
- * sgemm_gb300_probe.h -- measuring the FP32 peak that SGEMM is judged against.
+ * sgemm_gb300_probe.h -- measuring the FP32 and TF32 peaks that SGEMM is judged
+ * against.
  *
  * The peak of a GPU's FP32 units is cores x 2 FLOP (one FMA) x clock
  * (DD2360 workbook, section 3, worked example on the T4's FP32 peak).  This
@@ -40,6 +41,24 @@ int sgemm_probe_fp32_fma(int packed, int64_t iterations, float *out, double *flo
 
 /* Number of floats `out` must hold on the current device. */
 int64_t sgemm_probe_out_elems(void);
+
+/*
+ * Launch the TF32 tensor-pipe probe on `stream`: one CTA per SM issues
+ * `iterations` rounds of four tcgen05.mma.kind::tf32 M128 N256 K8 (the
+ * tensor-core path's wide-tile MMA) on operand tiles held in shared memory,
+ * accumulating in tensor memory, with no global traffic.  The caller times the
+ * launch and divides *flops_out by the time: the measured TF32 peak that the
+ * 3xTF32 path's tensor-pipe work is compared with.  The pages have no
+ * counterpart; they quote TF32 throughput only for a whole GEMM.
+ *   iterations  1 .. 2^20 (2^20 rounds take about 0.3 s).
+ *   out         device buffer of at least sgemm_probe_out_elems() floats;
+ *               receives one accumulator value per CTA (finite when the work
+ *               was done).
+ *   flops_out   host pointer; receives the FLOPs of one launch.
+ * SGEMM_EDEVICE unless the current device is sm_103.  If the completion wait
+ * runs out, bit 0 of the device status word is set (sgemm_device_status).
+ */
+int sgemm_probe_tf32_mma(int64_t iterations, float *out, double *flops_out, void *stream);
 
 /*
  * Self-test of the library's failure path (no counterpart on the source

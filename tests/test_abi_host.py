@@ -127,3 +127,15 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sg, "_LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(sg.SgemmUnavailable):
         sg.sgemm_f32(4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4)
+
+
+def test_probe_arguments_rejected_on_host(lib):
+    flops = ctypes.c_double(0.0)
+    probe = lib.sgemm_probe_tf32_mma
+    assert probe(0, ctypes.c_void_p(FAKE), ctypes.byref(flops), None) == 1
+    assert probe((1 << 20) + 1, ctypes.c_void_p(FAKE), ctypes.byref(flops), None) == 1
+    assert probe(10, None, ctypes.byref(flops), None) == 3
+    assert probe(10, ctypes.c_void_p(FAKE), None, None) == 3
+    fma = lib.sgemm_probe_fp32_fma
+    assert fma(2, 10, ctypes.c_void_p(FAKE), ctypes.byref(flops), None) == 1
+    assert fma(1, 0, ctypes.c_void_p(FAKE), ctypes.byref(flops), None) == 1

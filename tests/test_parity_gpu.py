@@ -517,6 +517,26 @@ def test_bounded_wait_gives_up_and_reports():
     assert sg.device_status() == 0
 
 
+def test_tf32_tensor_probe_runs_and_reports():
+    """The TF32 tensor-pipe probe does its work (a finite accumulator per CTA),
+    leaves the status word clear, and measures a rate between the tensor
+    path's own throughput and the nominal dense TF32 peak with margin."""
+    import torch
+    out = torch.full((sg.probe_out_elems(),), float("nan"), device="cuda")
+    assert sg.device_status(reset=True) == 0
+    sg.probe_tf32_mma(64, out.data_ptr())                  # warm-up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    flops = sg.probe_tf32_mma(8192, out.data_ptr())
+    b.record()
+    torch.cuda.synchronize()
+    tflops = flops / (a.elapsed_time(b) * 1e-3) / 1e12
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert torch.isfinite(out[:sms]).all()
+    assert sg.device_status() == 0
+    assert 200 < tflops < 1500, tflops
+
+
 def test_matmul_convenience_epilogue_and_splitk():
     import torch
     torch.manual_seed(1)
