@@ -462,6 +462,7 @@ def main():
             dist.barrier()
     clocks = clk.summary()
     durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms
+
     total_ms = reduce_max_over_ranks(sum(durs), dev)
     ms_per_step = total_ms / args.steps
     value = weak_scaling_tflops(flops, args.steps, total_ms, world)
@@ -512,6 +513,22 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1), dev) / e2e_steps
+
+    # cold L2: the same call after writing a 512 MiB buffer on the same stream
+    # before each step (the flush sits outside the events around the call)
+    flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
+    cold_steps = max(5, min(args.steps, 20))
+    c0 = [torch.cuda.Event(enable_timing=True) for _ in range(cold_steps)]
+    c1 = [torch.cuda.Event(enable_timing=True) for _ in range(cold_steps)]
+    for i in range(cold_steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(float(i))
+        c0[i].record(stream)
+        step(i)
+        c1[i].record(stream)
+    torch.cuda.synchronize(dev)
+    cold = sorted(a.elapsed_time(b) for a, b in zip(c0, c1))
+    del flush
     h2d = (case["A"].size + case["B"].size) * 4
     d2h = batch * M * ldc * 4
 
@@ -626,12 +643,23 @@ def main():
         def gemv():
             sg.sgemm_f32(gm, 1, gk, vA.data_ptr(), gk, vx.data_ptr(), 1, vy.data_ptr(), 1, 0, 0, sp)
 
+        def colsum():   # M = 1: y = x^T B with B (the same 8192 x 8192 buffer) row-major
+            sg.sgemm_f32(1, gm, gk, vx.data_ptr(), gk, vA.data_ptr(), gm, vy.data_ptr(), gm, 0, 0,
+                         sp)
+
         t_gemv = timed(gemv)
+        t_colsum = timed(colsum)
         gbytes = 4.0 * (gm * gk + gk + gm)
         hbm = float(measured_peaks().get("hbm_gbs") or 6787.0)
         gemv_line = {"shape": [gm, 1, gk], "ms": t_gemv, "gbs": gbytes / (t_gemv * 1e-3) / 1e9,
                      "frac_of_hbm": gbytes / (t_gemv * 1e-3) / 1e9 / hbm,
-                     "hbm_peak_gbs": hbm, "bound": "hbm"}
+                     "hbm_peak_gbs": hbm, "bound": "hbm",
+                     "kernel": "gemv_dot_kernel (N = 1, A row-major: two rows per warp)",
+                     "colsum": {"shape": [1, gm, gk], "ms": t_colsum,
+                                "gbs": gbytes / (t_colsum * 1e-3) / 1e9,
+                                "frac_of_hbm": gbytes / (t_colsum * 1e-3) / 1e9 / hbm,
+                                "kernel": "gemv_colsum_kernel (M = 1, B row-major: K split over "
+                                          "warps and a CTA cluster)"}}
         del vA, vx, vy
 
     # every named workload on both FP32-accuracy paths (not the timed step)
@@ -696,6 +724,13 @@ def main():
                 "method": "pinned host A, B -> device, sgemm_f32, C -> pinned host, every step; "
                           "two buffer sets on upload/compute/download streams, CUDA events"},
         "gpu_launches": args.steps,
+        "timing": {"mean_ms": ms_per_step, "median_ms": sorted(durs)[len(durs) // 2],
+                   "min_ms": min(durs), "max_ms": max(durs),
+                   "cold_l2": {"median_ms": cold[len(cold) // 2],
+                               "tflops": flops / (cold[len(cold) // 2] * 1e-3) / 1e12,
+                               "steps": cold_steps, "flush_bytes": 512 * 2**20,
+                               "method": "512 MiB written on the stream before each call, "
+                                         "outside the call's events"}},
         "wall_s": wall,
     }
     if tc is not None:

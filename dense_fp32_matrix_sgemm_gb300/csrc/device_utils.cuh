@@ -72,4 +72,13 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t local, uint32_t rank) {
     return v;
 }
 
+// 4-byte load from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(local), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 }  // namespace sgemm

@@ -618,3 +618,23 @@ def test_tensor_store_edges_exact(entry_name, M, N, K):
                                    key=600 + M + N + K)
     got = run(case, entry=entry_name)
     check_full(case, got, exact=True, label=f"{entry_name} {M}x{N}x{K}")
+
+
+# Column-sum matrix-vector kernel (M == 1 with row-major B, N == 1 with A
+# stored transposed): K split over 16 or 32 warps and a cluster of 1-8 CTAs,
+# each thread 8 outputs with 16-byte loads (1 otherwise).  Exact on integers.
+@pytest.mark.parametrize("M,N,K,batch,tA,offset", [
+    (1, 8191, 4096, 1, 0, 0),      # 16 warps, clusters of 8, ragged last thread
+    (1, 1000, 8192, 1, 0, 0),      # 32 warps
+    (1, 300, 40, 1, 0, 0),         # K too short to split: cluster of 1, idle warps
+    (1, 2050, 700, 3, 0, 0),       # batched
+    (1, 777, 3000, 1, 0, 1),       # misaligned: one output per thread
+    (2049, 1, 1537, 1, 1, 0),      # N == 1 with A stored transposed
+    (3000, 1, 5000, 2, 1, 3),      # the same, batched and misaligned
+])
+def test_gemv_colsum_cluster_exact(M, N, K, batch, tA, offset):
+    case = workloads.make_operands(M, N, K, batch=batch, transA=tA, dist="int", seed=70,
+                                   key=700 + M + N + K)
+    entry = "sgemm_f32_strided_batched" if batch > 1 else "sgemm_f32"
+    check_full(case, run(case, entry=entry, offset=offset), exact=True,
+               label=f"colsum {batch}x{M}x{N}x{K} tA={tA} offset={offset}")
