@@ -165,7 +165,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "sgemm_simt_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh",
                           "simt_nn.cu"],
-    "tf32x3_gemm_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
+    "tf32x3_persistent_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
 }
 
 
@@ -578,12 +578,14 @@ def main():
         tf32_probe = tf32_probe_tflops(torch, sg, dev, stream)
         tc = {
             "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
-            "kernels": "split (2 launches) + tf32x3_gemm_kernel (128x256 or 128x128 tile by wave count, tcgen05 kind::tf32)",
+            "kernels": "split (2 launches) + tf32x3_persistent_kernel (one CTA per SM; 128x256 or "
+                       "128x128 tiles by wave count; TMA ring, tcgen05 kind::tf32, TMEM, TMA-store "
+                       "epilogue)",
             "gpu_launches_per_step": 3,
             "pct_of_fp32_peak_at_max_clock": None,
             "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_peak,
                          "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_peak,
-                         "traffic": profiled_traffic("tf32x3_gemm_kernel", args.workload),
+                         "traffic": profiled_traffic("tf32x3_persistent_kernel", args.workload),
                          "peak_source": ("measured bf16 burst x nominal TF32/BF16 ratio 1.1/2.25"
                                          if bf16 else "nominal dense TF32"),
                          "note": "achieved = tensor-pipe work (3 TF32 MMAs per product) / time of "

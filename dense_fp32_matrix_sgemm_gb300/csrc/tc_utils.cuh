@@ -27,6 +27,11 @@ __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// One arrival on `bar` (release semantics for this thread's earlier writes).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(bar), "r"(bytes) : "memory");

@@ -13,20 +13,20 @@
 //   workspace as K-major planes [batch][TERMS == 3 ? hi|lo : hi][rows][Kp]
 //   (Kp = K rounded up to 4 so rows are 16-byte aligned for TMA).  M- or
 //   N-major operands are corner-turned through a padded shared tile.
-// Stage 2 (GEMM kernel, one 128 x BN output tile per CTA, BN = 256 or 128
-//   picked per problem by counting waves, 128 threads):
+// Stage 2 (persistent GEMM kernel, one CTA per SM walking 128 x BN output
+//   tiles, BN = 256 or 128 picked per problem; 192 threads in three roles):
 //   warp 0 / lane 0 issues TMA loads of the swizzled K slices (BK fp32 of K,
-//   swizzle span = BK * 4 bytes:
-//   A planes 128 rows, B planes BN rows) into a STAGES-deep ring; warp 1
-//   owns the TMEM accumulators and lane 0 issues TERMS MMAs (M128 N=BN K8)
-//   per 8-wide K step, releasing each stage with tcgen05.commit; after the
-//   last commit all four warps read their 32 TMEM lanes (= tile rows) 32
-//   columns at a time and add the accumulators.  For the plain product into
-//   a 16-byte-aligned C with N a multiple of 4, each warp writes its 32 x 32
-//   block into shared memory (the now idle operand ring; 128-byte swizzle,
-//   two buffers per warp) and one lane stores it with a TMA tensor store,
-//   which writes whole rows and clips the ragged edges; otherwise the threads
-//   store their own rows.
+//   swizzle span = BK * 4 bytes; A planes 128 rows, B planes BN rows) into a
+//   STAGES-deep ring that runs on across tiles; warp 1 owns TMEM and its lane
+//   0 issues TERMS MMAs (M128 N=BN K8) per 8-wide K step into one of two
+//   accumulator buffers where they fit, releasing each stage with
+//   tcgen05.commit; warps 2-5 drain a finished accumulator 32 columns at a
+//   time, add the two accumulators and store the tile while the MMAs of the
+//   next one run.  For the plain product into a 16-byte-aligned C with N a
+//   multiple of 4, each warp writes its 32 x 32 block into its own shared
+//   staging buffers (128-byte swizzle, two per warp) and one lane stores it
+//   with a TMA tensor store, which writes whole rows and clips the ragged
+//   edges; otherwise the threads store their own rows.
 // The tensor cores add each MMA's partial sum into its fp32 accumulator with
 // a rounding that is biased towards zero, so the error of a long K grows with
 // the number of updates.  hi*hi therefore has an accumulator of its own (K/8
@@ -52,7 +52,7 @@ namespace sgemm {
 namespace tf32x3 {
 
 constexpr int BM = 128;
-constexpr int THREADS = 128;
+constexpr int THREADS = 128;   // the TF32 probe's CTA
 
 template <int BK_, int STAGES_, int TERMS_, int BN_ = 256>
 struct Config {
@@ -66,10 +66,7 @@ struct Config {
     static constexpr int A_TILE = BM * ROW_BYTES;
     static constexpr int B_TILE = BN * ROW_BYTES;
     static constexpr int STAGE_BYTES = PLANES * (A_TILE + B_TILE);
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-    static constexpr int TMEM_COLS = TERMS == 3 ? 2 * ACC_COLS : ACC_COLS;
     static_assert(BN == 128 || BN == 256, "tile width");
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 __device__ unsigned int g_tf32x3_error = 0;   // bit 0: a pipeline wait ran out
@@ -157,13 +154,13 @@ struct Tf32x3Params {
     int tiles_m, tiles_n, group_m;
     int vec_c;   // C rows allow 16-byte stores
     int tma_c;   // store C through the tmC tensor map (plain epilogue, aligned C)
+    int batch;
     float alpha, beta;      // epilogue C = alpha * acc + beta * C + bias[col]
     const float *bias;
 };
 
-__device__ __forceinline__ void raster(const Tf32x3Params &p, int &z, int &tm, int &tn) {
+__device__ __forceinline__ void raster(const Tf32x3Params &p, int bid, int &z, int &tm, int &tn) {
     const int per_batch = p.tiles_m * p.tiles_n;
-    const int bid = blockIdx.x;
     z = bid / per_batch;
     const int t = bid - z * per_batch;
     const int group = p.group_m * p.tiles_n;
@@ -175,124 +172,27 @@ __device__ __forceinline__ void raster(const Tf32x3Params &p, int &z, int &tm, i
     tn = r / rows;
 }
 
+// Stores the 32 tile rows held in TMEM lanes 32q..32q+31 of the accumulator
+// at `acc` (small-term accumulator ACC_COLS columns further) to C.  The
+// calling warp must be a warp whose TMEM lane quarter is q.
+//   TMA path (p.tma_c): 32 columns at a time through the warp's two 4 KB
+//   staging buffers at `stage` (1024-byte aligned; the 128-byte swizzle puts
+//   16-byte chunk j of row r at chunk j ^ (r & 7), so the eight rows a
+//   quarter-warp writes hit distinct banks), one TMA store per chunk issued by
+//   lane 0.  `cc` counts the chunks staged so far (across calls), picks the
+//   buffer and says when to wait for the store two chunks back.
+//   Otherwise: each thread stores its own row, with the epilogue applied.
 template <class CFG>
-__global__ void __launch_bounds__(THREADS, 1)
-tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
-    constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
+__device__ __forceinline__ void store_tile_rows(const Tf32x3Params &p, const CUtensorMap *tmC,
+                                                uint32_t acc, int q, int lane, int z, int m0,
+                                                int n0, uint32_t stage, int &cc) {
     constexpr int BN = CFG::BN, ACC_COLS = CFG::ACC_COLS;
-    constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled tiles
-    const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
-    const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
-    uint8_t *smem = smem_raw + pad;
-    const uint32_t tiles = tc::smem_u32_generic(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    const uint32_t full0 = tc::smem_u32_generic(bars);           // full[s]  = full0 + 8 s
-    const uint32_t empty0 = full0 + 8 * STAGES;                    // empty[s] = empty0 + 8 s
-    const uint32_t done_bar = empty0 + 8 * STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int z, tm, tn;
-    raster(p, z, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
-    const int kblocks = (p.K + BK - 1) / BK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(full0 + 8 * s, 1);
-            tc::mbar_init(empty0 + 8 * s, 1);
-        }
-        tc::mbar_init(done_bar, 1);
-        *abort_flag = 0;
-        tc::fence_barrier_init();
-        tc::tma_prefetch_desc(&tmA);
-        tc::tma_prefetch_desc(&tmB);
-    }
-    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), CFG::TMEM_COLS);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-
-    // stage layout: A planes (hi[, lo]) then B planes (hi[, lo])
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer
-        int issued = 0;
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % STAGES;
-            if (kb >= STAGES && !tc::mbar_wait(empty0 + 8 * s, ((kb / STAGES) & 1) ^ 1, abort_flag))
-                break;
-            const uint32_t st = tiles + s * STAGE_BYTES;
-            const uint32_t fb = full0 + 8 * s;
-            tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            const int k0 = kb * BK;
-#pragma unroll
-            for (int pl = 0; pl < PLANES; ++pl) {
-                tc::tma_load_3d(st + pl * A_TILE, &tmA, fb, k0, m0, PLANES * z + pl);
-                tc::tma_load_3d(st + PLANES * A_TILE + pl * B_TILE, &tmB, fb, k0, n0,
-                                PLANES * z + pl);
-            }
-            issued = kb + 1;
-        }
-        if (*abort_flag) {
-            // let this thread's copies in flight land before the CTA exits
-            for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb) {
-                const int s = kb % STAGES;
-                const long long t0 = clock64();
-                while (!tc::mbar_try_wait(full0 + 8 * s, (kb / STAGES) & 1) &&
-                       clock64() - t0 < tc::kWaitLimitCycles) {
-                }
-            }
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
-        constexpr uint32_t idesc = tc::tf32_idesc<BM, BN>();
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % STAGES;
-            if (!tc::mbar_wait(full0 + 8 * s, (kb / STAGES) & 1, abort_flag)) break;
-            tc::fence_after_sync();
-            const uint32_t st = tiles + s * STAGE_BYTES;
-            const uint64_t ahi = tc::kmajor_desc<CFG::ROW_BYTES>(st);
-            const uint64_t bhi = tc::kmajor_desc<CFG::ROW_BYTES>(st + PLANES * A_TILE);
-#pragma unroll
-            for (int kk = 0; kk < BK / 8; ++kk) {
-                const uint64_t step = (uint64_t)(kk * 32) >> 4;   // 8 tf32 = 32 bytes along K
-                const uint32_t acc = (kb == 0 && kk == 0) ? 0u : 1u;
-                if constexpr (CFG::TERMS == 3) {
-                    const uint64_t alo = tc::kmajor_desc<CFG::ROW_BYTES>(st + A_TILE);
-                    const uint64_t blo = tc::kmajor_desc<CFG::ROW_BYTES>(st + 2 * A_TILE + B_TILE);
-                    tc::mma_tf32(tmem + ACC_COLS, alo + step, bhi + step, idesc, acc);
-                    tc::mma_tf32(tmem + ACC_COLS, ahi + step, blo + step, idesc, 1u);
-                }
-                tc::mma_tf32(tmem, ahi + step, bhi + step, idesc, acc);
-            }
-            tc::mma_commit(empty0 + 8 * s);
-        }
-        tc::mma_commit(done_bar);   // tracks every MMA issued above, also on abort
-    }
-    __syncwarp();
-
-    // ---------------- epilogue: TMEM lane (32*warp + lane) holds tile row m0 + 32*warp + lane
-    const bool ok = tc::mbar_wait(done_bar, 0, abort_flag);
-    __syncwarp();   // reconverge before the warp-collective TMEM loads
-    tc::fence_after_sync();
-    // one warp-uniform decision: the TMEM loads below are warp-collective
-    const bool go = __all_sync(0xffffffffu, ok && !*abort_flag);
-    if (go && p.tma_c) {
-        // Warp w stages rows 32w..32w+31 of the tile, 32 columns at a time, in
-        // two 4 KB buffers at ring offset 8 KB * w (1024-byte aligned: the
-        // 128-byte swizzle puts 16-byte chunk j of row r at chunk j ^ (r & 7),
-        // so the eight rows a quarter-warp writes hit distinct banks).
-        const uint32_t stage = tiles + (uint32_t)warp * 8192u;
-        const int row0 = m0 + 32 * warp;
-        int c = 0;
-        for (; row0 < p.M && c < BN / 32 && n0 + 32 * c < p.N; ++c) {
+    const uint32_t lane_base = acc + ((uint32_t)(32 * q) << 16);
+    if (p.tma_c) {
+        const int row0 = m0 + 32 * q;
+        for (int c = 0; row0 < p.M && c < BN / 32 && n0 + 32 * c < p.N; ++c, ++cc) {
             float v[32];
-            const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c);
+            const uint32_t ta = lane_base + (uint32_t)(32 * c);
             tc::tmem_ld_32(ta, v);
             if constexpr (CFG::TERMS == 3) {
                 float w[32];
@@ -300,9 +200,9 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] += w[j];
             }
-            const uint32_t buf = stage + (uint32_t)(c & 1) * 4096u;
-            if (c >= 2) {
-                if (lane == 0) tc::bulk_wait_group_read<1>();   // the store of chunk c-2 has read it
+            const uint32_t buf = stage + (uint32_t)(cc & 1) * 4096u;
+            if (cc >= 2) {
+                if (lane == 0) tc::bulk_wait_group_read<1>();   // the store of chunk cc-2 has read it
                 __syncwarp();
             }
             const uint32_t rbase = buf + (uint32_t)lane * 128u;
@@ -313,59 +213,245 @@ tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tc::tma_store_3d(&tmC, buf, n0 + 32 * c, row0, z);
+                tc::tma_store_3d(tmC, buf, n0 + 32 * c, row0, z);
                 tc::bulk_commit_group();
             }
         }
-        // the staging buffers must be read before the CTA's shared memory is
-        // released; the global writes complete with the kernel
-        if (lane == 0 && c > 0) tc::bulk_wait_group_read<0>();
-        __syncwarp();
-    } else if (go) {
-        const int row = m0 + 32 * warp + lane;
-        float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
+        return;
+    }
+    const int row = m0 + 32 * q + lane;
+    float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c);
-            tc::tmem_ld_32(ta, v);
-            if constexpr (CFG::TERMS == 3) {
-                float w[32];
-                tc::tmem_ld_32(ta + ACC_COLS, w);
+    for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        const uint32_t ta = lane_base + (uint32_t)(32 * c);
+        tc::tmem_ld_32(ta, v);
+        if constexpr (CFG::TERMS == 3) {
+            float w[32];
+            tc::tmem_ld_32(ta + ACC_COLS, w);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] += w[j];
+            for (int j = 0; j < 32; ++j) v[j] += w[j];
+        }
+        if (row < p.M) {
+            const int col0 = n0 + 32 * c;
+            if (!(p.alpha == 1.f && p.beta == 0.f && p.bias == nullptr)) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = col0 + j;
+                    const float old = (p.beta != 0.f && col < p.N) ? crow[col] : 0.f;
+                    const float b = (p.bias != nullptr && col < p.N) ? p.bias[col] : 0.f;
+                    v[j] = fmaf(p.beta, old, p.alpha * v[j]) + b;
+                }
             }
-            if (row < p.M) {
-                const int col0 = n0 + 32 * c;
-                if (!(p.alpha == 1.f && p.beta == 0.f && p.bias == nullptr)) {
+            if (p.vec_c && col0 + 31 < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = col0 + j;
-                        const float old = (p.beta != 0.f && col < p.N) ? crow[col] : 0.f;
-                        const float b = (p.bias != nullptr && col < p.N) ? p.bias[col] : 0.f;
-                        v[j] = fmaf(p.beta, old, p.alpha * v[j]) + b;
-                    }
-                }
-                if (p.vec_c && col0 + 31 < p.N) {
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(crow + col0 + j) =
+                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            } else {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(crow + col0 + j) =
-                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (col0 + j < p.N) crow[col0 + j] = v[j];
-                }
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N) crow[col0 + j] = v[j];
             }
         }
     }
+}
+
+// ------------------------------------------------------------------ GEMM
+
+// Persistent GEMM kernel: one CTA per SM walks tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... with warp-specialised roles.
+//   warp 0, lane 0: TMA producer; the ring runs on across tile boundaries,
+//                   so the next tile's slices load while this one finishes;
+//   warp 1, lane 0: MMA issuer, into accumulator buffer i % ACC_BUFS; warp 1
+//                   allocates and frees TMEM;
+//   warps 2-5:      epilogue, warp w draining TMEM lane quarter w % 4 through
+//                   its own staging buffers (outside the ring), then arriving
+//                   on the buffer's "empty" barrier.
+// With ACC_BUFS = 2 the MMAs of tile i+1 overlap the epilogue of tile i; the
+// 128 x 256 three-term tile needs all 512 TMEM columns for one tile
+// (ACC_BUFS = 1), and there only the next tile's loads overlap its epilogue.
+// Barrier phases: a ring stage's j-th fill is waited on with parity j & 1 and
+// its (j-1)-th release with parity (j-1) & 1; accumulator buffer b's u-th
+// result likewise.  Every wait is bounded and the abort word stops all roles.
+constexpr int PTHREADS = 192;
+
+template <class CFG, int ACC_BUFS>
+struct Persist {
+    static constexpr int BUF_COLS = CFG::TERMS == 3 ? 2 * CFG::BN : CFG::BN;
+    static constexpr int TMEM_COLS = ACC_BUFS * BUF_COLS <= 256 ? 256 : 512;
+    static constexpr int STAGING = 4 * 8192;   // 4 epilogue warps x two 4 KB buffers
+    static constexpr int BARS = 2 * CFG::STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int SMEM_BYTES = CFG::STAGES * CFG::STAGE_BYTES + STAGING + 1024 + 256;
+    static_assert(ACC_BUFS * BUF_COLS <= 512, "accumulators exceed tensor memory");
+    static_assert(BARS * 8 + 8 <= 256, "barrier area");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+template <class CFG, int ACC_BUFS>
+__global__ void __launch_bounds__(PTHREADS, 1)
+tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
+    using P = Persist<CFG, ACC_BUFS>;
+    constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
+    constexpr int BN = CFG::BN, ACC_COLS = CFG::ACC_COLS;
+    constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
+    const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t ring = tc::smem_u32_generic(smem);
+    const uint32_t staging = ring + STAGES * STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + P::STAGING);
+    const uint32_t full0 = tc::smem_u32_generic(bars);
+    const uint32_t empty0 = full0 + 8 * STAGES;
+    const uint32_t accf0 = empty0 + 8 * STAGES;     // accumulator b holds a finished tile
+    const uint32_t acce0 = accf0 + 8 * ACC_BUFS;    // accumulator b has been drained
+    const uint32_t done_bar = acce0 + 8 * ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + P::BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.batch * p.tiles_m * p.tiles_n;
+    const int nlocal = ((int)blockIdx.x < total) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int kblocks = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < ACC_BUFS; ++b) {
+            tc::mbar_init(accf0 + 8 * b, 1);
+            tc::mbar_init(acce0 + 8 * b, 4);   // one arrival per epilogue warp
+        }
+        tc::mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), P::TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            long long issued = 0;
+            bool stop = false;
+            for (int i = 0; i < nlocal && !stop; ++i) {
+                int z, tm, tn;
+                raster(p, (int)blockIdx.x + i * (int)gridDim.x, z, tm, tn);
+                const int m0 = tm * BM, n0 = tn * BN;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const long long g = (long long)i * kblocks + kb;
+                    const int s = (int)(g % STAGES);
+                    const int j = (int)(g / STAGES);
+                    if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * s, (j & 1) ^ 1, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t st = ring + s * STAGE_BYTES;
+                    const uint32_t fb = full0 + 8 * s;
+                    tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    const int k0 = kb * BK;
+#pragma unroll
+                    for (int pl = 0; pl < PLANES; ++pl) {
+                        tc::tma_load_3d(st + pl * A_TILE, &tmA, fb, k0, m0, PLANES * z + pl);
+                        tc::tma_load_3d(st + PLANES * A_TILE + pl * B_TILE, &tmB, fb, k0, n0,
+                                        PLANES * z + pl);
+                    }
+                    issued = g + 1;
+                }
+            }
+            if (*abort_flag) {
+                // let this thread's copies in flight land before the CTA exits
+                for (long long g = (issued > STAGES ? issued - STAGES : 0); g < issued; ++g) {
+                    const int s = (int)(g % STAGES);
+                    const long long t0 = clock64();
+                    while (!tc::mbar_try_wait(full0 + 8 * s, (int)((g / STAGES) & 1)) &&
+                           clock64() - t0 < tc::kWaitLimitCycles) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = tc::tf32_idesc<BM, BN>();
+            bool stop = false;
+            for (int i = 0; i < nlocal && !stop; ++i) {
+                const int b = i % ACC_BUFS, u = i / ACC_BUFS;
+                if (i >= ACC_BUFS && !tc::mbar_wait(acce0 + 8 * b, (u - 1) & 1, abort_flag)) break;
+                tc::fence_after_sync();
+                const uint32_t acc = tmem + (uint32_t)(b * P::BUF_COLS);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const long long g = (long long)i * kblocks + kb;
+                    const int s = (int)(g % STAGES);
+                    if (!tc::mbar_wait(full0 + 8 * s, (int)((g / STAGES) & 1), abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t st = ring + s * STAGE_BYTES;
+                    const uint64_t ahi = tc::kmajor_desc<CFG::ROW_BYTES>(st);
+                    const uint64_t bhi = tc::kmajor_desc<CFG::ROW_BYTES>(st + PLANES * A_TILE);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        const uint64_t step = (uint64_t)(kk * 32) >> 4;
+                        const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
+                        if constexpr (CFG::TERMS == 3) {
+                            const uint64_t alo = tc::kmajor_desc<CFG::ROW_BYTES>(st + A_TILE);
+                            const uint64_t blo =
+                                tc::kmajor_desc<CFG::ROW_BYTES>(st + 2 * A_TILE + B_TILE);
+                            tc::mma_tf32(acc + ACC_COLS, alo + step, bhi + step, idesc, first);
+                            tc::mma_tf32(acc + ACC_COLS, ahi + step, blo + step, idesc, 1u);
+                        }
+                        tc::mma_tf32(acc, ahi + step, bhi + step, idesc, first);
+                    }
+                    tc::mma_commit(empty0 + 8 * s);
+                }
+                if (!stop) tc::mma_commit(accf0 + 8 * b);
+            }
+            tc::mma_commit(done_bar);   // tracks every MMA issued above, also on abort
+        }
+    } else {
+        // ---------------- epilogue warps 2-5: TMEM lane quarter warp % 4
+        const int q = warp & 3;
+        const uint32_t stage = staging + (uint32_t)(warp - 2) * 8192u;
+        int cc = 0;
+        for (int i = 0; i < nlocal; ++i) {
+            const int b = i % ACC_BUFS, u = i / ACC_BUFS;
+            const bool ok = tc::mbar_wait(accf0 + 8 * b, u & 1, abort_flag);
+            __syncwarp();
+            // one warp-uniform decision: the TMEM loads are warp-collective
+            if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
+            tc::fence_after_sync();
+            int z, tm, tn;
+            raster(p, (int)blockIdx.x + i * (int)gridDim.x, z, tm, tn);
+            store_tile_rows<CFG>(p, &tmC, tmem + (uint32_t)(b * P::BUF_COLS), q, lane, z, tm * BM,
+                                 tn * BN, stage, cc);
+            tc::fence_before_sync();   // the TMEM loads above precede the release
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(acce0 + 8 * b);
+        }
+        if (lane == 0 && cc > 0) tc::bulk_wait_group_read<0>();
+    }
+    __syncwarp();
     if (*abort_flag && threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
 
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
+        // every MMA issued has completed before TMEM is freed
+        int local_abort = 0;
+        (void)tc::mbar_wait(done_bar, 0, &local_abort);
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, CFG::TMEM_COLS);
+        tc::tmem_dealloc(tmem, P::TMEM_COLS);
     }
 }
 
@@ -528,8 +614,11 @@ size_t plane_bytes(int64_t rows, int64_t K, int64_t batch, int planes) {
     return align_up((size_t)planes * (size_t)batch * (size_t)rows * Kp * 4, 256);
 }
 
+// Encodes the tensor maps, launches the two split kernels into `ws` and fills
+// the GEMM kernel's parameters: everything both GEMM kernels need.
 template <class CFG>
-cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s,
+                    CUtensorMap &tmA, CUtensorMap &tmB, CUtensorMap &tmC, Tf32x3Params &p) {
     constexpr int PLANES = CFG::PLANES;
     const int Kp = (a.K + 3) / 4 * 4;
     float *wsA = static_cast<float *>(ws);
@@ -537,24 +626,9 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
 
     // tensor maps first (they depend only on the workspace and the sizes), so
     // no host work separates the split launches from the GEMM launch
-    CUtensorMap tmA, tmB;
     if (!make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
         !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN))
         return cudaErrorInvalidValue;
-    {
-        // the opt-in shared-memory size is a per-device function attribute
-        static std::atomic<unsigned long long> configured{0};
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        const unsigned long long bit = 1ull << (dev & 63);
-        if (!(configured.load() & bit)) {
-            e = cudaFuncSetAttribute(tf32x3_gemm_kernel<CFG>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, CFG::SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            configured.fetch_or(bit);
-        }
-    }
 
     // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes
     auto split = [&](const float *X, int64_t ld, int64_t sX, int R, bool kcontig, float *out) {
@@ -579,14 +653,13 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // stage 2: the tensor-core GEMM
-    Tf32x3Params p;
     p.C = a.C;
     p.ldc = a.ldc;
     p.strideC = a.strideC;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
+    p.batch = a.batch;
     p.tiles_m = (a.M + BM - 1) / BM;
     p.tiles_n = (a.N + CFG::BN - 1) / CFG::BN;
     p.group_m = 8;
@@ -599,31 +672,71 @@ cudaError_t launch(const GemmArgs &a, bool transA, bool transB, void *ws, cudaSt
     // 16-byte granules: with N not a multiple of 4 the store was seen to
     // write the padding column next to column N-1, so such widths keep the
     // threads' own guarded stores.  The map is only read when tma_c is set.
-    CUtensorMap tmC = {};
+    tmC = CUtensorMap{};
     p.tma_c = p.vec_c && a.N % 4 == 0 && plain_epilogue(a) &&
               make_c_map(&tmC, a.C, a.M, a.N, a.ldc, a.strideC, a.batch);
-    const long long blocks = (long long)a.batch * p.tiles_m * p.tiles_n;
-    tf32x3_gemm_kernel<CFG><<<(unsigned)blocks, THREADS, CFG::SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
+    return cudaSuccess;
+}
+
+// Sets the opt-in dynamic shared-memory size of `kern` once per device.
+template <typename Kern>
+cudaError_t ensure_smem(Kern kern, int bytes, std::atomic<unsigned long long> &configured) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    return cudaSuccess;
+}
+
+// One CTA per SM, walking the tiles (see tf32x3_persistent_kernel).
+template <class CFG, int ACC_BUFS>
+cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void *ws,
+                              cudaStream_t s) {
+    using P = Persist<CFG, ACC_BUFS>;
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = ensure_smem(tf32x3_persistent_kernel<CFG, ACC_BUFS>, P::SMEM_BYTES, configured);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmA, tmB, tmC;
+    Tf32x3Params p;
+    e = prepare<CFG>(a, transA, transB, ws, s, tmA, tmB, tmC, p);
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
+    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+    tf32x3_persistent_kernel<CFG, ACC_BUFS><<<grid, PTHREADS, P::SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
     return cudaGetLastError();
 }
 
 }  // namespace tf32x3
 
-// Tuned configurations (K slice, stages, terms, tile width).  The ring is
-// latency-bound, so what counts is the bytes in flight: for the 128 x 256
-// tile, 3 of 4 stages of 48 KB (64-byte swizzle) beat 1 of 2 stages of 96 KB
-// by 13-16 %; the 128 x 128 tile does best with 32-float slices.
-using Tf32x3Wide = tf32x3::Config<16, 4, 3, 256>;
-using Tf32x3Narrow = tf32x3::Config<32, 3, 3, 128>;
-using Tf32Wide = tf32x3::Config<32, 4, 1, 256>;
-using Tf32Narrow = tf32x3::Config<32, 6, 1, 128>;
+// Tuned configurations (K slice, stages, terms, tile width) and accumulator
+// buffers.  The ring is latency-bound, so what counts is the bytes in flight:
+// for the 128 x 256 three-term tile, 4 stages of 48 KB (64-byte swizzle) beat 2
+// stages of 96 KB by 13-16 %; the 128 x 128 tile does best with 32-float slices.
+using Tf32x3Wide = tf32x3::Config<16, 4, 3, 256>;     // one accumulator buffer (512 columns)
+using Tf32x3Narrow = tf32x3::Config<32, 3, 3, 128>;   // two buffers of 256 columns
+using Tf32Wide = tf32x3::Config<32, 4, 1, 256>;       // two buffers of 256 columns
+using Tf32Narrow = tf32x3::Config<32, 6, 1, 128>;     // two buffers of 128 columns
 
 namespace {
 
 // A 128 x 256 tile costs about 1.75 128 x 128 tiles (8192 x 8192 x 4096,
-// where the wave tail is negligible); count waves of one CTA per SM and take
-// the cheaper tiling, the wide one on ties.
-bool tc_wide_tile(const GemmArgs &a) {
+// where the wave tail is negligible); count tiles per SM and take the cheaper
+// tiling, the wide one on ties.  For the three-term product a short K (at
+// most 256) takes the narrow tile whatever the count: only it has two
+// accumulator buffers, and with few K steps per tile the overlapped epilogue
+// matters most (96 x 512 x 512 x 64: 54.8 us narrow, 61.0 us wide).
+bool tc_wide_tile(const GemmArgs &a, int terms) {
+    if (terms == 3 && a.K <= 256) return false;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -647,13 +760,14 @@ size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
 }
 
 cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
-    return tc_wide_tile(a) ? tf32x3::launch<Tf32x3Wide>(a, transA, transB, ws, s)
-                           : tf32x3::launch<Tf32x3Narrow>(a, transA, transB, ws, s);
+    return tc_wide_tile(a, 3)
+               ? tf32x3::launch_persistent<Tf32x3Wide, 1>(a, transA, transB, ws, s)
+               : tf32x3::launch_persistent<Tf32x3Narrow, 2>(a, transA, transB, ws, s);
 }
 
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
-    return tc_wide_tile(a) ? tf32x3::launch<Tf32Wide>(a, transA, transB, ws, s)
-                           : tf32x3::launch<Tf32Narrow>(a, transA, transB, ws, s);
+    return tc_wide_tile(a, 1) ? tf32x3::launch_persistent<Tf32Wide, 2>(a, transA, transB, ws, s)
+                              : tf32x3::launch_persistent<Tf32Narrow, 2>(a, transA, transB, ws, s);
 }
 
 cudaError_t launch_tf32_mma_probe(long long iters, float *out, int ctas, cudaStream_t s) {
