@@ -638,3 +638,31 @@ def test_gemv_colsum_cluster_exact(M, N, K, batch, tA, offset):
     entry = "sgemm_f32_strided_batched" if batch > 1 else "sgemm_f32"
     check_full(case, run(case, entry=entry, offset=offset), exact=True,
                label=f"colsum {batch}x{M}x{N}x{K} tA={tA} offset={offset}")
+
+
+# The persistent tensor kernel walks several tiles per CTA and reuses its
+# accumulator buffers: many tiles per SM, both store paths, K on either side
+# of the short-K tile rule, exact on integers or within the FP32 bound.
+@pytest.mark.parametrize("entry_name", ["sgemm_f32_tf32x3", "sgemm_f32_tf32"])
+@pytest.mark.parametrize("M,N,K,ldc_pad", [(4096, 2048, 64, 0), (1000, 4001, 100, 3),
+                                           (3000, 2000, 257, 0), (2500, 1500, 256, 4)])
+def test_persistent_tensor_many_tiles_exact(entry_name, M, N, K, ldc_pad):
+    case = workloads.make_operands(M, N, K, ldc=N + ldc_pad, dist="int", seed=80,
+                                   key=800 + M + N + K)
+    check_full(case, run(case, entry=entry_name), exact=True,
+               label=f"{entry_name} {M}x{N}x{K} ldc+{ldc_pad}")
+
+
+def test_persistent_tensor_epilogue_many_tiles():
+    M, N, K = 4096, 2048, 96
+    case = workloads.make_operands(M, N, K, transA=1, dist="normal", seed=81, key=810)
+    rng = np.random.default_rng(82)
+    C_in = rng.standard_normal((M, N)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32)
+    got = _run_ex(case, 0.5, -0.75, C_in, bias, "sgemm_f32_tf32x3_ex")
+    rows = np.arange(0, M, 37)
+    ref, S = oracle.sgemm_ex(np.ascontiguousarray(case["A"][0]), case["B"][0], M, N, K, alpha=0.5,
+                             beta=-0.75, C_in=C_in, bias=bias, transA=1, lda=case["lda"])
+    ok = oracle.within_tolerance(got[rows], ref[rows], S[rows])
+    assert ok.all(), f"{int((~ok).sum())} outputs outside the bound"
+    assert sg.device_status() == 0
