@@ -578,10 +578,10 @@ def main():
         tf32_probe = tf32_probe_tflops(torch, sg, dev, stream)
         tc = {
             "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
-            "kernels": "split (2 launches) + tf32x3_persistent_kernel (one CTA per SM; 128x256 or "
+            "kernels": "split_kernel (both operands) + tf32x3_persistent_kernel (one CTA per SM; 128x256 or "
                        "128x128 tiles by wave count; TMA ring, tcgen05 kind::tf32, TMEM, TMA-store "
                        "epilogue)",
-            "gpu_launches_per_step": 3,
+            "gpu_launches_per_step": 2,
             "pct_of_fp32_peak_at_max_clock": None,
             "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_peak,
                          "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_peak,

@@ -9,10 +9,12 @@
 // below that and dropped), each term a TF32 MMA accumulated in fp32 in TMEM.
 // With TERMS = 1 only hi_a*hi_b is formed: the plain TF32 product.
 //
-// Stage 1 (split kernels): op(A) and op(B) are rewritten into a caller-owned
-//   workspace as K-major planes [batch][TERMS == 3 ? hi|lo : hi][rows][Kp]
-//   (Kp = K rounded up to 4 so rows are 16-byte aligned for TMA).  M- or
-//   N-major operands are corner-turned through a padded shared tile.
+// Stage 1 (one split launch for both operands): op(A) and op(B) are
+//   rewritten into a caller-owned workspace as K-major planes
+//   [batch][TERMS == 3 ? hi|lo : hi][rows][Kp] (Kp = K rounded up to 4 so
+//   rows are 16-byte aligned for TMA).  M- or N-major operands are
+//   corner-turned through a padded shared tile.  The GEMM is launched as a
+//   programmatic dependent of it and waits for it before reading a plane.
 // Stage 2 (persistent GEMM kernel, one CTA per SM walking 128 x BN output
 //   tiles, BN = 256 or 128 picked per problem; 192 threads in three roles):
 //   warp 0 / lane 0 issues TMA loads of the swizzled K slices (BK fp32 of K,
@@ -73,23 +75,40 @@ __device__ unsigned int g_tf32x3_error = 0;   // bit 0: a pipeline wait ran out
 
 // ------------------------------------------------------------------ split
 
-// K-contiguous operand, element (r, k) at X[z*sX + r*ld + k].  One thread per
-// four consecutive k of a row; 16-byte loads where the row allows, 16-byte
-// stores always (rows of the planes are Kp long; the padding gets zeros).
+// One operand to split: rows r of op(X) (R of them per problem), element
+// (r, k) at X[z*sX + r*ld + k] when kcontig, else at X[z*sX + k*ld + r];
+// planes written to `out`.  `blocks` CTAs of the split grid serve it.
+struct SplitJob {
+    const float *X;
+    int64_t ld, sX;
+    float *out;
+    int64_t blocks;
+    int R;
+    int kcontig;
+    int vec;   // kcontig rows allow 16-byte loads
+};
+
+struct SplitArgs {
+    SplitJob job[2];   // op(A) and op(B)
+    int K, Kp, batch;
+};
+
+// K-contiguous operand: one thread per four consecutive k of a row; 16-byte
+// loads where the row allows, 16-byte stores always (rows of the planes are
+// Kp long; the padding gets zeros).  CTA `b` of `blocks`, grid-stride.
 template <int PLANES>
-__global__ void split_kcontig_kernel(const float *__restrict__ X, int64_t ld, int64_t sX, int R,
-                                     int K, int Kp, int batch, int vec, float *__restrict__ ws) {
-    const int64_t plane = (int64_t)R * Kp;
+__device__ __forceinline__ void split_kcontig(const SplitJob &j, int K, int Kp, int batch,
+                                              int64_t b) {
+    const int64_t plane = (int64_t)j.R * Kp;
     const int quads = Kp / 4;
-    const int64_t total = (int64_t)batch * R * quads;
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
-         t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t total = (int64_t)batch * j.R * quads;
+    for (int64_t t = b * blockDim.x + threadIdx.x; t < total; t += j.blocks * blockDim.x) {
         const int64_t row = t / quads;
         const int k = (int)(t - row * quads) * 4;
-        const int64_t z = row / R, r = row - z * R;
-        const float *src = X + z * sX + r * ld + k;
+        const int64_t z = row / j.R, r = row - z * j.R;
+        const float *src = j.X + z * j.sX + r * j.ld + k;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (vec && k + 3 < K) {
+        if (j.vec && k + 3 < K) {
             x = __ldg(reinterpret_cast<const float4 *>(src));
         } else {
             if (k + 0 < K) x.x = __ldg(src + 0);
@@ -99,7 +118,7 @@ __global__ void split_kcontig_kernel(const float *__restrict__ X, int64_t ld, in
         }
         const float4 h = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
                                      tc::to_tf32(x.w));
-        float *hi = ws + (PLANES * z) * plane + r * Kp + k;
+        float *hi = j.out + (PLANES * z) * plane + r * Kp + k;
         *reinterpret_cast<float4 *>(hi) = h;
         if constexpr (PLANES == 2) {
             *reinterpret_cast<float4 *>(hi + plane) =
@@ -109,40 +128,57 @@ __global__ void split_kcontig_kernel(const float *__restrict__ X, int64_t ld, in
     }
 }
 
-// M/N-major operand: element (r, k) at X[z*sX + k*ld + r]; transposed through
-// a 32 x 33 shared tile so both the read and the write are coalesced.
+// M/N-major operand: transposed through a 32 x 33 shared tile (one 32 x 32
+// block of (k, r) per step, the 256 threads as 32 x 8) so both the read and
+// the write are coalesced.  Plane columns k >= K are not written: the GEMM's
+// tensor maps end at K.
 template <int PLANES>
-__global__ void split_transpose_kernel(const float *__restrict__ X, int64_t ld, int64_t sX, int R,
-                                       int K, int Kp, int batch, float *__restrict__ ws) {
-    __shared__ float tile[32][33];
-    const int64_t plane = (int64_t)R * Kp;
-    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
-    for (int z = blockIdx.z; z < batch; z += gridDim.z) {
-        const float *src = X + (int64_t)z * sX;
-        float *hi = ws + (PLANES * (int64_t)z) * plane;
-        for (int kt = blockIdx.y; kt * 32 < K; kt += gridDim.y) {
-            for (int rt = blockIdx.x; rt * 32 < R; rt += gridDim.x) {
-                const int k0 = kt * 32, r0 = rt * 32;
+__device__ __forceinline__ void split_transpose(const SplitJob &j, int K, int Kp, int batch,
+                                                int64_t b, float (*tile)[33]) {
+    const int64_t plane = (int64_t)j.R * Kp;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t rt_n = (j.R + 31) / 32, kt_n = (K + 31) / 32;
+    const int64_t total = (int64_t)batch * kt_n * rt_n;
+    for (int64_t t = b; t < total; t += j.blocks) {
+        const int64_t z = t / (kt_n * rt_n), rem = t - z * kt_n * rt_n;
+        const int k0 = (int)(rem / rt_n) * 32, r0 = (int)(rem % rt_n) * 32;
+        const float *src = j.X + z * j.sX;
+        float *hi = j.out + (PLANES * z) * plane;
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    const int k = k0 + ty + i, r = r0 + tx;
-                    tile[ty + i][tx] = (k < K && r < R) ? src[(int64_t)k * ld + r] : 0.f;
-                }
-                __syncthreads();
+        for (int i = 0; i < 32; i += 8) {
+            const int k = k0 + ty + i, r = r0 + tx;
+            tile[ty + i][tx] = (k < K && r < j.R) ? src[(int64_t)k * j.ld + r] : 0.f;
+        }
+        __syncthreads();
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    const int r = r0 + ty + i, k = k0 + tx;
-                    if (r < R && k < K) {
-                        const float x = tile[tx][ty + i];
-                        const float h = tc::to_tf32(x);
-                        hi[(int64_t)r * Kp + k] = h;
-                        if constexpr (PLANES == 2) hi[plane + (int64_t)r * Kp + k] = tc::to_tf32(x - h);
-                    }
-                }
-                __syncthreads();
+        for (int i = 0; i < 32; i += 8) {
+            const int r = r0 + ty + i, k = k0 + tx;
+            if (r < j.R && k < K) {
+                const float x = tile[tx][ty + i];
+                const float h = tc::to_tf32(x);
+                hi[(int64_t)r * Kp + k] = h;
+                if constexpr (PLANES == 2) hi[plane + (int64_t)r * Kp + k] = tc::to_tf32(x - h);
             }
         }
+        __syncthreads();
     }
+}
+
+// Both operands in one launch: CTAs [0, job[0].blocks) split op(A), the rest
+// op(B).  The GEMM that follows is launched as a programmatic dependent, so
+// this grid lets it start its set-up early; the GEMM waits for this grid's
+// completion before it reads a plane.
+template <int PLANES>
+__global__ void __launch_bounds__(256) split_kernel(const SplitArgs a) {
+    __shared__ float tile[32][33];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int w = (int64_t)blockIdx.x < a.job[0].blocks ? 0 : 1;
+    const int64_t b = (int64_t)blockIdx.x - (w ? a.job[0].blocks : 0);
+    const SplitJob j = w ? a.job[1] : a.job[0];   // no dynamic index into the parameters
+    if (j.kcontig)
+        split_kcontig<PLANES>(j, a.K, a.Kp, a.batch, b);
+    else
+        split_transpose<PLANES>(j, a.K, a.Kp, a.batch, b, tile);
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -337,6 +373,10 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the split kernel: the set-up above
+    // may overlap its tail; nothing below touches global memory before the
+    // split grid has completed and its planes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         if (lane == 0) {
@@ -630,26 +670,28 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, void *ws, cudaS
         !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN))
         return cudaErrorInvalidValue;
 
-    // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes
-    auto split = [&](const float *X, int64_t ld, int64_t sX, int R, bool kcontig, float *out) {
-        if (kcontig) {
-            const int vec = (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 && sX % 4 == 0;
-            const int64_t total = (int64_t)a.batch * R * (Kp / 4);
-            const int64_t want = (total + 255) / 256;
-            const int blocks = (int)(want < 152 * 32 ? want : 152 * 32);
-            split_kcontig_kernel<PLANES><<<blocks, 256, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch,
-                                                                vec, out);
-        } else {
-            dim3 block(32, 8);
-            dim3 grid((unsigned)((R + 31) / 32 < 65535 ? (R + 31) / 32 : 65535),
-                      (unsigned)((a.K + 31) / 32 < 65535 ? (a.K + 31) / 32 : 65535),
-                      (unsigned)(a.batch < 65535 ? a.batch : 65535));
-            split_transpose_kernel<PLANES><<<grid, block, 0, s>>>(X, ld, sX, R, a.K, Kp, a.batch,
-                                                                  out);
-        }
+    // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes,
+    // one launch for both
+    SplitArgs sa;
+    sa.K = a.K;
+    sa.Kp = Kp;
+    sa.batch = a.batch;
+    auto job = [&](SplitJob &j, const float *X, int64_t ld, int64_t sX, int R, bool kcontig,
+                   float *out) {
+        j.X = X;
+        j.ld = ld;
+        j.sX = sX;
+        j.out = out;
+        j.R = R;
+        j.kcontig = kcontig;
+        j.vec = kcontig && (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 && sX % 4 == 0;
+        const int64_t work = kcontig ? ((int64_t)a.batch * R * (Kp / 4) + 255) / 256
+                                     : (int64_t)a.batch * ((R + 31) / 32) * ((a.K + 31) / 32);
+        j.blocks = work < 152 * 16 ? (work > 0 ? work : 1) : 152 * 16;
     };
-    split(a.A, a.lda, a.strideA, a.M, !transA, wsA);
-    split(a.B, a.ldb, a.strideB, a.N, transB, wsB);
+    job(sa.job[0], a.A, a.lda, a.strideA, a.M, !transA, wsA);
+    job(sa.job[1], a.B, a.ldb, a.strideB, a.N, transB, wsB);
+    split_kernel<PLANES><<<(unsigned)(sa.job[0].blocks + sa.job[1].blocks), 256, 0, s>>>(sa);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -711,8 +753,18 @@ cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void 
     e = prepare<CFG>(a, transA, transB, ws, s, tmA, tmB, tmC, p);
     if (e != cudaSuccess) return e;
     const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
-    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-    tf32x3_persistent_kernel<CFG, ACC_BUFS><<<grid, PTHREADS, P::SMEM_BYTES, s>>>(tmA, tmB, tmC, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
+    cfg.blockDim = dim3(PTHREADS);
+    cfg.dynamicSmemBytes = P::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tf32x3_persistent_kernel<CFG, ACC_BUFS>, tmA, tmB, tmC, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
