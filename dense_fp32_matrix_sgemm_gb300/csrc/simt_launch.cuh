@@ -32,9 +32,10 @@ constexpr int kCommitWide = 8;
 // little.
 constexpr int kShortK = 256;
 // Cluster split-K: problems whose 128 x 128 tiles (all batches) cover at most
-// half the SMs split K over the S CTAs of a cluster, S in {2, 4, 8} (8 is the
-// portable cluster limit), each CTA taking whole 32-deep slices.
-constexpr int kMaxClusterSplit = 8;
+// half the SMs split K over the S CTAs of a cluster, S in {2, 4, 8, 16} (16
+// with the non-portable cluster-size opt-in), each CTA taking whole 32-deep
+// slices.
+constexpr int kMaxClusterSplit = 16;
 
 inline int sm_count() {
     static std::atomic<int> cached[64];
@@ -116,6 +117,15 @@ bool launch_cluster_split(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
     int dev = 0;
     err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return true;
+    // clusters of 16 need the non-portable size opt-in (a per-device attribute)
+    static std::atomic<unsigned long long> nonportable{0};
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(nonportable.load() & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+            (void)cudaGetLastError();   // then clusters of 16 report no residency below
+        nonportable.fetch_or(bit);
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS);
@@ -132,7 +142,7 @@ bool launch_cluster_split(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
     // -1: that size cannot run); a split that needs a second wave loses.
     static std::atomic<int> resident[64][4];
     auto fits = [&](int c) {
-        std::atomic<int> &slot = resident[dev & 63][c == 2 ? 0 : (c == 4 ? 1 : 2)];
+        std::atomic<int> &slot = resident[dev & 63][c == 2 ? 0 : (c == 4 ? 1 : (c == 8 ? 2 : 3))];
         int n = slot.load();
         if (n == 0) {
             attr[0].val.clusterDim.x = (unsigned)c;

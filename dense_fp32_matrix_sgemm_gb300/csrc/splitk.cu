@@ -28,7 +28,8 @@ int64_t chunk_len(int64_t K, int splits) {
     return ((K + splits - 1) / splits + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
 }
 
-// C[i][j] = sum over s = 0..S-1 of P[s][i][j], planes of M x Np floats.
+// C[i][j] = sum over s = 0..S-1 of P[s][i][j], planes of M x Np floats: one
+// thread per float4 of C, the planes added in ascending s (few planes).
 __global__ void splitk_reduce_kernel(const float *__restrict__ P, int S, int M, int N, int64_t Np,
                                      float *__restrict__ C, int64_t ldc, int vec) {
     const int64_t plane = (int64_t)M * Np;
@@ -57,6 +58,55 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ P, int S, int M, 
             if (j + 2 < N) c[2] = acc.z;
             if (j + 3 < N) c[3] = acc.w;
         }
+    }
+}
+
+constexpr int kWideSlots = 8;   // threads sharing one float4 of C in the many-plane form
+
+// The same sum for many planes (one tile split 64 ways: the single-thread
+// form reads 64 planes in sequence from only 16 CTAs): 8 threads share each
+// float4 of C, slot w adding planes w, w + 8, ... in ascending order, and slot
+// 0 then adds the 8 slot sums in slot order.  A fixed order: deterministic.
+__global__ void __launch_bounds__(256)
+splitk_reduce_wide_kernel(const float *__restrict__ P, int S, int M, int N, int64_t Np,
+                          float *__restrict__ C, int64_t ldc, int vec) {
+    constexpr int G = 256 / kWideSlots;   // float4 groups of C per CTA
+    __shared__ float4 part[256];
+    const int g = threadIdx.x % G, w = threadIdx.x / G;
+    const int64_t plane = (int64_t)M * Np;
+    const int64_t e = ((int64_t)blockIdx.x * G + g) * 4;   // element index in a plane
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e < plane) {
+#pragma unroll 4
+        for (int s = w; s < S; s += kWideSlots) {
+            const float4 v = *reinterpret_cast<const float4 *>(P + s * plane + e);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+    }
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    if (w != 0 || e >= plane) return;
+    for (int k = 1; k < kWideSlots; ++k) {
+        const float4 v = part[k * G + g];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    const int64_t i = e / Np;
+    const int j = (int)(e - i * Np);
+    float *c = C + i * ldc + j;
+    const bool full = vec && j + 3 < N;
+    if (full) {
+        *reinterpret_cast<float4 *>(c) = acc;
+    } else {
+        if (j + 0 < N) c[0] = acc.x;
+        if (j + 1 < N) c[1] = acc.y;
+        if (j + 2 < N) c[2] = acc.z;
+        if (j + 3 < N) c[3] = acc.w;
     }
 }
 
@@ -104,12 +154,20 @@ cudaError_t launch_simt_splitk(const GemmArgs &a, bool transA, bool transB, bool
     g.strideC = (int64_t)a.M * Np;
     cudaError_t e = launch_simt(g, transA, transB, vec, s);
     if (e != cudaSuccess) return e;
-    const int64_t total = (int64_t)a.M * (Np / 4);
-    const int64_t want = (total + 255) / 256;
-    const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
     const int vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && a.ldc % 4 == 0;
-    splitk_reduce_kernel<<<blocks, 256, 0, s>>>(static_cast<const float *>(ws), used, a.M, a.N, Np,
-                                                a.C, a.ldc, vec_c);
+    const float *P = static_cast<const float *>(ws);
+    if (used <= kWideSlots) {
+        // measured: with 2-8 planes the single-thread form is fastest
+        const int64_t total = (int64_t)a.M * (Np / 4);
+        const int64_t want = (total + 255) / 256;
+        const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+        splitk_reduce_kernel<<<blocks, 256, 0, s>>>(P, used, a.M, a.N, Np, a.C, a.ldc, vec_c);
+    } else {
+        const int64_t groups = ((int64_t)a.M * Np / 4 + 31) / 32;
+        if (groups > 0x7fffffff) return cudaErrorInvalidValue;
+        splitk_reduce_wide_kernel<<<(unsigned)groups, 256, 0, s>>>(P, used, a.M, a.N, Np, a.C,
+                                                                   a.ldc, vec_c);
+    }
     return cudaGetLastError();
 }
 

@@ -87,7 +87,7 @@ typedef enum {
  * sums, DD2360 workbook section 15.2); their sums run in a different but
  * fixed order, so they are deterministic too.  Problems whose 128 x 128
  * output tiles cover at most half the SMs (e.g. 256 x 256 x 256: four tiles)
- * split K over the 2, 4 or 8 CTAs of a thread-block cluster and add the
+ * split K over the 2, 4, 8 or 16 CTAs of a thread-block cluster and add the
  * partial tiles on chip through distributed shared memory, in chunk order:
  * the split-K of the ChetanC28/cuda-kernels page without a workspace.
  */

@@ -353,6 +353,16 @@ def test_splitk_layouts_integer_exact(tA, tB):
     check_full(case, got, exact=True, label=f"splitk int tA={tA} tB={tB}")
 
 
+@pytest.mark.parametrize("tA,tB,splits", [(0, 0, 0), (1, 1, 40), (0, 1, 9)])
+def test_splitk_many_chunks_ragged_exact(tA, tB, splits):
+    # more than 8 chunks: 8 threads share each output group of the reduction
+    M, N, K = 100, 131, 20000
+    case = workloads.make_operands(M, N, K, transA=tA, transB=tB, ldc=N + 1, dist="int",
+                                   poison=True, seed=32, key=212)
+    got = run(case, entry="sgemm_f32_splitk", splits=splits)
+    check_full(case, got, exact=True, label=f"splitk many chunks tA={tA} tB={tB} splits={splits}")
+
+
 def test_splitk_unaligned_and_deterministic():
     M, N, K = 77, 133, 2048
     case = workloads.make_operands(M, N, K, lda=K + 1, ldb=N + 1, ldc=N + 1, dist="normal",
