@@ -237,7 +237,19 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
                                                 w.batch, w.transA, w.transB, ws.data_ptr(), need,
                                                 sp)
 
-        for label, fn in (("simt", simt), ("tf32x3", tc)):
+        legs = [("simt", simt), ("tf32x3", tc)]
+        sk_need = sg.streamk_workspace_size(w.M, w.N, w.K) if (w.batch == 1 and w.transA and
+                                                                 not w.transB) else 0
+        if sk_need:
+            sk_ws = torch.empty(sk_need, dtype=torch.uint8, device=dev)
+
+            def streamk():
+                sg.sgemm_f32_streamk(w.M, w.N, w.K, dA.data_ptr(), lda, dB.data_ptr(), ldb,
+                                     dC.data_ptr(), ldc, w.transA, w.transB, sk_ws.data_ptr(),
+                                     sk_need, sp)
+
+            legs.append(("simt_streamk", streamk))
+        for label, fn in legs:
             for _ in range(2):
                 fn()
             ts = []
@@ -254,6 +266,8 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
             row[label + "_tflops"] = workloads.flops(w.M, w.N, w.K, w.batch) / (ms * 1e-3) / 1e12
         out[name] = row
         del dA, dB, dC, ws
+        if sk_need:
+            del sk_ws
     torch.cuda.empty_cache()
     return out
 

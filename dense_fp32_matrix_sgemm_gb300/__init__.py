@@ -25,6 +25,7 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32_tf32x3_noalloc", "tf32x3_noalloc_max_bytes", "sgemm_f32_tf32",
            "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
            "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex", "selftest_wait_timeout",
+           "sgemm_f32_streamk", "streamk_workspace_size",
            "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +61,9 @@ SIGNATURES = {
     "sgemm_f32_splitk": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
                                 _int, _vp, ctypes.c_uint64, _vp]),
     "sgemm_f32_splitk_auto_splits": (_int, [_i64, _i64, _i64]),
+    "sgemm_f32_streamk": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
+                                 _vp, ctypes.c_uint64, _vp]),
+    "sgemm_f32_streamk_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64]),
     "sgemm_f32_splitk_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _int]),
     "sgemm_f32_tf32x3": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
                                 _vp, ctypes.c_uint64, _vp]),
@@ -186,6 +190,19 @@ def sgemm_f32_tf32x3_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=0, tr
                                             C or None, ldc, bias or None, transA, transB,
                                             workspace or None, workspace_bytes, stream or None)
     return _check(st) if check else st
+
+
+def sgemm_f32_streamk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,
+                      workspace_bytes=0, stream=0, *, check=True):
+    """sgemm_f32 with the stream-K tile schedule (see include/sgemm_gb300.h)."""
+    st = load_library().sgemm_f32_streamk(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
+                                          transA, transB, workspace or None, workspace_bytes,
+                                          stream or None)
+    return _check(st) if check else st
+
+
+def streamk_workspace_size(M: int, N: int, K: int) -> int:
+    return load_library().sgemm_f32_streamk_workspace_size(M, N, K)
 
 
 def sgemm_f32_splitk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, splits=0, workspace=0,

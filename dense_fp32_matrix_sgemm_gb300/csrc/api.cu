@@ -25,6 +25,48 @@ cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, c
     return launch_simt_tt(a, vec, s);
 }
 
+cudaError_t launch_simt_streamk_nn(const GemmArgs &, bool, const StreamKPlan &, void *, cudaStream_t);
+cudaError_t launch_simt_streamk_nt(const GemmArgs &, bool, const StreamKPlan &, void *, cudaStream_t);
+cudaError_t launch_simt_streamk_tn(const GemmArgs &, bool, const StreamKPlan &, void *, cudaStream_t);
+cudaError_t launch_simt_streamk_tt(const GemmArgs &, bool, const StreamKPlan &, void *, cudaStream_t);
+
+cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
+                                const StreamKPlan &pl, void *ws, cudaStream_t s) {
+    if (!transA && !transB) return launch_simt_streamk_nn(a, vec, pl, ws, s);
+    if (!transA && transB) return launch_simt_streamk_nt(a, vec, pl, ws, s);
+    if (transA && !transB) return launch_simt_streamk_tn(a, vec, pl, ws, s);
+    return launch_simt_streamk_tt(a, vec, pl, ws, s);
+}
+
+// Only for A stored transposed with row-major B: the one layout whose
+// operands both arrive by cp.async.  Where an operand is corner-turned
+// through registers (row-major A, or B^T), a CTA that runs tile after tile
+// left those 16-byte global loads exposed (long-scoreboard stalls 0.007 ->
+// 0.75 per instruction, 15 % slower per tile on 2048 x 4864 x 4096), more
+// than the wave tail stream-K removes.  The wide 128 x 256 tile wherever the
+// kernel allows it (16-byte access): with the wave tail gone, the wider
+// tile's better operand reuse is all that remains of the choice.
+StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec) {
+    StreamKPlan pl = {};
+    if (!transA || transB) return pl;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return pl;
+    pl.wide = vec && !transB;
+    const int64_t bn = pl.wide ? 256 : 128;
+    const int64_t tiles = (int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + bn - 1) / bn);
+    pl.G = sms;
+    pl.kslices = (a.K + 31) / 32;
+    pl.use = tiles > sms && tiles % sms != 0 && pl.kslices >= 2 && tiles <= (1LL << 30);
+    if (!pl.use) return pl;
+    pl.tiles_dp = (int)(tiles / sms * sms);
+    pl.tiles_sk = (int)(tiles - pl.tiles_dp);
+    pl.units = (int64_t)pl.tiles_sk * pl.kslices;
+    pl.ws_bytes = (size_t)sms * 2 * 128 * (size_t)bn * sizeof(float);
+    return pl;
+}
+
 namespace {
 
 __global__ void epilogue_only_kernel(float *C, int64_t ldc, int64_t strideC, int M, int N,
@@ -221,6 +263,41 @@ int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, con
 // translation unit and returns `code`.
 int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
+// sgemm_f32 with the stream-K schedule (see StreamKPlan); problems it cannot
+// help run exactly as sgemm_f32 and need no workspace.
+int run_streamk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                int64_t ldb, float *C, int64_t ldc, int transA, int transB, void *workspace,
+                uint64_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    GemmArgs a;
+    bool nothing = false;
+    int st = validate(M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA, transB, a, nothing);
+    if (st != SGEMM_OK || nothing) return st;
+    const bool vec = vector_ok(a);
+    const StreamKPlan pl = (K > 0 && !gemv_shape(a)) ? streamk_plan(a, transA != 0, transB != 0, vec)
+                                                      : StreamKPlan{};
+    if (pl.use && (workspace == nullptr || !aligned(workspace, 256) ||
+                   workspace_bytes < pl.ws_bytes))
+        return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: stream-K needs %llu bytes, "
+                    "256-byte aligned", workspace, (unsigned long long)workspace_bytes,
+                    (unsigned long long)pl.ws_bytes);
+    st = check_device();
+    if (st != SGEMM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (K == 0)
+        e = launch_epilogue_only(a, s);
+    else if (gemv_shape(a))
+        e = launch_gemv(a, transA != 0, transB != 0, s);
+    else if (pl.use)
+        e = launch_simt_streamk(a, transA != 0, transB != 0, vec, pl, workspace, s);
+    else
+        e = launch_simt(a, transA != 0, transB != 0, vec, s);
+    if (e != cudaSuccess)
+        return fail(SGEMM_ELAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
+    return SGEMM_OK;
+}
+
 int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                int64_t ldb, float *C, int64_t ldc, int transA, int transB, int splits,
                void *workspace, uint64_t workspace_bytes, void *stream) {
@@ -360,6 +437,30 @@ int sgemm_f32_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t ld
                      void *workspace, uint64_t workspace_bytes, void *stream) {
     return sgemm::run_splitk(M, N, K, A, lda, B, ldb, C, ldc, transA, transB, splits, workspace,
                              workspace_bytes, stream);
+}
+
+int sgemm_f32_streamk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                      const float *B, int64_t ldb, float *C, int64_t ldc, int transA, int transB,
+                      void *workspace, uint64_t workspace_bytes, void *stream) {
+    return sgemm::run_streamk(M, N, K, A, lda, B, ldb, C, ldc, transA, transB, workspace,
+                              workspace_bytes, stream);
+}
+
+uint64_t sgemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 1 || N <= 1 || K <= 0 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return 0;
+    sgemm::GemmArgs a = {};
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.batch = 1;
+    // the layout that uses stream-K (A transposed, B row-major), with either
+    // tile width (it depends on alignment): the larger need of the two
+    const sgemm::StreamKPlan wide = sgemm::streamk_plan(a, true, false, true);
+    const sgemm::StreamKPlan narrow = sgemm::streamk_plan(a, true, false, false);
+    uint64_t need = 0;
+    if (wide.use) need = wide.ws_bytes;
+    if (narrow.use && narrow.ws_bytes > need) need = narrow.ws_bytes;
+    return need;
 }
 
 int sgemm_f32_splitk_auto_splits(int64_t M, int64_t N, int64_t K) {

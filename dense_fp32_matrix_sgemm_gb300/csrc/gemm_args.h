@@ -56,6 +56,22 @@ cudaError_t launch_simt_splitk(const GemmArgs &a, bool transA, bool transB, bool
 size_t splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int splits);
 int splitk_auto_splits(int64_t M, int64_t N, int64_t K);
 
+// Stream-K schedule of the SIMT kernel (sgemm_f32_streamk): whole waves of
+// tiles computed whole, the K slices of the remaining tiles dealt out evenly
+// over one CTA per SM, shared tiles finished by a fix-up pass from the
+// caller's workspace.  `use` is false where it cannot help (the tiles fill
+// the SMs a whole number of times, or fewer tiles than SMs) and for layouts
+// that corner-turn an operand through registers (see streamk_plan).
+struct StreamKPlan {
+    bool use, wide;                      // wide: 128 x 256 tiles
+    int tiles_dp, tiles_sk, kslices, G;  // G: CTAs (SMs)
+    int64_t units;                       // tiles_sk * kslices
+    size_t ws_bytes;                     // G * 2 partial tiles
+};
+StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec);
+cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
+                                const StreamKPlan &plan, void *ws, cudaStream_t s);
+
 // Matrix-vector shapes (N == 1 or M == 1): bandwidth-bound kernels.
 bool gemv_shape(const GemmArgs &a);
 cudaError_t launch_gemv(const GemmArgs &a, bool transA, bool transB, cudaStream_t s);

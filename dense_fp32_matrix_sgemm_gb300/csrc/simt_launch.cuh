@@ -199,5 +199,48 @@ cudaError_t launch_pair(const GemmArgs &a, bool vec, cudaStream_t s) {
     return vec ? launch_variant<TA, TB, true>(a, s) : launch_variant<TA, TB, false>(a, s);
 }
 
+// Stream-K launch: the tile kernel on one CTA per SM, then the fix-up pass.
+template <int STAGES, int BN_, bool TA, bool TB, bool VEC, int CK>
+cudaError_t launch_streamk_config(const GemmArgs &a, const StreamKPlan &pl, void *ws,
+                                  cudaStream_t s) {
+    auto kern = sgemm_simt_streamk_kernel<kBK, STAGES, BN_, TA, TB, VEC, kFfma2, kMinBlocks, CK>;
+    constexpr int smem = smem_bytes<kBK, STAGES, BN_>();
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = ensure_smem_attribute(kern, smem, configured);
+    if (e != cudaSuccess) return e;
+    GemmArgs g = a;
+    g.tiles_m = (a.M + BM - 1) / BM;
+    g.tiles_n = (a.N + BN_ - 1) / BN_;
+    StreamK sk;
+    sk.tiles_dp = pl.tiles_dp;
+    sk.tiles_sk = pl.tiles_sk;
+    sk.kslices = pl.kslices;
+    sk.G = pl.G;
+    sk.units = pl.units;
+    sk.ws = static_cast<float *>(ws);
+    kern<<<(unsigned)pl.G, THREADS, smem, s>>>(g, sk);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(BM * BN_ / 1024), (unsigned)pl.tiles_sk);
+    streamk_fixup_kernel<BN_, VEC><<<grid, 256, 0, s>>>(g, sk);
+    return cudaGetLastError();
+}
+
+template <bool TA, bool TB, bool VEC>
+cudaError_t launch_streamk_variant(const GemmArgs &a, const StreamKPlan &pl, void *ws,
+                                   cudaStream_t s) {
+    if constexpr (VEC && !TB) {
+        if (pl.wide) return launch_streamk_config<kStagesWide, 256, TA, TB, VEC, kCommitWide>(a, pl, ws, s);
+    }
+    return launch_streamk_config<kStagesNarrow, 128, TA, TB, VEC, kCommitNarrow>(a, pl, ws, s);
+}
+
+template <bool TA, bool TB>
+cudaError_t launch_streamk_pair(const GemmArgs &a, bool vec, const StreamKPlan &pl, void *ws,
+                                cudaStream_t s) {
+    return vec ? launch_streamk_variant<TA, TB, true>(a, pl, ws, s)
+               : launch_streamk_variant<TA, TB, false>(a, pl, ws, s);
+}
+
 }  // namespace simt
 }  // namespace sgemm

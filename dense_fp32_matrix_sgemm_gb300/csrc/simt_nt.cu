@@ -5,4 +5,8 @@ namespace sgemm {
 cudaError_t launch_simt_nt(const GemmArgs &a, bool vec, cudaStream_t s) {
     return simt::launch_pair<false, true>(a, vec, s);
 }
+cudaError_t launch_simt_streamk_nt(const GemmArgs &a, bool vec, const StreamKPlan &pl, void *ws,
+                                    cudaStream_t s) {
+    return simt::launch_streamk_pair<false, true>(a, vec, pl, ws, s);
+}
 }  // namespace sgemm

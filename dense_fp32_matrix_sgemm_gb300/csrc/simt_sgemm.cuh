@@ -223,73 +223,22 @@ __device__ __forceinline__ void store_c4(const GemmArgs &p, float *crow, int col
     }
 }
 
-// Block tile 128 x BN_ (BN_ = 128 or 256); each thread owns an 8 x (BN_/16)
-// register tile made of 4 x 4 sub-blocks spaced 64 rows / 64 columns apart.
-// CK: the k step of the tile loop at which register-staged (corner-turned)
-// slices are written to shared memory; BK means after the last step.
-// CSPLIT: launched in 1-D clusters of S CTAs (S divides 128); CTA q of the
-// cluster covers k in [q*kchunk, min(K, (q+1)*kchunk)) of tile blockIdx.x / S.
-template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int MINB,
-          int CK = BK, bool CSPLIT = false>
-__global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArgs p) {
-    static_assert(CK >= 0 && CK <= BK, "commit step out of range");
-    static_assert(!CSPLIT || BN_ == 128, "the cluster split uses 128 x 128 tiles");
-    static_assert(BK == 8 || BK == 16 || BK == 32, "BK must be 8, 16 or 32");
-    static_assert(BN_ == 128 || BN_ == 256, "BN must be 128 or 256");
-    static_assert(STAGES >= 2, "need at least two stages");
-    constexpr int TN = BN_ / 16;         // columns per thread
-    constexpr int NSB = BN_ / 64;        // 4-wide column sub-blocks per thread
+// The K-slice pipeline of one tile: zeroes acc, then accumulates the
+// loaders' K range (ktiles slices of BK; <= 0 loads nothing) into the
+// thread's 8 x (BN_/16) register tile.  Ends with no copy in flight.
+template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int CK>
+__device__ __forceinline__ void tile_mainloop(TileLoader<BK, BM, !TA, VEC> &la,
+                                              TileLoader<BK, BN_, TB, VEC> &lb, float *As,
+                                              float *Bs, int ktiles, int a_col, int b_col,
+                                              float (&acc)[8][BN_ / 16]) {
+    constexpr int TN = BN_ / 16;
+    constexpr int NSB = BN_ / 64;
     constexpr int ATILE = BK * BM;
     constexpr int BTILE = BK * BN_;
-    extern __shared__ __align__(16) float smem[];
-    float *As = smem;
-    float *Bs = smem + STAGES * ATILE;
-
-    int z, tm, tn;
-    raster(p, CSPLIT ? (int)(blockIdx.x / cluster_size()) : (int)blockIdx.x, z, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN_;
-    // split-K: the K-chunk [kq*kchunk, min(K, (kq+1)*kchunk)), where kq is the
-    // problem index z (partial planes; the strides step by one chunk) or,
-    // under CSPLIT, the rank in the cluster.  Ranks past the last chunk get
-    // Kz <= 0 and load nothing.
-    const int kq = CSPLIT ? (int)cluster_rank() : z;
-    const int Kz = (CSPLIT || p.kchunk > 0) ? min(p.kchunk, p.K - kq * p.kchunk) : p.K;
-
-    // A is contiguous along K unless stored transposed; B the other way round.
-    TileLoader<BK, BM, !TA, VEC> la;
-    la.base = p.A + (int64_t)z * p.strideA;
-    la.ld = p.lda;
-    la.mn0 = m0;
-    la.mn_ext = p.M;
-    la.K = Kz;
-    TileLoader<BK, BN_, TB, VEC> lb;
-    lb.base = p.B + (int64_t)z * p.strideB;
-    lb.ld = p.ldb;
-    lb.mn0 = n0;
-    lb.mn_ext = p.N;
-    lb.K = Kz;
-    if constexpr (CSPLIT) {
-        const int64_t kbeg = (int64_t)kq * p.kchunk;
-        la.base += TA ? kbeg * p.lda : kbeg;
-        lb.base += TB ? kbeg : kbeg * p.ldb;
-    }
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int lane_row = (lane & 1) | ((lane >> 4) << 1);   // Z-order 4 x 8
-    const int lane_col = (lane >> 1) & 7;
-    const int ty = (warp >> 1) * 4 + lane_row;               // 0..15
-    const int tx = (warp & 1) * 8 + lane_col;                // 0..15
-    const int a_col = 4 * ty;
-    const int b_col = 4 * tx;
-
-    float acc[8][TN];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-    const int ktiles = (Kz + BK - 1) / BK;   // <= 0: nothing to load
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
@@ -368,6 +317,70 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
         wstage = (wstage + 1 == STAGES) ? 0 : wstage + 1;
     }
     cp_async_wait<0>();
+}
+
+// Block tile 128 x BN_ (BN_ = 128 or 256); each thread owns an 8 x (BN_/16)
+// register tile made of 4 x 4 sub-blocks spaced 64 rows / 64 columns apart.
+// CK: the k step of the tile loop at which register-staged (corner-turned)
+// slices are written to shared memory; BK means after the last step.
+// CSPLIT: launched in 1-D clusters of S CTAs (S divides 128); CTA q of the
+// cluster covers k in [q*kchunk, min(K, (q+1)*kchunk)) of tile blockIdx.x / S.
+template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int MINB,
+          int CK = BK, bool CSPLIT = false>
+__global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArgs p) {
+    static_assert(CK >= 0 && CK <= BK, "commit step out of range");
+    static_assert(!CSPLIT || BN_ == 128, "the cluster split uses 128 x 128 tiles");
+    static_assert(BK == 8 || BK == 16 || BK == 32, "BK must be 8, 16 or 32");
+    static_assert(BN_ == 128 || BN_ == 256, "BN must be 128 or 256");
+    static_assert(STAGES >= 2, "need at least two stages");
+    constexpr int TN = BN_ / 16;         // columns per thread
+    constexpr int NSB = BN_ / 64;        // 4-wide column sub-blocks per thread
+    constexpr int ATILE = BK * BM;
+    extern __shared__ __align__(16) float smem[];
+    float *As = smem;
+    float *Bs = smem + STAGES * ATILE;
+
+    int z, tm, tn;
+    raster(p, CSPLIT ? (int)(blockIdx.x / cluster_size()) : (int)blockIdx.x, z, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN_;
+    // split-K: the K-chunk [kq*kchunk, min(K, (kq+1)*kchunk)), where kq is the
+    // problem index z (partial planes; the strides step by one chunk) or,
+    // under CSPLIT, the rank in the cluster.  Ranks past the last chunk get
+    // Kz <= 0 and load nothing.
+    const int kq = CSPLIT ? (int)cluster_rank() : z;
+    const int Kz = (CSPLIT || p.kchunk > 0) ? min(p.kchunk, p.K - kq * p.kchunk) : p.K;
+
+    // A is contiguous along K unless stored transposed; B the other way round.
+    TileLoader<BK, BM, !TA, VEC> la;
+    la.base = p.A + (int64_t)z * p.strideA;
+    la.ld = p.lda;
+    la.mn0 = m0;
+    la.mn_ext = p.M;
+    la.K = Kz;
+    TileLoader<BK, BN_, TB, VEC> lb;
+    lb.base = p.B + (int64_t)z * p.strideB;
+    lb.ld = p.ldb;
+    lb.mn0 = n0;
+    lb.mn_ext = p.N;
+    lb.K = Kz;
+    if constexpr (CSPLIT) {
+        const int64_t kbeg = (int64_t)kq * p.kchunk;
+        la.base += TA ? kbeg * p.lda : kbeg;
+        lb.base += TB ? kbeg : kbeg * p.ldb;
+    }
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int lane_row = (lane & 1) | ((lane >> 4) << 1);   // Z-order 4 x 8
+    const int lane_col = (lane >> 1) & 7;
+    const int ty = (warp >> 1) * 4 + lane_row;               // 0..15
+    const int tx = (warp & 1) * 8 + lane_col;                // 0..15
+    const int a_col = 4 * ty;
+    const int b_col = 4 * tx;
+
+    float acc[8][TN];
+    tile_mainloop<BK, STAGES, BN_, TA, TB, VEC, FFMA2, CK>(la, lb, As, Bs, (Kz + BK - 1) / BK, a_col,
+                                                         b_col, acc);
 
     float *Cz = p.C + (int64_t)z * p.strideC;
     const bool plain = plain_epilogue(p);
@@ -422,6 +435,159 @@ __global__ void __launch_bounds__(THREADS, MINB) sgemm_simt_kernel(const GemmArg
             }
         }
     }
+}
+
+// ------------------------------------------------------------------ stream-K
+
+// Stream-K schedule of the tile kernel over G CTAs (one per SM), for problems
+// whose tiles fill the SMs a non-whole number of times (3072^3: 288 tiles of
+// 128 x 256 on 152 SMs, so a second wave of 136).  The first tiles_dp tiles
+// (whole waves) are computed whole, tile c + i*G on CTA c.  The K slices of
+// the remaining tiles_sk tiles are dealt out evenly: CTA c takes units
+// [c*U/G, (c+1)*U/G) of U = tiles_sk * kslices, in tile order, slices
+// ascending.  A tile whose slices all fall to one CTA is stored to C.  A tile
+// shared between CTAs is a piece of each: the CTA's first piece goes to
+// workspace slot [c][0], its last to [c][1], and streamk_fixup_kernel adds a
+// tile's pieces in K order.  No CTA waits for another.
+struct StreamK {
+    int tiles_dp, tiles_sk, kslices, G;
+    int64_t units;
+    float *ws;   // [G][2][BM * BN] partial tiles, row-major
+};
+
+// Units [0, u) of CTA c start at floor(c*U/G); the CTA owning unit u.
+__host__ __device__ inline int streamk_owner(int64_t u, int64_t U, int G) {
+    return (int)(((u + 1) * G - 1) / U);
+}
+
+template <int BK, int STAGES, int BN_, bool TA, bool TB, bool VEC, bool FFMA2, int MINB, int CK>
+__global__ void __launch_bounds__(THREADS, MINB)
+sgemm_simt_streamk_kernel(const GemmArgs p, const StreamK sk) {
+    constexpr int TN = BN_ / 16;
+    constexpr int NSB = BN_ / 64;
+    constexpr int ATILE = BK * BM;
+    extern __shared__ __align__(16) float smem[];
+    float *As = smem;
+    float *Bs = smem + STAGES * ATILE;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int lane_row = (lane & 1) | ((lane >> 4) << 1);   // Z-order 4 x 8
+    const int lane_col = (lane >> 1) & 7;
+    const int a_col = 4 * ((warp >> 1) * 4 + lane_row);
+    const int b_col = 4 * ((warp & 1) * 8 + lane_col);
+
+    // Everything about piece i is recomputed from (blockIdx.x, i): no schedule
+    // state lives across the main loop.  tiles_sk < G, so a CTA's stream-K
+    // range is at most kslices units long: at most two pieces.
+    const int c = blockIdx.x;
+    const int ndp = c < sk.tiles_dp ? (sk.tiles_dp - 1 - c) / sk.G + 1 : 0;
+    int nsk;
+    {
+        const int64_t u0 = (int64_t)c * sk.units / sk.G, u1 = ((int64_t)c + 1) * sk.units / sk.G;
+        nsk = u0 == u1 ? 0 : (u0 / sk.kslices == (u1 - 1) / sk.kslices ? 1 : 2);
+    }
+#pragma unroll 1
+    for (int i = 0; i < ndp + nsk; ++i) {
+        int t, s0, s1;
+        float *part = nullptr;   // null: store the finished tile to C
+        if (i < ndp) {
+            t = c + i * sk.G;
+            s0 = 0;
+            s1 = sk.kslices;
+        } else {
+            const int k = i - ndp;   // 0: the range's first piece, 1: its last
+            const int64_t u0 = (int64_t)c * sk.units / sk.G;
+            const int64_t u1 = ((int64_t)c + 1) * sk.units / sk.G;
+            const int64_t ub = k == 0 ? u0 : (u0 / sk.kslices + 1) * sk.kslices;
+            const int tl = (int)(ub / sk.kslices);
+            s0 = (int)(ub - (int64_t)tl * sk.kslices);
+            s1 = (int)min((int64_t)sk.kslices, s0 + (u1 - ub));
+            t = sk.tiles_dp + tl;
+            if (!(s0 == 0 && s1 == sk.kslices))
+                part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
+        }
+        int z, tm, tn;
+        raster(p, t, z, tm, tn);
+        const int m0 = tm * BM, n0 = tn * BN_;
+        const int64_t kbeg = (int64_t)s0 * BK;
+        const int Kz = min(p.K, s1 * BK) - s0 * BK;
+        TileLoader<BK, BM, !TA, VEC> la;
+        la.base = p.A + (int64_t)z * p.strideA + (TA ? kbeg * p.lda : kbeg);
+        la.ld = p.lda;
+        la.mn0 = m0;
+        la.mn_ext = p.M;
+        la.K = Kz;
+        TileLoader<BK, BN_, TB, VEC> lb;
+        lb.base = p.B + (int64_t)z * p.strideB + (TB ? kbeg : kbeg * p.ldb);
+        lb.ld = p.ldb;
+        lb.mn0 = n0;
+        lb.mn_ext = p.N;
+        lb.K = Kz;
+        float acc[8][TN];
+        tile_mainloop<BK, STAGES, BN_, TA, TB, VEC, FFMA2, CK>(la, lb, As, Bs, (Kz + BK - 1) / BK,
+                                                             a_col, b_col, acc);
+        if (part != nullptr) {
+            // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int row = r < 4 ? a_col + r : 64 + a_col + (r - 4);
+#pragma unroll
+                for (int h = 0; h < NSB; ++h)
+                    *reinterpret_cast<float4 *>(part + row * BN_ + h * 64 + b_col) =
+                        make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
+                                    acc[r][4 * h + 3]);
+            }
+        } else {
+            float *Cz = p.C + (int64_t)z * p.strideC;
+            const bool plain = plain_epilogue(p);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int row = m0 + (r < 4 ? a_col + r : 64 + a_col + (r - 4));
+                if (row >= p.M) continue;
+                float *crow = Cz + (int64_t)row * p.ldc;
+#pragma unroll
+                for (int h = 0; h < NSB; ++h) {
+                    const int col = n0 + h * 64 + b_col;
+                    store_c4(p, crow, col,
+                             make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
+                                         acc[r][4 * h + 3]),
+                             VEC, plain);
+                }
+            }
+        }
+        __syncthreads();   // every warp is done with the ring before the next prologue refills it
+    }
+}
+
+// Adds the pieces of the shared stream-K tiles: grid (BM * BN_ / 1024, tiles_sk),
+// one float4 per thread; pieces added in K order (CTA order), then stored to C
+// with the epilogue.  Tiles that fell whole to one CTA are skipped.
+template <int BN_, bool VEC>
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmArgs p, const StreamK sk) {
+    const int tl = blockIdx.y;
+    const int64_t U = sk.units, f = (int64_t)tl * sk.kslices, l = f + sk.kslices - 1;
+    const int c0 = streamk_owner(f, U, sk.G), c1 = streamk_owner(l, U, sk.G);
+    if (c0 == c1) return;
+    const int e = (blockIdx.x * 256 + threadIdx.x) * 4;   // element of the 128 x BN_ tile
+    if (e >= BM * BN_) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c0; c <= c1; ++c) {
+        const int64_t start = (int64_t)c * U / sk.G;
+        if (((int64_t)c + 1) * U / sk.G == start) continue;   // a CTA with no units has no piece
+        const int slot = start >= f ? 0 : 1;   // the tile is c's first piece or its last
+        const float4 v = *reinterpret_cast<const float4 *>(sk.ws + ((int64_t)c * 2 + slot) * (BM * BN_) + e);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    int z, tm, tn;
+    raster(p, sk.tiles_dp + tl, z, tm, tn);
+    const int row = tm * BM + e / BN_, col = tn * BN_ + e % BN_;
+    if (row >= p.M) return;
+    store_c4(p, p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc, col, acc, VEC,
+             plain_epilogue(p));
 }
 
 }  // namespace simt

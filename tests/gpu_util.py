@@ -40,6 +40,10 @@ def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
     s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     fn = getattr(sg, entry)
     extra = ()
+    if entry == "sgemm_f32_streamk":
+        need = sg.streamk_workspace_size(M, N, K)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        extra = (ws.data_ptr(), need)
     if entry == "sgemm_f32_splitk":
         need = sg.splitk_workspace_size(M, N, K, splits)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
