@@ -238,8 +238,7 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
                                                 sp)
 
         legs = [("simt", simt), ("tf32x3", tc)]
-        sk_need = sg.streamk_workspace_size(w.M, w.N, w.K) if (w.batch == 1 and w.transA and
-                                                                 not w.transB) else 0
+        sk_need = sg.streamk_workspace_size(w.M, w.N, w.K, w.transA, w.transB) if w.batch == 1 else 0
         if sk_need:
             sk_ws = torch.empty(sk_need, dtype=torch.uint8, device=dev)
 

@@ -63,7 +63,7 @@ SIGNATURES = {
     "sgemm_f32_splitk_auto_splits": (_int, [_i64, _i64, _i64]),
     "sgemm_f32_streamk": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
                                  _vp, ctypes.c_uint64, _vp]),
-    "sgemm_f32_streamk_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64]),
+    "sgemm_f32_streamk_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _int, _int]),
     "sgemm_f32_splitk_workspace_size": (ctypes.c_uint64, [_i64, _i64, _i64, _int]),
     "sgemm_f32_tf32x3": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _int, _int,
                                 _vp, ctypes.c_uint64, _vp]),
@@ -194,15 +194,15 @@ def sgemm_f32_tf32x3_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=0, tr
 
 def sgemm_f32_streamk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,
                       workspace_bytes=0, stream=0, *, check=True):
-    """sgemm_f32 with the stream-K tile schedule (see include/sgemm_gb300.h)."""
+    """sgemm_f32 with turned operands and the stream-K tile schedule (see include/sgemm_gb300.h)."""
     st = load_library().sgemm_f32_streamk(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
                                           transA, transB, workspace or None, workspace_bytes,
                                           stream or None)
     return _check(st) if check else st
 
 
-def streamk_workspace_size(M: int, N: int, K: int) -> int:
-    return load_library().sgemm_f32_streamk_workspace_size(M, N, K)
+def streamk_workspace_size(M: int, N: int, K: int, transA: int = 0, transB: int = 0) -> int:
+    return load_library().sgemm_f32_streamk_workspace_size(M, N, K, transA, transB)
 
 
 def sgemm_f32_splitk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, splits=0, workspace=0,

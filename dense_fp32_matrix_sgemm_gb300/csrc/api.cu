@@ -263,8 +263,60 @@ int run_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, con
 // translation unit and returns `code`.
 int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
-// sgemm_f32 with the stream-K schedule (see StreamKPlan); problems it cannot
-// help run exactly as sgemm_f32 and need no workspace.
+// The workspace plan of sgemm_f32_streamk.  A K-contiguous operand (row-major
+// A, B stored transposed) of a large problem is first turned into an
+// M/N-contiguous copy, so the tile kernel sees A^T with row-major B (both
+// operands by cp.async, and the layout stream-K runs well on); the copy costs
+// about 8 bytes per element against 2N (for A) or 2M (for B) flops.  The
+// stream-K partial tiles follow the copies.
+struct TurnPlan {
+    bool turnA = false, turnB = false;
+    int64_t ldA = 0, ldB = 0;     // leading dimensions of the copies
+    size_t offA = 0, offB = 0, offP = 0, bytes = 0;
+    StreamKPlan sk = {};
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// `vec`: whether the problem the tile kernel sees allows 16-byte access
+// (callers that do not know pass true: the larger workspace).
+TurnPlan turn_plan(const GemmArgs &a, bool transA, bool transB, bool vec) {
+    TurnPlan tp;
+    const bool big = 2.0 * a.M * (double)a.N * a.K >= 1.6e10;
+    tp.turnA = big && !transA && a.N >= 1024;
+    tp.turnB = big && transB && a.M >= 1024;
+    size_t off = 0;
+    if (tp.turnA) {
+        tp.ldA = ((int64_t)a.M + 3) / 4 * 4;
+        tp.offA = off;
+        off += round256((size_t)a.K * tp.ldA * sizeof(float));
+    }
+    if (tp.turnB) {
+        tp.ldB = ((int64_t)a.N + 3) / 4 * 4;
+        tp.offB = off;
+        off += round256((size_t)a.K * tp.ldB * sizeof(float));
+    }
+    tp.sk = streamk_plan(a, transA || tp.turnA, transB && !tp.turnB, vec);
+    if (tp.sk.use) {
+        tp.offP = off;
+        off += tp.sk.ws_bytes;
+    }
+    tp.bytes = off;
+    return tp;
+}
+
+// The workspace the call may need: whether the tile kernel gets 16-byte access
+// is only known from the pointers, and both the tile width and whether
+// stream-K applies follow from it, so the larger need of the two.
+size_t turn_plan_bytes(const GemmArgs &a, bool transA, bool transB) {
+    const size_t wide = turn_plan(a, transA, transB, true).bytes;
+    const size_t narrow = turn_plan(a, transA, transB, false).bytes;
+    return wide > narrow ? wide : narrow;
+}
+
+// sgemm_f32 with turned operands and the stream-K schedule (see TurnPlan and
+// StreamKPlan); problems neither helps run exactly as sgemm_f32 and need no
+// workspace.
 int run_streamk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                 int64_t ldb, float *C, int64_t ldc, int transA, int transB, void *workspace,
                 uint64_t workspace_bytes, void *stream) {
@@ -273,26 +325,50 @@ int run_streamk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, co
     bool nothing = false;
     int st = validate(M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, transA, transB, a, nothing);
     if (st != SGEMM_OK || nothing) return st;
-    const bool vec = vector_ok(a);
-    const StreamKPlan pl = (K > 0 && !gemv_shape(a)) ? streamk_plan(a, transA != 0, transB != 0, vec)
-                                                      : StreamKPlan{};
-    if (pl.use && (workspace == nullptr || !aligned(workspace, 256) ||
-                   workspace_bytes < pl.ws_bytes))
-        return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: stream-K needs %llu bytes, "
+    const bool matvec = K == 0 || gemv_shape(a);
+    const TurnPlan need = matvec ? TurnPlan{} : turn_plan(a, transA != 0, transB != 0, true);
+    const size_t need_bytes = matvec ? 0 : turn_plan_bytes(a, transA != 0, transB != 0);
+    if (need_bytes > 0 && (workspace == nullptr || !aligned(workspace, 256) ||
+                           workspace_bytes < need_bytes))
+        return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: this problem needs %llu bytes, "
                     "256-byte aligned", workspace, (unsigned long long)workspace_bytes,
-                    (unsigned long long)pl.ws_bytes);
+                    (unsigned long long)need_bytes);
     st = check_device();
     if (st != SGEMM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (K == 0)
+    cudaError_t e = cudaSuccess;
+    if (K == 0) {
         e = launch_epilogue_only(a, s);
-    else if (gemv_shape(a))
+    } else if (gemv_shape(a)) {
         e = launch_gemv(a, transA != 0, transB != 0, s);
-    else if (pl.use)
-        e = launch_simt_streamk(a, transA != 0, transB != 0, vec, pl, workspace, s);
-    else
-        e = launch_simt(a, transA != 0, transB != 0, vec, s);
+    } else {
+        // the problem the tile kernel sees: turned copies in the workspace
+        GemmArgs t = a;
+        bool tA = transA != 0, tB = transB != 0;
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        if (need.turnA) {
+            float *copy = reinterpret_cast<float *>(ws + need.offA);
+            e = launch_transpose(a.A, a.lda, a.M, a.K, copy, need.ldA, s);   // M x K -> K x M
+            t.A = copy;
+            t.lda = need.ldA;
+            tA = true;
+        }
+        if (e == cudaSuccess && need.turnB) {
+            float *copy = reinterpret_cast<float *>(ws + need.offB);
+            e = launch_transpose(a.B, a.ldb, a.N, a.K, copy, need.ldB, s);   // N x K -> K x N
+            t.B = copy;
+            t.ldb = need.ldB;
+            tB = false;
+        }
+        if (e == cudaSuccess) {
+            const bool vec = vector_ok(t);
+            const StreamKPlan sk = streamk_plan(t, tA, tB, vec);
+            if (sk.use)
+                e = launch_simt_streamk(t, tA, tB, vec, sk, ws + need.offP, s);
+            else
+                e = launch_simt(t, tA, tB, vec, s);
+        }
+    }
     if (e != cudaSuccess)
         return fail(SGEMM_ELAUNCH, "kernel launch failed: %s", cudaGetErrorString(e));
     return SGEMM_OK;
@@ -446,21 +522,16 @@ int sgemm_f32_streamk(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
                               workspace_bytes, stream);
 }
 
-uint64_t sgemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K) {
-    if (M <= 1 || N <= 1 || K <= 0 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return 0;
+uint64_t sgemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K, int transA, int transB) {
+    if (M <= 1 || N <= 1 || K <= 0 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30) ||
+        (transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return 0;
     sgemm::GemmArgs a = {};
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
     a.batch = 1;
-    // the layout that uses stream-K (A transposed, B row-major), with either
-    // tile width (it depends on alignment): the larger need of the two
-    const sgemm::StreamKPlan wide = sgemm::streamk_plan(a, true, false, true);
-    const sgemm::StreamKPlan narrow = sgemm::streamk_plan(a, true, false, false);
-    uint64_t need = 0;
-    if (wide.use) need = wide.ws_bytes;
-    if (narrow.use && narrow.ws_bytes > need) need = narrow.ws_bytes;
-    return need;
+    return sgemm::turn_plan_bytes(a, transA != 0, transB != 0);
 }
 
 int sgemm_f32_splitk_auto_splits(int64_t M, int64_t N, int64_t K) {

@@ -72,6 +72,11 @@ StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec);
 cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
                                 const StreamKPlan &plan, void *ws, cudaStream_t s);
 
+// Y = X^T for a rows x cols row-major X (leading dimension ldx) into Y
+// (cols x rows, leading dimension ldy): exact copy, coalesced both ways.
+cudaError_t launch_transpose(const float *X, int64_t ldx, int rows, int cols, float *Y, int64_t ldy,
+                             cudaStream_t s);
+
 // Matrix-vector shapes (N == 1 or M == 1): bandwidth-bound kernels.
 bool gemv_shape(const GemmArgs &a);
 cudaError_t launch_gemv(const GemmArgs &a, bool transA, bool transB, cudaStream_t s);

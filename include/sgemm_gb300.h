@@ -167,29 +167,34 @@ int sgemm_f32_splitk(int64_t M, int64_t N, int64_t K,
                      void *workspace, uint64_t workspace_bytes, void *stream);
 
 /*
- * sgemm_f32 with a stream-K schedule, for problems whose output tiles fill
- * the SMs a non-whole number of times (3072 x 3072 x 3072: 288 tiles of
- * 128 x 256 on 152 SMs leaves 16 SMs idle through the second wave), with A
- * stored transposed (transA = 1) and B row-major (transB = 0); other layouts
- * corner-turn an operand through registers, which the stream-K kernel runs
- * slower than it gains, and they run exactly as sgemm_f32.  Whole
- * waves of tiles are computed whole; the K slices of the remaining tiles are
- * dealt out evenly over one CTA per SM, and the tiles shared between CTAs are
- * finished by a second pass that adds their pieces in K order from the
- * workspace.  Deterministic on a given device (the split points depend on
- * the SM count), not bit-identical to sgemm_f32 on the shared tiles, meets
- * the same FP32 bound and is exact on small integers.
- * Defined by: the split-K stage of the ChetanC28/cuda-kernels page (K split
- * across blocks, partial sums reduced afterwards), applied to the tail of the
- * tile schedule; each piece computed as in sgemm_f32.
+ * sgemm_f32 using a caller workspace for two things the tile kernel gains
+ * from.  Deterministic on a given device, not bit-identical to sgemm_f32,
+ * meets the same FP32 bound and is exact on small integers.
+ *   1. Operand turning.  In a large problem (2MNK >= 1.6e10) an operand
+ *      contiguous along K (row-major A with N >= 1024, or B stored transposed
+ *      with M >= 1024) is first copied, transposed, into the workspace.  The
+ *      tile kernel then streams both operands with 16-byte cp.async instead
+ *      of corner-turning one through registers, as it does for A stored
+ *      transposed with row-major B, the fastest layout (3072^3: 61.3 against
+ *      58.0 TFLOP/s).  The copy is exact and costs about 8 bytes per element.
+ *   2. A stream-K schedule, for that layout, when the output tiles fill the
+ *      SMs a non-whole number of times (3072^3: 288 tiles of 128 x 256 on 152
+ *      SMs leaves 16 SMs idle through the second wave).  Whole waves of tiles
+ *      are computed whole; the K slices of the remaining tiles are dealt out
+ *      evenly over one CTA per SM, and the tiles shared between CTAs are
+ *      finished by a second pass that adds their pieces in K order.
+ * Defined by: the GEMM of "CUDA GEMM operator performance optimization",
+ * section 1.1, with the transposed-operand layout of its section 7.3 and the
+ * split-K stage of the ChetanC28/cuda-kernels page (K split across blocks,
+ * partial sums reduced afterwards) applied to the tail of the tile schedule.
  *   workspace  caller-owned device memory of at least
- *              sgemm_f32_streamk_workspace_size(M, N, K) bytes, 256-byte
- *              aligned, not overlapping A, B or C, not used by other work
- *              while this call runs on `stream`.  Problems that stream-K
- *              cannot help (other layouts, tiles fewer than SMs or a whole
- *              multiple of them, matrix-vector shapes, K = 0) run as sgemm_f32
- *              and need none: workspace may then be NULL.
- *              SGEMM_EWORKSPACE if required and missing or too small.
+ *              sgemm_f32_streamk_workspace_size(M, N, K, transA, transB)
+ *              bytes, 256-byte aligned, not overlapping A, B or C, not used
+ *              by other work while this call runs on `stream`.  Problems that
+ *              neither step helps (small ones, matrix-vector shapes, K = 0)
+ *              run as sgemm_f32 and need none: the size is then 0 and
+ *              workspace may be NULL.  SGEMM_EWORKSPACE if required and
+ *              missing or too small.
  * Not batched.  Arguments otherwise as sgemm_f32.
  */
 int sgemm_f32_streamk(int64_t M, int64_t N, int64_t K,
@@ -199,11 +204,11 @@ int sgemm_f32_streamk(int64_t M, int64_t N, int64_t K,
                       int transA, int transB,
                       void *workspace, uint64_t workspace_bytes, void *stream);
 
-/* Workspace bytes for sgemm_f32_streamk on the current device when A is
- * stored transposed and B row-major: two partial tiles per SM (about 40 MB on
- * GB300), or 0 when such a problem does not use the stream-K schedule.  Other
- * layouts need none. */
-uint64_t sgemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K);
+/* Workspace bytes for sgemm_f32_streamk on the current device: the turned
+ * copies (K x round_up(M, 4) and/or K x round_up(N, 4) floats) and, when the
+ * stream-K schedule applies, two partial tiles per SM (about 40 MB on
+ * GB300); 0 when the call needs none. */
+uint64_t sgemm_f32_streamk_workspace_size(int64_t M, int64_t N, int64_t K, int transA, int transB);
 
 /* Number of K chunks chosen for splits = 0: enough 128 x 128 tiles to put one
  * CTA on every SM of the current device, each chunk at least 32 deep (one K

@@ -41,7 +41,7 @@ def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
     fn = getattr(sg, entry)
     extra = ()
     if entry == "sgemm_f32_streamk":
-        need = sg.streamk_workspace_size(M, N, K)
+        need = sg.streamk_workspace_size(M, N, K, case["transA"], case["transB"])
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
         extra = (ws.data_ptr(), need)
     if entry == "sgemm_f32_splitk":

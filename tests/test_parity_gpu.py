@@ -680,22 +680,26 @@ def test_persistent_tensor_epilogue_many_tiles():
 
 # ---------------------------------------------------------------- stream-K
 
-# sgemm_f32_streamk (A stored transposed, B row-major): whole waves of tiles
-# computed whole, the K slices of the remaining tiles dealt out over one CTA
-# per SM and the shared tiles finished from the workspace.  Shapes give a
-# wide-tile tail (3072^3), ragged edges, pieces of a single K slice, a shape
-# with fewer tiles than SMs, and other layouts (which run as sgemm_f32).
-STREAMK = [(3072, 3072, 3072, 1, 0), (3072, 3072, 3072, 0, 0), (2049, 3071, 1537, 1, 0),
-           (1300, 2100, 700, 1, 0), (2000, 2600, 64, 1, 0), (200, 300, 100, 1, 0),
-           (1300, 2100, 700, 0, 1)]
+# sgemm_f32_streamk: K-contiguous operands of large problems turned into
+# copies in the workspace, then (A stored transposed, B row-major) whole waves
+# of tiles computed whole, the K slices of the remaining tiles dealt out over
+# one CTA per SM and the shared tiles finished from the workspace.  Shapes
+# give a wide-tile tail (3072^3) in every layout (turned or not), ragged edges,
+# pieces of a single K slice, misaligned operands (narrow tiles), and shapes
+# too small for either step (which run as sgemm_f32).
+STREAMK = [(3072, 3072, 3072, 1, 0, 0), (3072, 3072, 3072, 0, 0, 0), (3000, 3000, 1000, 0, 1, 0),
+           (2500, 2500, 1500, 1, 1, 0), (2049, 3071, 1537, 1, 0, 0), (1300, 2100, 700, 1, 0, 0),
+           (2000, 2600, 64, 1, 0, 0), (200, 300, 100, 1, 0, 0), (1300, 2100, 700, 0, 1, 0),
+           (3000, 2900, 1000, 0, 0, 1), (2100, 3100, 1900, 1, 0, 3)]
 
 
-@pytest.mark.parametrize("M,N,K,tA,tB", STREAMK)
-def test_streamk_exact_on_integers(M, N, K, tA, tB):
+@pytest.mark.parametrize("M,N,K,tA,tB,offset", STREAMK)
+def test_streamk_exact_on_integers(M, N, K, tA, tB, offset):
     case = workloads.make_operands(M, N, K, transA=tA, transB=tB, ldc=N + 4, dist="int",
                                    poison=True, seed=90, key=900 + M + N + K)
-    got = run(case, entry="sgemm_f32_streamk")
-    check_full(case, got, exact=True, label=f"streamk {M}x{N}x{K} tA={tA} tB={tB}")
+    got = run(case, entry="sgemm_f32_streamk", offset=offset)
+    check_full(case, got, exact=True,
+               label=f"streamk {M}x{N}x{K} tA={tA} tB={tB} offset={offset}")
 
 
 def test_streamk_within_bound_and_deterministic():
@@ -708,12 +712,15 @@ def test_streamk_within_bound_and_deterministic():
 def test_streamk_workspace_checked_on_host():
     import torch
     M = N = K = 3072
-    need = sg.streamk_workspace_size(M, N, K)
+    need = sg.streamk_workspace_size(M, N, K, 1, 0)
     assert need > 0
+    # row-major A is turned first: its copy (K x M floats) comes on top
+    assert sg.streamk_workspace_size(M, N, K, 0, 0) == need + K * M * 4
+    assert sg.streamk_workspace_size(M, N, K, 0, 1) == need + 2 * K * M * 4
     A = torch.empty(K, M, device="cuda")   # stored transposed
     B = torch.empty(K, N, device="cuda")
     C = torch.empty(M, N, device="cuda")
     st = sg.sgemm_f32_streamk(M, N, K, A.data_ptr(), M, B.data_ptr(), N, C.data_ptr(), N, 1, 0,
                               0, 0, check=False)
     assert st == 8, sg.last_error()
-    assert sg.streamk_workspace_size(256, 256, 256) == 0   # fewer tiles than SMs: plain kernel
+    assert sg.streamk_workspace_size(256, 256, 256, 0, 0) == 0   # small: runs as sgemm_f32
