@@ -166,6 +166,8 @@ KERNEL_SOURCES = {
     "sgemm_simt_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh",
                           "simt_nn.cu"],
     "tf32x3_persistent_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
+    "sgemm_simt_streamk_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh",
+                                  "simt_launch.cuh", "simt_tn.cu"],
 }
 
 
@@ -288,6 +290,37 @@ def tf32_probe_tflops(torch, sg, dev, stream, iters=16384, reps=5):
         ts.append(e0.elapsed_time(e1))
     ms = sorted(ts)[len(ts) // 2]
     return flops / (ms * 1e-3) / 1e12
+
+
+def streamk_plan(M, N, K, transA, transB, need):
+    """(transposes, stream-K used) of one sgemm_f32_streamk call: a transpose
+    per turned operand, then the tile kernel, plus the fix-up pass when
+    stream-K applies.  Mirrors the library's rule (include/sgemm_gb300.h):
+    in problems with 2MNK >= 1.6e10, row-major A is turned when N >= 1024 and
+    B^T when M >= 1024; the workspace beyond the copies is stream-K's."""
+    big = 2.0 * M * N * K >= 1.6e10
+    turn_a = big and not transA and N >= 1024
+    turn_b = big and transB and M >= 1024
+    copies = 0
+    for on, rows in ((turn_a, M), (turn_b, N)):
+        if on:
+            copies += (K * ((rows + 3) // 4 * 4) * 4 + 255) // 256 * 256
+    return int(turn_a) + int(turn_b), need > copies
+
+
+def streamk_launches(M, N, K, transA, transB, need) -> int:
+    turned, sk = streamk_plan(M, N, K, transA, transB, need)
+    return turned + 1 + int(sk)
+
+
+def step_kernel_label(M, N, K, transA, transB, need, batch, plain_label) -> str:
+    if batch != 1:
+        return plain_label
+    turned, sk = streamk_plan(M, N, K, transA, transB, need)
+    parts = ["transpose_kernel (K-contiguous operand -> workspace copy)"] * turned
+    parts.append("sgemm_simt_streamk_kernel (one CTA per SM) + streamk_fixup_kernel" if sk
+                 else plain_label)
+    return " + ".join(parts)
 
 
 def cpu_baseline(case, target_s: float):
@@ -444,7 +477,15 @@ def main():
             sets.append((dA, dB, dC))
     torch.cuda.synchronize(dev)
 
-    def step(i):
+    # The step is one sgemm_f32_streamk call (single problems): the library's
+    # fastest FP32 CUDA-core path, with its workspace allocated once here.
+    # Batched problems use sgemm_f32_strided_batched.  Plain sgemm_f32 is
+    # timed the same way afterwards and reported beside it.
+    sk_need = sg.streamk_workspace_size(M, N, K, w.transA, w.transB) if batch == 1 else 0
+    sk_ws = torch.empty(max(sk_need, 1), dtype=torch.uint8, device=dev)
+    launches = streamk_launches(M, N, K, w.transA, w.transB, sk_need) if batch == 1 else 1
+
+    def plain_step(i):
         dA, dB, dC = sets[i % nsets]
         if batch == 1:
             sg.sgemm_f32(M, N, K, dA.data_ptr(), lda, dB.data_ptr(), ldb, dC.data_ptr(), ldc,
@@ -453,6 +494,13 @@ def main():
             sg.sgemm_f32_strided_batched(M, N, K, dA.data_ptr(), lda, case["A"][0].size,
                                          dB.data_ptr(), ldb, case["B"][0].size, dC.data_ptr(),
                                          ldc, M * ldc, batch, w.transA, w.transB, sp)
+
+    def step(i):
+        if batch != 1:
+            return plain_step(i)
+        dA, dB, dC = sets[i % nsets]
+        sg.sgemm_f32_streamk(M, N, K, dA.data_ptr(), lda, dB.data_ptr(), ldb, dC.data_ptr(), ldc,
+                             w.transA, w.transB, sk_ws.data_ptr(), sk_need, sp)
 
     for i in range(args.warmup):
         step(i)
@@ -542,6 +590,21 @@ def main():
     torch.cuda.synchronize(dev)
     cold = sorted(a.elapsed_time(b) for a, b in zip(c0, c1))
     del flush
+
+    # plain sgemm_f32 (one kernel), same protocol, reported beside the step
+    plain_ms = None
+    if batch == 1:
+        for i in range(args.warmup):
+            plain_step(i)
+        torch.cuda.synchronize(dev)
+        p0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        p1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            p0[i].record(stream)
+            plain_step(i)
+            p1[i].record(stream)
+        torch.cuda.synchronize(dev)
+        plain_ms = reduce_max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(p0, p1)), dev) / args.steps
     h2d = (case["A"].size + case["B"].size) * 4
     d2h = batch * M * ldc * 4
 
@@ -714,7 +777,12 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"{nsets} rotating input sets of {workloads.min_bytes(M, N, K, batch) / 1e6:.0f} MB "
                          f"(> 129 MB L2 together); each step starts with its operands evicted",
-                   "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label, K)},
+                   "entry": "sgemm_f32_streamk" if batch == 1 else "sgemm_f32_strided_batched",
+                   "workspace_bytes": sk_need,
+                   "kernels_per_step": launches,
+                   "kernel": step_kernel_label(M, N, K, w.transA, w.transB, sk_need, batch,
+                                               simt_kernel_label(M, N, batch, w.transB,
+                                                                 sms_for_label, K))},
         "pct_of_fp32_peak": {
             "at_max_clock": 100.0 * per_gpu / peak_max,
             "peak_tflops_at_max_clock": peak_max,
@@ -727,18 +795,23 @@ def main():
             "peak": peak_max,
             "unit": "TFLOP/s",
             "frac": achieved / peak_max,
-            "traffic": profiled_traffic("sgemm_simt_kernel", args.workload),
+            "traffic": profiled_traffic("sgemm_simt_streamk_kernel"
+                                        if batch == 1 and streamk_plan(M, N, K, w.transA, w.transB,
+                                                                       sk_need)[1]
+                                        else "sgemm_simt_kernel", args.workload),
             "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
                            f"{sm_max:.0f} MHz",
             "algorithmic_flops_per_launch": flops,
+            "note": "achieved = algorithmic FLOPs / CUDA-event time of the whole call (transpose "
+                    "and fix-up kernels included), so the tile kernel alone runs a little faster",
         },
         "clocks": clocks,
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": e2e_steps,
-                "method": "pinned host A, B -> device, sgemm_f32, C -> pinned host, every step; "
-                          "two buffer sets on upload/compute/download streams, CUDA events"},
-        "gpu_launches": args.steps,
+                "method": "pinned host A, B -> device, the step's call, C -> pinned host, every "
+                          "step; two buffer sets on upload/compute/download streams, CUDA events"},
+        "gpu_launches": args.steps * launches,
         "timing": {"mean_ms": ms_per_step, "median_ms": sorted(durs)[len(durs) // 2],
                    "min_ms": min(durs), "max_ms": max(durs),
                    "cold_l2": {"median_ms": cold[len(cold) // 2],
@@ -748,6 +821,16 @@ def main():
                                          "outside the call's events"}},
         "wall_s": wall,
     }
+    if plain_ms is not None:
+        plain = flops / (plain_ms * 1e-3) / 1e12
+        line["sgemm_f32"] = {
+            "value": world * plain, "unit": "TFLOP/s", "ms_per_step": plain_ms,
+            "pct_of_fp32_peak_at_max_clock": 100.0 * plain / peak_max,
+            "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label, K),
+            "roofline": {"bound": "alu", "achieved": plain, "peak": peak_max, "unit": "TFLOP/s",
+                         "frac": plain / peak_max,
+                         "traffic": profiled_traffic("sgemm_simt_kernel", args.workload)},
+            "note": "the same product through plain sgemm_f32 (one kernel, no workspace)"}
     if tc is not None:
         tc["pct_of_fp32_peak_at_max_clock"] = 100.0 * tc["value"] / world / peak_max
         line["tf32x3"] = tc
