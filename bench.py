@@ -168,6 +168,10 @@ KERNEL_SOURCES = {
     "tf32x3_persistent_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
     "sgemm_simt_streamk_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh",
                                   "simt_launch.cuh", "simt_tn.cu"],
+    "sgemm_simt_streamk_tma_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh",
+                                      "simt_launch.cuh", "tc_utils.cuh", "simt_tma.cu"],
+    "sgemm_simt_tma_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh",
+                              "simt_launch.cuh", "tc_utils.cuh", "simt_tma.cu"],
 }
 
 
@@ -197,11 +201,15 @@ def profiled_traffic(kernel: str, workload: str):
     return None
 
 
-def simt_kernel_label(M, N, batch, transB, sms, K=3072):
+def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
     """The tile the library's launcher picks (same rules as
-    csrc/simt_launch.cuh: K <= 256 takes two CTAs per SM; otherwise waves of
-    one CTA per SM, a 128x256 tile costing 1.95 128x128 tiles, the wide tile
-    only for row-major B)."""
+    csrc/simt_launch.cuh, for 16-byte aligned operands: A stored transposed
+    with row-major B takes the TMA-fed kernel; else K <= 256 takes two CTAs
+    per SM; otherwise waves of one CTA per SM, a 128x256 tile costing 1.95
+    128x128 tiles, the wide tile only for row-major B)."""
+    if transA and not transB:
+        return ("sgemm_simt_tma_kernel 128x128 tile, BK 32, 3 stages, 2 CTAs/SM, TMA-fed, "
+                "fma.rn.f32x2")
     if K <= 256:
         return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
     tm = -(-M // 128)
@@ -318,8 +326,8 @@ def step_kernel_label(M, N, K, transA, transB, need, batch, plain_label) -> str:
         return plain_label
     turned, sk = streamk_plan(M, N, K, transA, transB, need)
     parts = ["transpose_kernel (K-contiguous operand -> workspace copy)"] * turned
-    parts.append("sgemm_simt_streamk_kernel (one CTA per SM) + streamk_fixup_kernel" if sk
-                 else plain_label)
+    parts.append("sgemm_simt_streamk_tma_kernel (TMA-fed, two CTAs per SM) + streamk_fixup_kernel"
+                 if sk else plain_label)
     return " + ".join(parts)
 
 
@@ -795,7 +803,7 @@ def main():
             "peak": peak_max,
             "unit": "TFLOP/s",
             "frac": achieved / peak_max,
-            "traffic": profiled_traffic("sgemm_simt_streamk_kernel"
+            "traffic": profiled_traffic("sgemm_simt_streamk_tma_kernel"
                                         if batch == 1 and streamk_plan(M, N, K, w.transA, w.transB,
                                                                        sk_need)[1]
                                         else "sgemm_simt_kernel", args.workload),
@@ -826,7 +834,7 @@ def main():
         line["sgemm_f32"] = {
             "value": world * plain, "unit": "TFLOP/s", "ms_per_step": plain_ms,
             "pct_of_fp32_peak_at_max_clock": 100.0 * plain / peak_max,
-            "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label, K),
+            "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label, K, w.transA),
             "roofline": {"bound": "alu", "achieved": plain, "peak": peak_max, "unit": "TFLOP/s",
                          "frac": plain / peak_max,
                          "traffic": profiled_traffic("sgemm_simt_kernel", args.workload)},

@@ -32,6 +32,12 @@ cudaError_t launch_simt_streamk_tt(const GemmArgs &, bool, const StreamKPlan &, 
 
 cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
                                 const StreamKPlan &pl, void *ws, cudaStream_t s) {
+    if (pl.tma) {
+        // the same schedule on the cp.async kernel (128 x 128 tiles) if the
+        // operands cannot be described as tensor maps
+        cudaError_t e = cudaSuccess;
+        if (launch_simt_streamk_tma(a, pl, ws, s, e)) return e;
+    }
     if (!transA && !transB) return launch_simt_streamk_nn(a, vec, pl, ws, s);
     if (!transA && transB) return launch_simt_streamk_nt(a, vec, pl, ws, s);
     if (transA && !transB) return launch_simt_streamk_tn(a, vec, pl, ws, s);
@@ -39,13 +45,14 @@ cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, boo
 }
 
 // Only for A stored transposed with row-major B: the one layout whose
-// operands both arrive by cp.async.  Where an operand is corner-turned
-// through registers (row-major A, or B^T), a CTA that runs tile after tile
-// left those 16-byte global loads exposed (long-scoreboard stalls 0.007 ->
-// 0.75 per instruction, 15 % slower per tile on 2048 x 4864 x 4096), more
-// than the wave tail stream-K removes.  The wide 128 x 256 tile wherever the
-// kernel allows it (16-byte access): with the wave tail gone, the wider
-// tile's better operand reuse is all that remains of the choice.
+// operands both arrive without a corner turn.  Where an operand is
+// corner-turned through registers (row-major A, or B^T), a CTA that runs tile
+// after tile left those 16-byte global loads exposed (long-scoreboard stalls
+// 0.007 -> 0.75 per instruction, 15 % slower per tile on 2048 x 4864 x 4096),
+// more than the wave tail stream-K removes.  With 16-byte aligned operands
+// the TMA-fed kernel runs it on 128 x 128 tiles over every resident CTA (two
+// per SM); otherwise the cp.async kernel on one CTA per SM, with 128 x 256
+// tiles where it can use 16-byte access.
 StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec) {
     StreamKPlan pl = {};
     if (!transA || transB) return pl;
@@ -53,17 +60,18 @@ StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec) 
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return pl;
-    pl.wide = vec && !transB;
+    pl.tma = simt_tma_eligible(a, transA, transB, vec);
+    pl.wide = !pl.tma && vec && !transB;
     const int64_t bn = pl.wide ? 256 : 128;
     const int64_t tiles = (int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + bn - 1) / bn);
-    pl.G = sms;
+    pl.G = sms * (pl.tma ? simt_tma_ctas_per_sm() : 1);
     pl.kslices = (a.K + 31) / 32;
-    pl.use = tiles > sms && tiles % sms != 0 && pl.kslices >= 2 && tiles <= (1LL << 30);
+    pl.use = tiles > pl.G && tiles % pl.G != 0 && pl.kslices >= 2 && tiles <= (1LL << 30);
     if (!pl.use) return pl;
-    pl.tiles_dp = (int)(tiles / sms * sms);
+    pl.tiles_dp = (int)(tiles / pl.G * pl.G);
     pl.tiles_sk = (int)(tiles - pl.tiles_dp);
     pl.units = (int64_t)pl.tiles_sk * pl.kslices;
-    pl.ws_bytes = (size_t)sms * 2 * 128 * (size_t)bn * sizeof(float);
+    pl.ws_bytes = (size_t)pl.G * 2 * 128 * (size_t)bn * sizeof(float);
     return pl;
 }
 

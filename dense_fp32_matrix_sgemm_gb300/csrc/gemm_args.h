@@ -58,19 +58,35 @@ int splitk_auto_splits(int64_t M, int64_t N, int64_t K);
 
 // Stream-K schedule of the SIMT kernel (sgemm_f32_streamk): whole waves of
 // tiles computed whole, the K slices of the remaining tiles dealt out evenly
-// over one CTA per SM, shared tiles finished by a fix-up pass from the
+// over every resident CTA, shared tiles finished by a fix-up pass from the
 // caller's workspace.  `use` is false where it cannot help (the tiles fill
 // the SMs a whole number of times, or fewer tiles than SMs) and for layouts
 // that corner-turn an operand through registers (see streamk_plan).
 struct StreamKPlan {
     bool use, wide;                      // wide: 128 x 256 tiles
-    int tiles_dp, tiles_sk, kslices, G;  // G: CTAs (SMs)
+    bool tma;                            // the TMA-fed kernel (128 x 128 tiles)
+    int tiles_dp, tiles_sk, kslices, G;  // G: CTAs (SMs x resident CTAs per SM)
     int64_t units;                       // tiles_sk * kslices
     size_t ws_bytes;                     // G * 2 partial tiles
 };
 StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec);
 cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
                                 const StreamKPlan &plan, void *ws, cudaStream_t s);
+
+// The SIMT kernel fed by TMA (A stored transposed, row-major B, 16-byte
+// aligned operands, no split-K chunks): one 128 x 128 tile per CTA, two CTAs
+// per SM.  The launchers return false, launching nothing, when the operands
+// cannot be described as tensor maps; else they launch and store the status
+// in `err`.
+bool simt_tma_eligible(const GemmArgs &a, bool transA, bool transB, bool vec);
+int simt_tma_ctas_per_sm();
+bool launch_simt_tma(const GemmArgs &a, cudaStream_t s, cudaError_t &err);
+bool launch_simt_streamk_tma(const GemmArgs &a, const StreamKPlan &plan, void *ws, cudaStream_t s,
+                             cudaError_t &err);
+
+// Device address of the library's status word (bit 0: a bounded pipeline
+// wait ran out), for kernels that report into it; null if unavailable.
+unsigned int *device_error_word();
 
 // Y = X^T for a rows x cols row-major X (leading dimension ldx) into Y
 // (cols x rows, leading dimension ldy): exact copy, coalesced both ways.

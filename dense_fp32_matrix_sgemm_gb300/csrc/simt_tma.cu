@@ -1,0 +1,378 @@
+// SIMT FP32 SGEMM fed by TMA, for A stored transposed (K x M) with row-major
+// B: the layout in which both operands are contiguous along M or N, so a K
+// slice of either is a plain 2-D box of global memory.
+//
+// Same arithmetic as sgemm_simt_kernel (each output accumulated by one thread
+// in ascending k with packed fp32 FMAs, 8 x 8 register tile of 4 x 4
+// sub-blocks, Z-order warps; "CUDA GEMM operator performance optimization",
+// sections 4-8), so results are bit-identical to it.  What changes is the
+// operand pipeline (sections 9-10 of that page, with Hopper-and-later bulk
+// copies in place of per-thread loads):
+//   * one thread issues each stage as two cp.async.bulk.tensor loads (an A
+//     box of 128 x 32 and a B box of 128 x 32) that complete on the stage's
+//     mbarrier; nobody else computes a global address;
+//   * the boxes land K-major ([32][128]) with no swizzle: a warp's fragment
+//     loads touch 4 (A) and 8 (B) consecutive 16-byte chunks of one row, so
+//     they are conflict-free as they are;
+//   * the tensor map zero-fills rows, columns and K beyond the operand, so
+//     ragged tiles need no per-element predicates;
+//   * without per-thread copy state the kernel fits 128 registers: two CTAs
+//     (16 warps) per SM, 4 warps per scheduler to hide the FMA and
+//     shared-load latencies.  The cp.async kernel needs 8 x 16 tiles and one
+//     CTA per SM to avoid spilling.
+// Two kernels: one tile per CTA (sgemm_f32, strided batches as the third
+// tensor dimension) and the stream-K schedule (sgemm_f32_streamk) over two
+// CTAs per SM.  Every mbarrier wait is bounded; one that runs out sets bit 0
+// of the library's device status word and the CTA finishes without waiting
+// again.
+#include <atomic>
+#include <cstdint>
+
+#include "simt_launch.cuh"
+#include "tc_utils.cuh"
+#include "tma_encode.h"
+
+namespace sgemm {
+namespace simt {
+
+constexpr int kTmaBK = 32;       // K slice per stage
+constexpr int kTmaStages = 3;    // 3 x 32 KB of operands per CTA
+constexpr int kTmaBN = 128;      // tile 128 x 128
+constexpr int kTmaMinBlocks = 2;
+
+template <int BK, int STAGES, int BN_>
+constexpr int tma_smem_bytes() {
+    // operand ring, then STAGES "full" mbarriers and the CTA's abort word
+    return STAGES * BK * (BM + BN_) * (int)sizeof(float) + 8 * STAGES + 16;
+}
+
+// Initialises the stage barriers (one arrival each: the issuing thread's
+// expect_tx) and the abort word; returns the shared address of barrier 0.
+template <int BK, int STAGES, int BN_>
+__device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int *&abort) {
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * BK * (BM + BN_));
+    abort = reinterpret_cast<volatile int *>(bars + STAGES);
+    const uint32_t full0 = smem_u32(bars);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * s, 1);
+        *abort = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    return full0;
+}
+
+// Accumulates slices [0, ktiles) of one piece, starting at K offset kbeg, of
+// the tile at (m0, n0) of problem z into acc (zeroed first).  gk counts the
+// slices this CTA has consumed before the piece: slice g uses stage
+// g % STAGES in its (g / STAGES)-th round, so the stage barrier's phase
+// parity is (g / STAGES) & 1.  Every thread keeps the same count.  On return
+// no copy of this piece is in flight (every issued slice has been waited on).
+template <int BK, int STAGES, int BN_>
+__device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                             float *As, float *Bs, uint32_t full0, uint32_t &gk,
+                                             int m0, int n0, int z, int kbeg, int ktiles,
+                                             int a_col, int b_col, float (&acc)[8][BN_ / 16],
+                                             volatile int *abort) {
+    constexpr int TN = BN_ / 16;
+    constexpr int NSB = BN_ / 64;
+    constexpr int ATILE = BK * BM;
+    constexpr int BTILE = BK * BN_;
+    constexpr uint32_t STAGE_BYTES = (ATILE + BTILE) * sizeof(float);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    const bool issuer = threadIdx.x == 0;
+    const uint32_t g0 = gk;          // the piece's slice j is the CTA's slice g0 + j
+    auto issue = [&](int slice) {   // slice of this piece -> its stage
+        const uint32_t st = (g0 + (uint32_t)slice) % STAGES;
+        const uint32_t bar = full0 + 8 * st;
+        tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, m0, kbeg + slice * BK, z);
+        tc::tma_load_3d(smem_u32(Bs + st * BTILE), tmB, bar, n0, kbeg + slice * BK, z);
+    };
+    // The stages of the piece's first slices were last read by slices that
+    // every thread finished before the previous barrier: safe to refill.
+    if (issuer) {
+#pragma unroll
+        for (int s = 0; s < STAGES - 1; ++s)
+            if (s < ktiles) issue(s);
+    }
+    for (int kt = 0; kt < ktiles; ++kt) {
+        // every warp is done with the stage of slice kt - 1, which is the
+        // stage slice kt + STAGES - 1 goes to
+        __syncthreads();
+        if (issuer && kt + STAGES - 1 < ktiles) issue(kt + STAGES - 1);
+        const uint32_t rs = gk % STAGES;
+        (void)tc::mbar_wait(full0 + 8 * rs, (gk / STAGES) & 1, abort);
+        ++gk;
+        const float *at = As + rs * ATILE;
+        const float *bt = Bs + rs * BTILE;
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            const float *ar = at + kk * BM;
+            const float *br = bt + kk * BN_;
+            const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float b[TN];
+#pragma unroll
+            for (int h = 0; h < NSB; ++h) {
+                const float4 bv = *reinterpret_cast<const float4 *>(br + 64 * h + b_col);
+                b[4 * h + 0] = bv.x;
+                b[4 * h + 1] = bv.y;
+                b[4 * h + 2] = bv.z;
+                b[4 * h + 3] = bv.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                for (int j = 0; j < TN; j += 2) {
+                    float2 c = make_float2(acc[i][j], acc[i][j + 1]);
+                    c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
+                    acc[i][j] = c.x;
+                    acc[i][j + 1] = c.y;
+                }
+            }
+        }
+    }
+}
+
+// The thread's place in the tile: rows a_col..a_col+3 and +64, columns
+// b_col..b_col+3 and +64 (Z-order 4 x 8 warps, 2 warps across).
+__device__ __forceinline__ void thread_coords(int &a_col, int &b_col) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane_row = (lane & 1) | ((lane >> 4) << 1);
+    const int lane_col = (lane >> 1) & 7;
+    a_col = 4 * ((warp >> 1) * 4 + lane_row);
+    b_col = 4 * ((warp & 1) * 8 + lane_col);
+}
+
+template <int BN_>
+__device__ __forceinline__ void store_tile(const GemmArgs &p, int z, int m0, int n0, int a_col,
+                                           int b_col, const float (&acc)[8][BN_ / 16]) {
+    constexpr int NSB = BN_ / 64;
+    float *Cz = p.C + (int64_t)z * p.strideC;
+    const bool plain = plain_epilogue(p);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int row = m0 + (r < 4 ? a_col + r : 64 + a_col + (r - 4));
+        if (row >= p.M) continue;
+        float *crow = Cz + (int64_t)row * p.ldc;
+#pragma unroll
+        for (int h = 0; h < NSB; ++h)
+            store_c4(p, crow, n0 + h * 64 + b_col,
+                     make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
+                                 acc[r][4 * h + 3]),
+                     true, plain);
+    }
+}
+
+// One 128 x BN_ tile per CTA, all of K.
+template <int BK, int STAGES, int BN_, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB)
+sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
+                      unsigned int *status) {
+    extern __shared__ __align__(128) float smem[];
+    float *As = smem;
+    float *Bs = smem + STAGES * BK * BM;
+    volatile int *abort;
+    const uint32_t full0 = tma_pipeline_init<BK, STAGES, BN_>(smem, abort);
+    if (threadIdx.x == 0) {
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    int z, tm, tn;
+    raster(p, (int)blockIdx.x, z, tm, tn);
+    int a_col, b_col;
+    thread_coords(a_col, b_col);
+    float acc[8][BN_ / 16];
+    uint32_t gk = 0;
+    tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
+                                  (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
+    if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+    store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+}
+
+// The stream-K schedule of sgemm_simt_streamk_kernel (see StreamK), fed by
+// TMA; K slices are BK deep.
+template <int BK, int STAGES, int BN_, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB)
+sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
+                              const StreamK sk, unsigned int *status) {
+    constexpr int NSB = BN_ / 64;
+    extern __shared__ __align__(128) float smem[];
+    float *As = smem;
+    float *Bs = smem + STAGES * BK * BM;
+    volatile int *abort;
+    const uint32_t full0 = tma_pipeline_init<BK, STAGES, BN_>(smem, abort);
+    if (threadIdx.x == 0) {
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    int a_col, b_col;
+    thread_coords(a_col, b_col);
+
+    // Everything about piece i is recomputed from (blockIdx.x, i), as in
+    // sgemm_simt_streamk_kernel: at most two stream-K pieces per CTA.
+    const int c = blockIdx.x;
+    const int ndp = c < sk.tiles_dp ? (sk.tiles_dp - 1 - c) / sk.G + 1 : 0;
+    int nsk;
+    {
+        const int64_t u0 = (int64_t)c * sk.units / sk.G, u1 = ((int64_t)c + 1) * sk.units / sk.G;
+        nsk = u0 == u1 ? 0 : (u0 / sk.kslices == (u1 - 1) / sk.kslices ? 1 : 2);
+    }
+    uint32_t gk = 0;
+#pragma unroll 1
+    for (int i = 0; i < ndp + nsk; ++i) {
+        int t, s0, s1;
+        float *part = nullptr;   // null: store the finished tile to C
+        if (i < ndp) {
+            t = c + i * sk.G;
+            s0 = 0;
+            s1 = sk.kslices;
+        } else {
+            const int k = i - ndp;   // 0: the range's first piece, 1: its last
+            const int64_t u0 = (int64_t)c * sk.units / sk.G;
+            const int64_t u1 = ((int64_t)c + 1) * sk.units / sk.G;
+            const int64_t ub = k == 0 ? u0 : (u0 / sk.kslices + 1) * sk.kslices;
+            const int tl = (int)(ub / sk.kslices);
+            s0 = (int)(ub - (int64_t)tl * sk.kslices);
+            s1 = (int)min((int64_t)sk.kslices, s0 + (u1 - ub));
+            t = sk.tiles_dp + tl;
+            if (!(s0 == 0 && s1 == sk.kslices))
+                part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
+        }
+        int z, tm, tn;
+        raster(p, t, z, tm, tn);
+        float acc[8][BN_ / 16];
+        tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, s0 * BK,
+                                      s1 - s0, a_col, b_col, acc, abort);
+        if (part != nullptr) {
+            // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int row = r < 4 ? a_col + r : 64 + a_col + (r - 4);
+#pragma unroll
+                for (int h = 0; h < NSB; ++h)
+                    *reinterpret_cast<float4 *>(part + row * BN_ + h * 64 + b_col) =
+                        make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
+                                    acc[r][4 * h + 3]);
+            }
+        } else {
+            store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+        }
+    }
+    if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+}
+
+namespace {
+
+// [batch][K][cols] fp32 with row stride ld and batch stride zstride (elements),
+// boxes of box_cols x BK x 1, zero fill outside.  False when the driver
+// rejects the description (the caller then uses the cp.async kernels).
+bool make_operand_map(CUtensorMap *map, const float *base, int cols, int K, int64_t ld,
+                      int64_t zstride, int batch, int box_cols) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const int64_t zs = batch > 1 ? zstride : ld * (int64_t)K;
+    if (zs <= 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)K, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)zs * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)kTmaBK, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_maps(const GemmArgs &a, CUtensorMap &tmA, CUtensorMap &tmB) {
+    return make_operand_map(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM) &&
+           make_operand_map(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, kTmaBN);
+}
+
+}  // namespace
+}  // namespace simt
+
+bool simt_tma_eligible(const GemmArgs &a, bool transA, bool transB, bool vec) {
+    // 16-byte aligned bases and rows (vec), whole problems (no split-K
+    // chunks), distinct batches (a zero batch stride is not a tensor stride)
+    return transA && !transB && vec && a.kchunk == 0 &&
+           (a.batch == 1 || (a.strideA > 0 && a.strideB > 0));
+}
+
+int simt_tma_ctas_per_sm() {
+    using namespace simt;
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    int v = cached[dev & 63].load();
+    if (v <= 0) {
+        auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, kTmaMinBlocks>;
+        constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, THREADS, smem) != cudaSuccess ||
+            v <= 0) {
+            (void)cudaGetLastError();
+            v = 1;
+        }
+        cached[dev & 63].store(v);
+    }
+    return v;
+}
+
+bool launch_simt_tma(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
+    using namespace simt;
+    CUtensorMap tmA, tmB;
+    if (!make_maps(a, tmA, tmB)) return false;
+    auto kern = sgemm_simt_tma_kernel<kTmaBK, kTmaStages, kTmaBN, kTmaMinBlocks>;
+    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
+    static std::atomic<unsigned long long> configured{0};
+    err = ensure_smem_attribute(kern, smem, configured);
+    if (err != cudaSuccess) return true;
+    GemmArgs g = a;
+    g.tiles_m = (a.M + BM - 1) / BM;
+    g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
+    const long long blocks = (long long)g.batch * g.tiles_m * g.tiles_n;
+    kern<<<(unsigned)blocks, THREADS, smem, s>>>(tmA, tmB, g, device_error_word());
+    err = cudaGetLastError();
+    return true;
+}
+
+bool launch_simt_streamk_tma(const GemmArgs &a, const StreamKPlan &pl, void *ws, cudaStream_t s,
+                             cudaError_t &err) {
+    using namespace simt;
+    CUtensorMap tmA, tmB;
+    if (!make_maps(a, tmA, tmB)) return false;
+    auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, kTmaMinBlocks>;
+    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
+    static std::atomic<unsigned long long> configured{0};
+    err = ensure_smem_attribute(kern, smem, configured);
+    if (err != cudaSuccess) return true;
+    GemmArgs g = a;
+    g.tiles_m = (a.M + BM - 1) / BM;
+    g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
+    StreamK sk;
+    sk.tiles_dp = pl.tiles_dp;
+    sk.tiles_sk = pl.tiles_sk;
+    sk.kslices = pl.kslices;
+    sk.G = pl.G;
+    sk.units = pl.units;
+    sk.ws = static_cast<float *>(ws);
+    kern<<<(unsigned)pl.G, THREADS, smem, s>>>(tmA, tmB, g, sk, device_error_word());
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return true;
+    const dim3 grid((unsigned)(BM * kTmaBN / 1024), (unsigned)pl.tiles_sk);
+    streamk_fixup_kernel<kTmaBN, true><<<grid, 256, 0, s>>>(g, sk);
+    err = cudaGetLastError();
+    return true;
+}
+
+}  // namespace sgemm

@@ -49,6 +49,7 @@
 
 #include "gemm_args.h"
 #include "tc_utils.cuh"
+#include "tma_encode.h"
 
 namespace sgemm {
 namespace tf32x3 {
@@ -71,7 +72,9 @@ struct Config {
     static_assert(BN == 128 || BN == 256, "tile width");
 };
 
-__device__ unsigned int g_tf32x3_error = 0;   // bit 0: a pipeline wait ran out
+// The library's device status word (sgemm_device_status).  Bit 0: a
+// pipeline wait in one of its kernels ran out.
+__device__ unsigned int g_tf32x3_error = 0;
 
 // ------------------------------------------------------------------ split
 
@@ -595,26 +598,12 @@ __global__ void __launch_bounds__(THREADS, 1) tf32_mma_probe_kernel(long long it
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // Planes [planes*batch][rows][Kp] of fp32, box BK (K) x box_rows x 1, with
 // the swizzle whose span equals the BK-float row.
 template <class CFG>
 bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp, int batch,
                     int box_rows) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows,
                                 (cuuint64_t)(CFG::PLANES * batch)};
@@ -634,7 +623,7 @@ bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp
 // 32 x 32 x 1 with the 128-byte swizzle the epilogue writes in.
 bool make_c_map(CUtensorMap *map, float *C, int M, int N, int64_t ldc, int64_t strideC,
                 int batch) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batch};
     const int64_t zstride = batch > 1 ? strideC : (int64_t)M * ldc;
@@ -843,6 +832,34 @@ double tf32_mma_probe_flops_per_iteration() { return 4.0 * 2.0 * tf32x3::BM * 25
 cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t s) {
     tf32x3::wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(limit_cycles);
     return cudaGetLastError();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+unsigned int *device_error_word() {
+    static std::atomic<unsigned int *> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    unsigned int *w = cached[dev & 63].load();
+    if (w == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, tf32x3::g_tf32x3_error) != cudaSuccess) return nullptr;
+        w = static_cast<unsigned int *>(p);
+        cached[dev & 63].store(w);
+    }
+    return w;
 }
 
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset) {

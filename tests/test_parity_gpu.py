@@ -724,3 +724,61 @@ def test_streamk_workspace_checked_on_host():
                               0, 0, check=False)
     assert st == 8, sg.last_error()
     assert sg.streamk_workspace_size(256, 256, 256, 0, 0) == 0   # small: runs as sgemm_f32
+
+
+# ---------------------------------------------------------------- TMA-fed SIMT kernel
+
+# A stored transposed with row-major B and 16-byte aligned operands run on the
+# TMA-fed SIMT kernel: one thread loads each K slice as two tensor-map boxes,
+# the map zero-fills whatever lies past M, N or K, and two CTAs share an SM.
+# The same buffers shifted by one float fall back to the cp.async kernel.
+# Both accumulate every output in ascending k with the same FMAs, so the two
+# results must agree bit for bit as well as with the oracle.  The shapes have
+# either more tiles than the cluster split takes or a single K slice, so the
+# TMA kernel is the one that runs: 1 to 100 tiles, ragged M, N and K, a
+# K tail of one element, single rows of tiles and columns of tiles.
+def _rup4(x):
+    return (x + 3) // 4 * 4
+
+
+TMA = [(2, 8, 5), (129, 132, 32), (1100, 1300, 77), (1200, 1204, 999), (260, 4100, 31),
+       (4100, 260, 2049), (9000, 132, 64), (1100, 1300, 33)]
+
+
+@pytest.mark.parametrize("M,N,K", TMA)
+@pytest.mark.parametrize("dist", ["normal", "int"])
+def test_tma_kernel_matches_oracle_and_cpasync_bits(M, N, K, dist):
+    case = workloads.make_operands(M, N, K, transA=1, lda=_rup4(M), ldb=_rup4(N), ldc=N + 4,
+                                   dist=dist, poison=True, seed=95, key=950 + M + 3 * N + 7 * K)
+    assert sg.device_status(reset=True) == 0
+    got = run(case)
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    check_full(case, got, exact=dist == "int", label=f"tma {M}x{N}x{K} {dist}")
+    assert np.array_equal(got, run(case, offset=1)), "TMA and cp.async kernels differ"
+
+
+def test_tma_kernel_strided_batches():
+    # 4 problems of 6 x 6 tiles: the batch is the third tensor-map dimension
+    M, N, K, batch = 700, 708, 70, 4
+    case = workloads.make_operands(M, N, K, batch=batch, transA=1, lda=704, ldb=N, ldc=N + 4,
+                                   dist="int", poison=True, seed=96, key=960)
+    got = run(case, entry="sgemm_f32_strided_batched")
+    assert sg.device_status(reset=True) == 0
+    check_full(case, got, exact=True, label="tma batched")
+    assert np.array_equal(got, run(case, entry="sgemm_f32_strided_batched", offset=1))
+
+
+# Stream-K on the TMA kernel (aligned A^T by B, 128 x 128 tiles, two CTAs per
+# SM): ragged edges, two K slices per tile (pieces of one slice), more CTAs
+# than stream-K units, and a large K.
+STREAMK_TMA = [(2049, 3071, 1537), (3000, 2900, 33), (2000, 2600, 64), (2100, 2500, 4100)]
+
+
+@pytest.mark.parametrize("M,N,K", STREAMK_TMA)
+def test_streamk_tma_exact_on_integers(M, N, K):
+    case = workloads.make_operands(M, N, K, transA=1, lda=_rup4(M), ldb=_rup4(N), ldc=N + 4,
+                                   dist="int", poison=True, seed=97, key=970 + M + N + K)
+    assert sg.device_status(reset=True) == 0
+    got = run(case, entry="sgemm_f32_streamk")
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    check_full(case, got, exact=True, label=f"streamk tma {M}x{N}x{K}")
