@@ -300,34 +300,52 @@ def tf32_probe_tflops(torch, sg, dev, stream, iters=16384, reps=5):
     return flops / (ms * 1e-3) / 1e12
 
 
-def streamk_plan(M, N, K, transA, transB, need):
-    """(transposes, stream-K used) of one sgemm_f32_streamk call: a transpose
-    per turned operand, then the tile kernel, plus the fix-up pass when
-    stream-K applies.  Mirrors the library's rule (include/sgemm_gb300.h):
-    in problems with 2MNK >= 1.6e10, row-major A is turned when N >= 1024 and
-    B^T when M >= 1024; the workspace beyond the copies is stream-K's."""
+def streamk_plan(M, N, K, transA, transB, sms, aligned=True):
+    """(transposes, stream-K used, tile kernel) of one sgemm_f32_streamk call:
+    a transpose per turned operand, then the tile kernel, plus the fix-up pass
+    when stream-K applies.  Mirrors the library's rule (include/sgemm_gb300.h,
+    csrc/api.cu): in problems with 2MNK >= 1.6e10, row-major A is turned when
+    N >= 1024 and B^T when M >= 1024 (the copies are 16-byte aligned).  Then A
+    stored transposed with row-major B takes the TMA-fed kernel when aligned:
+    128 x 128 tiles, G = 2 CTAs per SM, stream-K when G < tiles < 4G and the
+    tiles do not fill whole waves."""
     big = 2.0 * M * N * K >= 1.6e10
     turn_a = big and not transA and N >= 1024
     turn_b = big and transB and M >= 1024
-    copies = 0
-    for on, rows in ((turn_a, M), (turn_b, N)):
-        if on:
-            copies += (K * ((rows + 3) // 4 * 4) * 4 + 255) // 256 * 256
-    return int(turn_a) + int(turn_b), need > copies
+    tA, tB = bool(transA or turn_a), bool(transB and not turn_b)
+    aligned = aligned or (turn_a or turn_b)
+    kslices = -(-K // 32)
+    if tA and not tB and aligned:
+        G = 2 * sms
+        tiles = -(-M // 128) * -(-N // 128)
+        sk = G < tiles < 4 * G and tiles % G != 0 and kslices >= 2
+        kernel = "sgemm_simt_streamk_tma_kernel" if sk else "sgemm_simt_tma_kernel"
+    elif tA and not tB:
+        tiles = -(-M // 128) * -(-N // 128)
+        sk = tiles > sms and tiles % sms != 0 and kslices >= 2
+        kernel = "sgemm_simt_streamk_kernel" if sk else "sgemm_simt_kernel"
+    else:
+        sk, kernel = False, "sgemm_simt_kernel"
+    return int(turn_a) + int(turn_b), sk, kernel
 
 
-def streamk_launches(M, N, K, transA, transB, need) -> int:
-    turned, sk = streamk_plan(M, N, K, transA, transB, need)
+def streamk_launches(M, N, K, transA, transB, sms, aligned=True) -> int:
+    turned, sk, _ = streamk_plan(M, N, K, transA, transB, sms, aligned)
     return turned + 1 + int(sk)
 
 
-def step_kernel_label(M, N, K, transA, transB, need, batch, plain_label) -> str:
+def step_kernel_label(M, N, K, transA, transB, sms, batch, plain_label, aligned=True) -> str:
     if batch != 1:
         return plain_label
-    turned, sk = streamk_plan(M, N, K, transA, transB, need)
+    turned, sk, kernel = streamk_plan(M, N, K, transA, transB, sms, aligned)
     parts = ["transpose_kernel (K-contiguous operand -> workspace copy)"] * turned
-    parts.append("sgemm_simt_streamk_tma_kernel (TMA-fed, two CTAs per SM) + streamk_fixup_kernel"
-                 if sk else plain_label)
+    if sk:
+        parts.append(f"{kernel} (whole-wave tiles, then one stream-K range per CTA; TMA-fed, "
+                     "two CTAs per SM) + streamk_fixup_kernel")
+    elif kernel == "sgemm_simt_tma_kernel":
+        parts.append(simt_kernel_label(M, N, batch, 0, sms, K, 1))
+    else:
+        parts.append(plain_label)
     return " + ".join(parts)
 
 
@@ -491,7 +509,10 @@ def main():
     # timed the same way afterwards and reported beside it.
     sk_need = sg.streamk_workspace_size(M, N, K, w.transA, w.transB) if batch == 1 else 0
     sk_ws = torch.empty(max(sk_need, 1), dtype=torch.uint8, device=dev)
-    launches = streamk_launches(M, N, K, w.transA, w.transB, sk_need) if batch == 1 else 1
+    sms_dev = torch.cuda.get_device_properties(dev).multi_processor_count
+    aligned = lda % 4 == 0 and ldb % 4 == 0 and ldc % 4 == 0
+    launches = (streamk_launches(M, N, K, w.transA, w.transB, sms_dev, aligned) if batch == 1
+                else 1)
 
     def plain_step(i):
         dA, dB, dC = sets[i % nsets]
@@ -788,9 +809,10 @@ def main():
                    "entry": "sgemm_f32_streamk" if batch == 1 else "sgemm_f32_strided_batched",
                    "workspace_bytes": sk_need,
                    "kernels_per_step": launches,
-                   "kernel": step_kernel_label(M, N, K, w.transA, w.transB, sk_need, batch,
+                   "kernel": step_kernel_label(M, N, K, w.transA, w.transB, sms_dev, batch,
                                                simt_kernel_label(M, N, batch, w.transB,
-                                                                 sms_for_label, K))},
+                                                                 sms_for_label, K),
+                                               aligned)},
         "pct_of_fp32_peak": {
             "at_max_clock": 100.0 * per_gpu / peak_max,
             "peak_tflops_at_max_clock": peak_max,
@@ -803,10 +825,9 @@ def main():
             "peak": peak_max,
             "unit": "TFLOP/s",
             "frac": achieved / peak_max,
-            "traffic": profiled_traffic("sgemm_simt_streamk_tma_kernel"
-                                        if batch == 1 and streamk_plan(M, N, K, w.transA, w.transB,
-                                                                       sk_need)[1]
-                                        else "sgemm_simt_kernel", args.workload),
+            "traffic": profiled_traffic(streamk_plan(M, N, K, w.transA, w.transB, sms_dev,
+                                                     aligned)[2]
+                                        if batch == 1 else "sgemm_simt_kernel", args.workload),
             "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
                            f"{sm_max:.0f} MHz",
             "algorithmic_flops_per_launch": flops,

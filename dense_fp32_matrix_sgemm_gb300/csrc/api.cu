@@ -50,9 +50,13 @@ cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, boo
 // after tile left those 16-byte global loads exposed (long-scoreboard stalls
 // 0.007 -> 0.75 per instruction, 15 % slower per tile on 2048 x 4864 x 4096),
 // more than the wave tail stream-K removes.  With 16-byte aligned operands
-// the TMA-fed kernel runs it on 128 x 128 tiles over every resident CTA (two
-// per SM); otherwise the cp.async kernel on one CTA per SM, with 128 x 256
-// tiles where it can use 16-byte access.
+// the TMA-fed kernel runs it on 128 x 128 tiles with G = every resident CTA
+// (two per SM), and only below four waves of G: two CTAs per SM already
+// absorb most of a wave tail (a lone CTA runs faster), so beyond that the
+// partial tiles and the fix-up cost more than the tail (8192^3: 70.9 TFLOP/s
+// plain, 69.3 with stream-K; 2048 x 3072 x 1536: 56.9 plain, 62.8 with it).
+// Otherwise the cp.async kernel on one CTA per SM, with 128 x 256 tiles where
+// it can use 16-byte access.
 StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec) {
     StreamKPlan pl = {};
     if (!transA || transB) return pl;
@@ -66,7 +70,8 @@ StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec) 
     const int64_t tiles = (int64_t)a.batch * ((a.M + 127) / 128) * ((a.N + bn - 1) / bn);
     pl.G = sms * (pl.tma ? simt_tma_ctas_per_sm() : 1);
     pl.kslices = (a.K + 31) / 32;
-    pl.use = tiles > pl.G && tiles % pl.G != 0 && pl.kslices >= 2 && tiles <= (1LL << 30);
+    pl.use = tiles > pl.G && tiles % pl.G != 0 && pl.kslices >= 2 && tiles <= (1LL << 30) &&
+             (!pl.tma || tiles < 4LL * pl.G);
     if (!pl.use) return pl;
     pl.tiles_dp = (int)(tiles / pl.G * pl.G);
     pl.tiles_sk = (int)(tiles - pl.tiles_dp);

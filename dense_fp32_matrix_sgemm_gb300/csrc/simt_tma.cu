@@ -10,7 +10,11 @@
 // copies in place of per-thread loads):
 //   * one thread issues each stage as two cp.async.bulk.tensor loads (an A
 //     box of 128 x 32 and a B box of 128 x 32) that complete on the stage's
-//     mbarrier; nobody else computes a global address;
+//     "full" mbarrier; nobody else computes a global address;
+//   * no CTA-wide barrier in the main loop: each warp, done with a stage,
+//     arrives on the stage's "empty" mbarrier, and only the issuing thread
+//     waits for all eight arrivals before it refills the stage, so warps
+//     drift apart by up to a stage instead of meeting every 32 k steps;
 //   * the boxes land K-major ([32][128]) with no swizzle: a warp's fragment
 //     loads touch 4 (A) and 8 (B) consecutive 16-byte chunks of one row, so
 //     they are conflict-free as they are;
@@ -21,8 +25,8 @@
 //     shared-load latencies.  The cp.async kernel needs 8 x 16 tiles and one
 //     CTA per SM to avoid spilling.
 // Two kernels: one tile per CTA (sgemm_f32, strided batches as the third
-// tensor dimension) and the stream-K schedule (sgemm_f32_streamk) over two
-// CTAs per SM.  Every mbarrier wait is bounded; one that runs out sets bit 0
+// tensor dimension) and the stream-K schedule (sgemm_f32_streamk) as one
+// grid: whole waves of tiles, one per CTA, then one CTA per stream-K range.  Every mbarrier wait is bounded; one that runs out sets bit 0
 // of the library's device status word and the CTA finishes without waiting
 // again.
 #include <atomic>
@@ -42,19 +46,23 @@ constexpr int kTmaMinBlocks = 2;
 
 template <int BK, int STAGES, int BN_>
 constexpr int tma_smem_bytes() {
-    // operand ring, then STAGES "full" mbarriers and the CTA's abort word
-    return STAGES * BK * (BM + BN_) * (int)sizeof(float) + 8 * STAGES + 16;
+    // operand ring, then STAGES "full" and STAGES "empty" mbarriers and the
+    // CTA's abort word
+    return STAGES * BK * (BM + BN_) * (int)sizeof(float) + 16 * STAGES + 16;
 }
 
-// Initialises the stage barriers (one arrival each: the issuing thread's
-// expect_tx) and the abort word; returns the shared address of barrier 0.
+// Initialises the stage barriers and the abort word: "full" barriers take one
+// arrival (the issuing thread's expect_tx) plus the stage's bytes, "empty"
+// barriers one arrival per warp.  Returns the shared address of full barrier
+// 0; the empty barriers follow the full ones.
 template <int BK, int STAGES, int BN_>
 __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int *&abort) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * BK * (BM + BN_));
-    abort = reinterpret_cast<volatile int *>(bars + STAGES);
+    abort = reinterpret_cast<volatile int *>(bars + 2 * STAGES);
     const uint32_t full0 = smem_u32(bars);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * s, 1);
+        for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * (STAGES + s), THREADS / 32);
         *abort = 0;
         tc::fence_barrier_init();
     }
@@ -64,10 +72,13 @@ __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int 
 
 // Accumulates slices [0, ktiles) of one piece, starting at K offset kbeg, of
 // the tile at (m0, n0) of problem z into acc (zeroed first).  gk counts the
-// slices this CTA has consumed before the piece: slice g uses stage
-// g % STAGES in its (g / STAGES)-th round, so the stage barrier's phase
-// parity is (g / STAGES) & 1.  Every thread keeps the same count.  On return
-// no copy of this piece is in flight (every issued slice has been waited on).
+// slices this CTA has consumed before the piece: slice g lives in stage
+// g % STAGES during its round g / STAGES, so the phase parity of the stage's
+// barriers is (g / STAGES) & 1.  Every thread keeps the same count.
+// Thread 0 issues slice g only after every warp has released slice
+// g - STAGES from the same stage; each warp releases a slice once its lanes
+// have read it.  On return no copy of this piece is in flight (every issued
+// slice has been waited on), and the next piece may start at once.
 template <int BK, int STAGES, int BN_>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
@@ -79,6 +90,7 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
     constexpr int ATILE = BK * BM;
     constexpr int BTILE = BK * BN_;
     constexpr uint32_t STAGE_BYTES = (ATILE + BTILE) * sizeof(float);
+    const uint32_t empty0 = full0 + 8 * STAGES;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -86,25 +98,22 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
 
     const bool issuer = threadIdx.x == 0;
     const uint32_t g0 = gk;          // the piece's slice j is the CTA's slice g0 + j
-    auto issue = [&](int slice) {   // slice of this piece -> its stage
-        const uint32_t st = (g0 + (uint32_t)slice) % STAGES;
+    auto issue = [&](int slice) {
+        const uint32_t g = g0 + (uint32_t)slice;
+        const uint32_t st = g % STAGES;
+        if (g >= STAGES)   // slice g - STAGES released by every warp
+            (void)tc::mbar_wait(empty0 + 8 * st, ((g / STAGES) - 1) & 1, abort);
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, m0, kbeg + slice * BK, z);
         tc::tma_load_3d(smem_u32(Bs + st * BTILE), tmB, bar, n0, kbeg + slice * BK, z);
     };
-    // The stages of the piece's first slices were last read by slices that
-    // every thread finished before the previous barrier: safe to refill.
     if (issuer) {
 #pragma unroll
         for (int s = 0; s < STAGES - 1; ++s)
             if (s < ktiles) issue(s);
     }
     for (int kt = 0; kt < ktiles; ++kt) {
-        // every warp is done with the stage of slice kt - 1, which is the
-        // stage slice kt + STAGES - 1 goes to
-        __syncthreads();
-        if (issuer && kt + STAGES - 1 < ktiles) issue(kt + STAGES - 1);
         const uint32_t rs = gk % STAGES;
         (void)tc::mbar_wait(full0 + 8 * rs, (gk / STAGES) & 1, abort);
         ++gk;
@@ -138,6 +147,10 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
                 }
             }
         }
+        // the warp's lanes have all read the stage: release it
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
+        if (issuer && kt + STAGES - 1 < ktiles) issue(kt + STAGES - 1);
     }
 }
 
@@ -198,8 +211,12 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
 
-// The stream-K schedule of sgemm_simt_streamk_kernel (see StreamK), fed by
-// TMA; K slices are BK deep.
+// The stream-K schedule (see StreamK) as one grid of tiles_dp + G CTAs:
+// CTA b < tiles_dp computes tile b whole, like sgemm_simt_tma_kernel; CTA
+// tiles_dp + c takes stream-K range c (units [c*U/G, (c+1)*U/G) of the
+// remaining tiles' K slices, at most two pieces), so the whole-wave tiles
+// run one per CTA and the ranges fill the last wave.  Pieces that are not a
+// whole tile go to workspace slots [c][0|1] for streamk_fixup_kernel.
 template <int BK, int STAGES, int BN_, int MINB>
 __global__ void __launch_bounds__(THREADS, MINB)
 sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -217,44 +234,36 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     int a_col, b_col;
     thread_coords(a_col, b_col);
-
-    // Everything about piece i is recomputed from (blockIdx.x, i), as in
-    // sgemm_simt_streamk_kernel: at most two stream-K pieces per CTA.
-    const int c = blockIdx.x;
-    const int ndp = c < sk.tiles_dp ? (sk.tiles_dp - 1 - c) / sk.G + 1 : 0;
-    int nsk;
-    {
-        const int64_t u0 = (int64_t)c * sk.units / sk.G, u1 = ((int64_t)c + 1) * sk.units / sk.G;
-        nsk = u0 == u1 ? 0 : (u0 / sk.kslices == (u1 - 1) / sk.kslices ? 1 : 2);
-    }
     uint32_t gk = 0;
-#pragma unroll 1
-    for (int i = 0; i < ndp + nsk; ++i) {
-        int t, s0, s1;
-        float *part = nullptr;   // null: store the finished tile to C
-        if (i < ndp) {
-            t = c + i * sk.G;
-            s0 = 0;
-            s1 = sk.kslices;
-        } else {
-            const int k = i - ndp;   // 0: the range's first piece, 1: its last
-            const int64_t u0 = (int64_t)c * sk.units / sk.G;
-            const int64_t u1 = ((int64_t)c + 1) * sk.units / sk.G;
-            const int64_t ub = k == 0 ? u0 : (u0 / sk.kslices + 1) * sk.kslices;
-            const int tl = (int)(ub / sk.kslices);
-            s0 = (int)(ub - (int64_t)tl * sk.kslices);
-            s1 = (int)min((int64_t)sk.kslices, s0 + (u1 - ub));
-            t = sk.tiles_dp + tl;
-            if (!(s0 == 0 && s1 == sk.kslices))
-                part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
-        }
+    const int b = blockIdx.x;
+    if (b < sk.tiles_dp) {
         int z, tm, tn;
-        raster(p, t, z, tm, tn);
+        raster(p, b, z, tm, tn);
+        float acc[8][BN_ / 16];
+        tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
+                                      sk.kslices, a_col, b_col, acc, abort);
+        if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+        store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+        return;
+    }
+    const int c = b - sk.tiles_dp;
+    const int64_t u0 = (int64_t)c * sk.units / sk.G, u1 = ((int64_t)c + 1) * sk.units / sk.G;
+    // tiles_sk < G, so a range is at most kslices units long: at most two pieces
+    const int nsk = u0 == u1 ? 0 : (u0 / sk.kslices == (u1 - 1) / sk.kslices ? 1 : 2);
+#pragma unroll 1
+    for (int k = 0; k < nsk; ++k) {   // 0: the range's first piece, 1: its last
+        const int64_t ub = k == 0 ? u0 : (u0 / sk.kslices + 1) * sk.kslices;
+        const int tl = (int)(ub / sk.kslices);
+        const int s0 = (int)(ub - (int64_t)tl * sk.kslices);
+        const int s1 = (int)min((int64_t)sk.kslices, s0 + (u1 - ub));
+        int z, tm, tn;
+        raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
         tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, s0 * BK,
                                       s1 - s0, a_col, b_col, acc, abort);
-        if (part != nullptr) {
+        if (!(s0 == 0 && s1 == sk.kslices)) {
             // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
+            float *part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int row = r < 4 ? a_col + r : 64 + a_col + (r - 4);
@@ -366,7 +375,8 @@ bool launch_simt_streamk_tma(const GemmArgs &a, const StreamKPlan &pl, void *ws,
     sk.G = pl.G;
     sk.units = pl.units;
     sk.ws = static_cast<float *>(ws);
-    kern<<<(unsigned)pl.G, THREADS, smem, s>>>(tmA, tmB, g, sk, device_error_word());
+    kern<<<(unsigned)(pl.tiles_dp + pl.G), THREADS, smem, s>>>(tmA, tmB, g, sk,
+                                                                device_error_word());
     err = cudaGetLastError();
     if (err != cudaSuccess) return true;
     const dim3 grid((unsigned)(BM * kTmaBN / 1024), (unsigned)pl.tiles_sk);

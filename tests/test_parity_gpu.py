@@ -683,7 +683,7 @@ def test_persistent_tensor_epilogue_many_tiles():
 # sgemm_f32_streamk: K-contiguous operands of large problems turned into
 # copies in the workspace, then (A stored transposed, B row-major) whole waves
 # of tiles computed whole, the K slices of the remaining tiles dealt out over
-# one CTA per SM and the shared tiles finished from the workspace.  Shapes
+# the resident CTAs and the shared tiles finished from the workspace.  Shapes
 # give a wide-tile tail (3072^3) in every layout (turned or not), ragged edges,
 # pieces of a single K slice, misaligned operands (narrow tiles), and shapes
 # too small for either step (which run as sgemm_f32).
@@ -768,10 +768,13 @@ def test_tma_kernel_strided_batches():
     assert np.array_equal(got, run(case, entry="sgemm_f32_strided_batched", offset=1))
 
 
-# Stream-K on the TMA kernel (aligned A^T by B, 128 x 128 tiles, two CTAs per
-# SM): ragged edges, two K slices per tile (pieces of one slice), more CTAs
-# than stream-K units, and a large K.
-STREAMK_TMA = [(2049, 3071, 1537), (3000, 2900, 33), (2000, 2600, 64), (2100, 2500, 4100)]
+# Stream-K on the TMA kernel (aligned A^T by B, 128 x 128 tiles, G = two CTAs
+# per SM, one grid of whole-wave tiles then one range per CTA): ragged edges,
+# two K slices per tile (pieces of one slice), more CTAs than stream-K units,
+# a large K; and 1681 tiles (four waves of G or more), where the entry runs
+# the plain TMA kernel instead.
+STREAMK_TMA = [(2049, 3071, 1537), (3000, 2900, 33), (2000, 2600, 64), (2100, 2500, 4100),
+               (5200, 5200, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", STREAMK_TMA)
