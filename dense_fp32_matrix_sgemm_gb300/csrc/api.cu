@@ -36,7 +36,7 @@ cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, boo
         // the same schedule on the cp.async kernel (128 x 128 tiles) if the
         // operands cannot be described as tensor maps
         cudaError_t e = cudaSuccess;
-        if (launch_simt_streamk_tma(a, pl, ws, s, e)) return e;
+        if (launch_simt_streamk_tma(a, transA, pl, ws, s, e)) return e;
     }
     if (!transA && !transB) return launch_simt_streamk_nn(a, vec, pl, ws, s);
     if (!transA && transB) return launch_simt_streamk_nt(a, vec, pl, ws, s);

@@ -73,16 +73,15 @@ StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec);
 cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
                                 const StreamKPlan &plan, void *ws, cudaStream_t s);
 
-// The SIMT kernel fed by TMA (A stored transposed, row-major B, 16-byte
-// aligned operands, no split-K chunks): one 128 x 128 tile per CTA, two CTAs
-// per SM.  The launchers return false, launching nothing, when the operands
-// cannot be described as tensor maps; else they launch and store the status
-// in `err`.
+// The SIMT kernel fed by TMA (row-major B, A either way, 16-byte aligned
+// operands, no split-K chunks): one 128 x 128 tile per CTA, two CTAs per SM.
+// The launchers return false, launching nothing, when the operands cannot be
+// described as tensor maps; else they launch and store the status in `err`.
 bool simt_tma_eligible(const GemmArgs &a, bool transA, bool transB, bool vec);
 int simt_tma_ctas_per_sm();
-bool launch_simt_tma(const GemmArgs &a, cudaStream_t s, cudaError_t &err);
-bool launch_simt_streamk_tma(const GemmArgs &a, const StreamKPlan &plan, void *ws, cudaStream_t s,
-                             cudaError_t &err);
+bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t &err);
+bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &plan, void *ws,
+                             cudaStream_t s, cudaError_t &err);
 
 // Device address of the library's status word (bit 0: a bounded pipeline
 // wait ran out), for kernels that report into it; null if unavailable.

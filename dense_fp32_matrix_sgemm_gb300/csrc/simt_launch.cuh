@@ -185,10 +185,10 @@ template <bool TA, bool TB, bool VEC>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t s) {
     cudaError_t err = cudaSuccess;
     if (launch_cluster_split<TA, TB, VEC>(a, s, err)) return err;
-    // A^T by row-major B with 16-byte access: the TMA-fed kernel (two CTAs
-    // per SM), unless the operands cannot be described as tensor maps
-    if constexpr (TA && !TB && VEC) {
-        if (simt_tma_eligible(a, TA, TB, VEC) && launch_simt_tma(a, s, err)) return err;
+    // row-major B with 16-byte access: the TMA-fed kernel (two CTAs per SM),
+    // unless the operands cannot be described as tensor maps
+    if constexpr (!TB && VEC) {
+        if (simt_tma_eligible(a, TA, TB, VEC) && launch_simt_tma(a, TA, s, err)) return err;
     }
     if constexpr (VEC) {
         if (a.K <= kShortK) return launch_config<2, 128, TA, TB, VEC, 2>(a, s);

@@ -1,6 +1,6 @@
-// SIMT FP32 SGEMM fed by TMA, for A stored transposed (K x M) with row-major
-// B: the layout in which both operands are contiguous along M or N, so a K
-// slice of either is a plain 2-D box of global memory.
+// SIMT FP32 SGEMM fed by TMA, for row-major B with A either stored
+// transposed (K x M, contiguous along M) or row-major (contiguous along K):
+// a K slice of either operand is then a plain 2-D box of global memory.
 //
 // Same arithmetic as sgemm_simt_kernel (each output accumulated by one thread
 // in ascending k with packed fp32 FMAs, 8 x 8 register tile of 4 x 4
@@ -15,9 +15,16 @@
 //     arrives on the stage's "empty" mbarrier, and only the issuing thread
 //     waits for all eight arrivals before it refills the stage, so warps
 //     drift apart by up to a stage instead of meeting every 32 k steps;
-//   * the boxes land K-major ([32][128]) with no swizzle: a warp's fragment
-//     loads touch 4 (A) and 8 (B) consecutive 16-byte chunks of one row, so
-//     they are conflict-free as they are;
+//   * B boxes and M-contiguous A boxes land K-major ([32][128]) with no
+//     swizzle: a warp's fragment loads touch 4 (A) and 8 (B) consecutive
+//     16-byte chunks of one row, so they are conflict-free as they are;
+//   * a K-contiguous (row-major) A box lands M-major ([128][32], one 128-byte
+//     row per m) with the 128-byte swizzle (16-byte chunk c of row m stored
+//     at c ^ (m % 8)).  Instead of a corner turn, each thread owns rows
+//     ty + 16 j (j = 0..7) and reads 4 consecutive k of a row with one
+//     16-byte load; all of a thread's rows share m % 8 = ty % 8, and the 4
+//     row groups of a warp land in 4 different chunks: conflict-free, and as
+//     many loads per k step as the K-major layout;
 //   * the tensor map zero-fills rows, columns and K beyond the operand, so
 //     ragged tiles need no per-element predicates;
 //   * without per-thread copy state the kernel fits 128 registers: two CTAs
@@ -46,9 +53,17 @@ constexpr int kTmaMinBlocks = 2;
 
 template <int BK, int STAGES, int BN_>
 constexpr int tma_smem_bytes() {
-    // operand ring, then STAGES "full" and STAGES "empty" mbarriers and the
-    // CTA's abort word
-    return STAGES * BK * (BM + BN_) * (int)sizeof(float) + 16 * STAGES + 16;
+    // 1 KB to align the ring to the 1024-byte swizzle atom, the operand ring,
+    // then STAGES "full" and STAGES "empty" mbarriers and the CTA's abort word
+    return 1024 + STAGES * BK * (BM + BN_) * (int)sizeof(float) + 16 * STAGES + 16;
+}
+
+// The operand ring starts at the first 1024-byte boundary of the dynamic
+// shared memory (the 128-byte swizzle pattern repeats every 8 rows of 128
+// bytes and is laid out relative to such a boundary).
+__device__ __forceinline__ float *align_ring(float *raw) {
+    const uint32_t a = smem_u32(raw);
+    return raw + ((1024u - (a & 1023u)) & 1023u) / sizeof(float);
 }
 
 // Initialises the stage barriers and the abort word: "full" barriers take one
@@ -79,7 +94,7 @@ __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int 
 // g - STAGES from the same stage; each warp releases a slice once its lanes
 // have read it.  On return no copy of this piece is in flight (every issued
 // slice has been waited on), and the next piece may start at once.
-template <int BK, int STAGES, int BN_>
+template <int BK, int STAGES, int BN_, bool KA>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
                                              int m0, int n0, int z, int kbeg, int ktiles,
@@ -105,7 +120,10 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
             (void)tc::mbar_wait(empty0 + 8 * st, ((g / STAGES) - 1) & 1, abort);
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
-        tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, m0, kbeg + slice * BK, z);
+        if constexpr (KA)   // box (k, m): 32 k x 128 rows
+            tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, kbeg + slice * BK, m0, z);
+        else                // box (m, k): 128 m x 32 k
+            tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, m0, kbeg + slice * BK, z);
         tc::tma_load_3d(smem_u32(Bs + st * BTILE), tmB, bar, n0, kbeg + slice * BK, z);
     };
     if (issuer) {
@@ -119,13 +137,9 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
         ++gk;
         const float *at = As + rs * ATILE;
         const float *bt = Bs + rs * BTILE;
-#pragma unroll
-        for (int kk = 0; kk < BK; ++kk) {
-            const float *ar = at + kk * BM;
+        // one k step: acc[i][.] += a[i] * b[.] in packed pairs along n
+        auto step = [&](const float (&a)[8], int kk) {
             const float *br = bt + kk * BN_;
-            const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
-            const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             float b[TN];
 #pragma unroll
             for (int h = 0; h < NSB; ++h) {
@@ -146,6 +160,49 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
                     acc[i][j + 1] = c.y;
                 }
             }
+        };
+        if constexpr (KA) {
+            // rows ty + 16 j of the [128][32] swizzled stage; k in ascending order
+            static_assert(BK == 32, "the 128-byte swizzle spans one 32-float row");
+            const int ty = a_col >> 2;
+            const float *arow = at + ty * BK;
+#pragma unroll
+            for (int kq = 0; kq < BK / 4; ++kq) {
+                const int chunk = 4 * (kq ^ (ty & 7));
+                float4 av[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    av[j] = *reinterpret_cast<const float4 *>(arow + j * 16 * BK + chunk);
+                {
+                    const float a[8] = {av[0].x, av[1].x, av[2].x, av[3].x,
+                                        av[4].x, av[5].x, av[6].x, av[7].x};
+                    step(a, 4 * kq + 0);
+                }
+                {
+                    const float a[8] = {av[0].y, av[1].y, av[2].y, av[3].y,
+                                        av[4].y, av[5].y, av[6].y, av[7].y};
+                    step(a, 4 * kq + 1);
+                }
+                {
+                    const float a[8] = {av[0].z, av[1].z, av[2].z, av[3].z,
+                                        av[4].z, av[5].z, av[6].z, av[7].z};
+                    step(a, 4 * kq + 2);
+                }
+                {
+                    const float a[8] = {av[0].w, av[1].w, av[2].w, av[3].w,
+                                        av[4].w, av[5].w, av[6].w, av[7].w};
+                    step(a, 4 * kq + 3);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                const float *ar = at + kk * BM;
+                const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
+                const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                step(a, kk);
+            }
         }
         // the warp's lanes have all read the stage: release it
         __syncwarp();
@@ -164,7 +221,15 @@ __device__ __forceinline__ void thread_coords(int &a_col, int &b_col) {
     b_col = 4 * ((warp & 1) * 8 + lane_col);
 }
 
-template <int BN_>
+// Tile row of accumulator row r: a_col + r and 64 + a_col + r - 4 when A
+// fragments come K-major, ty + 16 r (ty = a_col / 4) when they come M-major.
+template <bool KA>
+__device__ __forceinline__ int acc_row(int a_col, int r) {
+    if constexpr (KA) return (a_col >> 2) + 16 * r;
+    return r < 4 ? a_col + r : 64 + a_col + (r - 4);
+}
+
+template <int BN_, bool KA>
 __device__ __forceinline__ void store_tile(const GemmArgs &p, int z, int m0, int n0, int a_col,
                                            int b_col, const float (&acc)[8][BN_ / 16]) {
     constexpr int NSB = BN_ / 64;
@@ -172,7 +237,7 @@ __device__ __forceinline__ void store_tile(const GemmArgs &p, int z, int m0, int
     const bool plain = plain_epilogue(p);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-        const int row = m0 + (r < 4 ? a_col + r : 64 + a_col + (r - 4));
+        const int row = m0 + acc_row<KA>(a_col, r);
         if (row >= p.M) continue;
         float *crow = Cz + (int64_t)row * p.ldc;
 #pragma unroll
@@ -185,12 +250,13 @@ __device__ __forceinline__ void store_tile(const GemmArgs &p, int z, int m0, int
 }
 
 // One 128 x BN_ tile per CTA, all of K.
-template <int BK, int STAGES, int BN_, int MINB>
+template <int BK, int STAGES, int BN_, bool KA, int MINB>
 __global__ void __launch_bounds__(THREADS, MINB)
 sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
                       unsigned int *status) {
-    extern __shared__ __align__(128) float smem[];
+    extern __shared__ __align__(128) float smem_raw[];
+    float *smem = align_ring(smem_raw);
     float *As = smem;
     float *Bs = smem + STAGES * BK * BM;
     volatile int *abort;
@@ -205,10 +271,10 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     thread_coords(a_col, b_col);
     float acc[8][BN_ / 16];
     uint32_t gk = 0;
-    tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
+    tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
                                   (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
     if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
-    store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+    store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
 
 // The stream-K schedule (see StreamK) as one grid of tiles_dp + G CTAs:
@@ -217,13 +283,14 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
 // remaining tiles' K slices, at most two pieces), so the whole-wave tiles
 // run one per CTA and the ranges fill the last wave.  Pieces that are not a
 // whole tile go to workspace slots [c][0|1] for streamk_fixup_kernel.
-template <int BK, int STAGES, int BN_, int MINB>
+template <int BK, int STAGES, int BN_, bool KA, int MINB>
 __global__ void __launch_bounds__(THREADS, MINB)
 sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
                               const StreamK sk, unsigned int *status) {
     constexpr int NSB = BN_ / 64;
-    extern __shared__ __align__(128) float smem[];
+    extern __shared__ __align__(128) float smem_raw[];
+    float *smem = align_ring(smem_raw);
     float *As = smem;
     float *Bs = smem + STAGES * BK * BM;
     volatile int *abort;
@@ -240,10 +307,10 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, b, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
+        tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
                                       sk.kslices, a_col, b_col, acc, abort);
         if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
-        store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+        store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         return;
     }
     const int c = b - sk.tiles_dp;
@@ -259,14 +326,14 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, s0 * BK,
+        tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, s0 * BK,
                                       s1 - s0, a_col, b_col, acc, abort);
         if (!(s0 == 0 && s1 == sk.kslices)) {
             // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
             float *part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
-                const int row = r < 4 ? a_col + r : 64 + a_col + (r - 4);
+                const int row = acc_row<KA>(a_col, r);
 #pragma unroll
                 for (int h = 0; h < NSB; ++h)
                     *reinterpret_cast<float4 *>(part + row * BN_ + h * 64 + b_col) =
@@ -274,7 +341,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                                     acc[r][4 * h + 3]);
             }
         } else {
-            store_tile<BN_>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+            store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         }
     }
     if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
@@ -283,8 +350,9 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
 namespace {
 
 // [batch][K][cols] fp32 with row stride ld and batch stride zstride (elements),
-// boxes of box_cols x BK x 1, zero fill outside.  False when the driver
-// rejects the description (the caller then uses the cp.async kernels).
+// boxes of box_cols x BK x 1, zero fill outside: an operand contiguous along
+// M or N.  False when the driver rejects the description (the caller then
+// uses the cp.async kernels).
 bool make_operand_map(CUtensorMap *map, const float *base, int cols, int K, int64_t ld,
                       int64_t zstride, int batch, int box_cols) {
     auto fn = tensor_map_encoder();
@@ -301,19 +369,65 @@ bool make_operand_map(CUtensorMap *map, const float *base, int cols, int K, int6
     return r == CUDA_SUCCESS;
 }
 
-bool make_maps(const GemmArgs &a, CUtensorMap &tmA, CUtensorMap &tmB) {
-    return make_operand_map(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM) &&
-           make_operand_map(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, kTmaBN);
+// [batch][rows][K] fp32 (contiguous along K) with row stride ld, boxes of
+// BK x box_rows x 1 with the 128-byte swizzle (BK floats = 128 bytes).
+bool make_kmajor_map(CUtensorMap *map, const float *base, int rows, int K, int64_t ld,
+                     int64_t zstride, int batch, int box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const int64_t zs = batch > 1 ? zstride : ld * (int64_t)rows;
+    if (zs <= 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)zs * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)kTmaBK, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_maps(const GemmArgs &a, bool ka, CUtensorMap &tmA, CUtensorMap &tmB) {
+    const bool okA = ka ? make_kmajor_map(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM)
+                        : make_operand_map(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM);
+    return okA && make_operand_map(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, kTmaBN);
+}
+
+template <bool KA>
+cudaError_t launch_tile_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &g,
+                               cudaStream_t s) {
+    auto kern = sgemm_simt_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
+    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t err = ensure_smem_attribute(kern, smem, configured);
+    if (err != cudaSuccess) return err;
+    const long long blocks = (long long)g.batch * g.tiles_m * g.tiles_n;
+    kern<<<(unsigned)blocks, THREADS, smem, s>>>(tmA, tmB, g, device_error_word());
+    return cudaGetLastError();
+}
+
+template <bool KA>
+cudaError_t launch_streamk_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                  const GemmArgs &g, const StreamK &sk, cudaStream_t s) {
+    auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
+    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t err = ensure_smem_attribute(kern, smem, configured);
+    if (err != cudaSuccess) return err;
+    kern<<<(unsigned)(sk.tiles_dp + sk.G), THREADS, smem, s>>>(tmA, tmB, g, sk,
+                                                              device_error_word());
+    return cudaGetLastError();
 }
 
 }  // namespace
 }  // namespace simt
 
 bool simt_tma_eligible(const GemmArgs &a, bool transA, bool transB, bool vec) {
-    // 16-byte aligned bases and rows (vec), whole problems (no split-K
-    // chunks), distinct batches (a zero batch stride is not a tensor stride)
-    return transA && !transB && vec && a.kchunk == 0 &&
-           (a.batch == 1 || (a.strideA > 0 && a.strideB > 0));
+    // row-major B, 16-byte aligned bases and rows (vec), whole problems (no
+    // split-K chunks), distinct batches (a zero batch stride is not a tensor
+    // stride); A either way
+    (void)transA;
+    return !transB && vec && a.kchunk == 0 && (a.batch == 1 || (a.strideA > 0 && a.strideB > 0));
 }
 
 int simt_tma_ctas_per_sm() {
@@ -323,7 +437,7 @@ int simt_tma_ctas_per_sm() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
     int v = cached[dev & 63].load();
     if (v <= 0) {
-        auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, kTmaMinBlocks>;
+        auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, true, kTmaMinBlocks>;
         constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess ||
@@ -337,34 +451,22 @@ int simt_tma_ctas_per_sm() {
     return v;
 }
 
-bool launch_simt_tma(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
+bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t &err) {
     using namespace simt;
     CUtensorMap tmA, tmB;
-    if (!make_maps(a, tmA, tmB)) return false;
-    auto kern = sgemm_simt_tma_kernel<kTmaBK, kTmaStages, kTmaBN, kTmaMinBlocks>;
-    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
-    static std::atomic<unsigned long long> configured{0};
-    err = ensure_smem_attribute(kern, smem, configured);
-    if (err != cudaSuccess) return true;
+    if (!make_maps(a, !transA, tmA, tmB)) return false;
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
-    const long long blocks = (long long)g.batch * g.tiles_m * g.tiles_n;
-    kern<<<(unsigned)blocks, THREADS, smem, s>>>(tmA, tmB, g, device_error_word());
-    err = cudaGetLastError();
+    err = transA ? launch_tile_kernel<false>(tmA, tmB, g, s) : launch_tile_kernel<true>(tmA, tmB, g, s);
     return true;
 }
 
-bool launch_simt_streamk_tma(const GemmArgs &a, const StreamKPlan &pl, void *ws, cudaStream_t s,
-                             cudaError_t &err) {
+bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &pl, void *ws,
+                             cudaStream_t s, cudaError_t &err) {
     using namespace simt;
     CUtensorMap tmA, tmB;
-    if (!make_maps(a, tmA, tmB)) return false;
-    auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, kTmaMinBlocks>;
-    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
-    static std::atomic<unsigned long long> configured{0};
-    err = ensure_smem_attribute(kern, smem, configured);
-    if (err != cudaSuccess) return true;
+    if (!make_maps(a, !transA, tmA, tmB)) return false;
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
@@ -375,9 +477,8 @@ bool launch_simt_streamk_tma(const GemmArgs &a, const StreamKPlan &pl, void *ws,
     sk.G = pl.G;
     sk.units = pl.units;
     sk.ws = static_cast<float *>(ws);
-    kern<<<(unsigned)(pl.tiles_dp + pl.G), THREADS, smem, s>>>(tmA, tmB, g, sk,
-                                                                device_error_word());
-    err = cudaGetLastError();
+    err = transA ? launch_streamk_kernel<false>(tmA, tmB, g, sk, s)
+                 : launch_streamk_kernel<true>(tmA, tmB, g, sk, s);
     if (err != cudaSuccess) return true;
     const dim3 grid((unsigned)(BM * kTmaBN / 1024), (unsigned)pl.tiles_sk);
     streamk_fixup_kernel<kTmaBN, true><<<grid, 256, 0, s>>>(g, sk);
