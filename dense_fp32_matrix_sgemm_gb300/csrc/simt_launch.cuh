@@ -226,8 +226,7 @@ cudaError_t launch_streamk_config(const GemmArgs &a, const StreamKPlan &pl, void
     kern<<<(unsigned)pl.G, THREADS, smem, s>>>(g, sk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(BM * BN_ / 1024), (unsigned)pl.tiles_sk);
-    streamk_fixup_kernel<BN_, VEC><<<grid, 256, 0, s>>>(g, sk);
+    streamk_fixup_kernel<BN_, VEC><<<streamk_fixup_grid<BN_>(pl.tiles_sk), 256, 0, s>>>(g, sk);
     return cudaGetLastError();
 }
 

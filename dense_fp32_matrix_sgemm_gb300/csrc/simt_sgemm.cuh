@@ -560,34 +560,57 @@ sgemm_simt_streamk_kernel(const GemmArgs p, const StreamK sk) {
     }
 }
 
-// Adds the pieces of the shared stream-K tiles: grid (BM * BN_ / 1024, tiles_sk),
-// one float4 per thread; pieces added in K order (CTA order), then stored to C
-// with the epilogue.  Tiles that fell whole to one CTA are skipped.
+// Adds the pieces of the shared stream-K tiles: grid streamk_fixup_grid<BN_>,
+// kFixupVecs float4 per thread (256 float4 apart, so each load instruction is
+// coalesced across the CTA), all of a piece's loads issued before any add;
+// pieces added in K order (CTA order), then stored to C with the epilogue.
+// Tiles that fell whole to one CTA are skipped.
+constexpr int kFixupVecs = 4;
+
+template <int BN_>
+inline dim3 streamk_fixup_grid(int tiles_sk) {
+    return dim3((unsigned)(BM * BN_ / (1024 * kFixupVecs)), (unsigned)tiles_sk);
+}
+
 template <int BN_, bool VEC>
 __global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmArgs p, const StreamK sk) {
+    constexpr int V = kFixupVecs;
+    static_assert((BM * BN_) % (1024 * V) == 0, "whole float4 groups per CTA");
     const int tl = blockIdx.y;
     const int64_t U = sk.units, f = (int64_t)tl * sk.kslices, l = f + sk.kslices - 1;
     const int c0 = streamk_owner(f, U, sk.G), c1 = streamk_owner(l, U, sk.G);
     if (c0 == c1) return;
-    const int e = (blockIdx.x * 256 + threadIdx.x) * 4;   // element of the 128 x BN_ tile
-    if (e >= BM * BN_) return;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // element of the 128 x BN_ tile of this thread's vector r: e0 + 1024 r
+    const int e0 = (blockIdx.x * 256 * V + threadIdx.x) * 4;
+    float4 acc[V];
+#pragma unroll
+    for (int r = 0; r < V; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = c0; c <= c1; ++c) {
         const int64_t start = (int64_t)c * U / sk.G;
         if (((int64_t)c + 1) * U / sk.G == start) continue;   // a CTA with no units has no piece
         const int slot = start >= f ? 0 : 1;   // the tile is c's first piece or its last
-        const float4 v = *reinterpret_cast<const float4 *>(sk.ws + ((int64_t)c * 2 + slot) * (BM * BN_) + e);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+        const float *piece = sk.ws + ((int64_t)c * 2 + slot) * (BM * BN_) + e0;
+        float4 v[V];
+#pragma unroll
+        for (int r = 0; r < V; ++r) v[r] = *reinterpret_cast<const float4 *>(piece + 1024 * r);
+#pragma unroll
+        for (int r = 0; r < V; ++r) {
+            acc[r].x += v[r].x;
+            acc[r].y += v[r].y;
+            acc[r].z += v[r].z;
+            acc[r].w += v[r].w;
+        }
     }
     int z, tm, tn;
     raster(p, sk.tiles_dp + tl, z, tm, tn);
-    const int row = tm * BM + e / BN_, col = tn * BN_ + e % BN_;
-    if (row >= p.M) return;
-    store_c4(p, p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc, col, acc, VEC,
-             plain_epilogue(p));
+    float *Cz = p.C + (int64_t)z * p.strideC;
+    const bool plain = plain_epilogue(p);
+#pragma unroll
+    for (int r = 0; r < V; ++r) {
+        const int e = e0 + 1024 * r;
+        const int row = tm * BM + e / BN_, col = tn * BN_ + e % BN_;
+        if (row < p.M) store_c4(p, Cz + (int64_t)row * p.ldc, col, acc[r], VEC, plain);
+    }
 }
 
 }  // namespace simt

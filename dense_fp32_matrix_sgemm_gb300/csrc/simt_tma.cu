@@ -480,8 +480,8 @@ bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &
     err = transA ? launch_streamk_kernel<false>(tmA, tmB, g, sk, s)
                  : launch_streamk_kernel<true>(tmA, tmB, g, sk, s);
     if (err != cudaSuccess) return true;
-    const dim3 grid((unsigned)(BM * kTmaBN / 1024), (unsigned)pl.tiles_sk);
-    streamk_fixup_kernel<kTmaBN, true><<<grid, 256, 0, s>>>(g, sk);
+    streamk_fixup_kernel<kTmaBN, true><<<streamk_fixup_grid<kTmaBN>(pl.tiles_sk), 256, 0, s>>>(
+        g, sk);
     err = cudaGetLastError();
     return true;
 }
