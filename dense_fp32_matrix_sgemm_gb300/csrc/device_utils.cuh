@@ -40,6 +40,16 @@ __device__ __forceinline__ float4 ldg_f4(const float *p) {
 }
 
 // Rank of this CTA within its cluster, and the number of CTAs in the cluster.
+// Programmatic dependent launch.  pdl_wait: the calling thread waits until
+// the grids this launch depends on have completed and their memory is
+// visible (returns at once when the launch has no such dependency).
+// pdl_trigger: this CTA allows the next launch in the stream, if it was
+// launched as a programmatic dependent, to start being scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));

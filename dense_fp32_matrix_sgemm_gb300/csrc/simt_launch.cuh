@@ -4,6 +4,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 
 #include "simt_sgemm.cuh"
 
@@ -60,6 +61,26 @@ inline bool pick_wide_tile(const GemmArgs &a) {
     const double cost_narrow = (double)((narrow + sms - 1) / sms);
     const double cost_wide = kWideTileCost * (double)((wide + sms - 1) / sms);
     return cost_wide < cost_narrow;
+}
+
+// Launches `kern` as a programmatic dependent of the previous work in the
+// stream: its CTAs may be scheduled once every CTA of the previous launch has
+// called pdl_trigger (or exited), and must call pdl_wait before touching
+// memory that launch writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Sets the opt-in dynamic shared-memory size of `kern` once per device.
@@ -226,8 +247,8 @@ cudaError_t launch_streamk_config(const GemmArgs &a, const StreamKPlan &pl, void
     kern<<<(unsigned)pl.G, THREADS, smem, s>>>(g, sk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    streamk_fixup_kernel<BN_, VEC><<<streamk_fixup_grid<BN_>(pl.tiles_sk), 256, 0, s>>>(g, sk);
-    return cudaGetLastError();
+    return launch_pdl(streamk_fixup_kernel<BN_, VEC>, streamk_fixup_grid<BN_>(pl.tiles_sk),
+                      dim3(256), 0, s, g, sk);
 }
 
 template <bool TA, bool TB, bool VEC>

@@ -576,6 +576,7 @@ template <int BN_, bool VEC>
 __global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmArgs p, const StreamK sk) {
     constexpr int V = kFixupVecs;
     static_assert((BM * BN_) % (1024 * V) == 0, "whole float4 groups per CTA");
+    pdl_wait();   // launched as a dependent of the tile kernel: its pieces first
     const int tl = blockIdx.y;
     const int64_t U = sk.units, f = (int64_t)tl * sk.kslices, l = f + sk.kslices - 1;
     const int c0 = streamk_owner(f, U, sk.G), c1 = streamk_owner(l, U, sk.G);

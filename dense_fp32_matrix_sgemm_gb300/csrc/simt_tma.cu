@@ -265,6 +265,10 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         tc::tma_prefetch_desc(&tmA);
         tc::tma_prefetch_desc(&tmB);
     }
+    // launched as a programmatic dependent (of the transpose that turned an
+    // operand, say): the set-up above overlaps its tail; memory after this
+    pdl_wait();
+    pdl_trigger();
     int z, tm, tn;
     raster(p, (int)blockIdx.x, z, tm, tn);
     int a_col, b_col;
@@ -299,6 +303,10 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         tc::tma_prefetch_desc(&tmA);
         tc::tma_prefetch_desc(&tmB);
     }
+    // launched as a programmatic dependent (of the transpose that turned an
+    // operand, say): the set-up above overlaps its tail; memory after this
+    pdl_wait();
+    pdl_trigger();
     int a_col, b_col;
     thread_coords(a_col, b_col);
     uint32_t gk = 0;
@@ -402,8 +410,8 @@ cudaError_t launch_tile_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB, c
     cudaError_t err = ensure_smem_attribute(kern, smem, configured);
     if (err != cudaSuccess) return err;
     const long long blocks = (long long)g.batch * g.tiles_m * g.tiles_n;
-    kern<<<(unsigned)blocks, THREADS, smem, s>>>(tmA, tmB, g, device_error_word());
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(THREADS), smem, s, tmA, tmB, g,
+                      device_error_word());
 }
 
 template <bool KA>
@@ -414,9 +422,8 @@ cudaError_t launch_streamk_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB
     static std::atomic<unsigned long long> configured{0};
     cudaError_t err = ensure_smem_attribute(kern, smem, configured);
     if (err != cudaSuccess) return err;
-    kern<<<(unsigned)(sk.tiles_dp + sk.G), THREADS, smem, s>>>(tmA, tmB, g, sk,
-                                                              device_error_word());
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)(sk.tiles_dp + sk.G)), dim3(THREADS), smem, s, tmA, tmB,
+                      g, sk, device_error_word());
 }
 
 }  // namespace
@@ -480,9 +487,8 @@ bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &
     err = transA ? launch_streamk_kernel<false>(tmA, tmB, g, sk, s)
                  : launch_streamk_kernel<true>(tmA, tmB, g, sk, s);
     if (err != cudaSuccess) return true;
-    streamk_fixup_kernel<kTmaBN, true><<<streamk_fixup_grid<kTmaBN>(pl.tiles_sk), 256, 0, s>>>(
-        g, sk);
-    err = cudaGetLastError();
+    err = launch_pdl(streamk_fixup_kernel<kTmaBN, true>, streamk_fixup_grid<kTmaBN>(pl.tiles_sk),
+                     dim3(256), 0, s, g, sk);
     return true;
 }
 

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
                                                         int rows, int cols, float *__restrict__ Y,
                                                         int64_t ldy) {
     __shared__ float tile[32][33];
+    // the tile kernel that reads the copy may start its set-up meanwhile
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
     const int64_t tiles_c = (cols + 31) / 32, tiles_r = (rows + 31) / 32;
     for (int64_t t = blockIdx.x; t < tiles_c * tiles_r; t += gridDim.x) {
