@@ -858,7 +858,9 @@ def main():
             "kernel": simt_kernel_label(M, N, batch, w.transB, sms_for_label, K, w.transA),
             "roofline": {"bound": "alu", "achieved": plain, "peak": peak_max, "unit": "TFLOP/s",
                          "frac": plain / peak_max,
-                         "traffic": profiled_traffic("sgemm_simt_kernel", args.workload)},
+                         "traffic": profiled_traffic("sgemm_simt_tma_kernel"
+                                                     if not w.transB and aligned
+                                                     else "sgemm_simt_kernel", args.workload)},
             "note": "the same product through plain sgemm_f32 (one kernel, no workspace)"}
     if tc is not None:
         tc["pct_of_fp32_peak_at_max_clock"] = 100.0 * tc["value"] / world / peak_max
