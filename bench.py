@@ -308,7 +308,8 @@ def streamk_plan(M, N, K, transA, transB, sms, aligned=True):
     N >= 1024 and B^T when M >= 1024 (the copies are 16-byte aligned).  Then A
     stored transposed with row-major B takes the TMA-fed kernel when aligned:
     128 x 128 tiles, G = 2 CTAs per SM, stream-K when G < tiles < 4G and the
-    tiles do not fill whole waves."""
+    tiles do not fill whole waves.  Aligned row-major A that is not turned
+    runs the TMA kernel directly, without stream-K."""
     big = 2.0 * M * N * K >= 1.6e10
     turn_a = big and not transA and N >= 1024
     turn_b = big and transB and M >= 1024
@@ -324,6 +325,8 @@ def streamk_plan(M, N, K, transA, transB, sms, aligned=True):
         tiles = -(-M // 128) * -(-N // 128)
         sk = tiles > sms and tiles % sms != 0 and kslices >= 2
         kernel = "sgemm_simt_streamk_kernel" if sk else "sgemm_simt_kernel"
+    elif not tB and aligned:   # row-major A read directly by the TMA kernel, no stream-K
+        sk, kernel = False, "sgemm_simt_tma_kernel"
     else:
         sk, kernel = False, "sgemm_simt_kernel"
     return int(turn_a) + int(turn_b), sk, kernel

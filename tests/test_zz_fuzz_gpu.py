@@ -193,3 +193,56 @@ def test_random_case(idx):
         idx_bad = np.argwhere(~ok)[:5]
         raise AssertionError(f"{label}: {int((~ok).sum())} outputs outside the bound, first "
                              f"{idx_bad.tolist()} got {got[~ok][:5]} want {ref[~ok][:5]}")
+
+
+# sgemm_f32_streamk: sizes large enough that the entry's choices all occur:
+# a K-contiguous operand turned into a workspace copy (2MNK >= 1.6e10), the
+# TMA kernel or the cp.async kernel (alignment), stream-K below four waves of
+# two CTAs per SM and the plain grid above, pieces of one or two K slices.
+NSTREAMK = 24
+
+
+def _draw_streamk_cases():
+    rng = np.random.default_rng(20261203)
+    cases = []
+    for i in range(NSTREAMK):
+        c = dict(entry="sgemm_f32_streamk", key=5000 + i, seed=int(rng.integers(1 << 30)))
+        c["M"] = int(rng.integers(1000, 3600))
+        c["N"] = int(rng.integers(1000, 3600))
+        c["K"] = int(rng.choice([int(rng.integers(1, 64)), int(rng.integers(64, 2600))]))
+        c["batch"] = 1
+        c["transA"], c["transB"] = int(rng.integers(2)), int(rng.integers(2))
+        # most cases 16-byte aligned (the TMA kernels), the rest not (cp.async)
+        dims = [c["M"] if c["transA"] else c["K"], c["K"] if c["transB"] else c["N"], c["N"]]
+        if rng.random() < 0.6:
+            c["pads"] = [int((-d) % 4 + 4 * rng.integers(0, 2)) for d in dims]
+            c["offset"] = 0
+        else:
+            c["pads"] = [int(rng.choice([0, 1, 3])) for _ in dims]
+            c["offset"] = int(rng.choice([0, 1]))
+        c["dist"] = str(rng.choice(["uniform", "normal", "int"]))
+        cases.append(c)
+    return cases
+
+
+STREAMK_CASES = _draw_streamk_cases()
+
+
+@pytest.mark.parametrize("idx", range(NSTREAMK))
+def test_random_streamk_case(idx):
+    c = STREAMK_CASES[idx]
+    label = _label(c)
+    case = _operands(c)
+    M, N, K = case["M"], case["N"], case["K"]
+    assert sg.device_status(reset=True) == 0
+    got = run(case, entry="sgemm_f32_streamk", offset=c["offset"])
+    assert sg.device_status(reset=True) == 0, f"{label}: device status set"
+    ref, S = oracle.sgemm(case["A"][0], case["B"][0], M, N, K, transA=case["transA"],
+                          transB=case["transB"], lda=case["lda"], ldb=case["ldb"],
+                          with_scale=True)
+    assert np.isfinite(got).all(), f"{label}: non-finite outputs"
+    if c["dist"] == "int" and K * 16 < (1 << 24):
+        bad = got[0] != ref
+        assert not bad.any(), f"{label}: {int(bad.sum())} outputs differ from the exact result"
+    ok = oracle.within_tolerance(got[0], ref, S)
+    assert ok.all(), f"{label}: {int((~ok).sum())} outputs outside the bound"
