@@ -306,33 +306,66 @@ __device__ __forceinline__ void store_tile_rows(const Tf32x3Params &p, const CUt
 //                   allocates and frees TMEM;
 //   warps 2-5:      epilogue, warp w draining TMEM lane quarter w % 4 through
 //                   its own staging buffers (outside the ring), then arriving
-//                   on the buffer's "empty" barrier.
+//                   on the buffer's "empty" barrier;
+//   warps 6-9:      (RAW only) converters: wait for a stage to land, turn its
+//                   raw operand tiles into planes in place, fence the async
+//                   proxy and arrive on the stage's "converted" barrier, which
+//                   the MMA issuer then waits on instead of "full".
 // With ACC_BUFS = 2 the MMAs of tile i+1 overlap the epilogue of tile i; the
 // 128 x 256 three-term tile needs all 512 TMEM columns for one tile
 // (ACC_BUFS = 1), and there only the next tile's loads overlap its epilogue.
 // Barrier phases: a ring stage's j-th fill is waited on with parity j & 1 and
 // its (j-1)-th release with parity (j-1) & 1; accumulator buffer b's u-th
 // result likewise.  Every wait is bounded and the abort word stops all roles.
-constexpr int PTHREADS = 192;
+constexpr int PTHREADS = 192;   // producer, MMA and 4 epilogue warps
+constexpr int kConvWarps = 4;   // converter warps when an operand arrives raw
 
-template <class CFG, int ACC_BUFS>
+// RAW: bit 0 set when op(A), bit 1 when op(B), is loaded as the caller's
+// fp32 (K-contiguous rows) instead of split planes; converter warps then turn
+// each landed slice into its hi (and lo) planes inside the stage.
+template <class CFG, int ACC_BUFS, int RAW = 0>
 struct Persist {
+    static constexpr int CONV_WARPS = RAW ? kConvWarps : 0;
+    static constexpr int THREADS = PTHREADS + 32 * CONV_WARPS;
     static constexpr int BUF_COLS = CFG::TERMS == 3 ? 2 * CFG::BN : CFG::BN;
     static constexpr int TMEM_COLS = ACC_BUFS * BUF_COLS <= 256 ? 256 : 512;
     static constexpr int STAGING = 4 * 8192;   // 4 epilogue warps x two 4 KB buffers
-    static constexpr int BARS = 2 * CFG::STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int BARS = (RAW ? 3 : 2) * CFG::STAGES + 2 * ACC_BUFS + 1;
+    // transaction bytes of one stage: a raw operand lands as one plane
+    static constexpr int TX_BYTES = ((RAW & 1) ? CFG::A_TILE : CFG::PLANES * CFG::A_TILE) +
+                                    ((RAW & 2) ? CFG::B_TILE : CFG::PLANES * CFG::B_TILE);
     static constexpr int SMEM_BYTES = CFG::STAGES * CFG::STAGE_BYTES + STAGING + 1024 + 256;
     static_assert(ACC_BUFS * BUF_COLS <= 512, "accumulators exceed tensor memory");
     static_assert(BARS * 8 + 8 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <class CFG, int ACC_BUFS>
-__global__ void __launch_bounds__(PTHREADS, 1)
+// In place, over one landed operand tile of `bytes` bytes: the raw fp32 x at
+// each position of the hi plane becomes tf32_rn(x) and, for three terms, the
+// same position of the lo plane (`bytes` further) gets tf32_rn(x - hi): the
+// values the split kernel writes, so the MMAs see the same operands.  The
+// swizzle moves whole 16-byte chunks, so position-wise work ignores it.
+template <int PLANES>
+__device__ __forceinline__ void convert_tile(uint8_t *tile, int bytes, int t, int nt) {
+    float4 *hi = reinterpret_cast<float4 *>(tile);
+    float4 *lo = reinterpret_cast<float4 *>(tile + bytes);
+    for (int v = t; v < bytes / 16; v += nt) {
+        const float4 x = hi[v];
+        const float4 h = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
+                                     tc::to_tf32(x.w));
+        hi[v] = h;
+        if constexpr (PLANES == 2)
+            lo[v] = make_float4(tc::to_tf32(x.x - h.x), tc::to_tf32(x.y - h.y),
+                                tc::to_tf32(x.z - h.z), tc::to_tf32(x.w - h.w));
+    }
+}
+
+template <class CFG, int ACC_BUFS, int RAW>
+__global__ void __launch_bounds__(Persist<CFG, ACC_BUFS, RAW>::THREADS, 1)
 tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
-    using P = Persist<CFG, ACC_BUFS>;
+    using P = Persist<CFG, ACC_BUFS, RAW>;
     constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
     constexpr int BN = CFG::BN, ACC_COLS = CFG::ACC_COLS;
     constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
@@ -348,6 +381,8 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t accf0 = empty0 + 8 * STAGES;     // accumulator b holds a finished tile
     const uint32_t acce0 = accf0 + 8 * ACC_BUFS;    // accumulator b has been drained
     const uint32_t done_bar = acce0 + 8 * ACC_BUFS;
+    const uint32_t conv0 = done_bar + 8;            // (RAW) stage s converted
+    const uint32_t ready0 = RAW ? conv0 : full0;    // what the MMA waits for
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + P::BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -366,6 +401,8 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
             tc::mbar_init(acce0 + 8 * b, 4);   // one arrival per epilogue warp
         }
         tc::mbar_init(done_bar, 1);
+        if constexpr (RAW != 0)
+            for (int s = 0; s < STAGES; ++s) tc::mbar_init(conv0 + 8 * s, P::CONV_WARPS);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmA);
@@ -400,13 +437,23 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                     const uint32_t st = ring + s * STAGE_BYTES;
                     const uint32_t fb = full0 + 8 * s;
-                    tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    tc::mbar_arrive_expect_tx(fb, P::TX_BYTES);
                     const int k0 = kb * BK;
+                    // a raw operand: the caller's rows into the hi slot; else its planes
+                    if constexpr (RAW & 1) {
+                        tc::tma_load_3d(st, &tmA, fb, k0, m0, z);
+                    } else {
 #pragma unroll
-                    for (int pl = 0; pl < PLANES; ++pl) {
-                        tc::tma_load_3d(st + pl * A_TILE, &tmA, fb, k0, m0, PLANES * z + pl);
-                        tc::tma_load_3d(st + PLANES * A_TILE + pl * B_TILE, &tmB, fb, k0, n0,
-                                        PLANES * z + pl);
+                        for (int pl = 0; pl < PLANES; ++pl)
+                            tc::tma_load_3d(st + pl * A_TILE, &tmA, fb, k0, m0, PLANES * z + pl);
+                    }
+                    if constexpr (RAW & 2) {
+                        tc::tma_load_3d(st + PLANES * A_TILE, &tmB, fb, k0, n0, z);
+                    } else {
+#pragma unroll
+                        for (int pl = 0; pl < PLANES; ++pl)
+                            tc::tma_load_3d(st + PLANES * A_TILE + pl * B_TILE, &tmB, fb, k0, n0,
+                                            PLANES * z + pl);
                     }
                     issued = g + 1;
                 }
@@ -435,7 +482,7 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                 for (int kb = 0; kb < kblocks; ++kb) {
                     const long long g = (long long)i * kblocks + kb;
                     const int s = (int)(g % STAGES);
-                    if (!tc::mbar_wait(full0 + 8 * s, (int)((g / STAGES) & 1), abort_flag)) {
+                    if (!tc::mbar_wait(ready0 + 8 * s, (int)((g / STAGES) & 1), abort_flag)) {
                         stop = true;
                         break;
                     }
@@ -462,7 +509,7 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             tc::mma_commit(done_bar);   // tracks every MMA issued above, also on abort
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------- epilogue warps 2-5: TMEM lane quarter warp % 4
         const int q = warp & 3;
         const uint32_t stage = staging + (uint32_t)(warp - 2) * 8192u;
@@ -483,6 +530,31 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
             if (lane == 0) tc::mbar_arrive(acce0 + 8 * b);
         }
         if (lane == 0 && cc > 0) tc::bulk_wait_group_read<0>();
+    } else if constexpr (RAW != 0) {
+        // ---------------- converter warps 6..: raw operand tiles -> planes
+        constexpr int NT = 32 * P::CONV_WARPS;
+        const int t = (int)threadIdx.x - PTHREADS;
+        for (int i = 0; i < nlocal; ++i) {
+            bool stop = false;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                const long long g = (long long)i * kblocks + kb;
+                const int s = (int)(g % STAGES);
+                const bool ok = tc::mbar_wait(full0 + 8 * s, (int)((g / STAGES) & 1), abort_flag);
+                // one warp-uniform decision
+                if (!__all_sync(0xffffffffu, ok && !*abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t *st = smem + s * STAGE_BYTES;
+                if constexpr (RAW & 1) convert_tile<PLANES>(st, A_TILE, t, NT);
+                if constexpr (RAW & 2) convert_tile<PLANES>(st + PLANES * A_TILE, B_TILE, t, NT);
+                // the planes are read by the tensor cores (async proxy)
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(conv0 + 8 * s);
+            }
+            if (stop) break;
+        }
     }
     __syncwarp();
     if (*abort_flag && threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
@@ -619,6 +691,30 @@ bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp
     return r == CUDA_SUCCESS;
 }
 
+// The caller's K-contiguous operand as [batch][rows][K] fp32 (row stride ld,
+// batch stride zstride), box BK x box_rows x 1 in the planes' swizzle: the
+// raw slice lands where the hi plane would.  False when the driver rejects
+// the description (the operand is then split as usual).
+template <class CFG>
+bool make_raw_map(CUtensorMap *map, const float *base, int rows, int K, int64_t ld,
+                  int64_t zstride, int batch, int box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const int64_t zs = batch > 1 ? zstride : ld * (int64_t)rows;
+    if (zs <= 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)zs * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)CFG::BK, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = CFG::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : CFG::ROW_BYTES == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                         : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // C as a [batch][M][N] tensor (row stride ldc, batch stride strideC), box
 // 32 x 32 x 1 with the 128-byte swizzle the epilogue writes in.
 bool make_c_map(CUtensorMap *map, float *C, int M, int N, int64_t ldc, int64_t strideC,
@@ -643,30 +739,33 @@ size_t plane_bytes(int64_t rows, int64_t K, int64_t batch, int planes) {
     return align_up((size_t)planes * (size_t)batch * (size_t)rows * Kp * 4, 256);
 }
 
-// Encodes the tensor maps, launches the two split kernels into `ws` and fills
-// the GEMM kernel's parameters: everything both GEMM kernels need.
+// Encodes the tensor maps, launches the split kernel into `ws` for the
+// operands that need planes and fills the GEMM kernel's parameters.  `raw`
+// (bits as in Persist::RAW) marks operands the GEMM loads as they are; their
+// maps are already in tmA / tmB.
 template <class CFG>
-cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s,
-                    CUtensorMap &tmA, CUtensorMap &tmB, CUtensorMap &tmC, Tf32x3Params &p) {
+cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, void *ws,
+                    cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB, CUtensorMap &tmC,
+                    Tf32x3Params &p) {
     constexpr int PLANES = CFG::PLANES;
     const int Kp = (a.K + 3) / 4 * 4;
     float *wsA = static_cast<float *>(ws);
     float *wsB = wsA + plane_bytes(a.M, a.K, a.batch, PLANES) / 4;
 
     // tensor maps first (they depend only on the workspace and the sizes), so
-    // no host work separates the split launches from the GEMM launch
-    if (!make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM) ||
-        !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN))
+    // no host work separates the split launch from the GEMM launch
+    if ((!(raw & 1) && !make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM)) ||
+        (!(raw & 2) && !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN)))
         return cudaErrorInvalidValue;
 
     // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes,
-    // one launch for both
+    // one launch for both; a raw operand gets no CTAs
     SplitArgs sa;
     sa.K = a.K;
     sa.Kp = Kp;
     sa.batch = a.batch;
     auto job = [&](SplitJob &j, const float *X, int64_t ld, int64_t sX, int R, bool kcontig,
-                   float *out) {
+                   float *out, bool skip) {
         j.X = X;
         j.ld = ld;
         j.sX = sX;
@@ -676,13 +775,16 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, void *ws, cudaS
         j.vec = kcontig && (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 && sX % 4 == 0;
         const int64_t work = kcontig ? ((int64_t)a.batch * R * (Kp / 4) + 255) / 256
                                      : (int64_t)a.batch * ((R + 31) / 32) * ((a.K + 31) / 32);
-        j.blocks = work < 152 * 16 ? (work > 0 ? work : 1) : 152 * 16;
+        j.blocks = skip ? 0 : (work < 152 * 16 ? (work > 0 ? work : 1) : 152 * 16);
     };
-    job(sa.job[0], a.A, a.lda, a.strideA, a.M, !transA, wsA);
-    job(sa.job[1], a.B, a.ldb, a.strideB, a.N, transB, wsB);
-    split_kernel<PLANES><<<(unsigned)(sa.job[0].blocks + sa.job[1].blocks), 256, 0, s>>>(sa);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    job(sa.job[0], a.A, a.lda, a.strideA, a.M, !transA, wsA, (raw & 1) != 0);
+    job(sa.job[1], a.B, a.ldb, a.strideB, a.N, transB, wsB, (raw & 2) != 0);
+    const int64_t split_blocks = sa.job[0].blocks + sa.job[1].blocks;
+    if (split_blocks > 0) {
+        split_kernel<PLANES><<<(unsigned)split_blocks, 256, 0, s>>>(sa);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
 
     p.C = a.C;
     p.ldc = a.ldc;
@@ -725,36 +827,73 @@ cudaError_t ensure_smem(Kern kern, int bytes, std::atomic<unsigned long long> &c
 }
 
 // One CTA per SM, walking the tiles (see tf32x3_persistent_kernel).
-template <class CFG, int ACC_BUFS>
-cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void *ws,
-                              cudaStream_t s) {
-    using P = Persist<CFG, ACC_BUFS>;
+template <class CFG, int ACC_BUFS, int RAW>
+cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, void *ws,
+                                  cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB) {
+    using P = Persist<CFG, ACC_BUFS, RAW>;
     static std::atomic<unsigned long long> configured{0};
-    cudaError_t e = ensure_smem(tf32x3_persistent_kernel<CFG, ACC_BUFS>, P::SMEM_BYTES, configured);
+    cudaError_t e =
+        ensure_smem(tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW>, P::SMEM_BYTES, configured);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmC;
     Tf32x3Params p;
-    e = prepare<CFG>(a, transA, transB, ws, s, tmA, tmB, tmC, p);
+    e = prepare<CFG>(a, transA, transB, RAW, ws, s, tmA, tmB, tmC, p);
     if (e != cudaSuccess) return e;
     const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
-    cfg.blockDim = dim3(PTHREADS);
+    cfg.blockDim = dim3(P::THREADS);
     cfg.dynamicSmemBytes = P::SMEM_BYTES;
     cfg.stream = s;
+    // a programmatic dependent of the split launch (or, with no split, of
+    // whatever precedes): every global access waits on griddepcontrol.wait
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tf32x3_persistent_kernel<CFG, ACC_BUFS>, tmA, tmB, tmC, p);
+    e = cudaLaunchKernelEx(&cfg, tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW>, tmA, tmB, tmC, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// For short reductions (K <= kRawMaxK), operands stored K-contiguous
+// (row-major A, B stored transposed) with 16-byte aligned rows and batches
+// are loaded as they are and split inside the GEMM; everything else goes
+// through the split kernel.  The conversion adds shared-memory traffic and a
+// step to every stage of a ring that is already latency-bound, so it only
+// pays where the separate split launch dominates: 96 x 512 x 512 x 64 with
+// B^T 68.9 -> 81.5 TFLOP/s (no split launch at all), row-major 68.1 -> 73.1;
+// but 3072^3 257 -> 235 (A raw) and 265 -> 174 (both raw), 4096 x 4096 x 256
+// 165 -> 147 (results bit-identical either way).
+constexpr int kRawMaxK = 64;
+
+template <class CFG, int ACC_BUFS>
+cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void *ws,
+                              cudaStream_t s) {
+    auto raw_ok = [&](const float *X, int64_t ld, int64_t sX, bool kcontig) {
+        return a.K <= kRawMaxK && kcontig && reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
+               ld % 4 == 0 && (a.batch == 1 || (sX > 0 && sX % 4 == 0));
+    };
+    CUtensorMap tmA, tmB;
+    int raw = 0;
+    if (raw_ok(a.A, a.lda, a.strideA, !transA) &&
+        make_raw_map<CFG>(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM))
+        raw |= 1;
+    if (raw_ok(a.B, a.ldb, a.strideB, transB) &&
+        make_raw_map<CFG>(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, CFG::BN))
+        raw |= 2;
+    switch (raw) {
+        case 1: return launch_persistent_raw<CFG, ACC_BUFS, 1>(a, transA, transB, ws, s, tmA, tmB);
+        case 2: return launch_persistent_raw<CFG, ACC_BUFS, 2>(a, transA, transB, ws, s, tmA, tmB);
+        case 3: return launch_persistent_raw<CFG, ACC_BUFS, 3>(a, transA, transB, ws, s, tmA, tmB);
+        default: return launch_persistent_raw<CFG, ACC_BUFS, 0>(a, transA, transB, ws, s, tmA, tmB);
+    }
 }
 
 }  // namespace tf32x3

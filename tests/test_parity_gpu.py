@@ -785,3 +785,39 @@ def test_streamk_tma_exact_on_integers(M, N, K):
     got = run(case, entry="sgemm_f32_streamk")
     assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
     check_full(case, got, exact=True, label=f"streamk tma {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- in-kernel split
+
+# For short reductions (K <= 64) the tensor-core paths load K-contiguous
+# operands (row-major A, B stored transposed) with 16-byte aligned rows as
+# they are and split them into hi/lo TF32 planes inside the GEMM (converter
+# warps, in shared memory); the others go through the split kernel.  Both
+# produce the same planes, so a problem whose buffers are shifted by one
+# float (forcing the split kernel for every operand) must give the same
+# bits.  Layouts: NN (A raw), NT (both raw), TT (B raw), TN (neither), ragged
+# edges and K tails, batches, and longer K (split kernel on both sides).
+RAWSPLIT = [(0, 0, 300, 260, 61, 1), (0, 1, 513, 384, 64, 1), (1, 1, 200, 388, 33, 1),
+            (1, 0, 260, 300, 64, 1), (0, 1, 512, 512, 64, 3), (0, 0, 1100, 1300, 7, 1),
+            (0, 1, 700, 900, 300, 1)]
+
+
+@pytest.mark.parametrize("entry_name", ["sgemm_f32_tf32x3", "sgemm_f32_tf32"])
+@pytest.mark.parametrize("tA,tB,M,N,K,batch", RAWSPLIT)
+def test_in_kernel_split_matches_split_kernel(entry_name, tA, tB, M, N, K, batch):
+    pad = lambda d: (-d) % 4 + 4   # 16-byte rows, and a padding column
+    lda = (M if tA else K) + pad(M if tA else K)
+    ldb = (K if tB else N) + pad(K if tB else N)
+    case = workloads.make_operands(M, N, K, batch=batch, transA=tA, transB=tB, lda=lda, ldb=ldb,
+                                   ldc=N + 4, dist="normal", poison=True, seed=98,
+                                   key=980 + M + N + K + 7 * tA + 13 * tB)
+    entry = entry_name + ("_strided_batched" if batch > 1 else "")
+    assert sg.device_status(reset=True) == 0
+    raw = run(case, entry=entry)
+    split = run(case, entry=entry, offset=1)
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    assert np.array_equal(raw, split), "in-kernel split differs from the split kernel"
+    if entry_name == "sgemm_f32_tf32x3":
+        check_full(case, raw, label=f"tf32x3 raw {tA}{tB} {M}x{N}x{K}x{batch}")
+    else:
+        _check_tf32(case, raw, f"tf32 raw {tA}{tB} {M}x{N}x{K}x{batch}")
