@@ -221,8 +221,9 @@ def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
 
 
 def workload_table(torch, sg, dev, stream, sp, reps=5):
-    """ms and TFLOP/s of sgemm_f32 and sgemm_f32_tf32x3 on every named workload
-    (operands resident on the device, median of `reps` after two warm-ups)."""
+    """ms, TFLOP/s and compulsory-byte GB/s of sgemm_f32 and sgemm_f32_tf32x3 on
+    every named workload (operands resident on the device, median of `reps`
+    after two warm-ups)."""
     out = {}
     for name, w in workloads.WORKLOADS.items():
         case = workloads.make_case(w)
@@ -234,7 +235,7 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
         sA, sB, sC = case["A"][0].size, case["B"][0].size, w.M * ldc
         row = {"M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "transA": w.transA,
-               "transB": w.transB}
+               "transB": w.transB, "min_bytes": workloads.min_bytes(w.M, w.N, w.K, w.batch)}
 
         def simt():
             sg.sgemm_f32_strided_batched(w.M, w.N, w.K, dA.data_ptr(), lda, sA, dB.data_ptr(), ldb,
@@ -273,6 +274,9 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
             ms = sorted(ts)[len(ts) // 2]
             row[label + "_ms"] = ms
             row[label + "_tflops"] = workloads.flops(w.M, w.N, w.K, w.batch) / (ms * 1e-3) / 1e12
+            # compulsory bytes / time: the figure that matters where a path
+            # is bandwidth-bound (the batched QK^T shape on the tensor cores)
+            row[label + "_gbs"] = row["min_bytes"] / (ms * 1e-3) / 1e9
         out[name] = row
         del dA, dB, dC, ws
         if sk_need:
