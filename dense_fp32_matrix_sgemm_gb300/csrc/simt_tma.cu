@@ -50,6 +50,7 @@ constexpr int kTmaBK = 32;       // K slice per stage
 constexpr int kTmaStages = 3;    // 3 x 32 KB of operands per CTA
 constexpr int kTmaBN = 128;      // tile 128 x 128
 constexpr int kTmaMinBlocks = 2;
+constexpr int kPersistMaxSlices = 8;   // K <= 256: the persistent form (see below)
 
 template <int BK, int STAGES, int BN_>
 constexpr int tma_smem_bytes() {
@@ -85,6 +86,84 @@ __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int 
     return full0;
 }
 
+// One K slice of the tile from a landed stage (A part `at`, B part `bt`):
+// acc[i][.] += a[i] * b[.] for its BK k steps, k ascending, in packed pairs
+// along n.  A fragments come K-major (4 + 4 rows per 16-byte load) or, with
+// KA, from the M-major swizzled stage (4 k of a row per 16-byte load).
+template <int BK, int BN_, bool KA>
+__device__ __forceinline__ void slice_fma(const float *at, const float *bt, int a_col, int b_col,
+                                          float (&acc)[8][BN_ / 16]) {
+    constexpr int TN = BN_ / 16;
+    // one k step: acc[i][.] += a[i] * b[.] in packed pairs along n
+    auto step = [&](const float (&a)[8], int kk) {
+        constexpr int NSB = BN_ / 64;
+        const float *br = bt + kk * BN_;
+        float b[TN];
+#pragma unroll
+        for (int h = 0; h < NSB; ++h) {
+            const float4 bv = *reinterpret_cast<const float4 *>(br + 64 * h + b_col);
+            b[4 * h + 0] = bv.x;
+            b[4 * h + 1] = bv.y;
+            b[4 * h + 2] = bv.z;
+            b[4 * h + 3] = bv.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+            for (int j = 0; j < TN; j += 2) {
+                float2 c = make_float2(acc[i][j], acc[i][j + 1]);
+                c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
+                acc[i][j] = c.x;
+                acc[i][j + 1] = c.y;
+            }
+        }
+    };
+    if constexpr (KA) {
+        // rows ty + 16 j of the [128][32] swizzled stage; k in ascending order
+        static_assert(BK == 32, "the 128-byte swizzle spans one 32-float row");
+        const int ty = a_col >> 2;
+        const float *arow = at + ty * BK;
+#pragma unroll
+        for (int kq = 0; kq < BK / 4; ++kq) {
+            const int chunk = 4 * (kq ^ (ty & 7));
+            float4 av[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                av[j] = *reinterpret_cast<const float4 *>(arow + j * 16 * BK + chunk);
+            {
+                const float a[8] = {av[0].x, av[1].x, av[2].x, av[3].x,
+                                    av[4].x, av[5].x, av[6].x, av[7].x};
+                step(a, 4 * kq + 0);
+            }
+            {
+                const float a[8] = {av[0].y, av[1].y, av[2].y, av[3].y,
+                                    av[4].y, av[5].y, av[6].y, av[7].y};
+                step(a, 4 * kq + 1);
+            }
+            {
+                const float a[8] = {av[0].z, av[1].z, av[2].z, av[3].z,
+                                    av[4].z, av[5].z, av[6].z, av[7].z};
+                step(a, 4 * kq + 2);
+            }
+            {
+                const float a[8] = {av[0].w, av[1].w, av[2].w, av[3].w,
+                                    av[4].w, av[5].w, av[6].w, av[7].w};
+                step(a, 4 * kq + 3);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            const float *ar = at + kk * BM;
+            const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            step(a, kk);
+        }
+    }
+}
+
 // Accumulates slices [0, ktiles) of one piece, starting at K offset kbeg, of
 // the tile at (m0, n0) of problem z into acc (zeroed first).  gk counts the
 // slices this CTA has consumed before the piece: slice g lives in stage
@@ -101,7 +180,6 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
                                              int a_col, int b_col, float (&acc)[8][BN_ / 16],
                                              volatile int *abort) {
     constexpr int TN = BN_ / 16;
-    constexpr int NSB = BN_ / 64;
     constexpr int ATILE = BK * BM;
     constexpr int BTILE = BK * BN_;
     constexpr uint32_t STAGE_BYTES = (ATILE + BTILE) * sizeof(float);
@@ -135,75 +213,7 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
         const uint32_t rs = gk % STAGES;
         (void)tc::mbar_wait(full0 + 8 * rs, (gk / STAGES) & 1, abort);
         ++gk;
-        const float *at = As + rs * ATILE;
-        const float *bt = Bs + rs * BTILE;
-        // one k step: acc[i][.] += a[i] * b[.] in packed pairs along n
-        auto step = [&](const float (&a)[8], int kk) {
-            const float *br = bt + kk * BN_;
-            float b[TN];
-#pragma unroll
-            for (int h = 0; h < NSB; ++h) {
-                const float4 bv = *reinterpret_cast<const float4 *>(br + 64 * h + b_col);
-                b[4 * h + 0] = bv.x;
-                b[4 * h + 1] = bv.y;
-                b[4 * h + 2] = bv.z;
-                b[4 * h + 3] = bv.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 ai = make_float2(a[i], a[i]);
-#pragma unroll
-                for (int j = 0; j < TN; j += 2) {
-                    float2 c = make_float2(acc[i][j], acc[i][j + 1]);
-                    c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
-                    acc[i][j] = c.x;
-                    acc[i][j + 1] = c.y;
-                }
-            }
-        };
-        if constexpr (KA) {
-            // rows ty + 16 j of the [128][32] swizzled stage; k in ascending order
-            static_assert(BK == 32, "the 128-byte swizzle spans one 32-float row");
-            const int ty = a_col >> 2;
-            const float *arow = at + ty * BK;
-#pragma unroll
-            for (int kq = 0; kq < BK / 4; ++kq) {
-                const int chunk = 4 * (kq ^ (ty & 7));
-                float4 av[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    av[j] = *reinterpret_cast<const float4 *>(arow + j * 16 * BK + chunk);
-                {
-                    const float a[8] = {av[0].x, av[1].x, av[2].x, av[3].x,
-                                        av[4].x, av[5].x, av[6].x, av[7].x};
-                    step(a, 4 * kq + 0);
-                }
-                {
-                    const float a[8] = {av[0].y, av[1].y, av[2].y, av[3].y,
-                                        av[4].y, av[5].y, av[6].y, av[7].y};
-                    step(a, 4 * kq + 1);
-                }
-                {
-                    const float a[8] = {av[0].z, av[1].z, av[2].z, av[3].z,
-                                        av[4].z, av[5].z, av[6].z, av[7].z};
-                    step(a, 4 * kq + 2);
-                }
-                {
-                    const float a[8] = {av[0].w, av[1].w, av[2].w, av[3].w,
-                                        av[4].w, av[5].w, av[6].w, av[7].w};
-                    step(a, 4 * kq + 3);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int kk = 0; kk < BK; ++kk) {
-                const float *ar = at + kk * BM;
-                const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
-                const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
-                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                step(a, kk);
-            }
-        }
+        slice_fma<BK, BN_, KA>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
         // the warp's lanes have all read the stage: release it
         __syncwarp();
         if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
@@ -279,6 +289,83 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                                   (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
     if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
     store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+}
+
+// Persistent form for short reductions: CTA c of G walks tiles c, c + G, ...
+// of the whole grid, all of K each.  Slice g of the CTA (tile g / ktiles,
+// K slice g % ktiles) uses stage g % STAGES, and the issuing thread stays
+// STAGES - 1 slices ahead across tile boundaries: the next tile's first
+// slices are in flight while this tile's last ones compute and its results
+// are stored.  With 2 K slices per tile (K = 64) a CTA of the plain kernel
+// spends most of its life on set-up, the first load's latency and the store.
+template <int BK, int STAGES, int BN_, bool KA, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB)
+sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
+                              unsigned int *status) {
+    constexpr int ATILE = BK * BM;
+    constexpr int BTILE = BK * BN_;
+    constexpr uint32_t STAGE_BYTES = (ATILE + BTILE) * sizeof(float);
+    extern __shared__ __align__(128) float smem_raw[];
+    float *smem = align_ring(smem_raw);
+    float *As = smem;
+    float *Bs = smem + STAGES * BK * BM;
+    volatile int *abort;
+    const uint32_t full0 = tma_pipeline_init<BK, STAGES, BN_>(smem, abort);
+    const uint32_t empty0 = full0 + 8 * STAGES;
+    if (threadIdx.x == 0) {
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+    }
+    pdl_wait();
+    pdl_trigger();
+    int a_col, b_col;
+    thread_coords(a_col, b_col);
+    const int c = blockIdx.x, G = gridDim.x;
+    const int tiles = p.batch * p.tiles_m * p.tiles_n;
+    const int mine = c < tiles ? (tiles - 1 - c) / G + 1 : 0;
+    const int ktiles = (p.K + BK - 1) / BK;
+    const int total = mine * ktiles;   // slices of this CTA
+    const bool issuer = threadIdx.x == 0;
+    auto issue = [&](int g) {
+        const int i = g / ktiles, j = g - i * ktiles;
+        int z, tm, tn;
+        raster(p, c + i * G, z, tm, tn);
+        const uint32_t st = (uint32_t)g % STAGES;
+        if (g >= STAGES)   // slice g - STAGES released by every warp
+            (void)tc::mbar_wait(empty0 + 8 * st, ((uint32_t)g / STAGES - 1) & 1, abort);
+        const uint32_t bar = full0 + 8 * st;
+        tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        if constexpr (KA)
+            tc::tma_load_3d(smem_u32(As + st * ATILE), &tmA, bar, j * BK, tm * BM, z);
+        else
+            tc::tma_load_3d(smem_u32(As + st * ATILE), &tmA, bar, tm * BM, j * BK, z);
+        tc::tma_load_3d(smem_u32(Bs + st * BTILE), &tmB, bar, tn * BN_, j * BK, z);
+    };
+    if (issuer)
+        for (int g = 0; g < STAGES - 1 && g < total; ++g) issue(g);
+    int g = 0;
+#pragma unroll 1
+    for (int i = 0; i < mine; ++i) {
+        float acc[8][BN_ / 16];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int q = 0; q < BN_ / 16; ++q) acc[r][q] = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < ktiles; ++j, ++g) {
+            const uint32_t rs = (uint32_t)g % STAGES;
+            (void)tc::mbar_wait(full0 + 8 * rs, ((uint32_t)g / STAGES) & 1, abort);
+            slice_fma<BK, BN_, KA>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
+            if (issuer && g + STAGES - 1 < total) issue(g + STAGES - 1);
+        }
+        int z, tm, tn;
+        raster(p, c + i * G, z, tm, tn);
+        store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+    }
+    if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
 }
 
 // The stream-K schedule (see StreamK) as one grid of tiles_dp + G CTAs:
@@ -415,6 +502,18 @@ cudaError_t launch_tile_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB, c
 }
 
 template <bool KA>
+cudaError_t launch_persist_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                                  const GemmArgs &g, int ctas, cudaStream_t s) {
+    auto kern = sgemm_simt_persist_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
+    constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t err = ensure_smem_attribute(kern, smem, configured);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3((unsigned)ctas), dim3(THREADS), smem, s, tmA, tmB, g,
+                      device_error_word());
+}
+
+template <bool KA>
 cudaError_t launch_streamk_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                   const GemmArgs &g, const StreamK &sk, cudaStream_t s) {
     auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
@@ -465,6 +564,17 @@ bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
+    // A stored transposed, short reductions over at least two waves of
+    // resident CTAs: the persistent form, which prefetches across tile
+    // boundaries (96 x 512 x 512 x 64: 42.3 -> 45.9 TFLOP/s; 48 x 1024^2 x 64:
+    // 48.2 -> 52.0).  With row-major A it spills and gained nothing (96 x
+    // 512^2 x 128: 50.2 -> 47.5), so that layout keeps one tile per CTA.
+    const long long tiles = (long long)g.batch * g.tiles_m * g.tiles_n;
+    const long long G = (long long)sm_count() * simt_tma_ctas_per_sm();
+    if (transA && (a.K + kTmaBK - 1) / kTmaBK <= kPersistMaxSlices && tiles >= 2 * G) {
+        err = launch_persist_kernel<false>(tmA, tmB, g, (int)G, s);
+        return true;
+    }
     err = transA ? launch_tile_kernel<false>(tmA, tmB, g, s) : launch_tile_kernel<true>(tmA, tmB, g, s);
     return true;
 }

@@ -832,3 +832,28 @@ def test_in_kernel_split_matches_split_kernel(entry_name, tA, tB, M, N, K, batch
         check_full(case, raw, label=f"tf32x3 raw {tA}{tB} {M}x{N}x{K}x{batch}")
     else:
         _check_tf32(case, raw, f"tf32 raw {tA}{tB} {M}x{N}x{K}x{batch}")
+
+
+# Short reductions over many tiles (K <= 256, at least two waves of resident
+# CTAs) with A stored transposed run the persistent TMA kernel, which loads
+# the next tile's slices while it finishes the current one (row-major A keeps
+# one tile per CTA): batches, ragged edges and K tails; bit-identical to the
+# cp.async kernel (one-float offset).
+PERSIST = [(1, 0, 512, 512, 64, 96), (0, 0, 512, 512, 64, 96), (1, 0, 4100, 4000, 200, 1),
+           (0, 0, 4100, 4000, 33, 1), (1, 0, 1000, 3000, 256, 2)]
+
+
+@pytest.mark.parametrize("tA,tB,M,N,K,batch", PERSIST)
+def test_persistent_tma_kernel(tA, tB, M, N, K, batch):
+    pad = lambda d: (-d) % 4
+    lda = (M if tA else K) + pad(M if tA else K)
+    ldb = N + pad(N)
+    case = workloads.make_operands(M, N, K, batch=batch, transA=tA, transB=tB, lda=lda, ldb=ldb,
+                                   ldc=N + 4, dist="int", poison=True, seed=99,
+                                   key=990 + M + N + K + tA)
+    entry = "sgemm_f32_strided_batched" if batch > 1 else "sgemm_f32"
+    assert sg.device_status(reset=True) == 0
+    got = run(case, entry=entry)
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    check_full(case, got, exact=True, label=f"persistent {tA}{tB} {M}x{N}x{K}x{batch}")
+    assert np.array_equal(got, run(case, entry=entry, offset=1)), "TMA and cp.async kernels differ"
