@@ -543,7 +543,7 @@ int simt_tma_ctas_per_sm() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
     int v = cached[dev & 63].load();
     if (v <= 0) {
-        auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, true, kTmaMinBlocks>;
+        auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, false, kTmaMinBlocks>;
         constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess ||
@@ -582,8 +582,10 @@ bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t
 bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &pl, void *ws,
                              cudaStream_t s, cudaError_t &err) {
     using namespace simt;
+    // the stream-K plan covers A stored transposed only (see streamk_plan)
+    if (!transA) return false;
     CUtensorMap tmA, tmB;
-    if (!make_maps(a, !transA, tmA, tmB)) return false;
+    if (!make_maps(a, false, tmA, tmB)) return false;
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
@@ -594,8 +596,7 @@ bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &
     sk.G = pl.G;
     sk.units = pl.units;
     sk.ws = static_cast<float *>(ws);
-    err = transA ? launch_streamk_kernel<false>(tmA, tmB, g, sk, s)
-                 : launch_streamk_kernel<true>(tmA, tmB, g, sk, s);
+    err = launch_streamk_kernel<false>(tmA, tmB, g, sk, s);
     if (err != cudaSuccess) return true;
     err = launch_pdl(streamk_fixup_kernel<kTmaBN, true>, streamk_fixup_grid<kTmaBN>(pl.tiles_sk),
                      dim3(256), 0, s, g, sk);
