@@ -31,11 +31,17 @@
 //     (16 warps) per SM, 4 warps per scheduler to hide the FMA and
 //     shared-load latencies.  The cp.async kernel needs 8 x 16 tiles and one
 //     CTA per SM to avoid spilling.
-// Two kernels: one tile per CTA (sgemm_f32, strided batches as the third
-// tensor dimension) and the stream-K schedule (sgemm_f32_streamk) as one
-// grid: whole waves of tiles, one per CTA, then one CTA per stream-K range.  Every mbarrier wait is bounded; one that runs out sets bit 0
-// of the library's device status word and the CTA finishes without waiting
-// again.
+// Three kernels:
+//   * sgemm_simt_tma_kernel: one tile per CTA (sgemm_f32; strided batches
+//     are the third tensor dimension);
+//   * sgemm_simt_persist_tma_kernel: the same tiles walked by one CTA per
+//     resident slot, the loads running ahead across tile boundaries (short
+//     reductions with A stored transposed);
+//   * sgemm_simt_streamk_tma_kernel: the stream-K schedule
+//     (sgemm_f32_streamk) as one grid, whole waves of tiles one per CTA,
+//     then one CTA per stream-K range.
+// Every mbarrier wait is bounded; one that runs out sets bit 0 of the
+// library's device status word and the CTA finishes without waiting again.
 #include <atomic>
 #include <cstdint>
 
