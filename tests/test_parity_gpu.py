@@ -857,3 +857,31 @@ def test_persistent_tma_kernel(tA, tB, M, N, K, batch):
     assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
     check_full(case, got, exact=True, label=f"persistent {tA}{tB} {M}x{N}x{K}x{batch}")
     assert np.array_equal(got, run(case, entry=entry, offset=1)), "TMA and cp.async kernels differ"
+
+
+@pytest.mark.parametrize("tA", [1, 0])
+def test_tma_overlapping_batches(tA):
+    """Batches whose A matrices overlap in memory (0 < strideA < rows * lda)
+    reach the tensor-map path (A either way, row-major B); each batch must
+    match the oracle on its own view of the shared buffer."""
+    import torch
+    M, N, K, batch = 1100, 1300, 96, 3   # 297 tiles: past the cluster split's range
+    rows, lda = (K, M) if tA else (M, K)
+    strideA = (rows // 2) * lda          # each batch starts halfway into the previous one
+    sizeA = strideA * (batch - 1) + rows * lda
+    rng = np.random.default_rng(97)
+    A = rng.integers(-4, 5, size=sizeA).astype(np.float32)
+    B = rng.integers(-4, 5, size=(batch, K, N)).astype(np.float32)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B.reshape(-1)).cuda()
+    dC = torch.full((batch * M * N,), float("nan"), device="cuda")
+    sg.sgemm_f32_strided_batched(M, N, K, dA.data_ptr(), lda, strideA, dB.data_ptr(), N, K * N,
+                                 dC.data_ptr(), N, M * N, batch, tA, 0,
+                                 torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    got = dC.cpu().numpy().reshape(batch, M, N)
+    assert sg.device_status(reset=True) == 0
+    for z in range(batch):
+        Az = A[z * strideA:z * strideA + rows * lda].reshape(rows, lda)
+        ref = oracle.sgemm(Az, B[z], M, N, K, transA=tA, lda=lda, ldb=N)
+        assert np.array_equal(got[z], ref), f"batch {z} differs from the exact result"
