@@ -885,3 +885,52 @@ def test_tma_overlapping_batches(tA):
         Az = A[z * strideA:z * strideA + rows * lda].reshape(rows, lda)
         ref = oracle.sgemm(Az, B[z], M, N, K, transA=tA, lda=lda, ldb=N)
         assert np.array_equal(got[z], ref), f"batch {z} differs from the exact result"
+
+
+def test_cuda_graph_capture_and_replay():
+    """The entry points enqueue kernels only (no allocation, no synchronisation),
+    so they can be captured in a CUDA graph: sgemm_f32_streamk (transpose,
+    stream-K tile kernel, fix-up, chained as programmatic dependents) and
+    sgemm_f32_tf32x3 (split and persistent kernels).  Replays must give the
+    bits of direct calls, also after the inputs change in place."""
+    import torch
+    M, N, K = 2304, 2560, 1536
+    g = torch.Generator(device="cuda").manual_seed(7)
+    A = torch.rand(M, K, device="cuda", generator=g) * 2 - 1
+    B = torch.rand(K, N, device="cuda", generator=g) * 2 - 1
+    C_graph = torch.empty(M, N, device="cuda")
+    T_graph = torch.empty(M, N, device="cuda")
+    sk_need = sg.streamk_workspace_size(M, N, K, 0, 0)
+    tc_need = sg.tf32x3_workspace_size(M, N, K, 1)
+    sk_ws = torch.empty(sk_need, dtype=torch.uint8, device="cuda")
+    tc_ws = torch.empty(tc_need, dtype=torch.uint8, device="cuda")
+
+    def calls(C, T):
+        s = torch.cuda.current_stream().cuda_stream
+        sg.sgemm_f32_streamk(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, 0, 0,
+                             sk_ws.data_ptr(), sk_need, s)
+        sg.sgemm_f32_tf32x3(M, N, K, A.data_ptr(), K, B.data_ptr(), N, T.data_ptr(), N, 0, 0,
+                            tc_ws.data_ptr(), tc_need, s)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # warm-up: one-time attribute and map set-up
+        calls(C_graph, T_graph)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls(C_graph, T_graph)
+    for round_ in range(2):
+        if round_:
+            A.copy_(torch.rand(M, K, device="cuda", generator=g) * 2 - 1)
+        C_graph.fill_(float("nan"))
+        T_graph.fill_(float("nan"))
+        graph.replay()
+        C_direct = torch.empty(M, N, device="cuda")
+        T_direct = torch.empty(M, N, device="cuda")
+        calls(C_direct, T_direct)
+        torch.cuda.synchronize()
+        assert torch.equal(C_graph, C_direct), f"replay {round_}: sgemm_f32_streamk differs"
+        assert torch.equal(T_graph, T_direct), f"replay {round_}: sgemm_f32_tf32x3 differs"
+    assert sg.device_status(reset=True) == 0
