@@ -337,11 +337,13 @@ def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None, alpha=
     Transposed views are handled through the trans flags without copies.
     Runs on ``stream`` (default: torch's current stream).
 
-    precision="fp32": CUDA-core FMA (sgemm_f32*, or sgemm_f32_ex* with an
-    epilogue, or sgemm_f32_splitk when ``splits`` is given: 0 = automatic);
+    precision="fp32": CUDA-core FMA (sgemm_f32_streamk for single plain
+    products, which turns K-contiguous operands of large problems and uses
+    stream-K; sgemm_f32_strided_batched for batches; sgemm_f32_ex* with an
+    epilogue; sgemm_f32_splitk when ``splits`` is given: 0 = automatic);
     "tf32x3": tensor cores with the three-term TF32 split (sgemm_f32_tf32x3*);
-    "tf32": one TF32 product (sgemm_f32_tf32*, reduced precision).  The
-    tensor-core modes and split-K use ``workspace`` (a CUDA uint8 tensor) or a
+    "tf32": one TF32 product (sgemm_f32_tf32*, reduced precision).  Entries
+    that need scratch memory use ``workspace`` (a CUDA uint8 tensor) or a
     fresh one from torch's allocator.  beta != 0 needs ``out`` (its values are
     read)."""
     import torch
@@ -393,8 +395,16 @@ def matmul(A, B, out=None, stream=None, precision="fp32", workspace=None, alpha=
                                       B.stride(0), out.data_ptr(), ldc, out.stride(0), batch,
                                       tA, tB, sp)
         elif plain:
-            sgemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA, tB,
-                      sp)
+            # the fastest CUDA-core path: large problems turn K-contiguous
+            # operands and use stream-K, with a workspace; others need none
+            need = streamk_workspace_size(M, N, K, tA, tB)
+            if need:
+                ws, wsb = scratch(need)
+                sgemm_f32_streamk(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(),
+                                  ldc, tA, tB, ws, wsb, sp)
+            else:
+                sgemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, tA,
+                          tB, sp)
         elif batched:
             sgemm_f32_ex_strided_batched(M, N, K, alpha, A.data_ptr(), lda, A.stride(0),
                                          B.data_ptr(), ldb, B.stride(0), beta, out.data_ptr(), ldc,

@@ -934,3 +934,24 @@ def test_cuda_graph_capture_and_replay():
         assert torch.equal(C_graph, C_direct), f"replay {round_}: sgemm_f32_streamk differs"
         assert torch.equal(T_graph, T_direct), f"replay {round_}: sgemm_f32_tf32x3 differs"
     assert sg.device_status(reset=True) == 0
+
+
+def test_matmul_convenience_uses_streamk():
+    """sg.matmul on a large single product takes sgemm_f32_streamk (row-major
+    A turned into a workspace copy, stream-K tail): within the bound, and the
+    same bits as calling that entry directly."""
+    import torch
+    M, N, K = 2304, 2560, 1536
+    case = workloads.make_operands(M, N, K, dist="normal", seed=100, key=1000)
+    A = torch.from_numpy(case["A"][0]).cuda()
+    B = torch.from_numpy(case["B"][0]).cuda()
+    out = sg.matmul(A, B)
+    need = sg.streamk_workspace_size(M, N, K, 0, 0)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    direct = torch.empty(M, N, device="cuda")
+    sg.sgemm_f32_streamk(M, N, K, A.data_ptr(), K, B.data_ptr(), N, direct.data_ptr(), N, 0, 0,
+                         ws.data_ptr(), need, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(out, direct)
+    check_full(case, out.cpu().numpy()[None], label="matmul streamk")
