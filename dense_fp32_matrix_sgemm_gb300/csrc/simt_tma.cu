@@ -40,8 +40,9 @@
 //   * sgemm_simt_streamk_tma_kernel: the stream-K schedule
 //     (sgemm_f32_streamk) as one grid, whole waves of tiles one per CTA,
 //     then one CTA per stream-K range.
-// Every mbarrier wait is bounded; one that runs out sets bit 0 of the
-// library's device status word and the CTA finishes without waiting again.
+// Every mbarrier wait is bounded; once one runs out the CTA waits no more,
+// except for the issuing thread's own copies in flight (again bounded), and
+// bit 0 of the library's device status word is raised.
 #include <atomic>
 #include <cstdint>
 
@@ -227,6 +228,24 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
     }
 }
 
+// After a wait ran out (the abort word is set; every later wait returned at
+// once), thread 0 raises bit 0 of the status word and waits, with a limit,
+// for the copies of the last STAGES slices it issued (the CTA's slices
+// [n - STAGES, n)) to land, so that none writes into shared memory after the
+// CTA has exited.  Does nothing in a run whose waits all completed.
+template <int STAGES>
+__device__ __forceinline__ void finish_abort(uint32_t full0, uint32_t n, volatile int *abort,
+                                             unsigned int *status) {
+    if (threadIdx.x != 0 || !*abort) return;
+    if (status != nullptr) atomicOr(status, 1u);
+    for (uint32_t g = n > STAGES ? n - STAGES : 0; g < n; ++g) {
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(full0 + 8 * (g % STAGES), (g / STAGES) & 1) &&
+               clock64() - t0 < tc::kWaitLimitCycles) {
+        }
+    }
+}
+
 // The thread's place in the tile: rows a_col..a_col+3 and +64, columns
 // b_col..b_col+3 and +64 (Z-order 4 x 8 warps, 2 warps across).
 __device__ __forceinline__ void thread_coords(int &a_col, int &b_col) {
@@ -293,7 +312,7 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t gk = 0;
     tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
                                   (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
-    if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+    finish_abort<STAGES>(full0, gk, abort, status);
     store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
 
@@ -371,7 +390,7 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         raster(p, c + i * G, z, tm, tn);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
     }
-    if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+    finish_abort<STAGES>(full0, (uint32_t)total, abort, status);
 }
 
 // The stream-K schedule (see StreamK) as one grid of tiles_dp + G CTAs:
@@ -410,7 +429,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         float acc[8][BN_ / 16];
         tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
                                       sk.kslices, a_col, b_col, acc, abort);
-        if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+        finish_abort<STAGES>(full0, gk, abort, status);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         return;
     }
@@ -445,7 +464,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         }
     }
-    if (threadIdx.x == 0 && *abort && status != nullptr) atomicOr(status, 1u);
+    finish_abort<STAGES>(full0, gk, abort, status);
 }
 
 namespace {
