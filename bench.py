@@ -202,14 +202,22 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
-    """The tile the library's launcher picks (same rules as
-    csrc/simt_launch.cuh, for 16-byte aligned operands: A stored transposed
-    with row-major B takes the TMA-fed kernel; else K <= 256 takes two CTAs
-    per SM; otherwise waves of one CTA per SM, a 128x256 tile costing 1.95
-    128x128 tiles, the wide tile only for row-major B)."""
-    if transA and not transB:
-        return ("sgemm_simt_tma_kernel 128x128 tile, BK 32, 3 stages, 2 CTAs/SM, TMA-fed, "
-                "fma.rn.f32x2")
+    """The kernel the library's launcher picks for 16-byte aligned operands
+    (same rules as csrc/simt_launch.cuh and csrc/simt_tma.cu): problems whose
+    128x128 tiles cover at most half the SMs split K over a cluster; row-major
+    B takes the TMA-fed kernel (persistent for short reductions with A stored
+    transposed); else K <= 256 takes two CTAs per SM; otherwise waves of one
+    CTA per SM, a 128x256 tile costing 1.95 128x128 tiles."""
+    tiles = batch * -(-M // 128) * -(-N // 128)
+    if tiles * 2 <= sms and K > 32:
+        return "sgemm_simt_kernel 128x128 tile, K split over the CTAs of a cluster"
+    if not transB:
+        a = "A stored transposed" if transA else "row-major A as 128-byte-swizzled K boxes"
+        if transA and K <= 256 and tiles >= 4 * sms:
+            return ("sgemm_simt_persist_tma_kernel 128x128 tile, BK 32, 3 stages, 2 CTAs/SM, "
+                    f"TMA-fed ({a}), loads across tile boundaries, fma.rn.f32x2")
+        return ("sgemm_simt_tma_kernel 128x128 tile, BK 32, 3 stages, 2 CTAs/SM, "
+                f"TMA-fed ({a}), fma.rn.f32x2")
     if K <= 256:
         return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
     tm = -(-M // 128)
@@ -743,9 +751,11 @@ def main():
 
         t_plain, t_split = timed(plain), timed(split)
         fl = 2.0 * sm_ * sn_ * sk_
-        sk = {"shape": [sm_, sn_, sk_], "splits": splits, "plain_ms": t_plain,
-              "splitk_ms": t_split, "speedup": t_plain / t_split,
-              "splitk_tflops": fl / (t_split * 1e-3) / 1e12}
+        sk = {"shape": [sm_, sn_, sk_], "splits": splits, "sgemm_f32_ms": t_plain,
+              "splitk_ms": t_split, "speedup_over_sgemm_f32": t_plain / t_split,
+              "splitk_tflops": fl / (t_split * 1e-3) / 1e12,
+              "note": "sgemm_f32 already splits this K over the CTAs of one 16-CTA cluster "
+                      "(no workspace); sgemm_f32_splitk uses 64 chunks and a reduction pass"}
         del gA, gB, gC, wsk
 
         # matrix-vector shape (N = 1): bound by reading A once from HBM
