@@ -205,27 +205,23 @@ def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
     """The kernel the library's launcher picks for 16-byte aligned operands
     (same rules as csrc/simt_launch.cuh and csrc/simt_tma.cu): problems whose
     128x128 tiles cover at most half the SMs split K over a cluster; row-major
-    B takes the TMA-fed kernel (persistent for short reductions with A stored
-    transposed); else K <= 256 takes two CTAs per SM; otherwise waves of one
-    CTA per SM, a 128x256 tile costing 1.95 128x128 tiles."""
+    B, or both operands stored transposed, take the TMA-fed kernel (persistent
+    for short reductions with A stored transposed and row-major B); row-major
+    A with B stored transposed takes the cp.async kernel at two CTAs per SM."""
     tiles = batch * -(-M // 128) * -(-N // 128)
     if tiles * 2 <= sms and K > 32:
         return "sgemm_simt_kernel 128x128 tile, K split over the CTAs of a cluster"
-    if not transB:
-        a = "A stored transposed" if transA else "row-major A as 128-byte-swizzled K boxes"
-        if transA and K <= 256 and tiles >= 4 * sms:
+    if transA or not transB:
+        if transB:
+            a = "A stored transposed, B^T as 128-byte-swizzled K boxes"
+        else:
+            a = "A stored transposed" if transA else "row-major A as 128-byte-swizzled K boxes"
+        if transA and not transB and K <= 256 and tiles >= 4 * sms:
             return ("sgemm_simt_persist_tma_kernel 128x128 tile, BK 32, 3 stages, 2 CTAs/SM, "
                     f"TMA-fed ({a}), loads across tile boundaries, fma.rn.f32x2")
         return ("sgemm_simt_tma_kernel 128x128 tile, BK 32, 3 stages, 2 CTAs/SM, "
                 f"TMA-fed ({a}), fma.rn.f32x2")
-    if K <= 256:
-        return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
-    tm = -(-M // 128)
-    narrow = batch * tm * -(-N // 128)
-    wide = batch * tm * -(-N // 256)
-    if not transB and 1.95 * -(-wide // sms) < -(-narrow // sms):
-        return "sgemm_simt_kernel 128x256 tile, BK 32, 2 stages, fma.rn.f32x2"
-    return "sgemm_simt_kernel 128x128 tile, BK 32, 3 stages, fma.rn.f32x2"
+    return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
 
 
 def workload_table(torch, sg, dev, stream, sp, reps=5):
@@ -320,8 +316,9 @@ def streamk_plan(M, N, K, transA, transB, sms, aligned=True):
     N >= 1024 and B^T when M >= 1024 (the copies are 16-byte aligned).  Then A
     stored transposed with row-major B takes the TMA-fed kernel when aligned:
     128 x 128 tiles, G = 2 CTAs per SM, stream-K when G < tiles < 4G and the
-    tiles do not fill whole waves.  Aligned row-major A that is not turned
-    runs the TMA kernel directly, without stream-K."""
+    tiles do not fill whole waves.  Aligned row-major A that is not turned, or
+    both operands stored transposed and neither turned, run the TMA kernel
+    directly, without stream-K."""
     big = 2.0 * M * N * K >= 1.6e10
     turn_a = big and not transA and N >= 1024
     turn_b = big and transB and M >= 1024
@@ -337,7 +334,7 @@ def streamk_plan(M, N, K, transA, transB, sms, aligned=True):
         tiles = -(-M // 128) * -(-N // 128)
         sk = tiles > sms and tiles % sms != 0 and kslices >= 2
         kernel = "sgemm_simt_streamk_kernel" if sk else "sgemm_simt_kernel"
-    elif not tB and aligned:   # row-major A read directly by the TMA kernel, no stream-K
+    elif (tA or not tB) and aligned:   # read directly by the TMA kernel, no stream-K
         sk, kernel = False, "sgemm_simt_tma_kernel"
     else:
         sk, kernel = False, "sgemm_simt_kernel"
@@ -358,7 +355,10 @@ def step_kernel_label(M, N, K, transA, transB, sms, batch, plain_label, aligned=
         parts.append(f"{kernel} (whole-wave tiles, then one stream-K range per CTA; TMA-fed, "
                      "two CTAs per SM) + streamk_fixup_kernel")
     elif kernel == "sgemm_simt_tma_kernel":
-        parts.append(simt_kernel_label(M, N, batch, 0, sms, K, 1))
+        big = 2.0 * M * N * K >= 1.6e10
+        tA = bool(transA or (big and N >= 1024))
+        tB = bool(transB and not (big and M >= 1024))
+        parts.append(simt_kernel_label(M, N, batch, int(tB), sms, K, int(tA)))
     else:
         parts.append(plain_label)
     return " + ".join(parts)
@@ -876,7 +876,7 @@ def main():
             "roofline": {"bound": "alu", "achieved": plain, "peak": peak_max, "unit": "TFLOP/s",
                          "frac": plain / peak_max,
                          "traffic": profiled_traffic("sgemm_simt_tma_kernel"
-                                                     if not w.transB and aligned
+                                                     if (w.transA or not w.transB) and aligned
                                                      else "sgemm_simt_kernel", args.workload)},
             "note": "the same product through plain sgemm_f32 (one kernel, no workspace)"}
     if tc is not None:

@@ -73,13 +73,16 @@ StreamKPlan streamk_plan(const GemmArgs &a, bool transA, bool transB, bool vec);
 cudaError_t launch_simt_streamk(const GemmArgs &a, bool transA, bool transB, bool vec,
                                 const StreamKPlan &plan, void *ws, cudaStream_t s);
 
-// The SIMT kernel fed by TMA (row-major B, A either way, 16-byte aligned
-// operands, no split-K chunks): one 128 x 128 tile per CTA, two CTAs per SM.
+// The SIMT kernel fed by TMA (row-major B with A either way, or both stored
+// transposed; 16-byte aligned operands, no split-K chunks): one 128 x 128
+// tile per CTA, two CTAs per SM.  Its stream-K form takes A stored transposed
+// and row-major B.
 // The launchers return false, launching nothing, when the operands cannot be
 // described as tensor maps; else they launch and store the status in `err`.
 bool simt_tma_eligible(const GemmArgs &a, bool transA, bool transB, bool vec);
 int simt_tma_ctas_per_sm();
-bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t &err);
+bool launch_simt_tma(const GemmArgs &a, bool transA, bool transB, cudaStream_t s,
+                     cudaError_t &err);
 bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &plan, void *ws,
                              cudaStream_t s, cudaError_t &err);
 

@@ -1,6 +1,7 @@
 // SIMT FP32 SGEMM fed by TMA, for row-major B with A either stored
-// transposed (K x M, contiguous along M) or row-major (contiguous along K):
-// a K slice of either operand is then a plain 2-D box of global memory.
+// transposed (K x M, contiguous along M) or row-major (contiguous along K),
+// and for both operands stored transposed: a K slice of either operand is
+// then a plain 2-D box of global memory.
 //
 // Same arithmetic as sgemm_simt_kernel (each output accumulated by one thread
 // in ascending k with packed fp32 FMAs, 8 x 8 register tile of 4 x 4
@@ -25,6 +26,9 @@
 //     16-byte load; all of a thread's rows share m % 8 = ty % 8, and the 4
 //     row groups of a warp land in 4 different chunks: conflict-free, and as
 //     many loads per k step as the K-major layout;
+//   * a K-contiguous B (stored transposed, with A stored transposed) lands
+//     the same way, [128][32] per n, each thread owning columns tx + 16 j;
+//     its packed FMAs pair outputs along m (see slice_fma);
 //   * the tensor map zero-fills rows, columns and K beyond the operand, so
 //     ragged tiles need no per-element predicates;
 //   * without per-thread copy state the kernel fits 128 registers: two CTAs
@@ -94,79 +98,106 @@ __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int 
 }
 
 // One K slice of the tile from a landed stage (A part `at`, B part `bt`):
-// acc[i][.] += a[i] * b[.] for its BK k steps, k ascending, in packed pairs
-// along n.  A fragments come K-major (4 + 4 rows per 16-byte load) or, with
-// KA, from the M-major swizzled stage (4 k of a row per 16-byte load).
-template <int BK, int BN_, bool KA>
+// acc[i][j] += a[i] * b[j] for its BK k steps, k ascending.  A fragments come
+// K-major (4 + 4 rows per 16-byte load) or, with KA, from the M-major swizzled
+// stage (4 k of a row per 16-byte load).  B fragments come K-major (4 + 4
+// columns per 16-byte load) or, with KB, from the N-major swizzled stage (4 k
+// of a column per 16-byte load).  A packed FMA takes one operand pair from
+// adjacent registers and the other as one value twice: pairs run along n
+// (b[j], b[j+1] from one K-major float4) unless B comes N-major, whose 8
+// values of a k step sit in 8 different registers; then pairs run along m
+// (a[i], a[i+1] from one K-major float4).  Moving values into pairs costs
+// about a third of the throughput, so both operands M/N-major (A row-major
+// with B stored transposed) is not a form of this kernel.
+template <int BK, int BN_, bool KA, bool KB>
 __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int a_col, int b_col,
                                           float (&acc)[8][BN_ / 16]) {
     constexpr int TN = BN_ / 16;
-    // one k step: acc[i][.] += a[i] * b[.] in packed pairs along n
-    auto step = [&](const float (&a)[8], int kk) {
-        constexpr int NSB = BN_ / 64;
-        const float *br = bt + kk * BN_;
-        float b[TN];
+    static_assert(!(KA && KB), "no packed-FMA pairs when both operands come M/N-major");
+    static_assert(!KB || BN_ == 128, "N-major B fragments assume 128-column tiles");
+    static_assert(!(KA || KB) || BK == 32, "the 128-byte swizzle spans one 32-float row");
+    auto fma8 = [&](const float (&a)[8], const float (&b)[TN]) {
+        if constexpr (KB) {   // pairs along m, b[j] twice
 #pragma unroll
-        for (int h = 0; h < NSB; ++h) {
+            for (int j = 0; j < TN; ++j) {
+                const float2 bj = make_float2(b[j], b[j]);
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    float2 c = make_float2(acc[i][j], acc[i + 1][j]);
+                    c = __ffma2_rn(make_float2(a[i], a[i + 1]), bj, c);
+                    acc[i][j] = c.x;
+                    acc[i + 1][j] = c.y;
+                }
+            }
+        } else {              // pairs along n, a[i] twice
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                for (int j = 0; j < TN; j += 2) {
+                    float2 c = make_float2(acc[i][j], acc[i][j + 1]);
+                    c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
+                    acc[i][j] = c.x;
+                    acc[i][j + 1] = c.y;
+                }
+            }
+        }
+    };
+    // fragments of k step kk from a K-major stage: columns col..col+3, +64, ...
+    auto a_kmajor = [&](int kk, float (&a)[8]) {
+        const float *ar = at + kk * BM;
+        const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
+        const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
+        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+        a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+    };
+    auto b_kmajor = [&](int kk, float (&b)[TN]) {
+        const float *br = bt + kk * BN_;
+#pragma unroll
+        for (int h = 0; h < BN_ / 64; ++h) {
             const float4 bv = *reinterpret_cast<const float4 *>(br + 64 * h + b_col);
             b[4 * h + 0] = bv.x;
             b[4 * h + 1] = bv.y;
             b[4 * h + 2] = bv.z;
             b[4 * h + 3] = bv.w;
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float2 ai = make_float2(a[i], a[i]);
-#pragma unroll
-            for (int j = 0; j < TN; j += 2) {
-                float2 c = make_float2(acc[i][j], acc[i][j + 1]);
-                c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
-                acc[i][j] = c.x;
-                acc[i][j + 1] = c.y;
-            }
-        }
     };
-    if constexpr (KA) {
-        // rows ty + 16 j of the [128][32] swizzled stage; k in ascending order
-        static_assert(BK == 32, "the 128-byte swizzle spans one 32-float row");
-        const int ty = a_col >> 2;
-        const float *arow = at + ty * BK;
+    if constexpr (KA || KB) {
+        // rows ty + 16 j (columns tx + 16 j) of the [128][32] swizzled stage:
+        // they share ty % 8 (tx % 8), hence the 16-byte chunk of k quad kq;
+        // four k per load, the other operand K-major one k at a time
+        const int t = KA ? a_col >> 2 : b_col >> 2;
+        const float *qrow = (KA ? at : bt) + t * BK;
 #pragma unroll
         for (int kq = 0; kq < BK / 4; ++kq) {
-            const int chunk = 4 * (kq ^ (ty & 7));
-            float4 av[8];
+            float4 qv[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                av[j] = *reinterpret_cast<const float4 *>(arow + j * 16 * BK + chunk);
-            {
-                const float a[8] = {av[0].x, av[1].x, av[2].x, av[3].x,
-                                    av[4].x, av[5].x, av[6].x, av[7].x};
-                step(a, 4 * kq + 0);
-            }
-            {
-                const float a[8] = {av[0].y, av[1].y, av[2].y, av[3].y,
-                                    av[4].y, av[5].y, av[6].y, av[7].y};
-                step(a, 4 * kq + 1);
-            }
-            {
-                const float a[8] = {av[0].z, av[1].z, av[2].z, av[3].z,
-                                    av[4].z, av[5].z, av[6].z, av[7].z};
-                step(a, 4 * kq + 2);
-            }
-            {
-                const float a[8] = {av[0].w, av[1].w, av[2].w, av[3].w,
-                                    av[4].w, av[5].w, av[6].w, av[7].w};
-                step(a, 4 * kq + 3);
+                qv[j] = *reinterpret_cast<const float4 *>(qrow + j * 16 * BK + 4 * (kq ^ (t & 7)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float q[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    q[j] = e == 0 ? qv[j].x : e == 1 ? qv[j].y : e == 2 ? qv[j].z : qv[j].w;
+                if constexpr (KA) {
+                    float b[TN];
+                    b_kmajor(4 * kq + e, b);
+                    fma8(q, b);
+                } else {
+                    float a[8];
+                    a_kmajor(4 * kq + e, a);
+                    fma8(a, q);
+                }
             }
         }
     } else {
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            const float *ar = at + kk * BM;
-            const float4 a0 = *reinterpret_cast<const float4 *>(ar + a_col);
-            const float4 a1 = *reinterpret_cast<const float4 *>(ar + 64 + a_col);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            step(a, kk);
+            float a[8], b[TN];
+            a_kmajor(kk, a);
+            b_kmajor(kk, b);
+            fma8(a, b);
         }
     }
 }
@@ -180,7 +211,7 @@ __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int 
 // g - STAGES from the same stage; each warp releases a slice once its lanes
 // have read it.  On return no copy of this piece is in flight (every issued
 // slice has been waited on), and the next piece may start at once.
-template <int BK, int STAGES, int BN_, bool KA>
+template <int BK, int STAGES, int BN_, bool KA, bool KB>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
                                              int m0, int n0, int z, int kbeg, int ktiles,
@@ -209,7 +240,10 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
             tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, kbeg + slice * BK, m0, z);
         else                // box (m, k): 128 m x 32 k
             tc::tma_load_3d(smem_u32(As + st * ATILE), tmA, bar, m0, kbeg + slice * BK, z);
-        tc::tma_load_3d(smem_u32(Bs + st * BTILE), tmB, bar, n0, kbeg + slice * BK, z);
+        if constexpr (KB)   // box (k, n): 32 k x 128 columns
+            tc::tma_load_3d(smem_u32(Bs + st * BTILE), tmB, bar, kbeg + slice * BK, n0, z);
+        else                // box (n, k): 128 n x 32 k
+            tc::tma_load_3d(smem_u32(Bs + st * BTILE), tmB, bar, n0, kbeg + slice * BK, z);
     };
     if (issuer) {
 #pragma unroll
@@ -220,7 +254,7 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
         const uint32_t rs = gk % STAGES;
         (void)tc::mbar_wait(full0 + 8 * rs, (gk / STAGES) & 1, abort);
         ++gk;
-        slice_fma<BK, BN_, KA>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
+        slice_fma<BK, BN_, KA, KB>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
         // the warp's lanes have all read the stage: release it
         __syncwarp();
         if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
@@ -264,7 +298,11 @@ __device__ __forceinline__ int acc_row(int a_col, int r) {
     return r < 4 ? a_col + r : 64 + a_col + (r - 4);
 }
 
-template <int BN_, bool KA>
+// Stores the thread's outputs with the epilogue.  Columns b_col..b_col+3
+// (and +64) go out as 16-byte stores; with KB the thread's columns are
+// tx + 16 j (tx = b_col / 4), stored one by one with the same arithmetic as
+// store_c4, a warp writing 32 consecutive bytes of each of its rows per j.
+template <int BN_, bool KA, bool KB = false>
 __device__ __forceinline__ void store_tile(const GemmArgs &p, int z, int m0, int n0, int a_col,
                                            int b_col, const float (&acc)[8][BN_ / 16]) {
     constexpr int NSB = BN_ / 64;
@@ -275,17 +313,33 @@ __device__ __forceinline__ void store_tile(const GemmArgs &p, int z, int m0, int
         const int row = m0 + acc_row<KA>(a_col, r);
         if (row >= p.M) continue;
         float *crow = Cz + (int64_t)row * p.ldc;
+        if constexpr (KB) {
+            const int tx = b_col >> 2;
 #pragma unroll
-        for (int h = 0; h < NSB; ++h)
-            store_c4(p, crow, n0 + h * 64 + b_col,
-                     make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
-                                 acc[r][4 * h + 3]),
-                     true, plain);
+            for (int j = 0; j < 8; ++j) {
+                const int col = n0 + tx + 16 * j;
+                if (col >= p.N) continue;
+                float v = acc[r][j];
+                if (!plain) {
+                    const float o = p.beta != 0.f ? crow[col] : 0.f;
+                    const float b = p.bias != nullptr ? p.bias[col] : 0.f;
+                    v = fmaf(p.beta, o, p.alpha * v) + b;
+                }
+                crow[col] = v;
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < NSB; ++h)
+                store_c4(p, crow, n0 + h * 64 + b_col,
+                         make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
+                                     acc[r][4 * h + 3]),
+                         true, plain);
+        }
     }
 }
 
 // One 128 x BN_ tile per CTA, all of K.
-template <int BK, int STAGES, int BN_, bool KA, int MINB>
+template <int BK, int STAGES, int BN_, bool KA, bool KB, int MINB>
 __global__ void __launch_bounds__(THREADS, MINB)
 sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmArgs p,
@@ -310,10 +364,10 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     thread_coords(a_col, b_col);
     float acc[8][BN_ / 16];
     uint32_t gk = 0;
-    tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
-                                  (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
+    tma_mainloop<BK, STAGES, BN_, KA, KB>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
+                                          (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
     finish_abort<STAGES>(full0, gk, abort, status);
-    store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
+    store_tile<BN_, KA, KB>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
 
 // Persistent form for short reductions: CTA c of G walks tiles c, c + G, ...
@@ -381,7 +435,7 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int j = 0; j < ktiles; ++j, ++g) {
             const uint32_t rs = (uint32_t)g % STAGES;
             (void)tc::mbar_wait(full0 + 8 * rs, ((uint32_t)g / STAGES) & 1, abort);
-            slice_fma<BK, BN_, KA>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
+            slice_fma<BK, BN_, KA, false>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
             __syncwarp();
             if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
             if (issuer && g + STAGES - 1 < total) issue(g + STAGES - 1);
@@ -427,8 +481,8 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, b, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
-                                      sk.kslices, a_col, b_col, acc, abort);
+        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
+                                                 z, 0, sk.kslices, a_col, b_col, acc, abort);
         finish_abort<STAGES>(full0, gk, abort, status);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         return;
@@ -446,8 +500,8 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, s0 * BK,
-                                      s1 - s0, a_col, b_col, acc, abort);
+        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
+                                                 z, s0 * BK, s1 - s0, a_col, b_col, acc, abort);
         if (!(s0 == 0 && s1 == sk.kslices)) {
             // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
             float *part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
@@ -507,16 +561,18 @@ bool make_kmajor_map(CUtensorMap *map, const float *base, int rows, int K, int64
     return r == CUDA_SUCCESS;
 }
 
-bool make_maps(const GemmArgs &a, bool ka, CUtensorMap &tmA, CUtensorMap &tmB) {
+bool make_maps(const GemmArgs &a, bool ka, bool kb, CUtensorMap &tmA, CUtensorMap &tmB) {
     const bool okA = ka ? make_kmajor_map(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM)
                         : make_operand_map(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM);
-    return okA && make_operand_map(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, kTmaBN);
+    const bool okB = kb ? make_kmajor_map(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, kTmaBN)
+                        : make_operand_map(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, kTmaBN);
+    return okA && okB;
 }
 
-template <bool KA>
+template <bool KA, bool KB>
 cudaError_t launch_tile_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &g,
                                cudaStream_t s) {
-    auto kern = sgemm_simt_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
+    auto kern = sgemm_simt_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, KB, kTmaMinBlocks>;
     constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
     static std::atomic<unsigned long long> configured{0};
     cudaError_t err = ensure_smem_attribute(kern, smem, configured);
@@ -554,11 +610,12 @@ cudaError_t launch_streamk_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB
 }  // namespace simt
 
 bool simt_tma_eligible(const GemmArgs &a, bool transA, bool transB, bool vec) {
-    // row-major B, 16-byte aligned bases and rows (vec), whole problems (no
-    // split-K chunks), distinct batches (a zero batch stride is not a tensor
-    // stride); A either way
-    (void)transA;
-    return !transB && vec && a.kchunk == 0 && (a.batch == 1 || (a.strideA > 0 && a.strideB > 0));
+    // 16-byte aligned bases and rows (vec), whole problems (no split-K
+    // chunks), distinct batches (a zero batch stride is not a tensor stride);
+    // any layout but row-major A with B stored transposed, which would leave
+    // the packed FMAs no operand pair in adjacent registers (see slice_fma)
+    return vec && (transA || !transB) && a.kchunk == 0 &&
+           (a.batch == 1 || (a.strideA > 0 && a.strideB > 0));
 }
 
 int simt_tma_ctas_per_sm() {
@@ -582,10 +639,11 @@ int simt_tma_ctas_per_sm() {
     return v;
 }
 
-bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t &err) {
+bool launch_simt_tma(const GemmArgs &a, bool transA, bool transB, cudaStream_t s,
+                     cudaError_t &err) {
     using namespace simt;
     CUtensorMap tmA, tmB;
-    if (!make_maps(a, !transA, tmA, tmB)) return false;
+    if (!make_maps(a, !transA, transB, tmA, tmB)) return false;
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;
@@ -596,11 +654,15 @@ bool launch_simt_tma(const GemmArgs &a, bool transA, cudaStream_t s, cudaError_t
     // 512^2 x 128: 50.2 -> 47.5), so that layout keeps one tile per CTA.
     const long long tiles = (long long)g.batch * g.tiles_m * g.tiles_n;
     const long long G = (long long)sm_count() * simt_tma_ctas_per_sm();
-    if (transA && (a.K + kTmaBK - 1) / kTmaBK <= kPersistMaxSlices && tiles >= 2 * G) {
+    if (transA && !transB && (a.K + kTmaBK - 1) / kTmaBK <= kPersistMaxSlices && tiles >= 2 * G) {
         err = launch_persist_kernel<false>(tmA, tmB, g, (int)G, s);
         return true;
     }
-    err = transA ? launch_tile_kernel<false>(tmA, tmB, g, s) : launch_tile_kernel<true>(tmA, tmB, g, s);
+    if (transB)   // A stored transposed (see simt_tma_eligible)
+        err = launch_tile_kernel<false, true>(tmA, tmB, g, s);
+    else
+        err = transA ? launch_tile_kernel<false, false>(tmA, tmB, g, s)
+                     : launch_tile_kernel<true, false>(tmA, tmB, g, s);
     return true;
 }
 
@@ -610,7 +672,7 @@ bool launch_simt_streamk_tma(const GemmArgs &a, bool transA, const StreamKPlan &
     // the stream-K plan covers A stored transposed only (see streamk_plan)
     if (!transA) return false;
     CUtensorMap tmA, tmB;
-    if (!make_maps(a, false, tmA, tmB)) return false;
+    if (!make_maps(a, false, false, tmA, tmB)) return false;
     GemmArgs g = a;
     g.tiles_m = (a.M + BM - 1) / BM;
     g.tiles_n = (a.N + kTmaBN - 1) / kTmaBN;

@@ -779,6 +779,81 @@ def test_tma_kernel_strided_batches():
     assert np.array_equal(got, run(case, entry="sgemm_f32_strided_batched", offset=1))
 
 
+# Both operands stored transposed run the same TMA kernel with B arriving as
+# 128-byte-swizzled K boxes ([n][k], a thread's columns tx + 16 j): its packed
+# FMAs pair outputs along m and it stores one float at a time.  Bits against
+# the cp.async kernel (one-float offset) and against the same logical product
+# with row-major B (the kernel's other fragment and store path).
+@pytest.mark.parametrize("M,N,K", TMA)
+@pytest.mark.parametrize("dist", ["normal", "int"])
+def test_tma_kernel_transposed_b(M, N, K, dist):
+    kw = dict(transA=1, lda=_rup4(M), ldc=N + 4, dist=dist, poison=True, seed=95,
+              key=951 + M + 3 * N + 7 * K)
+    case = workloads.make_operands(M, N, K, transB=1, ldb=_rup4(K), **kw)
+    assert sg.device_status(reset=True) == 0
+    got = run(case)
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    check_full(case, got, exact=dist == "int", label=f"tma B^T {M}x{N}x{K} {dist}")
+    assert np.array_equal(got, run(case, offset=1)), "TMA and cp.async kernels differ"
+    row_b = workloads.make_operands(M, N, K, transB=0, ldb=_rup4(N), **kw)
+    assert np.array_equal(got, run(row_b)), "B stored transposed and row-major B differ"
+
+
+def test_tma_transposed_b_strided_batches():
+    M, N, K, batch = 700, 708, 70, 4
+    case = workloads.make_operands(M, N, K, batch=batch, transA=1, transB=1, lda=704, ldb=72,
+                                   ldc=N + 4, dist="int", poison=True, seed=96, key=961)
+    got = run(case, entry="sgemm_f32_strided_batched")
+    assert sg.device_status(reset=True) == 0
+    check_full(case, got, exact=True, label="tma B^T batched")
+    assert np.array_equal(got, run(case, entry="sgemm_f32_strided_batched", offset=1))
+
+
+@pytest.mark.parametrize("alpha,beta,with_bias", [(0.7, -1.3, True), (-2.0, 0.5, False),
+                                                  (1.0, 0.0, True), (0.0, 2.0, True)])
+def test_tma_transposed_b_epilogue(alpha, beta, with_bias):
+    """alpha, beta and bias on the per-float store path (99 tiles: past the
+    cluster split), against the oracle and bit for bit against the 16-byte
+    store path of the same logical product with row-major B."""
+    M, N, K = 1100, 1300, 77
+    kw = dict(transA=1, lda=_rup4(M), ldc=N + 4, dist="normal", seed=55, key=502)
+    case = workloads.make_operands(M, N, K, transB=1, ldb=_rup4(K), **kw)
+    rng = np.random.default_rng(56)
+    C_in = rng.standard_normal((M, N)).astype(np.float32)
+    bias = rng.standard_normal(N).astype(np.float32) if with_bias else None
+    c_in = C_in if beta != 0.0 else None
+    got = _run_ex(case, alpha, beta, c_in, bias, "sgemm_f32_ex")
+    ref, S = oracle.sgemm_ex(case["A"][0], case["B"][0], M, N, K, alpha=alpha, beta=beta,
+                             C_in=C_in, bias=bias, transA=1, transB=1, lda=case["lda"],
+                             ldb=case["ldb"])
+    ok = oracle.within_tolerance(got, ref, S)
+    assert ok.all(), f"{int((~ok).sum())} outputs outside the bound"
+    row_b = workloads.make_operands(M, N, K, transB=0, ldb=_rup4(N), **kw)
+    assert np.array_equal(got, _run_ex(row_b, alpha, beta, c_in, bias, "sgemm_f32_ex"))
+
+
+# Long reductions in all four storage layouts: row-major B and both operands
+# transposed on the TMA kernel, row-major A with B stored transposed on the
+# cp.async kernel at two CTAs per SM.  One logical product, four identical
+# results, exact on integers.
+@pytest.mark.parametrize("M,N,K", [(1200, 1204, 999), (4100, 260, 2049)])
+def test_four_layouts_bit_identical_long_k(M, N, K):
+    outs = []
+    for tA in (0, 1):
+        for tB in (0, 1):
+            case = workloads.make_operands(M, N, K, transA=tA, transB=tB,
+                                           lda=_rup4(M if tA else K), ldb=_rup4(K if tB else N),
+                                           ldc=N + 4, dist="int", poison=True, seed=98,
+                                           key=980 + M + N + K)
+            got = run(case)
+            if not outs:
+                check_full(case, got, exact=True, label=f"layouts {M}x{N}x{K}")
+            outs.append(got)
+    assert sg.device_status(reset=True) == 0
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o), "storage layouts differ"
+
+
 # Stream-K on the TMA kernel (aligned A^T by B, 128 x 128 tiles, G = two CTAs
 # per SM, one grid of whole-wave tiles then one range per CTA): ragged edges,
 # two K slices per tile (pieces of one slice), more CTAs than stream-K units,
