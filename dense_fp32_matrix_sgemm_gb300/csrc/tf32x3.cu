@@ -4,17 +4,23 @@
 // TF32 keeps 10 explicit mantissa bits, so one TF32 product loses about 750x
 // in accuracy against FP32 FMA (the RRMSE comparison of 1.03e-6 vs 7.78e-4 on
 // the ChetanC28/cuda-kernels page).  Writing every input as x = hi + lo with
-// hi = tf32(x) and lo = tf32(x - hi), the product a*b is recovered to about
-// 2^-21 relative by hi_a*hi_b + hi_a*lo_b + lo_a*hi_b (the lo*lo term is
-// below that and dropped), each term a TF32 MMA accumulated in fp32 in TMEM.
-// With TERMS = 1 only hi_a*hi_b is formed: the plain TF32 product.
+// hi = x cut to TF32 (see tf32_hi) and lo = tf32_rn(x - hi), the product a*b
+// is recovered to about 2^-20 relative by hi_a*hi_b + hi_a*lo_b + lo_a*hi_b
+// (the lo*lo term is below that and dropped), each term a TF32 MMA
+// accumulated in fp32 in TMEM.  With TERMS = 1 only hi_a*hi_b is formed, from
+// hi = tf32_rn(x): the plain TF32 product.
 //
 // Stage 1 (one split launch for both operands): op(A) and op(B) are
 //   rewritten into a caller-owned workspace as K-major planes
 //   [batch][TERMS == 3 ? hi|lo : hi][rows][Kp] (Kp = K rounded up to 4 so
 //   rows are 16-byte aligned for TMA).  M- or N-major operands are
-//   corner-turned through a padded shared tile.  The GEMM is launched as a
-//   programmatic dependent of it and waits for it before reading a plane.
+//   corner-turned through a padded shared tile.  A K-contiguous operand with
+//   16-byte aligned rows needs no hi plane for three terms (the GEMM loads
+//   the caller's rows, which the MMA reads as hi), so only its lo plane is
+//   written; for short reductions it needs no split at all (converter warps
+//   make lo, or the rounded hi of one term, inside the GEMM).  The GEMM is
+//   launched as a programmatic dependent of it and waits for it before
+//   reading a plane.
 // Stage 2 (persistent GEMM kernel, one CTA per SM walking 128 x BN output
 //   tiles, BN = 256 or 128 picked per problem; 192 threads in three roles):
 //   warp 0 / lane 0 issues TMA loads of the swizzled K slices (BK fp32 of K,
@@ -78,9 +84,23 @@ __device__ unsigned int g_tf32x3_error = 0;
 
 // ------------------------------------------------------------------ split
 
+// The three-term split of an fp32 x.  A kind::tf32 MMA takes the upper 19
+// bits of each 32-bit operand word (sign, exponent, 10 mantissa bits) and
+// ignores the low 13, so hi is x with those bits cleared: the value the
+// tensor core sees when it reads x itself, which lets a K-contiguous operand
+// serve as its own hi plane.  x - hi is exact (the 13 dropped bits), and lo
+// rounds it to TF32 (nearest, ties away).  |x - hi - lo| <= 2^-21 |x| and the
+// dropped lo_a lo_b term is below 2^-20 |a b|.
+__device__ __forceinline__ float tf32_hi(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+}
+__device__ __forceinline__ float tf32_lo(float x, float hi) { return tc::to_tf32(x - hi); }
+
 // One operand to split: rows r of op(X) (R of them per problem), element
 // (r, k) at X[z*sX + r*ld + k] when kcontig, else at X[z*sX + k*ld + r];
 // planes written to `out`.  `blocks` CTAs of the split grid serve it.
+// lo_only (three terms, K-contiguous X): the GEMM reads X itself as the hi
+// term, so only the lo plane is written, one plane per problem.
 struct SplitJob {
     const float *X;
     int64_t ld, sX;
@@ -89,6 +109,7 @@ struct SplitJob {
     int R;
     int kcontig;
     int vec;   // kcontig rows allow 16-byte loads
+    int lo_only;
 };
 
 struct SplitArgs {
@@ -119,14 +140,21 @@ __device__ __forceinline__ void split_kcontig(const SplitJob &j, int K, int Kp, 
             if (k + 2 < K) x.z = __ldg(src + 2);
             if (k + 3 < K) x.w = __ldg(src + 3);
         }
-        const float4 h = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
-                                     tc::to_tf32(x.w));
-        float *hi = j.out + (PLANES * z) * plane + r * Kp + k;
-        *reinterpret_cast<float4 *>(hi) = h;
         if constexpr (PLANES == 2) {
-            *reinterpret_cast<float4 *>(hi + plane) =
-                make_float4(tc::to_tf32(x.x - h.x), tc::to_tf32(x.y - h.y),
-                            tc::to_tf32(x.z - h.z), tc::to_tf32(x.w - h.w));
+            const float4 h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
+            const float4 l = make_float4(tf32_lo(x.x, h.x), tf32_lo(x.y, h.y), tf32_lo(x.z, h.z),
+                                         tf32_lo(x.w, h.w));
+            if (j.lo_only) {
+                *reinterpret_cast<float4 *>(j.out + z * plane + r * Kp + k) = l;
+            } else {
+                float *hi = j.out + (2 * z) * plane + r * Kp + k;
+                *reinterpret_cast<float4 *>(hi) = h;
+                *reinterpret_cast<float4 *>(hi + plane) = l;
+            }
+        } else {
+            *reinterpret_cast<float4 *>(j.out + z * plane + r * Kp + k) =
+                make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
+                            tc::to_tf32(x.w));
         }
     }
 }
@@ -158,9 +186,13 @@ __device__ __forceinline__ void split_transpose(const SplitJob &j, int K, int Kp
             const int r = r0 + ty + i, k = k0 + tx;
             if (r < j.R && k < K) {
                 const float x = tile[tx][ty + i];
-                const float h = tc::to_tf32(x);
-                hi[(int64_t)r * Kp + k] = h;
-                if constexpr (PLANES == 2) hi[plane + (int64_t)r * Kp + k] = tc::to_tf32(x - h);
+                if constexpr (PLANES == 2) {
+                    const float h = tf32_hi(x);
+                    hi[(int64_t)r * Kp + k] = h;
+                    hi[plane + (int64_t)r * Kp + k] = tf32_lo(x, h);
+                } else {
+                    hi[(int64_t)r * Kp + k] = tc::to_tf32(x);
+                }
             }
         }
         __syncthreads();
@@ -307,10 +339,10 @@ __device__ __forceinline__ void store_tile_rows(const Tf32x3Params &p, const CUt
 //   warps 2-5:      epilogue, warp w draining TMEM lane quarter w % 4 through
 //                   its own staging buffers (outside the ring), then arriving
 //                   on the buffer's "empty" barrier;
-//   warps 6-9:      (RAW only) converters: wait for a stage to land, turn its
-//                   raw operand tiles into planes in place, fence the async
-//                   proxy and arrive on the stage's "converted" barrier, which
-//                   the MMA issuer then waits on instead of "full".
+//   warps 6-9:      (CONV only) converters: wait for a stage to land, make
+//                   the planes of its raw operand tiles in place, fence the
+//                   async proxy and arrive on the stage's "converted" barrier,
+//                   which the MMA issuer then waits on instead of "full".
 // With ACC_BUFS = 2 the MMAs of tile i+1 overlap the epilogue of tile i; the
 // 128 x 256 three-term tile needs all 512 TMEM columns for one tile
 // (ACC_BUFS = 1), and there only the next tile's loads overlap its epilogue.
@@ -321,29 +353,36 @@ constexpr int PTHREADS = 192;   // producer, MMA and 4 epilogue warps
 constexpr int kConvWarps = 4;   // converter warps when an operand arrives raw
 
 // RAW: bit 0 set when op(A), bit 1 when op(B), is loaded as the caller's
-// fp32 (K-contiguous rows) instead of split planes; converter warps then turn
-// each landed slice into its hi (and lo) planes inside the stage.
-template <class CFG, int ACC_BUFS, int RAW = 0>
+// fp32 (K-contiguous rows) into the stage's hi slot instead of a hi plane.
+// CONV (a subset of RAW): converter warps make that operand's planes inside
+// the stage (three terms: the lo slot from the raw values, which the MMAs
+// read as hi as they are; one term: the hi slot rounded in place).  An
+// operand in RAW but not CONV (three terms only) takes its lo slot from a
+// lo-only plane the split kernel wrote.
+template <class CFG, int ACC_BUFS, int RAW = 0, int CONV = 0>
 struct Persist {
-    static constexpr int CONV_WARPS = RAW ? kConvWarps : 0;
+    static_assert((CONV & ~RAW) == 0, "converted operands are loaded raw");
+    static_assert(CFG::PLANES == 2 || RAW == CONV, "one term rounds its raw operand in place");
+    static constexpr int CONV_WARPS = CONV ? kConvWarps : 0;
     static constexpr int THREADS = PTHREADS + 32 * CONV_WARPS;
     static constexpr int BUF_COLS = CFG::TERMS == 3 ? 2 * CFG::BN : CFG::BN;
     static constexpr int TMEM_COLS = ACC_BUFS * BUF_COLS <= 256 ? 256 : 512;
     static constexpr int STAGING = 4 * 8192;   // 4 epilogue warps x two 4 KB buffers
-    static constexpr int BARS = (RAW ? 3 : 2) * CFG::STAGES + 2 * ACC_BUFS + 1;
-    // transaction bytes of one stage: a raw operand lands as one plane
-    static constexpr int TX_BYTES = ((RAW & 1) ? CFG::A_TILE : CFG::PLANES * CFG::A_TILE) +
-                                    ((RAW & 2) ? CFG::B_TILE : CFG::PLANES * CFG::B_TILE);
+    static constexpr int BARS = (CONV ? 3 : 2) * CFG::STAGES + 2 * ACC_BUFS + 1;
+    // transaction bytes of one stage: a converted operand lands as one plane
+    static constexpr int TX_BYTES = ((CONV & 1) ? CFG::A_TILE : CFG::PLANES * CFG::A_TILE) +
+                                    ((CONV & 2) ? CFG::B_TILE : CFG::PLANES * CFG::B_TILE);
     static constexpr int SMEM_BYTES = CFG::STAGES * CFG::STAGE_BYTES + STAGING + 1024 + 256;
     static_assert(ACC_BUFS * BUF_COLS <= 512, "accumulators exceed tensor memory");
     static_assert(BARS * 8 + 8 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// In place, over one landed operand tile of `bytes` bytes: the raw fp32 x at
-// each position of the hi plane becomes tf32_rn(x) and, for three terms, the
-// same position of the lo plane (`bytes` further) gets tf32_rn(x - hi): the
-// values the split kernel writes, so the MMAs see the same operands.  The
+// Over one landed operand tile of `bytes` bytes holding raw fp32 x in the hi
+// slot.  Three terms: the same position of the lo slot (`bytes` further) gets
+// tf32_lo(x, tf32_hi(x)) and the hi slot stays as it is (the MMAs read x as
+// tf32_hi(x)).  One term: the hi slot becomes tf32_rn(x) in place.  These are
+// the values the split kernel writes, so the MMAs see the same operands.  The
 // swizzle moves whole 16-byte chunks, so position-wise work ignores it.
 template <int PLANES>
 __device__ __forceinline__ void convert_tile(uint8_t *tile, int bytes, int t, int nt) {
@@ -351,21 +390,25 @@ __device__ __forceinline__ void convert_tile(uint8_t *tile, int bytes, int t, in
     float4 *lo = reinterpret_cast<float4 *>(tile + bytes);
     for (int v = t; v < bytes / 16; v += nt) {
         const float4 x = hi[v];
-        const float4 h = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
-                                     tc::to_tf32(x.w));
-        hi[v] = h;
         if constexpr (PLANES == 2)
-            lo[v] = make_float4(tc::to_tf32(x.x - h.x), tc::to_tf32(x.y - h.y),
-                                tc::to_tf32(x.z - h.z), tc::to_tf32(x.w - h.w));
+            lo[v] = make_float4(tf32_lo(x.x, tf32_hi(x.x)), tf32_lo(x.y, tf32_hi(x.y)),
+                                tf32_lo(x.z, tf32_hi(x.z)), tf32_lo(x.w, tf32_hi(x.w)));
+        else
+            hi[v] = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
+                                tc::to_tf32(x.w));
     }
 }
 
-template <class CFG, int ACC_BUFS, int RAW>
-__global__ void __launch_bounds__(Persist<CFG, ACC_BUFS, RAW>::THREADS, 1)
+// tmA / tmB: the operand's planes, or (RAW) its raw rows; tmAlo / tmBlo: the
+// lo-only plane of an operand in RAW but not CONV (unused otherwise).
+template <class CFG, int ACC_BUFS, int RAW, int CONV>
+__global__ void __launch_bounds__(Persist<CFG, ACC_BUFS, RAW, CONV>::THREADS, 1)
 tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmAlo,
+                         const __grid_constant__ CUtensorMap tmBlo,
                          const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
-    using P = Persist<CFG, ACC_BUFS, RAW>;
+    using P = Persist<CFG, ACC_BUFS, RAW, CONV>;
     constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
     constexpr int BN = CFG::BN, ACC_COLS = CFG::ACC_COLS;
     constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
@@ -381,8 +424,8 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t accf0 = empty0 + 8 * STAGES;     // accumulator b holds a finished tile
     const uint32_t acce0 = accf0 + 8 * ACC_BUFS;    // accumulator b has been drained
     const uint32_t done_bar = acce0 + 8 * ACC_BUFS;
-    const uint32_t conv0 = done_bar + 8;            // (RAW) stage s converted
-    const uint32_t ready0 = RAW ? conv0 : full0;    // what the MMA waits for
+    const uint32_t conv0 = done_bar + 8;            // (CONV) stage s converted
+    const uint32_t ready0 = CONV ? conv0 : full0;   // what the MMA waits for
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + P::BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -401,12 +444,14 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
             tc::mbar_init(acce0 + 8 * b, 4);   // one arrival per epilogue warp
         }
         tc::mbar_init(done_bar, 1);
-        if constexpr (RAW != 0)
+        if constexpr (CONV != 0)
             for (int s = 0; s < STAGES; ++s) tc::mbar_init(conv0 + 8 * s, P::CONV_WARPS);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmA);
         tc::tma_prefetch_desc(&tmB);
+        if constexpr ((RAW & ~CONV & 1) != 0) tc::tma_prefetch_desc(&tmAlo);
+        if constexpr ((RAW & ~CONV & 2) != 0) tc::tma_prefetch_desc(&tmBlo);
     }
     if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), P::TMEM_COLS);
     tc::fence_before_sync();
@@ -439,9 +484,12 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                     const uint32_t fb = full0 + 8 * s;
                     tc::mbar_arrive_expect_tx(fb, P::TX_BYTES);
                     const int k0 = kb * BK;
-                    // a raw operand: the caller's rows into the hi slot; else its planes
+                    // a raw operand: the caller's rows into the hi slot (and,
+                    // unless converted in the stage, its lo plane); else its planes
                     if constexpr (RAW & 1) {
                         tc::tma_load_3d(st, &tmA, fb, k0, m0, z);
+                        if constexpr (!(CONV & 1))
+                            tc::tma_load_3d(st + A_TILE, &tmAlo, fb, k0, m0, z);
                     } else {
 #pragma unroll
                         for (int pl = 0; pl < PLANES; ++pl)
@@ -449,6 +497,8 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                     if constexpr (RAW & 2) {
                         tc::tma_load_3d(st + PLANES * A_TILE, &tmB, fb, k0, n0, z);
+                        if constexpr (!(CONV & 2))
+                            tc::tma_load_3d(st + PLANES * A_TILE + B_TILE, &tmBlo, fb, k0, n0, z);
                     } else {
 #pragma unroll
                         for (int pl = 0; pl < PLANES; ++pl)
@@ -530,7 +580,7 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
             if (lane == 0) tc::mbar_arrive(acce0 + 8 * b);
         }
         if (lane == 0 && cc > 0) tc::bulk_wait_group_read<0>();
-    } else if constexpr (RAW != 0) {
+    } else if constexpr (CONV != 0) {
         // ---------------- converter warps 6..: raw operand tiles -> planes
         constexpr int NT = 32 * P::CONV_WARPS;
         const int t = (int)threadIdx.x - PTHREADS;
@@ -546,8 +596,8 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                     break;
                 }
                 uint8_t *st = smem + s * STAGE_BYTES;
-                if constexpr (RAW & 1) convert_tile<PLANES>(st, A_TILE, t, NT);
-                if constexpr (RAW & 2) convert_tile<PLANES>(st + PLANES * A_TILE, B_TILE, t, NT);
+                if constexpr (CONV & 1) convert_tile<PLANES>(st, A_TILE, t, NT);
+                if constexpr (CONV & 2) convert_tile<PLANES>(st + PLANES * A_TILE, B_TILE, t, NT);
                 // the planes are read by the tensor cores (async proxy)
                 tc::fence_proxy_async_smem();
                 __syncwarp();
@@ -674,11 +724,10 @@ __global__ void __launch_bounds__(THREADS, 1) tf32_mma_probe_kernel(long long it
 // the swizzle whose span equals the BK-float row.
 template <class CFG>
 bool make_plane_map(CUtensorMap *map, const float *base, int rows, int K, int Kp, int batch,
-                    int box_rows) {
+                    int box_rows, int planes = CFG::PLANES) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows,
-                                (cuuint64_t)(CFG::PLANES * batch)};
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)(planes * batch)};
     const cuuint64_t strides[2] = {(cuuint64_t)Kp * 4, (cuuint64_t)rows * Kp * 4};
     const cuuint32_t box[3] = {(cuuint32_t)CFG::BK, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
@@ -741,44 +790,53 @@ size_t plane_bytes(int64_t rows, int64_t K, int64_t batch, int planes) {
 
 // Encodes the tensor maps, launches the split kernel into `ws` for the
 // operands that need planes and fills the GEMM kernel's parameters.  `raw`
-// (bits as in Persist::RAW) marks operands the GEMM loads as they are; their
-// maps are already in tmA / tmB.
+// and `conv` (bits as in Persist) mark operands the GEMM loads as they are
+// (their maps are already in tmA / tmB) and those converted in the stage;
+// a raw operand that is not converted gets a lo-only plane and its map in
+// tmAlo / tmBlo (which are left empty otherwise).
 template <class CFG>
-cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, void *ws,
-                    cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB, CUtensorMap &tmC,
-                    Tf32x3Params &p) {
+cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int conv, void *ws,
+                    cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB, CUtensorMap &tmAlo,
+                    CUtensorMap &tmBlo, CUtensorMap &tmC, Tf32x3Params &p) {
     constexpr int PLANES = CFG::PLANES;
     const int Kp = (a.K + 3) / 4 * 4;
     float *wsA = static_cast<float *>(ws);
     float *wsB = wsA + plane_bytes(a.M, a.K, a.batch, PLANES) / 4;
+    const int lo_only = raw & ~conv;
 
     // tensor maps first (they depend only on the workspace and the sizes), so
     // no host work separates the split launch from the GEMM launch
+    tmAlo = CUtensorMap{};
+    tmBlo = CUtensorMap{};
     if ((!(raw & 1) && !make_plane_map<CFG>(&tmA, wsA, a.M, a.K, Kp, a.batch, BM)) ||
-        (!(raw & 2) && !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN)))
+        (!(raw & 2) && !make_plane_map<CFG>(&tmB, wsB, a.N, a.K, Kp, a.batch, CFG::BN)) ||
+        ((lo_only & 1) && !make_plane_map<CFG>(&tmAlo, wsA, a.M, a.K, Kp, a.batch, BM, 1)) ||
+        ((lo_only & 2) && !make_plane_map<CFG>(&tmBlo, wsB, a.N, a.K, Kp, a.batch, CFG::BN, 1)))
         return cudaErrorInvalidValue;
 
     // stage 1: split op(A) (rows M) and op(B) (rows N) into K-major TF32 planes,
-    // one launch for both; a raw operand gets no CTAs
+    // one launch for both; a converted operand gets no CTAs, a raw one only
+    // its lo plane
     SplitArgs sa;
     sa.K = a.K;
     sa.Kp = Kp;
     sa.batch = a.batch;
     auto job = [&](SplitJob &j, const float *X, int64_t ld, int64_t sX, int R, bool kcontig,
-                   float *out, bool skip) {
+                   float *out, bool skip, bool lo) {
         j.X = X;
         j.ld = ld;
         j.sX = sX;
         j.out = out;
         j.R = R;
         j.kcontig = kcontig;
+        j.lo_only = lo;
         j.vec = kcontig && (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 && sX % 4 == 0;
         const int64_t work = kcontig ? ((int64_t)a.batch * R * (Kp / 4) + 255) / 256
                                      : (int64_t)a.batch * ((R + 31) / 32) * ((a.K + 31) / 32);
         j.blocks = skip ? 0 : (work < 152 * 16 ? (work > 0 ? work : 1) : 152 * 16);
     };
-    job(sa.job[0], a.A, a.lda, a.strideA, a.M, !transA, wsA, (raw & 1) != 0);
-    job(sa.job[1], a.B, a.ldb, a.strideB, a.N, transB, wsB, (raw & 2) != 0);
+    job(sa.job[0], a.A, a.lda, a.strideA, a.M, !transA, wsA, (conv & 1) != 0, (lo_only & 1) != 0);
+    job(sa.job[1], a.B, a.ldb, a.strideB, a.N, transB, wsB, (conv & 2) != 0, (lo_only & 2) != 0);
     const int64_t split_blocks = sa.job[0].blocks + sa.job[1].blocks;
     if (split_blocks > 0) {
         split_kernel<PLANES><<<(unsigned)split_blocks, 256, 0, s>>>(sa);
@@ -827,22 +885,22 @@ cudaError_t ensure_smem(Kern kern, int bytes, std::atomic<unsigned long long> &c
 }
 
 // One CTA per SM, walking the tiles (see tf32x3_persistent_kernel).
-template <class CFG, int ACC_BUFS, int RAW>
+template <class CFG, int ACC_BUFS, int RAW, int CONV>
 cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, void *ws,
                                   cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB) {
-    using P = Persist<CFG, ACC_BUFS, RAW>;
+    using P = Persist<CFG, ACC_BUFS, RAW, CONV>;
     static std::atomic<unsigned long long> configured{0};
-    cudaError_t e =
-        ensure_smem(tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW>, P::SMEM_BYTES, configured);
+    cudaError_t e = ensure_smem(tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW, CONV>, P::SMEM_BYTES,
+                                configured);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    CUtensorMap tmC;
+    CUtensorMap tmC, tmAlo, tmBlo;
     Tf32x3Params p;
-    e = prepare<CFG>(a, transA, transB, RAW, ws, s, tmA, tmB, tmC, p);
+    e = prepare<CFG>(a, transA, transB, RAW, CONV, ws, s, tmA, tmB, tmAlo, tmBlo, tmC, p);
     if (e != cudaSuccess) return e;
     const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
     cudaLaunchConfig_t cfg = {};
@@ -857,28 +915,44 @@ cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, v
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW>, tmA, tmB, tmC, p);
+    e = cudaLaunchKernelEx(&cfg, tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW, CONV>, tmA, tmB,
+                           tmAlo, tmBlo, tmC, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-// For short reductions (K <= kRawMaxK), operands stored K-contiguous
-// (row-major A, B stored transposed) with 16-byte aligned rows and batches
-// are loaded as they are and split inside the GEMM; everything else goes
-// through the split kernel.  The conversion adds shared-memory traffic and a
-// step to every stage of a ring that is already latency-bound, so it only
-// pays where the separate split launch dominates: 96 x 512 x 512 x 64 with
-// B^T 68.9 -> 81.5 TFLOP/s (no split launch at all), row-major 68.1 -> 73.1;
-// but 3072^3 257 -> 235 (A raw) and 265 -> 174 (both raw), 4096 x 4096 x 256
-// 165 -> 147 (results bit-identical either way).
+// Operands stored K-contiguous (row-major A, B stored transposed) with
+// 16-byte aligned rows and batches are loaded as they are.  With three terms
+// the caller's rows are the hi term; the lo term comes, for short reductions
+// (K <= kRawMaxK), from converter warps inside the GEMM, else from a lo-only
+// plane the split kernel writes (half the split's output for that operand).
+// With one term the operand is rounded in the stage, for short reductions
+// only; everything else goes through the split kernel.  The conversion adds
+// shared-memory traffic and a step to every stage of a ring that is already
+// latency-bound, so it only pays where the separate split launch dominates:
+// 96 x 512 x 512 x 64 with B^T 68.9 -> 81.5 TFLOP/s (no split launch at
+// all), row-major 68.1 -> 73.1; but 3072^3 257 -> 235 (A converted) and
+// 265 -> 174 (both), 4096 x 4096 x 256 165 -> 147 (results bit-identical
+// either way).
 constexpr int kRawMaxK = 64;
+
+template <class CFG, int ACC_BUFS, int RAW>
+cudaError_t launch_raw_conv(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s,
+                            CUtensorMap &tmA, CUtensorMap &tmB) {
+    if (a.K <= kRawMaxK)
+        return launch_persistent_raw<CFG, ACC_BUFS, RAW, RAW>(a, transA, transB, ws, s, tmA, tmB);
+    if constexpr (CFG::PLANES == 2)
+        return launch_persistent_raw<CFG, ACC_BUFS, RAW, 0>(a, transA, transB, ws, s, tmA, tmB);
+    return cudaErrorInvalidValue;   // one term: raw only when converted (see launch_persistent)
+}
 
 template <class CFG, int ACC_BUFS>
 cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void *ws,
                               cudaStream_t s) {
     auto raw_ok = [&](const float *X, int64_t ld, int64_t sX, bool kcontig) {
-        return a.K <= kRawMaxK && kcontig && reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
-               ld % 4 == 0 && (a.batch == 1 || (sX > 0 && sX % 4 == 0));
+        return (a.K <= kRawMaxK || CFG::PLANES == 2) && kcontig &&
+               reinterpret_cast<uintptr_t>(X) % 16 == 0 && ld % 4 == 0 &&
+               (a.batch == 1 || (sX > 0 && sX % 4 == 0));
     };
     CUtensorMap tmA, tmB;
     int raw = 0;
@@ -889,10 +963,10 @@ cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void 
         make_raw_map<CFG>(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, CFG::BN))
         raw |= 2;
     switch (raw) {
-        case 1: return launch_persistent_raw<CFG, ACC_BUFS, 1>(a, transA, transB, ws, s, tmA, tmB);
-        case 2: return launch_persistent_raw<CFG, ACC_BUFS, 2>(a, transA, transB, ws, s, tmA, tmB);
-        case 3: return launch_persistent_raw<CFG, ACC_BUFS, 3>(a, transA, transB, ws, s, tmA, tmB);
-        default: return launch_persistent_raw<CFG, ACC_BUFS, 0>(a, transA, transB, ws, s, tmA, tmB);
+        case 1: return launch_raw_conv<CFG, ACC_BUFS, 1>(a, transA, transB, ws, s, tmA, tmB);
+        case 2: return launch_raw_conv<CFG, ACC_BUFS, 2>(a, transA, transB, ws, s, tmA, tmB);
+        case 3: return launch_raw_conv<CFG, ACC_BUFS, 3>(a, transA, transB, ws, s, tmA, tmB);
+        default: return launch_persistent_raw<CFG, ACC_BUFS, 0, 0>(a, transA, transB, ws, s, tmA, tmB);
     }
 }
 

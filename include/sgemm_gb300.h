@@ -221,11 +221,13 @@ uint64_t sgemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int sp
 
 /*
  * C = op(A) op(B) on the tensor cores with FP32 accuracy: every input is split
- * as x = hi + lo with hi = tf32(x), lo = tf32(x - hi), and the product is
- * formed as lo_a*hi_b + hi_a*lo_b + hi_a*hi_b (three TF32 MMAs per K step,
- * tcgen05 with the accumulator in tensor memory, fp32 accumulation).  The
- * dropped lo_a*lo_b term and the TF32 rounding of lo are below 2^-20 of
- * |a||b| per product, so results meet the same elementwise bound as
+ * as x = hi + lo with hi = x cut to TF32 (its 13 low mantissa bits cleared:
+ * the value a TF32 MMA reads from the fp32 word x) and lo = x - hi rounded to
+ * TF32 (nearest), and the product is formed as lo_a*hi_b + hi_a*lo_b +
+ * hi_a*hi_b (three TF32 MMAs per K step, tcgen05 with the accumulator in
+ * tensor memory, fp32 accumulation).  The dropped lo_a*lo_b term and the TF32
+ * rounding of lo are each below 2^-20 of |a||b| per product, so results meet
+ * the same elementwise bound as
  * sgemm_f32; small-integer inputs are exact.  Not bit-identical to
  * sgemm_f32 (different summation order), deterministic across calls.
  * Defined by: "CUDA GEMM operator performance optimization", section 1.1
@@ -263,8 +265,10 @@ int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K,
                                      void *workspace, uint64_t workspace_bytes, void *stream);
 
 /* Workspace bytes the tf32x3 entry points need: the hi and lo TF32 planes of
- * op(A) and op(B), 2 * batch * (M + N) * round_up(K, 4) floats plus padding.
- * 0 for empty problems or negative sizes. */
+ * op(A) and op(B), 2 * batch * (M + N) * round_up(K, 4) floats plus padding
+ * (an operand stored K-contiguous with 16-byte aligned rows is read as its own
+ * hi term and uses only its lo plane, but the size does not depend on the
+ * pointers).  0 for empty problems or negative sizes. */
 uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
 
 /*

@@ -875,17 +875,21 @@ def test_streamk_tma_exact_on_integers(M, N, K):
 
 # ---------------------------------------------------------------- in-kernel split
 
-# For short reductions (K <= 64) the tensor-core paths load K-contiguous
-# operands (row-major A, B stored transposed) with 16-byte aligned rows as
-# they are and split them into hi/lo TF32 planes inside the GEMM (converter
-# warps, in shared memory); the others go through the split kernel.  Both
-# produce the same planes, so a problem whose buffers are shifted by one
-# float (forcing the split kernel for every operand) must give the same
-# bits.  Layouts: NN (A raw), NT (both raw), TT (B raw), TN (neither), ragged
-# edges and K tails, batches, and longer K (split kernel on both sides).
+# The tensor-core paths load K-contiguous operands (row-major A, B stored
+# transposed) with 16-byte aligned rows as they are.  3xTF32 reads them as
+# their own hi term (the MMA drops the 13 low mantissa bits of each word) and
+# takes lo from converter warps inside the GEMM for short reductions (K <= 64)
+# or from a lo-only plane of the split kernel; plain TF32 rounds them inside
+# the GEMM for short reductions.  Everything else goes through the split
+# kernel's full planes.  The MMAs see the same values either way, so a problem
+# whose buffers are shifted by one float (forcing full planes for every
+# operand) must give the same bits.  Layouts: NN (A raw), NT (both raw), TT (B
+# raw), TN (neither), ragged edges and K tails, batches, and longer K (lo-only
+# planes for 3xTF32, full planes on both sides for plain TF32).
 RAWSPLIT = [(0, 0, 300, 260, 61, 1), (0, 1, 513, 384, 64, 1), (1, 1, 200, 388, 33, 1),
             (1, 0, 260, 300, 64, 1), (0, 1, 512, 512, 64, 3), (0, 0, 1100, 1300, 7, 1),
-            (0, 1, 700, 900, 300, 1)]
+            (0, 1, 700, 900, 300, 1), (0, 0, 1100, 1300, 257, 1), (1, 1, 600, 700, 501, 1),
+            (0, 1, 512, 512, 128, 3), (1, 0, 300, 400, 1000, 1)]
 
 
 @pytest.mark.parametrize("entry_name", ["sgemm_f32_tf32x3", "sgemm_f32_tf32"])
