@@ -923,27 +923,66 @@ cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, v
 
 // Operands stored K-contiguous (row-major A, B stored transposed) with
 // 16-byte aligned rows and batches are loaded as they are.  With three terms
-// the caller's rows are the hi term; the lo term comes, for short reductions
-// (K <= kRawMaxK), from converter warps inside the GEMM, else from a lo-only
-// plane the split kernel writes (half the split's output for that operand).
-// With one term the operand is rounded in the stage, for short reductions
-// only; everything else goes through the split kernel.  The conversion adds
-// shared-memory traffic and a step to every stage of a ring that is already
-// latency-bound, so it only pays where the separate split launch dominates:
-// 96 x 512 x 512 x 64 with B^T 68.9 -> 81.5 TFLOP/s (no split launch at
-// all), row-major 68.1 -> 73.1; but 3072^3 257 -> 235 (A converted) and
-// 265 -> 174 (both), 4096 x 4096 x 256 165 -> 147 (results bit-identical
-// either way).
+// the caller's rows are the hi term and the lo term comes either from
+// converter warps inside the GEMM or from a lo-only plane the split kernel
+// writes (half the split's output for that operand).  With one term the
+// operand is rounded in the stage, for short reductions only.  Everything
+// else goes through the split kernel's full planes.
+//
+// Converting in the GEMM saves the split's HBM round trip of that operand
+// but adds shared-memory traffic and a step to every stage of a ring that is
+// already latency-bound, and each operand panel is converted once per tile
+// that reads it (A once per tile column, B once per tile row).  Measured
+// (results bit-identical either way), three terms, lo plane -> converted:
+//   96 x 512 x 512 x K (4 x 4 tiles): K = 96 NT 84.0 -> 104.1, K = 256 NN
+//   103.6 -> 115.2, NT 112.5 -> 138.3 TFLOP/s;
+//   24 x 1024 x 1024 x 128 (8 x 8 tiles): NN 108.1 -> 113.9;
+//   4096 x 4096 x 128 (32 x 32): NN 119.9 -> 112.3, NT 119.3 -> 105.2;
+//   3072^3: NN 257.8 -> 244.5, NT 271.4 -> 195.5.
+// So an operand is converted when K <= kRawMaxK, or when K <= kConvMaxK and
+// at most kConvMaxReuse tiles read each of its panels (the 128-wide
+// three-term tile, which every K <= 256 takes).
 constexpr int kRawMaxK = 64;
+constexpr int kConvMaxK = 256;
+constexpr int kConvMaxReuse = 8;
 
+// Launches with the runtime choice `conv` (a subset of RAW) of converted
+// operands; a combination the configuration does not provide launches
+// nothing and returns an error (the caller never asks for one).
 template <class CFG, int ACC_BUFS, int RAW>
-cudaError_t launch_raw_conv(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s,
-                            CUtensorMap &tmA, CUtensorMap &tmB) {
-    if (a.K <= kRawMaxK)
-        return launch_persistent_raw<CFG, ACC_BUFS, RAW, RAW>(a, transA, transB, ws, s, tmA, tmB);
-    if constexpr (CFG::PLANES == 2)
-        return launch_persistent_raw<CFG, ACC_BUFS, RAW, 0>(a, transA, transB, ws, s, tmA, tmB);
-    return cudaErrorInvalidValue;   // one term: raw only when converted (see launch_persistent)
+cudaError_t launch_conv(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s,
+                        CUtensorMap &tmA, CUtensorMap &tmB, int conv) {
+    if constexpr (CFG::PLANES == 1) {
+        // one term: an operand is raw only when it is rounded in the stage
+        if (conv == RAW)
+            return launch_persistent_raw<CFG, ACC_BUFS, RAW, RAW>(a, transA, transB, ws, s, tmA, tmB);
+    } else if constexpr (CFG::BN == 128) {
+        switch (conv) {
+            case 0:
+                return launch_persistent_raw<CFG, ACC_BUFS, RAW, 0>(a, transA, transB, ws, s, tmA, tmB);
+            case 1:
+                if constexpr ((RAW & 1) != 0)
+                    return launch_persistent_raw<CFG, ACC_BUFS, RAW, 1>(a, transA, transB, ws, s, tmA,
+                                                                        tmB);
+                break;
+            case 2:
+                if constexpr ((RAW & 2) != 0)
+                    return launch_persistent_raw<CFG, ACC_BUFS, RAW, 2>(a, transA, transB, ws, s, tmA,
+                                                                        tmB);
+                break;
+            case 3:
+                if constexpr (RAW == 3)
+                    return launch_persistent_raw<CFG, ACC_BUFS, 3, 3>(a, transA, transB, ws, s, tmA, tmB);
+                break;
+            default:
+                break;
+        }
+    } else {
+        // the 256-wide three-term tile (K > 256 only): lo planes, no converters
+        if (conv == 0)
+            return launch_persistent_raw<CFG, ACC_BUFS, RAW, 0>(a, transA, transB, ws, s, tmA, tmB);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <class CFG, int ACC_BUFS>
@@ -962,10 +1001,21 @@ cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void 
     if (raw_ok(a.B, a.ldb, a.strideB, transB) &&
         make_raw_map<CFG>(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, CFG::BN))
         raw |= 2;
+    int conv = 0;
+    if (CFG::PLANES == 1) {
+        conv = raw;
+    } else if (CFG::BN == 128) {
+        const int64_t tiles_m = (a.M + BM - 1) / BM, tiles_n = (a.N + CFG::BN - 1) / CFG::BN;
+        auto convert = [&](int64_t reuse) {
+            return a.K <= kRawMaxK || (a.K <= kConvMaxK && reuse <= kConvMaxReuse);
+        };
+        if ((raw & 1) && convert(tiles_n)) conv |= 1;
+        if ((raw & 2) && convert(tiles_m)) conv |= 2;
+    }
     switch (raw) {
-        case 1: return launch_raw_conv<CFG, ACC_BUFS, 1>(a, transA, transB, ws, s, tmA, tmB);
-        case 2: return launch_raw_conv<CFG, ACC_BUFS, 2>(a, transA, transB, ws, s, tmA, tmB);
-        case 3: return launch_raw_conv<CFG, ACC_BUFS, 3>(a, transA, transB, ws, s, tmA, tmB);
+        case 1: return launch_conv<CFG, ACC_BUFS, 1>(a, transA, transB, ws, s, tmA, tmB, conv);
+        case 2: return launch_conv<CFG, ACC_BUFS, 2>(a, transA, transB, ws, s, tmA, tmB, conv);
+        case 3: return launch_conv<CFG, ACC_BUFS, 3>(a, transA, transB, ws, s, tmA, tmB, conv);
         default: return launch_persistent_raw<CFG, ACC_BUFS, 0, 0>(a, transA, transB, ws, s, tmA, tmB);
     }
 }
