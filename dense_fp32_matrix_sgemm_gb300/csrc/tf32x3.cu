@@ -926,8 +926,8 @@ cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, v
 // the caller's rows are the hi term and the lo term comes either from
 // converter warps inside the GEMM or from a lo-only plane the split kernel
 // writes (half the split's output for that operand).  With one term the
-// operand is rounded in the stage, for short reductions only.  Everything
-// else goes through the split kernel's full planes.
+// operand is rounded in the stage where it would be converted (below), else
+// split.  Everything else goes through the split kernel's full planes.
 //
 // Converting in the GEMM saves the split's HBM round trip of that operand
 // but adds shared-memory traffic and a step to every stage of a ring that is
@@ -940,8 +940,11 @@ cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, v
 //   4096 x 4096 x 128 (32 x 32): NN 119.9 -> 112.3, NT 119.3 -> 105.2;
 //   3072^3: NN 257.8 -> 244.5, NT 271.4 -> 195.5.
 // So an operand is converted when K <= kRawMaxK, or when K <= kConvMaxK and
-// at most kConvMaxReuse tiles read each of its panels (the 128-wide
-// three-term tile, which every K <= 256 takes).
+// at most kConvMaxReuse tiles read each of its panels (for three terms on
+// the 128-wide tile, which every K <= 256 takes).  The one-term product
+// gains the same way: 96 x 512 x 512 x 256 NT 160.3 -> 217.1, K = 128 NT
+// 121.1 -> 159.2, 24 x 1024 x 1024 x 128 NN 142.1 -> 151.5; 4096 x 4096 x 128
+// and 3072^3 unchanged.
 constexpr int kRawMaxK = 64;
 constexpr int kConvMaxK = 256;
 constexpr int kConvMaxReuse = 8;
@@ -988,27 +991,29 @@ cudaError_t launch_conv(const GemmArgs &a, bool transA, bool transB, void *ws, c
 template <class CFG, int ACC_BUFS>
 cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void *ws,
                               cudaStream_t s) {
-    auto raw_ok = [&](const float *X, int64_t ld, int64_t sX, bool kcontig) {
-        return (a.K <= kRawMaxK || CFG::PLANES == 2) && kcontig &&
+    const int64_t tiles_m = (a.M + BM - 1) / BM, tiles_n = (a.N + CFG::BN - 1) / CFG::BN;
+    // converting an operand whose panels `reuse` tiles read
+    auto convert = [&](int64_t reuse) {
+        return a.K <= kRawMaxK || (a.K <= kConvMaxK && reuse <= kConvMaxReuse);
+    };
+    // one term: raw only when converted (rounded in the stage)
+    auto raw_ok = [&](const float *X, int64_t ld, int64_t sX, bool kcontig, int64_t reuse) {
+        return (CFG::PLANES == 2 || convert(reuse)) && kcontig &&
                reinterpret_cast<uintptr_t>(X) % 16 == 0 && ld % 4 == 0 &&
                (a.batch == 1 || (sX > 0 && sX % 4 == 0));
     };
     CUtensorMap tmA, tmB;
     int raw = 0;
-    if (raw_ok(a.A, a.lda, a.strideA, !transA) &&
+    if (raw_ok(a.A, a.lda, a.strideA, !transA, tiles_n) &&
         make_raw_map<CFG>(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM))
         raw |= 1;
-    if (raw_ok(a.B, a.ldb, a.strideB, transB) &&
+    if (raw_ok(a.B, a.ldb, a.strideB, transB, tiles_m) &&
         make_raw_map<CFG>(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, CFG::BN))
         raw |= 2;
     int conv = 0;
     if (CFG::PLANES == 1) {
         conv = raw;
     } else if (CFG::BN == 128) {
-        const int64_t tiles_m = (a.M + BM - 1) / BM, tiles_n = (a.N + CFG::BN - 1) / CFG::BN;
-        auto convert = [&](int64_t reuse) {
-            return a.K <= kRawMaxK || (a.K <= kConvMaxK && reuse <= kConvMaxReuse);
-        };
         if ((raw & 1) && convert(tiles_n)) conv |= 1;
         if ((raw & 2) && convert(tiles_m)) conv |= 2;
     }

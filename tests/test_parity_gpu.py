@@ -880,7 +880,7 @@ def test_streamk_tma_exact_on_integers(M, N, K):
 # their own hi term (the MMA drops the 13 low mantissa bits of each word) and
 # takes lo from converter warps inside the GEMM (K <= 64, or K <= 256 with at
 # most 8 tiles reading each panel of the operand) or from a lo-only plane of
-# the split kernel; plain TF32 rounds them inside the GEMM for K <= 64.
+# the split kernel; plain TF32 rounds them inside the GEMM under the same rule.
 # Everything else goes through the split kernel's full planes.  The MMAs see
 # the same values either way, so a problem whose buffers are shifted by one
 # float (forcing full planes for every operand) must give the same bits.
