@@ -224,6 +224,35 @@ def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
     return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
 
 
+def tc_plan(M, N, K, batch, transA, transB, aligned=True):
+    """(kernels label, launches) of one 3xTF32 call, mirroring csrc/tf32x3.cu
+    for 16-byte aligned operands: a K-contiguous operand (row-major A, B
+    stored transposed) is read as its own hi term; its lo term is made by
+    converter warps inside the GEMM when K <= 64, or K <= 256 with at most 8
+    tiles reading each of its panels, else written by the split kernel as a
+    lo plane; other operands are split into hi and lo planes."""
+    tiles_m, tiles_n = -(-M // 128), -(-N // 128)   # K <= 256 takes 128-wide tiles
+
+    def conv(reuse):
+        return K <= 64 or (K <= 256 and reuse <= 8)
+    parts, split = [], []
+    for name, kcontig, reuse in (("A", not transA, tiles_n), ("B", bool(transB), tiles_m)):
+        if kcontig and aligned:
+            if conv(reuse):
+                parts.append(f"{name} raw, lo by converter warps")
+            else:
+                parts.append(f"{name} raw as hi")
+                split.append(f"{name} lo plane")
+        else:
+            split.append(f"{name} hi/lo planes")
+    gemm = ("tf32x3_persistent_kernel (one CTA per SM; 128x256 or 128x128 tiles by wave count; "
+            "TMA ring, tcgen05 kind::tf32, TMEM, TMA-store epilogue" +
+            ("; " + ", ".join(parts) if parts else "") + ")")
+    if split:
+        return f"split_kernel ({', '.join(split)}) + {gemm}", 2
+    return gemm, 1
+
+
 def workload_table(torch, sg, dev, stream, sp, reps=5):
     """ms, TFLOP/s and compulsory-byte GB/s of sgemm_f32 and sgemm_f32_tf32x3 on
     every named workload (operands resident on the device, median of `reps`
@@ -698,10 +727,8 @@ def main():
         tf32_probe = tf32_probe_tflops(torch, sg, dev, stream)
         tc = {
             "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
-            "kernels": "split_kernel (both operands) + tf32x3_persistent_kernel (one CTA per SM; 128x256 or "
-                       "128x128 tiles by wave count; TMA ring, tcgen05 kind::tf32, TMEM, TMA-store "
-                       "epilogue)",
-            "gpu_launches_per_step": 2,
+            "kernels": tc_plan(M, N, K, batch, w.transA, w.transB, aligned)[0],
+            "gpu_launches_per_step": tc_plan(M, N, K, batch, w.transA, w.transB, aligned)[1],
             "pct_of_fp32_peak_at_max_clock": None,
             "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_peak,
                          "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_peak,
