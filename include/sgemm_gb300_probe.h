@@ -1,6 +1,6 @@
 /*
- * sgemm_gb300_probe.h -- measuring the FP32 and TF32 peaks that SGEMM is judged
- * against.
+ * sgemm_gb300_probe.h -- measuring the FP32 and TF32 peaks that SGEMM's
+ * throughput is compared with.
  *
  * The peak of a GPU's FP32 units is cores x 2 FLOP (one FMA) x clock
  * (DD2360 workbook, section 3, worked example on the T4's FP32 peak).  This
