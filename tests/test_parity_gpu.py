@@ -887,14 +887,14 @@ def test_streamk_tma_exact_on_integers(M, N, K):
 # Layouts: NN (A raw), NT (both raw), TT (B raw), TN (neither); ragged edges
 # and K tails; batches; one operand converted and the other from its lo plane
 # (512 x 4096 and 4096 x 512 NT, 1100 x 1000: 9 tile rows against 8 tile
-# columns); K = 256 against 257; longer K (lo-only planes for 3xTF32, full
-# planes on both sides for plain TF32).
+# columns); K = 256 against 257; longer K (lo-only planes for 3xTF32, also
+# batched; full planes on both sides for plain TF32).
 RAWSPLIT = [(0, 0, 300, 260, 61, 1), (0, 1, 513, 384, 64, 1), (1, 1, 200, 388, 33, 1),
             (1, 0, 260, 300, 64, 1), (0, 1, 512, 512, 64, 3), (0, 0, 1100, 1300, 7, 1),
             (0, 1, 700, 900, 300, 1), (0, 0, 1100, 1300, 257, 1), (1, 1, 600, 700, 501, 1),
             (0, 1, 512, 512, 128, 3), (1, 0, 300, 400, 1000, 1), (0, 1, 512, 4096, 200, 1),
             (0, 1, 4096, 512, 100, 1), (1, 1, 700, 900, 256, 1), (0, 0, 1000, 1100, 257, 1),
-            (0, 1, 1100, 1000, 200, 1)]
+            (0, 1, 1100, 1000, 200, 1), (0, 1, 300, 260, 300, 3)]
 
 
 @pytest.mark.parametrize("entry_name", ["sgemm_f32_tf32x3", "sgemm_f32_tf32"])
