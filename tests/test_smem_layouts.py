@@ -1,0 +1,113 @@
+"""Shared-memory addressing of the TMA-fed SIMT kernel, checked on the CPU.
+
+csrc/simt_tma.cu reads its operand stages with 16-byte loads:
+  * K-major stages ([32][128] floats, as TMA writes an M- or N-contiguous box
+    with no swizzle): thread columns a_col..a_col+3 and +64 of row kk (A),
+    b_col..b_col+3 and +64 (B);
+  * M/N-major stages ([128][32] floats, a K-contiguous box written with the
+    128-byte swizzle, 16-byte chunk c of row r stored at chunk c ^ (r % 8)):
+    rows (or columns) t + 16 j of the thread, four k per load, at float
+    offset t*32 + 16*32*j + 4*(kq ^ (t % 8)).
+The thread's place comes from thread_coords (Z-order 4 x 8 lanes, 2 warps
+across).  For every thread and load this test checks that the offset the
+kernel computes is where the swizzle puts the element it wants, that it stays
+inside the stage, and that the eight lanes of each quarter-warp (the unit a
+16-byte shared load is served in) touch distinct 16-byte bank groups or the
+same address: no bank conflicts.
+"""
+import pytest
+
+BK, BM, BN, THREADS = 32, 128, 128, 256
+STAGE_FLOATS = BK * 128
+
+
+def thread_coords(tid):
+    lane, warp = tid & 31, tid >> 5
+    lane_row = (lane & 1) | ((lane >> 4) << 1)
+    lane_col = (lane >> 1) & 7
+    return 4 * ((warp >> 1) * 4 + lane_row), 4 * ((warp & 1) * 8 + lane_col)
+
+
+def swizzled_offset(r, k):
+    """Float offset of element (row r, k) in a [128][32] box with the 128-byte swizzle."""
+    return r * BK + 4 * ((k // 4) ^ (r % 8)) + k % 4
+
+
+def conflict_free(addrs):
+    """addrs: float offsets of one 16-byte load by the 32 lanes."""
+    for q in range(4):
+        groups = {}
+        for a in addrs[8 * q:8 * q + 8]:
+            assert a % 4 == 0, "16-byte load not 16-byte aligned"
+            groups.setdefault((a // 4) % 8, set()).add(a)
+        if any(len(v) > 1 for v in groups.values()):
+            return False
+    return True
+
+
+def test_thread_coords_cover_the_tile_once():
+    cells = set()
+    for tid in range(THREADS):
+        a_col, b_col = thread_coords(tid)
+        for r in list(range(a_col, a_col + 4)) + list(range(64 + a_col, 68 + a_col)):
+            for c in list(range(b_col, b_col + 4)) + list(range(64 + b_col, 68 + b_col)):
+                assert (r, c) not in cells
+                cells.add((r, c))
+    assert len(cells) == BM * BN
+
+
+def test_mn_major_strided_rows_cover_the_tile_once():
+    # the swizzled forms own rows ty + 16 j (A) or columns tx + 16 j (B)
+    cells = set()
+    for tid in range(THREADS):
+        a_col, b_col = thread_coords(tid)
+        ty, tx = a_col >> 2, b_col >> 2
+        for j in range(8):
+            for c in list(range(b_col, b_col + 4)) + list(range(64 + b_col, 68 + b_col)):
+                cells.add((ty + 16 * j, c))
+    assert len(cells) == BM * BN
+    cols = {(tid, (thread_coords(tid)[1] >> 2) + 16 * j) for tid in range(THREADS) for j in range(8)}
+    assert {c for _, c in cols} == set(range(BN))
+
+
+@pytest.mark.parametrize("operand", ["A", "B"])
+def test_kmajor_fragment_loads(operand):
+    for kk in range(BK):
+        for h in range(2):
+            addrs = []
+            for tid in range(THREADS):
+                a_col, b_col = thread_coords(tid)
+                col = (a_col if operand == "A" else b_col) + 64 * h
+                off = kk * 128 + col
+                assert 0 <= off and off + 4 <= STAGE_FLOATS
+                addrs.append(off)
+            for w in range(THREADS // 32):
+                assert conflict_free(addrs[32 * w:32 * w + 32]), (operand, kk, h, w)
+
+
+@pytest.mark.parametrize("operand", ["A", "B"])
+def test_swizzled_fragment_loads(operand):
+    for kq in range(BK // 4):
+        for j in range(8):
+            addrs = []
+            for tid in range(THREADS):
+                a_col, b_col = thread_coords(tid)
+                t = (a_col if operand == "A" else b_col) >> 2
+                off = t * BK + j * 16 * BK + 4 * (kq ^ (t & 7))   # the kernel's formula
+                r = t + 16 * j
+                for e in range(4):   # the four k of the load are elements (r, 4 kq + e)
+                    assert off + e == swizzled_offset(r, 4 * kq + e)
+                assert 0 <= off and off + 4 <= STAGE_FLOATS
+                addrs.append(off)
+            for w in range(THREADS // 32):
+                assert conflict_free(addrs[32 * w:32 * w + 32]), (operand, kq, j, w)
+
+
+def test_a_planted_conflict_is_detected():
+    # without the XOR the eight rows of a quarter-warp hit the same chunk
+    addrs = []
+    for tid in range(32):
+        a_col, _ = thread_coords(tid)
+        t = a_col >> 2
+        addrs.append(t * BK + 4 * 0)
+    assert not conflict_free(addrs)
