@@ -1,4 +1,5 @@
-"""Shared-memory addressing of the TMA-fed SIMT kernel, checked on the CPU.
+"""Shared-memory addressing of the SIMT kernels, checked on the CPU: the
+TMA-fed kernel here, the cp.async kernels further down.
 
 csrc/simt_tma.cu reads its operand stages with 16-byte loads:
   * K-major stages ([32][128] floats, as TMA writes an M- or N-contiguous box
@@ -111,3 +112,102 @@ def test_a_planted_conflict_is_detected():
         t = a_col >> 2
         addrs.append(t * BK + 4 * 0)
     assert not conflict_free(addrs)
+
+
+# ------------------------------------------------------------ cp.async kernels
+#
+# csrc/simt_sgemm.cuh keeps both operands K-major ([BK][ROWS] floats) with a
+# float4-granular XOR: row kk's column c is stored at c ^ swz(kk),
+# swz(kk) = (128 / BK) * (kk >> 2).  Writers: 16-byte cp.async of an M/N-
+# contiguous operand (element (mn = 4 mq + e, kk) at kk*ROWS + ((4 mq) ^
+# swz(kk)) + e) and, for a K-contiguous operand, the corner turn (thread g of
+# the slice holds row g / (BK/4), k quad g % (BK/4), and stores its four
+# values one float each to rows kk..kk+3 at column row ^ swz(kk)).  Readers:
+# the fragment loads at kk*ROWS + (col ^ swz(kk)), col = a_col (+64) or
+# b_col + 64 h.
+
+def swz(kk, bk=BK):
+    return (128 // bk) * (kk >> 2)
+
+
+def cpasync_layout(rows, bk=BK):
+    """(k, mn) -> float offset, as the 16-byte cp.async writer places it."""
+    where = {}
+    for kk in range(bk):
+        for mq in range(rows // 4):
+            for e in range(4):
+                where[(kk, 4 * mq + e)] = kk * rows + ((4 * mq) ^ swz(kk, bk)) + e
+    return where
+
+
+def cornerturn_layout(rows, bk=BK, threads=THREADS):
+    """(k, mn) -> float offset, and the per-instruction store addresses of
+    the corner turn (r: the thread's vector, e: which of its four floats)."""
+    kq_n = bk // 4
+    where, stores = {}, {}
+    for r in range(bk * rows // (4 * threads)):
+        for tid in range(threads):
+            g = tid + r * threads
+            row, kq = g // kq_n, g % kq_n
+            kk = 4 * kq
+            col = row ^ swz(kk, bk)
+            for e in range(4):
+                off = (kk + e) * rows + col
+                where[(kk + e, row)] = off
+                stores.setdefault((r, e), []).append(off)
+    return where, stores
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+def test_cpasync_layout_is_a_permutation_read_back_by_the_fragments(rows):
+    where = cpasync_layout(rows)
+    assert sorted(where.values()) == list(range(BK * rows))
+    nsb = rows // 64
+    for kk in range(BK):
+        for h in range(nsb):
+            addrs = []
+            for tid in range(THREADS):
+                _, b_col = thread_coords(tid)
+                col = b_col + 64 * h
+                off = kk * rows + (col ^ swz(kk))
+                for e in range(4):
+                    assert where[(kk, col + e)] == off + e
+                addrs.append(off)
+            for w in range(THREADS // 32):
+                assert conflict_free(addrs[32 * w:32 * w + 32]), (rows, kk, h, w)
+
+
+def test_cornerturn_layout_matches_the_reads_and_stores_without_conflicts():
+    rows = 128
+    where, stores = cornerturn_layout(rows)
+    assert where == cpasync_layout(rows), "the two writers disagree on the layout"
+    for (r, e), offs in stores.items():
+        for w in range(THREADS // 32):
+            banks = {}
+            for off in offs[32 * w:32 * w + 32]:
+                banks.setdefault(off % 32, set()).add(off)
+            assert all(len(v) == 1 for v in banks.values()), f"store conflict r={r} e={e} warp={w}"
+    # the A fragments (a_col and a_col + 64) read back the corner-turned rows
+    for kk in range(BK):
+        for h in range(2):
+            addrs = []
+            for tid in range(THREADS):
+                a_col, _ = thread_coords(tid)
+                col = a_col + 64 * h
+                off = kk * rows + (col ^ swz(kk))
+                for e in range(4):
+                    assert where[(kk, col + e)] == off + e
+                addrs.append(off)
+            for w in range(THREADS // 32):
+                assert conflict_free(addrs[32 * w:32 * w + 32])
+
+
+def test_cornerturn_without_swizzle_would_conflict():
+    offs = []
+    for tid in range(32):
+        row, kq = tid // (BK // 4), tid % (BK // 4)
+        offs.append((4 * kq) * 128 + row)   # no XOR
+    banks = {}
+    for off in offs:
+        banks.setdefault(off % 32, set()).add(off)
+    assert any(len(v) > 1 for v in banks.values())
