@@ -211,3 +211,55 @@ def test_cornerturn_without_swizzle_would_conflict():
     for off in offs:
         banks.setdefault(off % 32, set()).add(off)
     assert any(len(v) > 1 for v in banks.values())
+
+
+# ------------------------------------------------------------ other staging tiles
+
+def banks_conflict_free_32bit(offs):
+    """One 4-byte shared access by 32 lanes: distinct banks or one address."""
+    banks = {}
+    for off in offs:
+        banks.setdefault(off % 32, set()).add(off)
+    return all(len(v) == 1 for v in banks.values())
+
+
+def test_tensor_epilogue_staging_matches_the_c_map_swizzle():
+    # csrc/tf32x3.cu, store_tile_rows: lane r of the warp holds row r of a
+    # 32 x 32 fp32 block and writes its 16-byte chunk j to byte
+    # r * 128 + ((j ^ (r & 7)) << 4) of a 4 KB buffer, which the TMA store
+    # reads through a tensor map with the 128-byte swizzle (chunk c of row r
+    # at chunk c ^ (r % 8)).
+    for j in range(8):
+        offs = []
+        for lane in range(32):
+            byte = lane * 128 + ((j ^ (lane & 7)) << 4)
+            assert byte == lane * 128 + 16 * ((j) ^ (lane % 8))   # the swizzle's definition
+            assert 0 <= byte and byte + 16 <= 4096
+            offs.append(byte // 4)
+        assert conflict_free(offs), j
+
+
+@pytest.mark.parametrize("rows_in_tile", [32, 64])
+def test_padded_transpose_tiles(rows_in_tile):
+    # split_transpose (csrc/tf32x3.cu, tile[32][33]) and transpose_kernel
+    # (csrc/turn.cu, tile[64][33]): 256 threads as 32 x 8 (tx, ty); writes
+    # tile[ty + 8 i][tx], reads tile[tx + 32 (i / 4)][ty + 8 (i % 4)] (the
+    # 32-row tile reads tile[tx][ty + 8 i]).
+    pitch = 33
+    writes, reads = {}, {}
+    for tid in range(THREADS):
+        tx, ty = tid & 31, tid >> 5
+        for i in range(rows_in_tile // 8):
+            writes.setdefault(i, {})[tid] = (ty + 8 * i) * pitch + tx
+            if rows_in_tile == 64:
+                reads.setdefault(i, {})[tid] = (tx + 32 * (i >> 2)) * pitch + ty + 8 * (i & 3)
+            else:
+                reads.setdefault(i, {})[tid] = tx * pitch + ty + 8 * i
+    filled = sorted(o for d in writes.values() for o in d.values())
+    assert len(set(filled)) == len(filled) == rows_in_tile * 32
+    assert set(o for d in reads.values() for o in d.values()) == set(filled), \
+        "the reads do not cover exactly what was written"
+    for table in (writes, reads):
+        for i, per_tid in table.items():
+            for w in range(THREADS // 32):
+                assert banks_conflict_free_32bit([per_tid[t] for t in range(32 * w, 32 * w + 32)])
