@@ -730,17 +730,20 @@ def main():
             "kernels": tc_plan(M, N, K, batch, w.transA, w.transB, aligned)[0],
             "gpu_launches_per_step": tc_plan(M, N, K, batch, w.transA, w.transB, aligned)[1],
             "pct_of_fp32_peak_at_max_clock": None,
-            "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_peak,
-                         "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_peak,
+            "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_probe,
+                         "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_probe,
                          "traffic": profiled_traffic("tf32x3_persistent_kernel", args.workload),
-                         "peak_source": ("measured bf16 burst x nominal TF32/BF16 ratio 1.1/2.25"
-                                         if bf16 else "nominal dense TF32"),
+                         "peak_source": "measured in this run: the library's TF32 tensor-pipe "
+                                        "probe (sgemm_probe_tf32_mma: back-to-back "
+                                        "tcgen05.mma.kind::tf32 M128 N256 K8 from shared memory, "
+                                        "one CTA per SM)",
                          "note": "achieved = tensor-pipe work (3 TF32 MMAs per product) / time of "
                                  "the whole call, split kernels included",
-                         "peak_tf32_probe": tf32_probe,
-                         "frac_of_tf32_probe": 3 * tc_alg / tf32_probe,
-                         "tf32_probe": "sgemm_probe_tf32_mma: back-to-back tcgen05.mma.kind::tf32 "
-                                       "M128 N256 K8 from shared memory, one CTA per SM"},
+                         "peak_bf16_derived": tf32_peak,
+                         "frac_of_bf16_derived": 3 * tc_alg / tf32_peak,
+                         "bf16_derived": ("measured bf16 burst x nominal TF32/BF16 ratio 1.1/2.25 "
+                                          "(below what the TF32 probe reaches, so not the "
+                                          "denominator)" if bf16 else "nominal dense TF32")},
             "rrmse_vs_oracle": tc_rrmse,
             "device_status": status,
         }

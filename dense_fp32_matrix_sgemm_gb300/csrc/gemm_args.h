@@ -3,9 +3,56 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 namespace sgemm {
+
+// Unique id of the CUDA context current on the calling thread (the driver's
+// context id), 0 when none is current or the driver cannot say.  Ids are never
+// reused within a process: a context created after cudaDeviceReset, or another
+// context made current on the same device, never matches a value cached for an
+// earlier one.  Defined in tf32x3.cu, next to the other driver entry points.
+unsigned long long current_context_id();
+
+// A value looked up once per CUDA context (a device address, or the fact that
+// a kernel's shared-memory attribute has been set), keyed on the context id.
+// Id 0 (unknown context) is never cached, so the caller looks the value up
+// again.  A few contexts are kept; the oldest entry is replaced after that.
+template <class T>
+class PerContext {
+  public:
+    bool get(unsigned long long ctx, T &out) const {
+        if (ctx == 0) return false;
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < kSlots; ++i)
+            if (ids_[i] == ctx) {
+                out = vals_[i];
+                return true;
+            }
+        return false;
+    }
+    void put(unsigned long long ctx, const T &v) {
+        if (ctx == 0) return;
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < kSlots; ++i)
+            if (ids_[i] == ctx) {
+                vals_[i] = v;
+                return;
+            }
+        ids_[next_] = ctx;
+        vals_[next_] = v;
+        next_ = (next_ + 1) % kSlots;
+    }
+
+  private:
+    static constexpr int kSlots = 16;
+    mutable std::mutex mu_;
+    unsigned long long ids_[kSlots] = {};
+    T vals_[kSlots] = {};
+    int next_ = 0;
+};
 
 // One (possibly batched) problem after host-side validation.  All pointers are
 // device pointers; strides and leading dimensions are in elements.

@@ -4,13 +4,14 @@
 //
 // The scratch is the file-scope array below.  Host code cannot use the
 // array's name as a device address (in host code it names a host-side
-// stand-in), so the device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, and handed to the kernels.
+// stand-in), so the device address is looked up with cudaGetSymbolAddress,
+// once per context with that context current, and handed to the kernels.
 #include <cstdio>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
+#include "gemm_args.h"
 #include "sgemm_gb300.h"
 
 namespace sgemm {
@@ -24,30 +25,29 @@ namespace {
 constexpr unsigned long long kNoallocScratchBytes = 64ull << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device (looked up on the
-// first call made with that device current).
-int scratch_for_current_device(void **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return record_error(SGEMM_EDEVICE, "no usable CUDA device for the built-in scratch");
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            char msg[256];
-            snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the built-in scratch failed: %s",
-                     cudaGetErrorString(e));
-            return record_error(SGEMM_EDEVICE, msg);
-        }
-        g_scratch_ptr[dev] = p;
+// Device address of the scratch in the current context, looked up with
+// cudaGetSymbolAddress the first time a call runs in that context (which also
+// makes the runtime set up the device's context if it is not yet current).
+// The cache is keyed on the context's unique id, not on the device number:
+// after cudaDeviceReset, or with another context made current, the address is
+// looked up again instead of reusing one that belongs to a dead or different
+// context.
+int scratch_for_current_context(void **out) {
+    static PerContext<void *> cached;
+    void *p = nullptr;
+    if (cached.get(current_context_id(), p)) {
+        *out = p;
+        return SGEMM_OK;
     }
-    *out = g_scratch_ptr[dev];
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        char msg[256];
+        snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the built-in scratch failed: %s",
+                 cudaGetErrorString(e));
+        return record_error(SGEMM_EDEVICE, msg);
+    }
+    cached.put(current_context_id(), p);
+    *out = p;
     return SGEMM_OK;
 }
 
@@ -74,7 +74,7 @@ extern "C" int sgemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const f
     }
     void *scratch = nullptr;
     if (need > 0) {
-        const int st = sgemm::scratch_for_current_device(&scratch);
+        const int st = sgemm::scratch_for_current_context(&scratch);
         if (st != SGEMM_OK) return st;
     }
     // The split kernels write every scratch element the GEMM kernel reads, so

@@ -85,19 +85,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Sets the opt-in dynamic shared-memory size of `kern` once per device.
+// Sets the opt-in dynamic shared-memory size of `kern` once per context.
 template <typename Kern>
-cudaError_t ensure_smem_attribute(Kern kern, int smem, std::atomic<unsigned long long> &configured) {
+cudaError_t ensure_smem_attribute(Kern kern, int smem, PerContext<bool> &configured) {
     if (smem <= 48 * 1024) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    bool done = false;
+    if (configured.get(current_context_id(), done)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
-    }
+    configured.put(current_context_id(), true);
     return cudaSuccess;
 }
 
@@ -106,7 +102,7 @@ cudaError_t launch_config(const GemmArgs &a, cudaStream_t s) {
     constexpr int commit = BN_ == 256 ? kCommitWide : (STAGES == 2 ? kBK : kCommitNarrow);
     auto kern = sgemm_simt_kernel<kBK, STAGES, BN_, TA, TB, VEC, kFfma2, MINB, commit>;
     constexpr int smem = smem_bytes<kBK, STAGES, BN_>();
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     cudaError_t e = ensure_smem_attribute(kern, smem, configured);
     if (e != cudaSuccess) return e;
     GemmArgs g = a;
@@ -134,20 +130,21 @@ bool launch_cluster_split(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
     const long long slices = (a.K + kBK - 1) / kBK;
     if (slices < 2) return false;
 
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     err = ensure_smem_attribute(kern, smem, configured);
     if (err != cudaSuccess) return true;
     int dev = 0;
     err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return true;
-    // clusters of 16 need the non-portable size opt-in (a per-device attribute)
-    static std::atomic<unsigned long long> nonportable{0};
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(nonportable.load() & bit)) {
+    // clusters of 16 need the non-portable size opt-in (a function attribute,
+    // set once per context)
+    static PerContext<bool> nonportable;
+    bool opted = false;
+    if (!nonportable.get(current_context_id(), opted)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess)
             (void)cudaGetLastError();   // then clusters of 16 report no residency below
-        nonportable.fetch_or(bit);
+        nonportable.put(current_context_id(), true);
     }
 
     cudaLaunchConfig_t cfg = {};
@@ -233,7 +230,7 @@ cudaError_t launch_streamk_config(const GemmArgs &a, const StreamKPlan &pl, void
                                   cudaStream_t s) {
     auto kern = sgemm_simt_streamk_kernel<kBK, STAGES, BN_, TA, TB, VEC, kFfma2, kMinBlocks, CK>;
     constexpr int smem = smem_bytes<kBK, STAGES, BN_>();
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     cudaError_t e = ensure_smem_attribute(kern, smem, configured);
     if (e != cudaSuccess) return e;
     GemmArgs g = a;

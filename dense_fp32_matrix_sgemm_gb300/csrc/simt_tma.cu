@@ -211,12 +211,16 @@ __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int 
 // g - STAGES from the same stage; each warp releases a slice once its lanes
 // have read it.  On return no copy of this piece is in flight (every issued
 // slice has been waited on), and the next piece may start at once.
+// `issued` (thread 0's count) is one past the last slice whose copies were
+// started: once the abort word is set nothing more is issued, so a stage
+// never gets a second fill in one phase and finish_abort knows exactly which
+// copies can still be in flight.
 template <int BK, int STAGES, int BN_, bool KA, bool KB>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
-                                             int m0, int n0, int z, int kbeg, int ktiles,
-                                             int a_col, int b_col, float (&acc)[8][BN_ / 16],
-                                             volatile int *abort) {
+                                             uint32_t &issued, int m0, int n0, int z, int kbeg,
+                                             int ktiles, int a_col, int b_col,
+                                             float (&acc)[8][BN_ / 16], volatile int *abort) {
     constexpr int TN = BN_ / 16;
     constexpr int ATILE = BK * BM;
     constexpr int BTILE = BK * BN_;
@@ -232,8 +236,13 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
     auto issue = [&](int slice) {
         const uint32_t g = g0 + (uint32_t)slice;
         const uint32_t st = g % STAGES;
-        if (g >= STAGES)   // slice g - STAGES released by every warp
-            (void)tc::mbar_wait(empty0 + 8 * st, ((g / STAGES) - 1) & 1, abort);
+        // slice g - STAGES released by every warp; a warp whose wait ran out
+        // releases a stage whose copy may not have landed, so the abort word
+        // is read again after the release (the warps set it before arriving)
+        if (*abort) return;
+        if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * st, ((g / STAGES) - 1) & 1, abort)) return;
+        if (*abort) return;
+        issued = g + 1;
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         if constexpr (KA)   // box (k, m): 32 k x 128 rows
@@ -263,10 +272,12 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
 }
 
 // After a wait ran out (the abort word is set; every later wait returned at
-// once), thread 0 raises bit 0 of the status word and waits, with a limit,
-// for the copies of the last STAGES slices it issued (the CTA's slices
-// [n - STAGES, n)) to land, so that none writes into shared memory after the
-// CTA has exited.  Does nothing in a run whose waits all completed.
+// once, and no slice was issued after it), thread 0 raises bit 0 of the
+// status word and waits, with a limit, for the copies of the last STAGES
+// slices it issued (the CTA's slices [n - STAGES, n), n = its issued count:
+// the latest fill of each stage) to land, so that none writes into shared
+// memory after the CTA has exited.  Does nothing in a run whose waits all
+// completed.
 template <int STAGES>
 __device__ __forceinline__ void finish_abort(uint32_t full0, uint32_t n, volatile int *abort,
                                              unsigned int *status) {
@@ -363,10 +374,11 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     int a_col, b_col;
     thread_coords(a_col, b_col);
     float acc[8][BN_ / 16];
-    uint32_t gk = 0;
-    tma_mainloop<BK, STAGES, BN_, KA, KB>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
-                                          (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
-    finish_abort<STAGES>(full0, gk, abort, status);
+    uint32_t gk = 0, issued = 0;
+    tma_mainloop<BK, STAGES, BN_, KA, KB>(&tmA, &tmB, As, Bs, full0, gk, issued, tm * BM,
+                                          tn * BN_, z, 0, (p.K + BK - 1) / BK, a_col, b_col, acc,
+                                          abort);
+    finish_abort<STAGES>(full0, issued, abort, status);
     store_tile<BN_, KA, KB>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
 
@@ -406,13 +418,18 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     const int ktiles = (p.K + BK - 1) / BK;
     const int total = mine * ktiles;   // slices of this CTA
     const bool issuer = threadIdx.x == 0;
+    uint32_t issued = 0;   // thread 0: one past the last slice issued (see tma_mainloop)
     auto issue = [&](int g) {
         const int i = g / ktiles, j = g - i * ktiles;
         int z, tm, tn;
         raster(p, c + i * G, z, tm, tn);
         const uint32_t st = (uint32_t)g % STAGES;
-        if (g >= STAGES)   // slice g - STAGES released by every warp
-            (void)tc::mbar_wait(empty0 + 8 * st, ((uint32_t)g / STAGES - 1) & 1, abort);
+        // as in tma_mainloop: no new copy once the abort word is set
+        if (*abort) return;
+        if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * st, ((uint32_t)g / STAGES - 1) & 1, abort))
+            return;
+        if (*abort) return;
+        issued = (uint32_t)g + 1;
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         if constexpr (KA)
@@ -444,7 +461,7 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         raster(p, c + i * G, z, tm, tn);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
     }
-    finish_abort<STAGES>(full0, (uint32_t)total, abort, status);
+    finish_abort<STAGES>(full0, issued, abort, status);
 }
 
 // The stream-K schedule (see StreamK) as one grid of tiles_dp + G CTAs:
@@ -475,15 +492,16 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     pdl_trigger();
     int a_col, b_col;
     thread_coords(a_col, b_col);
-    uint32_t gk = 0;
+    uint32_t gk = 0, issued = 0;
     const int b = blockIdx.x;
     if (b < sk.tiles_dp) {
         int z, tm, tn;
         raster(p, b, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
-                                                 z, 0, sk.kslices, a_col, b_col, acc, abort);
-        finish_abort<STAGES>(full0, gk, abort, status);
+        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, issued, tm * BM,
+                                                 tn * BN_, z, 0, sk.kslices, a_col, b_col, acc,
+                                                 abort);
+        finish_abort<STAGES>(full0, issued, abort, status);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         return;
     }
@@ -493,6 +511,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     const int nsk = u0 == u1 ? 0 : (u0 / sk.kslices == (u1 - 1) / sk.kslices ? 1 : 2);
 #pragma unroll 1
     for (int k = 0; k < nsk; ++k) {   // 0: the range's first piece, 1: its last
+        if (*abort) break;            // a wait of the first piece ran out
         const int64_t ub = k == 0 ? u0 : (u0 / sk.kslices + 1) * sk.kslices;
         const int tl = (int)(ub / sk.kslices);
         const int s0 = (int)(ub - (int64_t)tl * sk.kslices);
@@ -500,8 +519,9 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
-                                                 z, s0 * BK, s1 - s0, a_col, b_col, acc, abort);
+        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, issued, tm * BM,
+                                                 tn * BN_, z, s0 * BK, s1 - s0, a_col, b_col, acc,
+                                                 abort);
         if (!(s0 == 0 && s1 == sk.kslices)) {
             // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
             float *part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
@@ -518,7 +538,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         }
     }
-    finish_abort<STAGES>(full0, gk, abort, status);
+    finish_abort<STAGES>(full0, issued, abort, status);
 }
 
 namespace {
@@ -574,7 +594,7 @@ cudaError_t launch_tile_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB, c
                                cudaStream_t s) {
     auto kern = sgemm_simt_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, KB, kTmaMinBlocks>;
     constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     cudaError_t err = ensure_smem_attribute(kern, smem, configured);
     if (err != cudaSuccess) return err;
     const long long blocks = (long long)g.batch * g.tiles_m * g.tiles_n;
@@ -587,7 +607,7 @@ cudaError_t launch_persist_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB
                                   const GemmArgs &g, int ctas, cudaStream_t s) {
     auto kern = sgemm_simt_persist_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
     constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     cudaError_t err = ensure_smem_attribute(kern, smem, configured);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3((unsigned)ctas), dim3(THREADS), smem, s, tmA, tmB, g,
@@ -599,7 +619,7 @@ cudaError_t launch_streamk_kernel(const CUtensorMap &tmA, const CUtensorMap &tmB
                                   const GemmArgs &g, const StreamK &sk, cudaStream_t s) {
     auto kern = sgemm_simt_streamk_tma_kernel<kTmaBK, kTmaStages, kTmaBN, KA, kTmaMinBlocks>;
     constexpr int smem = tma_smem_bytes<kTmaBK, kTmaStages, kTmaBN>();
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     cudaError_t err = ensure_smem_attribute(kern, smem, configured);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3((unsigned)(sk.tiles_dp + sk.G)), dim3(THREADS), smem, s, tmA, tmB,

@@ -869,18 +869,15 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int co
     return cudaSuccess;
 }
 
-// Sets the opt-in dynamic shared-memory size of `kern` once per device.
+// Sets the opt-in dynamic shared-memory size of `kern` once per context.
 template <typename Kern>
-cudaError_t ensure_smem(Kern kern, int bytes, std::atomic<unsigned long long> &configured) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+cudaError_t ensure_smem(Kern kern, int bytes, PerContext<bool> &configured) {
+    const unsigned long long ctx = current_context_id();
+    bool done = false;
+    if (configured.get(ctx, done)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
-    }
+    configured.put(current_context_id(), true);
     return cudaSuccess;
 }
 
@@ -889,7 +886,7 @@ template <class CFG, int ACC_BUFS, int RAW, int CONV>
 cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, void *ws,
                                   cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB) {
     using P = Persist<CFG, ACC_BUFS, RAW, CONV>;
-    static std::atomic<unsigned long long> configured{0};
+    static PerContext<bool> configured;
     cudaError_t e = ensure_smem(tf32x3_persistent_kernel<CFG, ACC_BUFS, RAW, CONV>, P::SMEM_BYTES,
                                 configured);
     if (e != cudaSuccess) return e;
@@ -1080,17 +1077,10 @@ cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, c
 }
 
 cudaError_t launch_tf32_mma_probe(long long iters, float *out, int ctas, cudaStream_t s) {
-    static std::atomic<unsigned long long> configured{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static PerContext<bool> configured;
+    cudaError_t e = tf32x3::ensure_smem(tf32x3::tf32_mma_probe_kernel, tf32x3::kProbeSmem,
+                                        configured);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(tf32x3::tf32_mma_probe_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tf32x3::kProbeSmem);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit);
-    }
     tf32x3::tf32_mma_probe_kernel<<<ctas, tf32x3::THREADS, tf32x3::kProbeSmem, s>>>(iters, out);
     return cudaGetLastError();
 }
@@ -1116,17 +1106,42 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-unsigned int *device_error_word() {
-    static std::atomic<unsigned int *> cached[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
-    unsigned int *w = cached[dev & 63].load();
-    if (w == nullptr) {
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, tf32x3::g_tf32x3_error) != cudaSuccess) return nullptr;
-        w = static_cast<unsigned int *>(p);
-        cached[dev & 63].store(w);
-    }
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// The status word's device address in the current context: looked up in each
+// context once (the lookup also makes the runtime set up a context that is
+// not yet current), so a kernel never gets an address from another context.
+unsigned int *device_error_word() {
+    static PerContext<unsigned int *> cached;
+    unsigned int *w = nullptr;
+    if (cached.get(current_context_id(), w)) return w;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, tf32x3::g_tf32x3_error) != cudaSuccess) return nullptr;
+    w = static_cast<unsigned int *>(p);
+    cached.put(current_context_id(), w);
     return w;
 }
 

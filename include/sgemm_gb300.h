@@ -319,9 +319,11 @@ uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
  * Limit: 2 * (M + N) * round_up(K, 4) * 4 bytes (plus 256-byte alignment
  * padding) must fit in the scratch, e.g. M = N = K = 2048; larger problems
  * return SGEMM_EWORKSPACE with the sizes in sgemm_last_error().
- * The first call with a given device current looks up the scratch's device
- * address (cudaGetSymbolAddress); make that first call before any stream
- * capture on that device.  Every call on a device shares the one scratch
+ * The first call in each CUDA context (per device, and again after
+ * cudaDeviceReset or when another context is made current) looks up the
+ * scratch's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture in that context.  Every call on a device shares
+ * the one scratch
  * array: calls whose kernels can overlap on the GPU (different streams
  * without ordering between them) race on it and give wrong results.  The
  * scratch keeps the last call's contents; no call relies on it being zero.

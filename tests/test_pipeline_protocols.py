@@ -211,6 +211,105 @@ def simt_tma_persistent(tiles, ktiles, stages, warps, seed):
         assert seen[w] == list(range(pieces_total))
 
 
+def simt_tma_abort(pieces, stages, warps, seed, abort_step):
+    """tma_mainloop with the abort path: at step `abort_step` some wait runs
+    out and sets the CTA's abort word.  From then on every wait returns at
+    once (a warp whose "full" wait gave up still releases the stage), thread 0
+    issues nothing more (it reads the abort word before the "empty" wait and
+    again after it), and finish_abort waits for the last `stages` slices it
+    issued.  Checks that no stage ever gets a second fill while its previous
+    copy is in flight, and that no copy is in flight when the CTA exits."""
+    rng = random.Random(seed)
+    full = [Barrier(1, f"full{s}") for s in range(stages)]
+    empty = [Barrier(warps, f"empty{s}") for s in range(stages)]
+    flying = [False] * stages
+    in_flight = []
+    state = {"abort": False, "step": 0, "issued": 0}
+
+    def wait(bar, k):
+        # bounded wait: gives up once the abort word is set
+        while True:
+            if bar.completed == k + 1:
+                return True
+            if state["abort"]:
+                return False
+            assert bar.completed == k, f"{bar.name}: parity wait on phase {k} with {bar.completed}"
+            yield
+
+    def issue(g):
+        s = g % stages
+        if state["abort"]:
+            return
+        if g >= stages:
+            ok = yield from wait(empty[s], g // stages - 1)
+            if not ok:
+                return
+        if state["abort"]:
+            return
+        assert not flying[s], "a stage got a second fill while its copy was in flight"
+        flying[s] = True
+        in_flight.append(g)
+        state["issued"] = g + 1
+
+    def tma():
+        while True:
+            if in_flight:
+                g = in_flight.pop(rng.randrange(len(in_flight)))
+                flying[g % stages] = False
+                full[g % stages].arrive()
+            yield
+
+    def warp(w):
+        gk = 0
+        for n in pieces:
+            g0 = gk
+            if w == 0:
+                for j in range(min(stages - 1, n)):
+                    yield from issue(g0 + j)
+            for kt in range(n):
+                s = gk % stages
+                yield from wait(full[s], gk // stages)
+                gk += 1
+                yield
+                empty[s].arrive()
+                if w == 0 and kt + stages - 1 < n:
+                    yield from issue(g0 + kt + stages - 1)
+        if w == 0 and state["abort"]:
+            # finish_abort: the latest fill of every stage lands before exit
+            n = state["issued"]
+            for g in range(max(0, n - stages), n):
+                while full[g % stages].completed < g // stages + 1:
+                    yield
+
+    t = tma()
+    alive = [warp(w) for w in range(warps)]
+    steps = 0
+    while alive:
+        steps += 1
+        assert steps < 500000, "no progress: the roles wait on one another"
+        if steps == abort_step:
+            state["abort"] = True
+        if rng.random() < 0.3:
+            next(t)
+            continue
+        i = rng.randrange(len(alive))
+        try:
+            next(alive[i])
+        except StopIteration:
+            alive.pop(i)
+    assert state["abort"] or steps < abort_step
+    assert not in_flight, "a copy was still in flight when the CTA exited"
+
+
+@pytest.mark.parametrize("pieces", [[96], [3], [5, 7], [2, 96]])
+def test_simt_tma_abort_path(pieces):
+    # the abort word set at many points of the run, 3 stages as the kernels use
+    for stages in (3, 2):
+        for seed in range(40):
+            abort_step = random.Random(1000 + seed).randrange(1, 400)
+            simt_tma_abort(pieces, stages, warps=8, seed=seed, abort_step=abort_step)
+
+
 @pytest.mark.parametrize("tiles,ktiles", [(6, 2), (1, 8), (5, 1), (3, 7)])
 def test_simt_tma_persistent_pipeline(tiles, ktiles):
     for seed in range(12):
