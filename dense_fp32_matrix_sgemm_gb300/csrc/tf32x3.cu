@@ -35,12 +35,16 @@
 //   staging buffers (128-byte swizzle, two per warp) and one lane stores it
 //   with a TMA tensor store, which writes whole rows and clips the ragged
 //   edges; otherwise the threads store their own rows.
+//   This single-pass kernel serves reductions up to 256 deep (three terms)
+//   and the plain product; longer three-term reductions run the K-chunked
+//   kernel (tf32x3_chunked_kernel, below), same roles, same ring.
 // The tensor cores add each MMA's partial sum into its fp32 accumulator with
 // a rounding that is biased towards zero, so the error of a long K grows with
 // the number of updates.  hi*hi therefore has an accumulator of its own (K/8
 // updates) and the two small terms share the second one, whose values are
 // 2^-10 smaller, so their rounding is negligible; one round-to-nearest add
-// combines the two in the epilogue.
+// combines the two in the epilogue.  The K-chunked kernel goes further and
+// adds the tensor cores' sums of every 128 of K in round-to-nearest fp32.
 // Every mbarrier wait is bounded; a wait that runs out flags the CTA, the
 // roles drain (copies in flight land, MMAs complete, TMEM is freed) and the
 // library's device error word is raised.
@@ -607,16 +611,389 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     }
     __syncwarp();
-    if (*abort_flag && threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
 
     tc::fence_before_sync();
     __syncthreads();
+    // after every role has finished, so a wait that ran out late is reported too
+    if (*abort_flag && threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
     if (warp == 1) {
         // every MMA issued has completed before TMEM is freed
         int local_abort = 0;
         (void)tc::mbar_wait(done_bar, 0, &local_abort);
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, P::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ K-chunked GEMM
+
+// The three-term product over long reductions, with the tensor cores' sums
+// promoted to round-to-nearest fp32 adds every 128 of K.
+//
+// The tensor cores add each MMA's result into its fp32 TMEM accumulator with
+// a rounding biased towards zero, so over K/8 updates the errors add up with
+// one sign: 3072^3 came out at an RRMSE of 7.3e-6 with hi*hi in an accumulator
+// of its own, seven times that of sequential FP32 FMA.  Here no accumulator
+// absorbs more than 16 K steps.  The MMAs of K chunk c of a tile go into chunk
+// accumulator c % 2 (TMEM columns [256 (c % 2), 256 (c % 2) + 256)), starting
+// from zero; once a chunk is complete, the epilogue warps load it and add it
+// into a running sum held in their registers with ordinary fp32 adds
+// (round to nearest even), and hand the accumulator back to the MMA issuer,
+// which meanwhile fills the other one.  After the last chunk the running sum
+// is the tile's result and is stored.  The chunk sums are added in ascending
+// chunk order, so results stay deterministic, and small-integer inputs stay
+// exact (every partial sum is an exact float).
+//
+// Chunk length: measured at 3072^3 (RRMSE / time of the whole call), 64 of K
+// 5.6e-7 / +2.7 %, 128 1.0e-6 / +1.1 %, 256 1.9e-6 / +0.3 %, against the same
+// kernel with one chunk per tile (2.2e-5).  What a chunk costs is the MMA
+// issuer waiting at the chunk boundary for the previous chunk's drain: the
+// epilogue's TMEM loads of one accumulator complete slowly while the tensor
+// cores write the other (the same kernel with the loads removed, or with the
+// issuer not waiting, runs as fast as one chunk per tile; halving the loaded
+// columns changes nothing).  128 gives the FP32-FMA path's accuracy (RRMSE
+// 9.9e-7 at 3072^3) for about 1 %.
+//
+// TMEM layout of one chunk accumulator (256 columns, lane = tile row):
+//   128-wide tile: hi*hi in columns [0, 128), the two small terms in
+//     [128, 256) (as in the single-pass kernel);
+//   256-wide tile: all three terms in one 256-column block (the small terms'
+//     updates round at hi*hi's magnitude, three per K step instead of one,
+//     which the chunking keeps well below the bound).
+// Warps: 0 TMA producer (as in the persistent kernel), 1 MMA issuer and TMEM
+// owner, 2-9 epilogue: warp w drains TMEM lane quarter w % 4 and column half
+// (w - 2) / 4, i.e. 32 rows x BN/2 columns of the running sum per warp.
+template <class CFG>
+struct Chunked {
+    static constexpr int BN = CFG::BN;
+    static constexpr bool SEP = BN == 128;   // hi*hi apart from the small terms
+    static constexpr int SLOT_COLS = 256;
+    static constexpr int NSLOT = 2;
+    static constexpr int KC = 128;                // K per chunk
+    static constexpr int KCB = KC / CFG::BK;      // K blocks per chunk
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int COLS = BN / 2;           // running-sum columns per epilogue thread
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int STAGING = EPI_WARPS * 4096;   // one 32 x 32 fp32 block per warp
+    static constexpr int BARS = 2 * CFG::STAGES + 2 * NSLOT + 1;
+    static constexpr int SMEM_BYTES = CFG::STAGES * CFG::STAGE_BYTES + STAGING + 1024 + 256;
+    static_assert(CFG::TERMS == 3, "the chunked kernel forms the three-term product");
+    static_assert(KC % CFG::BK == 0, "chunks are whole K blocks");
+    static_assert(NSLOT * SLOT_COLS == 512, "two chunk accumulators fill tensor memory");
+    static_assert((SEP ? 2 * BN : BN) == SLOT_COLS, "chunk accumulator width");
+    static_assert(BARS * 8 + 8 <= 256, "barrier area");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// Stores 32 rows x COLS columns of a finished tile from the running sums of
+// the calling warp's threads (thread `lane` holds row m0 + 32q + lane, columns
+// n0 .. n0 + COLS - 1), 32 columns at a time through the warp's 4 KB staging
+// block (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7), so
+// the eight rows a quarter-warp writes, and the 32 columns of one row the warp
+// reads back, hit distinct banks).
+//   TMA path (p.tma_c): one lane stores the block with a TMA tensor store,
+//   after the previous block's store has read the staging block; `cc` counts
+//   the blocks staged so far.
+//   Otherwise the warp reads the block back a row at a time, lane j taking
+//   column j, and stores it with the epilogue: each store is one 128-byte row
+//   segment.
+template <int COLS>
+__device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const CUtensorMap *tmC,
+                                                   const float (&run)[COLS], int q, int lane,
+                                                   int z, int m0, int n0, uint32_t stage,
+                                                   int &cc) {
+    const int row0 = m0 + 32 * q;
+    if (row0 >= p.M) return;
+    const uint32_t rbase = stage + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int c = 0; c < COLS / 32; ++c) {
+        if (n0 + 32 * c >= p.N) break;
+        if (p.tma_c && cc > 0) {
+            if (lane == 0) tc::bulk_wait_group_read<0>();   // the previous block has been read
+        }
+        __syncwarp();   // (and, without TMA, the warp's reads of the previous block are done)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            tc::st_shared_v4(rbase + ((uint32_t)(j ^ (lane & 7)) << 4), run[32 * c + 4 * j],
+                             run[32 * c + 4 * j + 1], run[32 * c + 4 * j + 2],
+                             run[32 * c + 4 * j + 3]);
+        if (p.tma_c) {
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::tma_store_3d(tmC, stage, n0 + 32 * c, row0, z);
+                tc::bulk_commit_group();
+            }
+            ++cc;
+            continue;
+        }
+        __syncwarp();
+        const int col = n0 + 32 * c + lane;
+        const uint32_t cofs = (uint32_t)((lane & 3) * 4);
+        const int rows = min(32, p.M - row0);
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r) {
+            float v;
+            asm volatile("ld.shared.f32 %0, [%1];"
+                         : "=f"(v)
+                         : "r"(stage + (uint32_t)r * 128u +
+                               ((uint32_t)((lane >> 2) ^ (r & 7)) << 4) + cofs)
+                         : "memory");
+            if (col < p.N) {
+                float *cp = p.C + (int64_t)z * p.strideC + (int64_t)(row0 + r) * p.ldc + col;
+                if (!(p.alpha == 1.f && p.beta == 0.f && p.bias == nullptr)) {
+                    const float old = p.beta != 0.f ? *cp : 0.f;
+                    const float b = p.bias != nullptr ? p.bias[col] : 0.f;
+                    v = fmaf(p.beta, old, p.alpha * v) + b;
+                }
+                *cp = v;
+            }
+        }
+    }
+}
+
+// One CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... (as the
+// persistent kernel); tile i's chunk c is the CTA's chunk gc = i * nchunks + c,
+// in accumulator gc % 2.  Barriers: a ring stage's j-th fill is waited on with
+// parity j & 1 and its (j-1)-th release with parity (j-1) & 1 (as in the
+// persistent kernel); accumulator s's u-th chunk ("chunk full", one
+// tcgen05.commit) with parity u & 1 and its (u-1)-th drain ("chunk free", one
+// arrival per epilogue warp) with parity (u-1) & 1.  Every wait is bounded
+// and the abort word stops all roles.  RAW as in the persistent kernel (no
+// converter warps: chunking applies to K > 256, where operands come from lo
+// planes).
+template <class CFG, int RAW>
+__global__ void __launch_bounds__(Chunked<CFG>::THREADS, 1)
+tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmAlo,
+                      const __grid_constant__ CUtensorMap tmBlo,
+                      const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
+    using P = Chunked<CFG>;
+    constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
+    constexpr int BN = CFG::BN;
+    constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
+    constexpr int NSLOT = P::NSLOT, KCB = P::KCB, COLS = P::COLS;
+    constexpr int TX_BYTES = PLANES * (A_TILE + B_TILE);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
+    const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t ring = tc::smem_u32_generic(smem);
+    const uint32_t staging = ring + STAGES * STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + P::STAGING);
+    const uint32_t full0 = tc::smem_u32_generic(bars);
+    const uint32_t empty0 = full0 + 8 * STAGES;
+    const uint32_t chf0 = empty0 + 8 * STAGES;     // chunk accumulator s holds a finished chunk
+    const uint32_t che0 = chf0 + 8 * NSLOT;        // chunk accumulator s has been drained
+    const uint32_t done_bar = che0 + 8 * NSLOT;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + P::BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.batch * p.tiles_m * p.tiles_n;
+    const int nlocal = ((int)blockIdx.x < total) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int kblocks = (p.K + BK - 1) / BK;
+    const int nchunks = (kblocks + KCB - 1) / KCB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < NSLOT; ++s) {
+            tc::mbar_init(chf0 + 8 * s, 1);
+            tc::mbar_init(che0 + 8 * s, P::EPI_WARPS);
+        }
+        tc::mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmA);
+        tc::tma_prefetch_desc(&tmB);
+        if constexpr ((RAW & 1) != 0) tc::tma_prefetch_desc(&tmAlo);
+        if constexpr ((RAW & 2) != 0) tc::tma_prefetch_desc(&tmBlo);
+    }
+    if (warp == 1) tc::tmem_alloc(tc::smem_u32_generic(tmem_slot), 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    // a programmatic dependent of the split kernel: no global access before
+    // its planes are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (the ring runs on across tiles)
+            long long issued = 0;
+            bool stop = false;
+            for (int i = 0; i < nlocal && !stop; ++i) {
+                int z, tm, tn;
+                raster(p, (int)blockIdx.x + i * (int)gridDim.x, z, tm, tn);
+                const int m0 = tm * BM, n0 = tn * BN;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const long long g = (long long)i * kblocks + kb;
+                    const int s = (int)(g % STAGES);
+                    const int j = (int)(g / STAGES);
+                    if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * s, (j & 1) ^ 1, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t st = ring + s * STAGE_BYTES;
+                    const uint32_t fb = full0 + 8 * s;
+                    tc::mbar_arrive_expect_tx(fb, TX_BYTES);
+                    const int k0 = kb * BK;
+                    if constexpr (RAW & 1) {
+                        tc::tma_load_3d(st, &tmA, fb, k0, m0, z);
+                        tc::tma_load_3d(st + A_TILE, &tmAlo, fb, k0, m0, z);
+                    } else {
+#pragma unroll
+                        for (int pl = 0; pl < PLANES; ++pl)
+                            tc::tma_load_3d(st + pl * A_TILE, &tmA, fb, k0, m0, PLANES * z + pl);
+                    }
+                    if constexpr (RAW & 2) {
+                        tc::tma_load_3d(st + PLANES * A_TILE, &tmB, fb, k0, n0, z);
+                        tc::tma_load_3d(st + PLANES * A_TILE + B_TILE, &tmBlo, fb, k0, n0, z);
+                    } else {
+#pragma unroll
+                        for (int pl = 0; pl < PLANES; ++pl)
+                            tc::tma_load_3d(st + PLANES * A_TILE + pl * B_TILE, &tmB, fb, k0, n0,
+                                            PLANES * z + pl);
+                    }
+                    issued = g + 1;
+                }
+            }
+            if (*abort_flag) {
+                // the latest fill of every stage lands before the CTA exits
+                for (long long g = (issued > STAGES ? issued - STAGES : 0); g < issued; ++g) {
+                    const int s = (int)(g % STAGES);
+                    const long long t0 = clock64();
+                    while (!tc::mbar_try_wait(full0 + 8 * s, (int)((g / STAGES) & 1)) &&
+                           clock64() - t0 < tc::kWaitLimitCycles) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = tc::tf32_idesc<BM, BN>();
+            bool stop = false;
+            long long gc = 0;   // the CTA's chunk counter
+            for (int i = 0; i < nlocal && !stop; ++i) {
+                for (int c = 0; c < nchunks; ++c, ++gc) {
+                    const int sl = (int)(gc % NSLOT);
+                    const long long u = gc / NSLOT;
+                    if (gc >= NSLOT && !tc::mbar_wait(che0 + 8 * sl, (int)((u - 1) & 1), abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t acc = tmem + (uint32_t)(sl * P::SLOT_COLS);
+                    const int kb0 = c * KCB;
+                    const int kb1 = min(kblocks, kb0 + KCB);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        const long long g = (long long)i * kblocks + kb;
+                        const int s = (int)(g % STAGES);
+                        if (!tc::mbar_wait(full0 + 8 * s, (int)((g / STAGES) & 1), abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t st = ring + s * STAGE_BYTES;
+                        const uint64_t ahi = tc::kmajor_desc<CFG::ROW_BYTES>(st);
+                        const uint64_t alo = tc::kmajor_desc<CFG::ROW_BYTES>(st + A_TILE);
+                        const uint64_t bhi = tc::kmajor_desc<CFG::ROW_BYTES>(st + 2 * A_TILE);
+                        const uint64_t blo =
+                            tc::kmajor_desc<CFG::ROW_BYTES>(st + 2 * A_TILE + B_TILE);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 8; ++kk) {
+                            const uint64_t step = (uint64_t)(kk * 32) >> 4;
+                            const uint32_t first = (kb == kb0 && kk == 0) ? 0u : 1u;
+                            if constexpr (P::SEP) {
+                                tc::mma_tf32(acc + BN, alo + step, bhi + step, idesc, first);
+                                tc::mma_tf32(acc + BN, ahi + step, blo + step, idesc, 1u);
+                                tc::mma_tf32(acc, ahi + step, bhi + step, idesc, first);
+                            } else {
+                                tc::mma_tf32(acc, alo + step, bhi + step, idesc, first);
+                                tc::mma_tf32(acc, ahi + step, blo + step, idesc, 1u);
+                                tc::mma_tf32(acc, ahi + step, bhi + step, idesc, 1u);
+                            }
+                        }
+                        tc::mma_commit(empty0 + 8 * s);
+                    }
+                    if (stop) break;
+                    tc::mma_commit(chf0 + 8 * sl);
+                }
+            }
+            tc::mma_commit(done_bar);   // tracks every MMA issued above, also on abort
+        }
+    } else {
+        // ---------------- epilogue warps 2-9: lane quarter warp % 4, column half
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const uint32_t stage = staging + (uint32_t)(warp - 2) * 4096u;
+        const uint32_t lane_off = ((uint32_t)(32 * q) << 16) + (uint32_t)(h * COLS);
+        int cc = 0;
+        long long gc = 0;
+        bool stop = false;
+        for (int i = 0; i < nlocal && !stop; ++i) {
+            float run[COLS];
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) run[j] = 0.f;
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int sl = (int)(gc % NSLOT);
+                const long long u = gc / NSLOT;
+                const bool ok = tc::mbar_wait(chf0 + 8 * sl, (int)(u & 1), abort_flag);
+                __syncwarp();
+                // one warp-uniform decision: the TMEM loads are warp-collective
+                if (!__all_sync(0xffffffffu, ok && !*abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t base = tmem + (uint32_t)(sl * P::SLOT_COLS) + lane_off;
+#pragma unroll
+                for (int b = 0; b < COLS / 16; ++b) {
+                    float v[16];
+                    tc::tmem_ld_16(base + 16 * b, v);
+                    if constexpr (P::SEP) {
+                        float w[16];
+                        tc::tmem_ld_16(base + BN + 16 * b, w);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] += w[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) run[16 * b + j] += v[j];
+                }
+                tc::fence_before_sync();   // the TMEM loads above precede the release
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(che0 + 8 * sl);
+            }
+            if (stop) break;
+            int z, tm, tn;
+            raster(p, (int)blockIdx.x + i * (int)gridDim.x, z, tm, tn);
+            store_running_rows<COLS>(p, &tmC, run, q, lane, z, tm * BM, tn * BN + h * COLS, stage,
+                                     cc);
+        }
+        if (lane == 0 && cc > 0) tc::bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+
+    tc::fence_before_sync();
+    __syncthreads();
+    // after every role has finished, so a wait that ran out late is reported too
+    if (*abort_flag && threadIdx.x == 0) atomicOr(&g_tf32x3_error, 1u);
+    if (warp == 1) {
+        // every MMA issued has completed before TMEM is freed
+        int local_abort = 0;
+        (void)tc::mbar_wait(done_bar, 0, &local_abort);
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -945,6 +1322,8 @@ cudaError_t launch_persistent_raw(const GemmArgs &a, bool transA, bool transB, v
 constexpr int kRawMaxK = 64;
 constexpr int kConvMaxK = 256;
 constexpr int kConvMaxReuse = 8;
+// Longer three-term reductions take the K-chunked kernel.
+constexpr int kChunkMinK = 256;
 
 // Launches with the runtime choice `conv` (a subset of RAW) of converted
 // operands; a combination the configuration does not provide launches
@@ -1022,6 +1401,65 @@ cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void 
     }
 }
 
+// The K-chunked kernel for three terms over K > kChunkMinK: one CTA per SM.
+// An operand stored K-contiguous with 16-byte aligned rows is loaded raw as
+// its own hi term with a lo-only plane from the split kernel; other operands
+// get hi and lo planes.
+template <class CFG, int RAW>
+cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void *ws,
+                               cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB) {
+    using P = Chunked<CFG>;
+    static PerContext<bool> configured;
+    cudaError_t e = ensure_smem(tf32x3_chunked_kernel<CFG, RAW>, P::SMEM_BYTES, configured);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmC, tmAlo, tmBlo;
+    Tf32x3Params p;
+    e = prepare<CFG>(a, transA, transB, RAW, 0, ws, s, tmA, tmB, tmAlo, tmBlo, tmC, p);
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
+    cfg.blockDim = dim3(P::THREADS);
+    cfg.dynamicSmemBytes = P::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tf32x3_chunked_kernel<CFG, RAW>, tmA, tmB, tmAlo, tmBlo, tmC, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <class CFG>
+cudaError_t launch_chunked(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+    static_assert(CFG::PLANES == 2, "three terms");
+    auto raw_ok = [&](const float *X, int64_t ld, int64_t sX, bool kcontig) {
+        return kcontig && reinterpret_cast<uintptr_t>(X) % 16 == 0 && ld % 4 == 0 &&
+               (a.batch == 1 || (sX > 0 && sX % 4 == 0));
+    };
+    CUtensorMap tmA, tmB;
+    int raw = 0;
+    if (raw_ok(a.A, a.lda, a.strideA, !transA) &&
+        make_raw_map<CFG>(&tmA, a.A, a.M, a.K, a.lda, a.strideA, a.batch, BM))
+        raw |= 1;
+    if (raw_ok(a.B, a.ldb, a.strideB, transB) &&
+        make_raw_map<CFG>(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, CFG::BN))
+        raw |= 2;
+    switch (raw) {
+        case 1: return launch_chunked_raw<CFG, 1>(a, transA, transB, ws, s, tmA, tmB);
+        case 2: return launch_chunked_raw<CFG, 2>(a, transA, transB, ws, s, tmA, tmB);
+        case 3: return launch_chunked_raw<CFG, 3>(a, transA, transB, ws, s, tmA, tmB);
+        default: return launch_chunked_raw<CFG, 0>(a, transA, transB, ws, s, tmA, tmB);
+    }
+}
+
 }  // namespace tf32x3
 
 // Tuned configurations (K slice, stages, terms, tile width) and accumulator
@@ -1065,10 +1503,15 @@ size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
     return tf32x3::plane_bytes(M, K, batch, 1) + tf32x3::plane_bytes(N, K, batch, 1);
 }
 
+// Three terms: reductions up to kChunkMinK run the single-pass persistent
+// kernel (128-wide tiles, converter warps where they pay); longer ones the
+// K-chunked kernel, whose sums are promoted to round-to-nearest fp32 adds
+// every 128 of K, on the tile width the wave count favours.
 cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
-    return tc_wide_tile(a, 3)
-               ? tf32x3::launch_persistent<Tf32x3Wide, 1>(a, transA, transB, ws, s)
-               : tf32x3::launch_persistent<Tf32x3Narrow, 2>(a, transA, transB, ws, s);
+    if (a.K <= tf32x3::kChunkMinK)
+        return tf32x3::launch_persistent<Tf32x3Narrow, 2>(a, transA, transB, ws, s);
+    return tc_wide_tile(a, 3) ? tf32x3::launch_chunked<Tf32x3Wide>(a, transA, transB, ws, s)
+                              : tf32x3::launch_chunked<Tf32x3Narrow>(a, transA, transB, ws, s);
 }
 
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {

@@ -443,3 +443,122 @@ def tensor_persistent(nlocal, kblocks, stages, acc_bufs, conv, seed):
 def test_tensor_persistent_pipeline(stages, acc_bufs, conv, nlocal, kblocks):
     for seed in range(4):
         tensor_persistent(nlocal, kblocks, stages, acc_bufs, conv, seed)
+
+
+# ------------------------------------------------------------ K-chunked tensor kernel
+
+def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
+    """tf32x3_chunked_kernel: the ring as in the persistent kernel; tile i's
+    chunk c (K blocks [c * kcb, min(kblocks, (c + 1) * kcb))) is the CTA's
+    chunk gc = i * nchunks + c, accumulated in chunk accumulator gc % nslot.
+    MMA: before chunk gc >= nslot waits "chunk free" of its accumulator
+    (parity (gc / nslot - 1) & 1), then per K block the "full" barrier, and
+    commits each stage to "empty" and the finished chunk to "chunk full".
+    Epilogue warps (8) wait "chunk full" (parity (gc / nslot) & 1), add the
+    chunk into their running sums and arrive on "chunk free"; after a tile's
+    last chunk they hold the tile's whole sum."""
+    rng = random.Random(seed)
+    nchunks = -(-kblocks // kcb)
+    full = [Barrier(1, f"full{s}") for s in range(stages)]
+    empty = [Barrier(1, f"empty{s}") for s in range(stages)]
+    chf = [Barrier(1, f"chunk_full{s}") for s in range(nslot)]
+    che = [Barrier(epi_warps, f"chunk_free{s}") for s in range(nslot)]
+    ring = [None] * stages
+    acc = [None] * nslot              # [chunk gc, K blocks accumulated]
+    in_flight, commits = [], []
+    sums = {}                         # (warp, tile) -> K blocks summed
+
+    def producer():
+        for i in range(nlocal):
+            for kb in range(kblocks):
+                g = i * kblocks + kb
+                s = g % stages
+                if g >= stages:
+                    while not empty[s].passed(g // stages - 1):
+                        yield
+                assert ring[s] is None or ring[s]["consumed"], "stage refilled before its MMAs completed"
+                ring[s] = {"g": g, "landed": False, "consumed": False}
+                in_flight.append(g)
+                yield
+
+    def mma():
+        gc = 0
+        for i in range(nlocal):
+            for c in range(nchunks):
+                sl, u = gc % nslot, gc // nslot
+                if gc >= nslot:
+                    while not che[sl].passed(u - 1):
+                        yield
+                assert acc[sl] is None, "MMAs into a chunk accumulator the epilogue has not drained"
+                acc[sl] = [gc, 0]
+                for kb in range(c * kcb, min(kblocks, (c + 1) * kcb)):
+                    g = i * kblocks + kb
+                    s = g % stages
+                    while not full[s].passed(g // stages):
+                        yield
+                    st = ring[s]
+                    assert st["g"] == g and st["landed"]
+                    acc[sl][1] += 1
+                    commits.append(("empty", s, g))
+                    yield
+                commits.append(("chf", sl, gc))
+                gc += 1
+
+    def epilogue(w):
+        gc = 0
+        for i in range(nlocal):
+            total = 0
+            for c in range(nchunks):
+                sl, u = gc % nslot, gc // nslot
+                while not chf[sl].passed(u):
+                    yield
+                want = min(kblocks, (c + 1) * kcb) - c * kcb
+                assert acc[sl] == [gc, want], f"epilogue read {acc[sl]} for chunk {gc}"
+                total += acc[sl][1]
+                if che[sl].pending == 1:
+                    acc[sl] = None   # the last warp's arrival frees the accumulator
+                che[sl].arrive()
+                gc += 1
+                yield
+            sums[(w, i)] = total
+
+    def engines():
+        while True:
+            r = rng.random()
+            if in_flight and r < 0.5:
+                g = in_flight.pop(rng.randrange(len(in_flight)))
+                ring[g % stages]["landed"] = True
+                full[g % stages].arrive()
+            elif commits:
+                kind, x, n = commits.pop(0)
+                if kind == "empty":
+                    ring[x]["consumed"] = True
+                    empty[x].arrive()
+                else:
+                    chf[x].arrive()
+            yield
+
+    roles = [producer(), mma()] + [epilogue(w) for w in range(epi_warps)]
+    eng = engines()
+    alive = list(roles)
+    steps = 0
+    while alive:
+        steps += 1
+        assert steps < 2000000, "no progress: the roles wait on one another"
+        if rng.random() < 0.3:
+            next(eng)
+            continue
+        i = rng.randrange(len(alive))
+        try:
+            next(alive[i])
+        except StopIteration:
+            alive.pop(i)
+    assert sums == {(w, i): kblocks for w in range(epi_warps) for i in range(nlocal)}
+    assert not in_flight and not commits
+
+
+@pytest.mark.parametrize("stages,kcb", [(4, 4), (3, 2)])   # the 256- and 128-wide tiles
+@pytest.mark.parametrize("nlocal,kblocks", [(2, 9), (3, 8), (1, 1), (4, 3), (2, 193)])
+def test_tensor_chunked_pipeline(stages, kcb, nlocal, kblocks):
+    for seed in range(4):
+        tensor_chunked(nlocal, kblocks, stages, kcb, seed)
