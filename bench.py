@@ -55,6 +55,12 @@ def parse():
     p.add_argument("--no-tf32x3", action="store_true", help="skip the tensor-core path report")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the per-workload table (every named workload, both FP32 paths)")
+    p.add_argument("--raster-group", type=int, default=0,
+                   help="tile rows per raster group for every call (sgemm_set_raster_group; "
+                        "0 = the library's 8): for L2 measurements of the block order")
+    p.add_argument("--plain-only", action="store_true",
+                   help="time only plain sgemm_f32 on the workload (W warm-up, K timed calls) and "
+                        "print one JSON object of that measurement, not the bench line")
     return p.parse_args()
 
 
@@ -166,6 +172,7 @@ KERNEL_SOURCES = {
     "sgemm_simt_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh", "simt_launch.cuh",
                           "simt_nn.cu"],
     "tf32x3_persistent_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
+    "tf32x3_chunked_kernel": ["gemm_args.h", "tc_utils.cuh", "tf32x3.cu"],
     "sgemm_simt_streamk_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh",
                                   "simt_launch.cuh", "simt_tn.cu"],
     "sgemm_simt_streamk_tma_kernel": ["gemm_args.h", "device_utils.cuh", "simt_sgemm.cuh",
@@ -245,12 +252,24 @@ def tc_plan(M, N, K, batch, transA, transB, aligned=True):
                 split.append(f"{name} lo plane")
         else:
             split.append(f"{name} hi/lo planes")
-    gemm = ("tf32x3_persistent_kernel (one CTA per SM; 128x256 or 128x128 tiles by wave count; "
-            "TMA ring, tcgen05 kind::tf32, TMEM, TMA-store epilogue" +
-            ("; " + ", ".join(parts) if parts else "") + ")")
+    if K <= 256:
+        gemm = ("tf32x3_persistent_kernel (one CTA per SM; 128x128 tiles; TMA ring, tcgen05 "
+                "kind::tf32, TMEM, TMA-store epilogue" +
+                ("; " + ", ".join(parts) if parts else "") + ")")
+    else:
+        gemm = ("tf32x3_chunked_kernel (one CTA per SM; 128x256 or 128x128 tiles by wave count; "
+                "TMA ring, tcgen05 kind::tf32 into two TMEM chunk accumulators, each 128 of K "
+                "added into fp32 registers by 8 epilogue warps, TMA-store epilogue" +
+                ("; " + ", ".join(parts) if parts else "") + ")")
     if split:
         return f"split_kernel ({', '.join(split)}) + {gemm}", 2
     return gemm, 1
+
+
+def tc_kernel_name(K: int) -> str:
+    """The 3xTF32 GEMM kernel csrc/tf32x3.cu runs for reduction depth K: the
+    single-pass persistent kernel up to K = 256, the K-chunked one beyond."""
+    return "tf32x3_persistent_kernel" if K <= 256 else "tf32x3_chunked_kernel"
 
 
 def workload_table(torch, sg, dev, stream, sp, reps=5):
@@ -520,6 +539,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
+    if args.raster_group:
+        sg.set_raster_group(args.raster_group)
     w = workloads.get(args.workload)
     case = workloads.make_case(w)
     M, N, K, batch = w.M, w.N, w.K, w.batch
@@ -567,6 +588,29 @@ def main():
             sg.sgemm_f32_strided_batched(M, N, K, dA.data_ptr(), lda, case["A"][0].size,
                                          dB.data_ptr(), ldb, case["B"][0].size, dC.data_ptr(),
                                          ldc, M * ldc, batch, w.transA, w.transB, sp)
+
+    if args.plain_only:
+        # one kernel family, nothing else launched: the form the L2 / raster
+        # captures of profiles/ use
+        for i in range(args.warmup):
+            plain_step(i)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            plain_step(i)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ts = sorted(a.elapsed_time(b) for a, b in ev)
+        ms = ts[len(ts) // 2]
+        if rank == 0:
+            print(json.dumps({"mode": "plain_only", "entry": "sgemm_f32", "workload": args.workload,
+                              "raster_group": args.raster_group or 8, "steps": args.steps,
+                              "median_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                              "kernel": simt_kernel_label(M, N, batch, w.transB, sms_dev, K,
+                                                          w.transA)}))
+        return
 
     def step(i):
         if batch != 1:
@@ -732,7 +776,8 @@ def main():
             "pct_of_fp32_peak_at_max_clock": None,
             "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_probe,
                          "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_probe,
-                         "traffic": profiled_traffic("tf32x3_persistent_kernel", args.workload),
+                         "traffic": profiled_traffic(tc_kernel_name(K), args.workload),
+                         "traffic_kernel": tc_kernel_name(K),
                          "peak_source": "measured in this run: the library's TF32 tensor-pipe "
                                         "probe (sgemm_probe_tf32_mma: back-to-back "
                                         "tcgen05.mma.kind::tf32 M128 N256 K8 from shared memory, "
@@ -854,6 +899,7 @@ def main():
                    "l2": f"{nsets} rotating input sets of {workloads.min_bytes(M, N, K, batch) / 1e6:.0f} MB "
                          f"(> 129 MB L2 together); each step starts with its operands evicted",
                    "entry": "sgemm_f32_streamk" if batch == 1 else "sgemm_f32_strided_batched",
+                   "raster_group": args.raster_group or 8,
                    "workspace_bytes": sk_need,
                    "kernels_per_step": launches,
                    "kernel": step_kernel_label(M, N, K, w.transA, w.transB, sms_dev, batch,

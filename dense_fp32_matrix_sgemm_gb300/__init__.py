@@ -26,7 +26,7 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
            "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex", "selftest_wait_timeout",
            "sgemm_f32_streamk", "streamk_workspace_size",
-           "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex"]
+           "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex", "set_raster_group"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -85,6 +85,7 @@ SIGNATURES = {
     "sgemm_probe_out_elems": (_i64, []),
     "sgemm_probe_tf32_mma": (_int, [_i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_selftest_wait_timeout": (_int, [_i64, _vp]),
+    "sgemm_set_raster_group": (_int, [_int]),
 }
 
 
@@ -307,6 +308,15 @@ def probe_tf32_mma(iterations: int, out_ptr: int, stream=0) -> float:
 
 def probe_out_elems() -> int:
     return load_library().sgemm_probe_out_elems()
+
+
+def set_raster_group(group_m: int) -> int:
+    """Tile rows per raster group for later calls (0 restores the library's 8);
+    returns the previous value (see include/sgemm_gb300_probe.h)."""
+    prev = load_library().sgemm_set_raster_group(group_m)
+    if prev < 0:
+        raise ValueError(f"group_m={group_m}: must be 0 .. 65536")
+    return prev
 
 
 def selftest_wait_timeout(limit_cycles: int = 10_000_000, stream=0) -> int:

@@ -199,7 +199,7 @@ int validate(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int64
     a.batch = (int)batch;
     a.tiles_m = (int)tiles_m;
     a.tiles_n = (int)tiles_n;
-    a.group_m = 8;
+    a.group_m = raster_group();
     a.kchunk = 0;
     a.alpha = 1.f;
     a.beta = 0.f;

@@ -150,6 +150,10 @@ cudaError_t launch_gemv(const GemmArgs &a, bool transA, bool transB, cudaStream_
 // product term vanishes (K == 0 or alpha == 0); zeros for the plain epilogue.
 cudaError_t launch_epilogue_only(const GemmArgs &a, cudaStream_t s);
 
+// Tile rows per raster group for the launches that follow (the library's
+// choice is 8; sgemm_set_raster_group changes it for measurements).
+int raster_group();
+
 // Smallest block tile of any kernel: bounds the grid size during validation.
 constexpr int kSimtTileM = 128;
 constexpr int kSimtTileN = 128;

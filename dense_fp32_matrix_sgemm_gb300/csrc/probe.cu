@@ -1,5 +1,7 @@
 // Peak probes: FP32 FMA throughput (the measured denominator of "% of FP32
-// peak") and the TF32 tensor-pipe throughput of tcgen05.mma.
+// peak") and the TF32 tensor-pipe throughput of tcgen05.mma; the raster-group
+// knob that the L2 measurements of the block order use.
+#include <atomic>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -48,8 +50,18 @@ int64_t probe_ctas() {
     return (int64_t)sms * kCtasPerSm;
 }
 
+std::atomic<int> g_raster_group{8};
+
 }  // namespace
+
+int raster_group() { return g_raster_group.load(std::memory_order_relaxed); }
+
 }  // namespace sgemm
+
+extern "C" int sgemm_set_raster_group(int group_m) {
+    if (group_m < 0 || group_m > 65536) return -1;
+    return sgemm::g_raster_group.exchange(group_m == 0 ? 8 : group_m);
+}
 
 extern "C" int64_t sgemm_probe_out_elems(void) { return sgemm::probe_ctas() * sgemm::kThreads; }
 

@@ -66,7 +66,8 @@ constexpr int kPersistMaxSlices = 8;   // K <= 256: the persistent form (see bel
 template <int BK, int STAGES, int BN_>
 constexpr int tma_smem_bytes() {
     // 1 KB to align the ring to the 1024-byte swizzle atom, the operand ring,
-    // then STAGES "full" and STAGES "empty" mbarriers and the CTA's abort word
+    // then STAGES "full" and STAGES "empty" mbarriers, the CTA's abort word and
+    // the issuing thread's slice count
     return 1024 + STAGES * BK * (BM + BN_) * (int)sizeof(float) + 16 * STAGES + 16;
 }
 
@@ -90,11 +91,18 @@ __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * s, 1);
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * (STAGES + s), THREADS / 32);
-        *abort = 0;
+        abort[0] = 0;
+        abort[1] = 0;   // slices issued (see issued_word)
         tc::fence_barrier_init();
     }
     __syncthreads();
     return full0;
+}
+
+// The issuing thread's count of slices whose copies it started (the word
+// after the abort word).
+__device__ __forceinline__ volatile uint32_t &issued_word(volatile int *abort) {
+    return *reinterpret_cast<volatile uint32_t *>(abort + 1);
 }
 
 // One K slice of the tile from a landed stage (A part `at`, B part `bt`):
@@ -211,16 +219,17 @@ __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int 
 // g - STAGES from the same stage; each warp releases a slice once its lanes
 // have read it.  On return no copy of this piece is in flight (every issued
 // slice has been waited on), and the next piece may start at once.
-// `issued` (thread 0's count) is one past the last slice whose copies were
-// started: once the abort word is set nothing more is issued, so a stage
-// never gets a second fill in one phase and finish_abort knows exactly which
-// copies can still be in flight.
+// The issuing thread records one past the last slice whose copies it started
+// in the word after the abort word (issued_word): once the abort word is set
+// nothing more is issued, so a stage never gets a second fill in one phase
+// and finish_abort knows exactly which copies can still be in flight.  The
+// count lives in shared memory, not in a register held across the loop.
 template <int BK, int STAGES, int BN_, bool KA, bool KB>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
-                                             uint32_t &issued, int m0, int n0, int z, int kbeg,
-                                             int ktiles, int a_col, int b_col,
-                                             float (&acc)[8][BN_ / 16], volatile int *abort) {
+                                             int m0, int n0, int z, int kbeg, int ktiles,
+                                             int a_col, int b_col, float (&acc)[8][BN_ / 16],
+                                             volatile int *abort) {
     constexpr int TN = BN_ / 16;
     constexpr int ATILE = BK * BM;
     constexpr int BTILE = BK * BN_;
@@ -238,11 +247,10 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
         const uint32_t st = g % STAGES;
         // slice g - STAGES released by every warp; a warp whose wait ran out
         // releases a stage whose copy may not have landed, so the abort word
-        // is read again after the release (the warps set it before arriving)
-        if (*abort) return;
+        // is read after the release (the warps set it before arriving)
         if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * st, ((g / STAGES) - 1) & 1, abort)) return;
         if (*abort) return;
-        issued = g + 1;
+        issued_word(abort) = g + 1;
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         if constexpr (KA)   // box (k, m): 32 k x 128 rows
@@ -279,9 +287,10 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
 // memory after the CTA has exited.  Does nothing in a run whose waits all
 // completed.
 template <int STAGES>
-__device__ __forceinline__ void finish_abort(uint32_t full0, uint32_t n, volatile int *abort,
+__device__ __forceinline__ void finish_abort(uint32_t full0, volatile int *abort,
                                              unsigned int *status) {
     if (threadIdx.x != 0 || !*abort) return;
+    const uint32_t n = issued_word(abort);
     if (status != nullptr) atomicOr(status, 1u);
     for (uint32_t g = n > STAGES ? n - STAGES : 0; g < n; ++g) {
         const long long t0 = clock64();
@@ -374,11 +383,10 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     int a_col, b_col;
     thread_coords(a_col, b_col);
     float acc[8][BN_ / 16];
-    uint32_t gk = 0, issued = 0;
-    tma_mainloop<BK, STAGES, BN_, KA, KB>(&tmA, &tmB, As, Bs, full0, gk, issued, tm * BM,
-                                          tn * BN_, z, 0, (p.K + BK - 1) / BK, a_col, b_col, acc,
-                                          abort);
-    finish_abort<STAGES>(full0, issued, abort, status);
+    uint32_t gk = 0;
+    tma_mainloop<BK, STAGES, BN_, KA, KB>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
+                                          (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
+    finish_abort<STAGES>(full0, abort, status);
     store_tile<BN_, KA, KB>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
 
@@ -418,18 +426,16 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     const int ktiles = (p.K + BK - 1) / BK;
     const int total = mine * ktiles;   // slices of this CTA
     const bool issuer = threadIdx.x == 0;
-    uint32_t issued = 0;   // thread 0: one past the last slice issued (see tma_mainloop)
     auto issue = [&](int g) {
         const int i = g / ktiles, j = g - i * ktiles;
         int z, tm, tn;
         raster(p, c + i * G, z, tm, tn);
         const uint32_t st = (uint32_t)g % STAGES;
         // as in tma_mainloop: no new copy once the abort word is set
-        if (*abort) return;
         if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * st, ((uint32_t)g / STAGES - 1) & 1, abort))
             return;
         if (*abort) return;
-        issued = (uint32_t)g + 1;
+        issued_word(abort) = (uint32_t)g + 1;
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         if constexpr (KA)
@@ -461,7 +467,7 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         raster(p, c + i * G, z, tm, tn);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
     }
-    finish_abort<STAGES>(full0, issued, abort, status);
+    finish_abort<STAGES>(full0, abort, status);
 }
 
 // The stream-K schedule (see StreamK) as one grid of tiles_dp + G CTAs:
@@ -492,16 +498,15 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     pdl_trigger();
     int a_col, b_col;
     thread_coords(a_col, b_col);
-    uint32_t gk = 0, issued = 0;
+    uint32_t gk = 0;
     const int b = blockIdx.x;
     if (b < sk.tiles_dp) {
         int z, tm, tn;
         raster(p, b, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, issued, tm * BM,
-                                                 tn * BN_, z, 0, sk.kslices, a_col, b_col, acc,
-                                                 abort);
-        finish_abort<STAGES>(full0, issued, abort, status);
+        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
+                                                 z, 0, sk.kslices, a_col, b_col, acc, abort);
+        finish_abort<STAGES>(full0, abort, status);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         return;
     }
@@ -510,8 +515,10 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     // tiles_sk < G, so a range is at most kslices units long: at most two pieces
     const int nsk = u0 == u1 ? 0 : (u0 / sk.kslices == (u1 - 1) / sk.kslices ? 1 : 2);
 #pragma unroll 1
+    // After a wait of the first piece ran out, the second piece issues no copy
+    // (tma_mainloop issues nothing once the abort word is set) and its waits
+    // return at once; skipping it explicitly cost registers in the main loop.
     for (int k = 0; k < nsk; ++k) {   // 0: the range's first piece, 1: its last
-        if (*abort) break;            // a wait of the first piece ran out
         const int64_t ub = k == 0 ? u0 : (u0 / sk.kslices + 1) * sk.kslices;
         const int tl = (int)(ub / sk.kslices);
         const int s0 = (int)(ub - (int64_t)tl * sk.kslices);
@@ -519,9 +526,8 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, issued, tm * BM,
-                                                 tn * BN_, z, s0 * BK, s1 - s0, a_col, b_col, acc,
-                                                 abort);
+        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
+                                                 z, s0 * BK, s1 - s0, a_col, b_col, acc, abort);
         if (!(s0 == 0 && s1 == sk.kslices)) {
             // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
             float *part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);
@@ -538,7 +544,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         }
     }
-    finish_abort<STAGES>(full0, issued, abort, status);
+    finish_abort<STAGES>(full0, abort, status);
 }
 
 namespace {

@@ -1230,7 +1230,7 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int co
     p.batch = a.batch;
     p.tiles_m = (a.M + BM - 1) / BM;
     p.tiles_n = (a.N + CFG::BN - 1) / CFG::BN;
-    p.group_m = 8;
+    p.group_m = a.group_m;
     p.vec_c = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && a.ldc % 4 == 0 && a.strideC % 4 == 0;
     p.alpha = a.alpha;
     p.beta = a.beta;

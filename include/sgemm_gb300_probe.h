@@ -61,6 +61,22 @@ int64_t sgemm_probe_out_elems(void);
 int sgemm_probe_tf32_mma(int64_t iterations, float *out, double *flops_out, void *stream);
 
 /*
+ * Measurement knob for the block raster ("CUDA GEMM operator performance
+ * optimization", section 2.3: the order in which output tiles are scheduled
+ * decides how often L2 re-serves operand panels).  Every kernel walks its
+ * 128-row tiles in groups of `group_m` tile rows, sweeping each group down a
+ * column of tiles before moving right; the library's choice is 8.  This sets
+ * group_m for the calls made after it on any thread (1 = row-major order,
+ * a value at least the tile-row count = column-major order), 0 restores 8.
+ * Results are bit-identical for every value: only the order in which tiles
+ * run changes, never the arithmetic of an output.  It exists to measure the
+ * L2 hit rate against the order; calls already enqueued are not affected.
+ * Returns the previous value, or -1 (nothing changed) if group_m is outside
+ * 0 .. 65536.
+ */
+int sgemm_set_raster_group(int group_m);
+
+/*
  * Self-test of the library's failure path (no counterpart on the source
  * pages): launches one CTA that waits, with the bounded wait of the tensor-core
  * pipeline, on a barrier nothing ever arrives on.  After about `limit_cycles`

@@ -139,3 +139,12 @@ def test_probe_arguments_rejected_on_host(lib):
     fma = lib.sgemm_probe_fp32_fma
     assert fma(2, 10, ctypes.c_void_p(FAKE), ctypes.byref(flops), None) == 1
     assert fma(1, 0, ctypes.c_void_p(FAKE), ctypes.byref(flops), None) == 1
+
+
+def test_raster_group_knob(lib):
+    # returns the previous value; 0 restores the library's 8; out of range changes nothing
+    assert sg.set_raster_group(3) == 8
+    assert sg.set_raster_group(0) == 3
+    assert lib.sgemm_set_raster_group(-1) == -1
+    assert lib.sgemm_set_raster_group(65537) == -1
+    assert sg.set_raster_group(0) == 8

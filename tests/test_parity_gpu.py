@@ -1100,3 +1100,22 @@ def test_matmul_convenience_uses_streamk():
     torch.cuda.synchronize()
     assert torch.equal(out, direct)
     check_full(case, out.cpu().numpy()[None], label="matmul streamk")
+
+
+# The raster-group knob (sgemm_set_raster_group) changes only the order in
+# which tiles run, never an output's arithmetic: bit-identical results on the
+# SIMT tile kernel, the cp.async kernel (row-major A with B^T) and the tensor
+# path, for row-major, grouped and column-major orders.
+@pytest.mark.parametrize("entry_name", ["sgemm_f32", "sgemm_f32_tf32x3"])
+@pytest.mark.parametrize("tB", [0, 1])
+def test_raster_group_changes_no_bits(entry_name, tB):
+    case = workloads.make_operands(1500, 1300, 700, transB=tB, dist="normal", seed=95,
+                                   key=950 + tB)
+    try:
+        ref = run(case, entry=entry_name)
+        for g in (1, 3, 64):
+            sg.set_raster_group(g)
+            assert np.array_equal(run(case, entry=entry_name), ref), f"group_m={g}"
+    finally:
+        sg.set_raster_group(0)
+    check_full(case, ref, label=f"raster {entry_name} tB={tB}")

@@ -215,9 +215,9 @@ def simt_tma_abort(pieces, stages, warps, seed, abort_step):
     """tma_mainloop with the abort path: at step `abort_step` some wait runs
     out and sets the CTA's abort word.  From then on every wait returns at
     once (a warp whose "full" wait gave up still releases the stage), thread 0
-    issues nothing more (it reads the abort word before the "empty" wait and
-    again after it), and finish_abort waits for the last `stages` slices it
-    issued.  Checks that no stage ever gets a second fill while its previous
+    issues nothing more (it reads the abort word after the "empty" wait, which
+    itself gives up once the word is set), and finish_abort waits for the last
+    `stages` slices it issued.  Checks that no stage ever gets a second fill while its previous
     copy is in flight, and that no copy is in flight when the CTA exits."""
     rng = random.Random(seed)
     full = [Barrier(1, f"full{s}") for s in range(stages)]
@@ -238,8 +238,6 @@ def simt_tma_abort(pieces, stages, warps, seed, abort_step):
 
     def issue(g):
         s = g % stages
-        if state["abort"]:
-            return
         if g >= stages:
             ok = yield from wait(empty[s], g // stages - 1)
             if not ok:
