@@ -58,6 +58,12 @@ def parse():
     p.add_argument("--raster-group", type=int, default=0,
                    help="tile rows per raster group for every call (sgemm_set_raster_group; "
                         "0 = the library's 8): for L2 measurements of the block order")
+    p.add_argument("--tf32x3-chunk-k", type=int, default=0,
+                   help="K per chunk of the 3xTF32 K-chunked kernel for every call "
+                        "(sgemm_set_tf32x3_chunk_k; 0 = the library's 128)")
+    p.add_argument("--tc-only", action="store_true",
+                   help="time only sgemm_f32_tf32x3 on the workload (W warm-up, K timed calls) "
+                        "and print one JSON object with its RRMSE against the oracle")
     p.add_argument("--plain-only", action="store_true",
                    help="time only plain sgemm_f32 on the workload (W warm-up, K timed calls) and "
                         "print one JSON object of that measurement, not the bench line")
@@ -541,6 +547,8 @@ def main():
 
     if args.raster_group:
         sg.set_raster_group(args.raster_group)
+    if args.tf32x3_chunk_k:
+        sg.set_tf32x3_chunk_k(args.tf32x3_chunk_k)
     w = workloads.get(args.workload)
     case = workloads.make_case(w)
     M, N, K, batch = w.M, w.N, w.K, w.batch
@@ -588,6 +596,43 @@ def main():
             sg.sgemm_f32_strided_batched(M, N, K, dA.data_ptr(), lda, case["A"][0].size,
                                          dB.data_ptr(), ldb, case["B"][0].size, dC.data_ptr(),
                                          ldc, M * ldc, batch, w.transA, w.transB, sp)
+
+    if args.tc_only:
+        need = sg.tf32x3_workspace_size(M, N, K, batch)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+        def tc_call(i):
+            dA, dB, dC = sets[i % nsets]
+            sg.sgemm_f32_tf32x3_strided_batched(
+                M, N, K, dA.data_ptr(), lda, case["A"][0].size, dB.data_ptr(), ldb,
+                case["B"][0].size, dC.data_ptr(), ldc, M * ldc, batch, w.transA, w.transB,
+                ws.data_ptr(), need, sp)
+        for i in range(args.warmup):
+            tc_call(i)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            tc_call(i)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ts = sorted(a.elapsed_time(b) for a, b in ev)
+        ms = ts[len(ts) // 2]
+        out = {"mode": "tc_only", "entry": "sgemm_f32_tf32x3", "workload": args.workload,
+               "chunk_k": args.tf32x3_chunk_k or 128, "steps": args.steps, "median_ms": ms,
+               "tflops": flops / (ms * 1e-3) / 1e12}
+        if rank == 0 and batch == 1 and not w.transA:
+            import oracle
+            dC = sets[(args.steps - 1) % nsets][2]
+            rows = np.arange(0, M, max(1, M // 256))
+            got = dC.view(M, ldc)[rows, :N].cpu().numpy()
+            ref = oracle.sgemm(np.ascontiguousarray(case["A"][0][rows]), case["B"][0], len(rows),
+                               N, K, lda=lda, ldb=ldb)
+            out["rrmse_vs_oracle_256_rows"] = oracle.rrmse(got, ref)
+        if rank == 0:
+            print(json.dumps(out))
+        return
 
     if args.plain_only:
         # one kernel family, nothing else launched: the form the L2 / raster

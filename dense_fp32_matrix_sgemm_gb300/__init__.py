@@ -26,7 +26,8 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "sgemm_f32_tf32_strided_batched", "tf32_workspace_size", "sgemm_f32_splitk",
            "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex", "selftest_wait_timeout",
            "sgemm_f32_streamk", "streamk_workspace_size",
-           "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex", "set_raster_group"]
+           "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex", "set_raster_group",
+           "set_tf32x3_chunk_k"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -86,6 +87,7 @@ SIGNATURES = {
     "sgemm_probe_tf32_mma": (_int, [_i64, _vp, ctypes.POINTER(ctypes.c_double), _vp]),
     "sgemm_selftest_wait_timeout": (_int, [_i64, _vp]),
     "sgemm_set_raster_group": (_int, [_int]),
+    "sgemm_set_tf32x3_chunk_k": (_int, [_int]),
 }
 
 
@@ -316,6 +318,16 @@ def set_raster_group(group_m: int) -> int:
     prev = load_library().sgemm_set_raster_group(group_m)
     if prev < 0:
         raise ValueError(f"group_m={group_m}: must be 0 .. 65536")
+    return prev
+
+
+def set_tf32x3_chunk_k(chunk_k: int) -> int:
+    """K per chunk of the three-term product over K > 256 for later calls (0
+    restores the library's 128); returns the previous value (see
+    include/sgemm_gb300_probe.h)."""
+    prev = load_library().sgemm_set_tf32x3_chunk_k(chunk_k)
+    if prev < 0:
+        raise ValueError(f"chunk_k={chunk_k}: must be 0 or a multiple of 32 from 32 to 2^30")
     return prev
 
 

@@ -154,6 +154,11 @@ cudaError_t launch_epilogue_only(const GemmArgs &a, cudaStream_t s);
 // choice is 8; sgemm_set_raster_group changes it for measurements).
 int raster_group();
 
+// K per chunk of the K-chunked three-term kernel for the launches that follow
+// (0: the library's 128; else a multiple of 32); returns the previous value,
+// or -1 when chunk_k is not allowed (sgemm_set_tf32x3_chunk_k).
+int set_tf32x3_chunk_k(int chunk_k);
+
 // Smallest block tile of any kernel: bounds the grid size during validation.
 constexpr int kSimtTileM = 128;
 constexpr int kSimtTileN = 128;

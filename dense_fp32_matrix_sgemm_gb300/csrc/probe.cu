@@ -1,6 +1,7 @@
 // Peak probes: FP32 FMA throughput (the measured denominator of "% of FP32
 // peak") and the TF32 tensor-pipe throughput of tcgen05.mma; the raster-group
-// knob that the L2 measurements of the block order use.
+// and chunk-length knobs that measurements of the block order's L2 reuse and
+// of the K-chunked kernel's accuracy use.
 #include <atomic>
 #include <cstdint>
 
@@ -62,6 +63,8 @@ extern "C" int sgemm_set_raster_group(int group_m) {
     if (group_m < 0 || group_m > 65536) return -1;
     return sgemm::g_raster_group.exchange(group_m == 0 ? 8 : group_m);
 }
+
+extern "C" int sgemm_set_tf32x3_chunk_k(int chunk_k) { return sgemm::set_tf32x3_chunk_k(chunk_k); }
 
 extern "C" int64_t sgemm_probe_out_elems(void) { return sgemm::probe_ctas() * sgemm::kThreads; }
 

@@ -67,8 +67,9 @@ template <int BK, int STAGES, int BN_>
 constexpr int tma_smem_bytes() {
     // 1 KB to align the ring to the 1024-byte swizzle atom, the operand ring,
     // then STAGES "full" and STAGES "empty" mbarriers, the CTA's abort word and
-    // the issuing thread's slice count
-    return 1024 + STAGES * BK * (BM + BN_) * (int)sizeof(float) + 16 * STAGES + 16;
+    // the slice last issued into each stage
+    return 1024 + STAGES * BK * (BM + BN_) * (int)sizeof(float) + 16 * STAGES +
+           (4 + 4 * STAGES + 15) / 16 * 16;
 }
 
 // The operand ring starts at the first 1024-byte boundary of the dynamic
@@ -92,17 +93,17 @@ __device__ __forceinline__ uint32_t tma_pipeline_init(float *smem, volatile int 
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * s, 1);
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(full0 + 8 * (STAGES + s), THREADS / 32);
         abort[0] = 0;
-        abort[1] = 0;   // slices issued (see issued_word)
+        for (int s = 0; s < STAGES; ++s) abort[1 + s] = -1;   // nothing issued (last_issued)
         tc::fence_barrier_init();
     }
     __syncthreads();
     return full0;
 }
 
-// The issuing thread's count of slices whose copies it started (the word
-// after the abort word).
-__device__ __forceinline__ volatile uint32_t &issued_word(volatile int *abort) {
-    return *reinterpret_cast<volatile uint32_t *>(abort + 1);
+// The slice whose copies the issuing thread last started into stage `st`
+// (the words after the abort word; 0xffffffff: none yet).
+__device__ __forceinline__ volatile uint32_t &last_issued(volatile int *abort, uint32_t st) {
+    return *reinterpret_cast<volatile uint32_t *>(abort + 1 + st);
 }
 
 // One K slice of the tile from a landed stage (A part `at`, B part `bt`):
@@ -219,12 +220,25 @@ __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int 
 // g - STAGES from the same stage; each warp releases a slice once its lanes
 // have read it.  On return no copy of this piece is in flight (every issued
 // slice has been waited on), and the next piece may start at once.
-// The issuing thread records one past the last slice whose copies it started
-// in the word after the abort word (issued_word): once the abort word is set
-// nothing more is issued, so a stage never gets a second fill in one phase
-// and finish_abort knows exactly which copies can still be in flight.  The
-// count lives in shared memory, not in a register held across the loop.
-template <int BK, int STAGES, int BN_, bool KA, bool KB>
+// The issuing thread records the slice it last started into each stage in
+// the words after the abort word (last_issued), so finish_abort knows which
+// copies can still be in flight.  A stage is refilled only after all eight
+// warps released it, and a warp does not release it once the abort word is
+// set (a wait that gave up sets the word before the warp gets to its release,
+// so every release in an aborted run follows a copy that landed), so a stage
+// never gets a second
+// fill in one phase, also after an abort; after an abort a slice may be
+// skipped while a later one whose stage was already released still goes out,
+// hence a record per stage.  The records live in shared memory, not in
+// registers held across the loop.
+// GUARD_FLAG picks how a warp decides to skip its release after an abort:
+// by reading the abort word at the release (true) or by keeping its own wait's
+// result (false).  Both are exact; they differ only in the registers the
+// compiler gives the loop, and each kernel takes the one it runs faster with
+// (3072^3, CUDA events: stream-K kernel 66.7 TFLOP/s by the word, 66.1 by the
+// flag; row-major A 60.3 by the flag, 59.1 by the word; A^T by B 65.5 by the
+// word, 64.2 by the flag).
+template <int BK, int STAGES, int BN_, bool KA, bool KB, bool GUARD_FLAG>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
                                              int m0, int n0, int z, int kbeg, int ktiles,
@@ -245,12 +259,12 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
     auto issue = [&](int slice) {
         const uint32_t g = g0 + (uint32_t)slice;
         const uint32_t st = g % STAGES;
-        // slice g - STAGES released by every warp; a warp whose wait ran out
-        // releases a stage whose copy may not have landed, so the abort word
-        // is read after the release (the warps set it before arriving)
+        // slice g - STAGES released by every warp.  No warp releases a stage
+        // after the abort word is set, so a completed release means the
+        // stage holds no copy in flight; once the word is set the wait gives
+        // up instead of waiting for releases that will not come.
         if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * st, ((g / STAGES) - 1) & 1, abort)) return;
-        if (*abort) return;
-        issued_word(abort) = g + 1;
+        last_issued(abort, st) = g;
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         if constexpr (KA)   // box (k, m): 32 k x 128 rows
@@ -269,32 +283,35 @@ __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUten
     }
     for (int kt = 0; kt < ktiles; ++kt) {
         const uint32_t rs = gk % STAGES;
-        (void)tc::mbar_wait(full0 + 8 * rs, (gk / STAGES) & 1, abort);
+        const bool landed = tc::mbar_wait(full0 + 8 * rs, (gk / STAGES) & 1, abort);
         ++gk;
         slice_fma<BK, BN_, KA, KB>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
-        // the warp's lanes have all read the stage: release it
+        // the warp's lanes have all read the stage: release it, unless the
+        // abort word is set (a wait that gave up sets it first, and its copy
+        // may still be in flight)
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
+        if ((threadIdx.x & 31) == 0 && (GUARD_FLAG ? landed : !*abort))
+            tc::mbar_arrive(empty0 + 8 * rs);
         if (issuer && kt + STAGES - 1 < ktiles) issue(kt + STAGES - 1);
     }
 }
 
 // After a wait ran out (the abort word is set; every later wait returned at
-// once, and no slice was issued after it), thread 0 raises bit 0 of the
-// status word and waits, with a limit, for the copies of the last STAGES
-// slices it issued (the CTA's slices [n - STAGES, n), n = its issued count:
-// the latest fill of each stage) to land, so that none writes into shared
+// once, and no stage was refilled unless its last copy had landed), thread 0
+// raises bit 0 of the status word and waits, with a limit, for the latest
+// copy it issued into each stage to land, so that none writes into shared
 // memory after the CTA has exited.  Does nothing in a run whose waits all
 // completed.
 template <int STAGES>
 __device__ __forceinline__ void finish_abort(uint32_t full0, volatile int *abort,
                                              unsigned int *status) {
     if (threadIdx.x != 0 || !*abort) return;
-    const uint32_t n = issued_word(abort);
     if (status != nullptr) atomicOr(status, 1u);
-    for (uint32_t g = n > STAGES ? n - STAGES : 0; g < n; ++g) {
+    for (uint32_t st = 0; st < STAGES; ++st) {
+        const uint32_t g = last_issued(abort, st);
+        if (g == 0xffffffffu) continue;
         const long long t0 = clock64();
-        while (!tc::mbar_try_wait(full0 + 8 * (g % STAGES), (g / STAGES) & 1) &&
+        while (!tc::mbar_try_wait(full0 + 8 * st, (g / STAGES) & 1) &&
                clock64() - t0 < tc::kWaitLimitCycles) {
         }
     }
@@ -384,8 +401,8 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     thread_coords(a_col, b_col);
     float acc[8][BN_ / 16];
     uint32_t gk = 0;
-    tma_mainloop<BK, STAGES, BN_, KA, KB>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z, 0,
-                                          (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
+    tma_mainloop<BK, STAGES, BN_, KA, KB, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z,
+                                              0, (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
     finish_abort<STAGES>(full0, abort, status);
     store_tile<BN_, KA, KB>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
 }
@@ -431,11 +448,10 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, c + i * G, z, tm, tn);
         const uint32_t st = (uint32_t)g % STAGES;
-        // as in tma_mainloop: no new copy once the abort word is set
+        // as in tma_mainloop: released stages hold no copy in flight
         if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * st, ((uint32_t)g / STAGES - 1) & 1, abort))
             return;
-        if (*abort) return;
-        issued_word(abort) = (uint32_t)g + 1;
+        last_issued(abort, st) = (uint32_t)g;
         const uint32_t bar = full0 + 8 * st;
         tc::mbar_arrive_expect_tx(bar, STAGE_BYTES);
         if constexpr (KA)
@@ -460,7 +476,7 @@ sgemm_simt_persist_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             (void)tc::mbar_wait(full0 + 8 * rs, ((uint32_t)g / STAGES) & 1, abort);
             slice_fma<BK, BN_, KA, false>(As + rs * ATILE, Bs + rs * BTILE, a_col, b_col, acc);
             __syncwarp();
-            if ((threadIdx.x & 31) == 0) tc::mbar_arrive(empty0 + 8 * rs);
+            if ((threadIdx.x & 31) == 0 && !*abort) tc::mbar_arrive(empty0 + 8 * rs);
             if (issuer && g + STAGES - 1 < total) issue(g + STAGES - 1);
         }
         int z, tm, tn;
@@ -504,8 +520,9 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, b, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
-                                                 z, 0, sk.kslices, a_col, b_col, acc, abort);
+        tma_mainloop<BK, STAGES, BN_, KA, false, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM,
+                                                        tn * BN_, z, 0, sk.kslices, a_col, b_col,
+                                                        acc, abort);
         finish_abort<STAGES>(full0, abort, status);
         store_tile<BN_, KA>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
         return;
@@ -526,8 +543,9 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_,
-                                                 z, s0 * BK, s1 - s0, a_col, b_col, acc, abort);
+        tma_mainloop<BK, STAGES, BN_, KA, false, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM,
+                                                        tn * BN_, z, s0 * BK, s1 - s0, a_col,
+                                                        b_col, acc, abort);
         if (!(s0 == 0 && s1 == sk.kslices)) {
             // the whole 128 x BN_ block, unmasked: the workspace holds full tiles
             float *part = sk.ws + ((int64_t)c * 2 + k) * (BM * BN_);

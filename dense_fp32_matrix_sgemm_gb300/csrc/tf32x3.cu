@@ -67,6 +67,12 @@ namespace tf32x3 {
 constexpr int BM = 128;
 constexpr int THREADS = 128;   // the TF32 probe's CTA
 
+// K-chunked kernel: K per chunk (the library's choice, see tf32x3_chunked_kernel)
+// and the step a measurement may set it in (whole K blocks of both tile widths).
+constexpr int kChunkK = 128;
+constexpr int kChunkStep = 32;
+std::atomic<int> g_chunk_k{kChunkK};
+
 template <int BK_, int STAGES_, int TERMS_, int BN_ = 256>
 struct Config {
     static constexpr int BK = BK_;             // fp32 of K per stage (one swizzled row)
@@ -232,6 +238,7 @@ struct Tf32x3Params {
     int batch;
     float alpha, beta;      // epilogue C = alpha * acc + beta * C + bias[col]
     const float *bias;
+    int kcb;                // K-chunked kernel: K blocks per chunk (>= 1)
 };
 
 __device__ __forceinline__ void raster(const Tf32x3Params &p, int bid, int &z, int &tm, int &tn) {
@@ -669,8 +676,7 @@ struct Chunked {
     static constexpr bool SEP = BN == 128;   // hi*hi apart from the small terms
     static constexpr int SLOT_COLS = 256;
     static constexpr int NSLOT = 2;
-    static constexpr int KC = 128;                // K per chunk
-    static constexpr int KCB = KC / CFG::BK;      // K blocks per chunk
+    static constexpr int KC = kChunkK;            // K per chunk unless measured otherwise (Tf32x3Params::kcb)
     static constexpr int EPI_WARPS = 8;
     static constexpr int COLS = BN / 2;           // running-sum columns per epilogue thread
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -679,6 +685,7 @@ struct Chunked {
     static constexpr int SMEM_BYTES = CFG::STAGES * CFG::STAGE_BYTES + STAGING + 1024 + 256;
     static_assert(CFG::TERMS == 3, "the chunked kernel forms the three-term product");
     static_assert(KC % CFG::BK == 0, "chunks are whole K blocks");
+    static_assert(kChunkStep % CFG::BK == 0, "every chunk length is whole K blocks");
     static_assert(NSLOT * SLOT_COLS == 512, "two chunk accumulators fill tensor memory");
     static_assert((SEP ? 2 * BN : BN) == SLOT_COLS, "chunk accumulator width");
     static_assert(BARS * 8 + 8 <= 256, "barrier area");
@@ -773,7 +780,8 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
     constexpr int BN = CFG::BN;
     constexpr int A_TILE = CFG::A_TILE, B_TILE = CFG::B_TILE, STAGE_BYTES = CFG::STAGE_BYTES;
-    constexpr int NSLOT = P::NSLOT, KCB = P::KCB, COLS = P::COLS;
+    constexpr int NSLOT = P::NSLOT, COLS = P::COLS;
+    const int KCB = p.kcb;   // K blocks per chunk
     constexpr int TX_BYTES = PLANES * (A_TILE + B_TILE);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = tc::smem_u32_generic(smem_raw);
@@ -1235,6 +1243,7 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int co
     p.alpha = a.alpha;
     p.beta = a.beta;
     p.bias = a.bias;
+    p.kcb = 1;
     // The TMA store takes the plain product into a C whose base, rows and
     // batches are 16-byte aligned and whose width is a whole number of
     // 16-byte granules: with N not a multiple of 4 the store was seen to
@@ -1421,6 +1430,7 @@ cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void
     Tf32x3Params p;
     e = prepare<CFG>(a, transA, transB, RAW, 0, ws, s, tmA, tmB, tmAlo, tmBlo, tmC, p);
     if (e != cudaSuccess) return e;
+    p.kcb = g_chunk_k.load(std::memory_order_relaxed) / CFG::BK;
     const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
@@ -1517,6 +1527,13 @@ cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws,
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
     return tc_wide_tile(a, 1) ? tf32x3::launch_persistent<Tf32Wide, 2>(a, transA, transB, ws, s)
                               : tf32x3::launch_persistent<Tf32Narrow, 2>(a, transA, transB, ws, s);
+}
+
+int set_tf32x3_chunk_k(int chunk_k) {
+    if (chunk_k == 0) chunk_k = tf32x3::kChunkK;
+    if (chunk_k < tf32x3::kChunkStep || chunk_k > (1 << 30) || chunk_k % tf32x3::kChunkStep != 0)
+        return -1;
+    return tf32x3::g_chunk_k.exchange(chunk_k);
 }
 
 cudaError_t launch_tf32_mma_probe(long long iters, float *out, int ctas, cudaStream_t s) {

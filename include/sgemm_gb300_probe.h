@@ -77,6 +77,22 @@ int sgemm_probe_tf32_mma(int64_t iterations, float *out, double *flops_out, void
 int sgemm_set_raster_group(int group_m);
 
 /*
+ * Measurement knob for the accuracy of sgemm_f32_tf32x3* over long reductions
+ * (no counterpart on the source pages; the accuracy it trades is the FMA vs
+ * TF32 RRMSE comparison of the ChetanC28/cuda-kernels page).  Products with
+ * K > 256 accumulate on the tensor cores in chunks of `chunk_k` of K and add
+ * the chunk sums in round-to-nearest fp32; the tensor cores' own accumulation
+ * rounds towards zero, so shorter chunks are more accurate and cost a little
+ * more (3072^3: 64 -> RRMSE 5.6e-7, 128 -> 1.0e-6, 256 -> 1.9e-6).  The
+ * library's choice is 128.  Sets chunk_k for the calls made after it on any
+ * thread: a multiple of 32 from 32 to 2^30 (a value at least K puts the whole
+ * reduction in one chunk), 0 restores 128.  Results stay deterministic and
+ * exact on small integers for every value.  Returns the previous value, or -1
+ * (nothing changed) for any other chunk_k.
+ */
+int sgemm_set_tf32x3_chunk_k(int chunk_k);
+
+/*
  * Self-test of the library's failure path (no counterpart on the source
  * pages): launches one CTA that waits, with the bounded wait of the tensor-core
  * pipeline, on a barrier nothing ever arrives on.  After about `limit_cycles`

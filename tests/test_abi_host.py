@@ -148,3 +148,13 @@ def test_raster_group_knob(lib):
     assert lib.sgemm_set_raster_group(-1) == -1
     assert lib.sgemm_set_raster_group(65537) == -1
     assert sg.set_raster_group(0) == 8
+
+
+def test_tf32x3_chunk_knob(lib):
+    # returns the previous value; 0 restores 128; only multiples of 32 from 32 are taken
+    assert sg.set_tf32x3_chunk_k(64) == 128
+    assert sg.set_tf32x3_chunk_k(1 << 30) == 64
+    assert sg.set_tf32x3_chunk_k(0) == 1 << 30
+    for bad in (-32, 16, 48, 100, (1 << 30) + 32):
+        assert lib.sgemm_set_tf32x3_chunk_k(bad) == -1
+    assert sg.set_tf32x3_chunk_k(0) == 128

@@ -1119,3 +1119,29 @@ def test_raster_group_changes_no_bits(entry_name, tB):
     finally:
         sg.set_raster_group(0)
     check_full(case, ref, label=f"raster {entry_name} tB={tB}")
+
+
+# The chunk-length knob of the K-chunked kernel (sgemm_set_tf32x3_chunk_k):
+# every length gives results within the bound, exact on small integers, and
+# shorter chunks are more accurate (the tensor cores' rounding toward zero
+# acts within a chunk only).  Both tile widths: 1000 x 1000 takes 128-wide
+# tiles, 3000 x 2000 256-wide ones.
+@pytest.mark.parametrize("M,N,K", [(1000, 1000, 2000), (3000, 2000, 1500)])
+def test_tf32x3_chunk_length(M, N, K):
+    case = workloads.make_operands(M, N, K, dist="uniform", seed=97, key=970 + M)
+    ref, S = _oracle_full(case)
+    icase = workloads.make_operands(M, N, K, dist="int", seed=98, key=980 + M)
+    errs = {}
+    try:
+        for ck in (32, 64, 128, 256, 1 << 20):
+            sg.set_tf32x3_chunk_k(ck)
+            got = run(case, entry="sgemm_f32_tf32x3")
+            assert oracle.within_tolerance(got, ref, S).all(), f"chunk {ck}"
+            errs[ck] = oracle.rrmse(got, ref)
+            check_full(icase, run(icase, entry="sgemm_f32_tf32x3"), exact=True,
+                       label=f"int chunk {ck}")
+    finally:
+        sg.set_tf32x3_chunk_k(0)
+    print({k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs[64] < errs[256] < errs[1 << 20]
+    assert sg.device_status(reset=True) == 0

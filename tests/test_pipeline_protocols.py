@@ -214,17 +214,20 @@ def simt_tma_persistent(tiles, ktiles, stages, warps, seed):
 def simt_tma_abort(pieces, stages, warps, seed, abort_step):
     """tma_mainloop with the abort path: at step `abort_step` some wait runs
     out and sets the CTA's abort word.  From then on every wait returns at
-    once (a warp whose "full" wait gave up still releases the stage), thread 0
-    issues nothing more (it reads the abort word after the "empty" wait, which
-    itself gives up once the word is set), and finish_abort waits for the last
-    `stages` slices it issued.  Checks that no stage ever gets a second fill while its previous
-    copy is in flight, and that no copy is in flight when the CTA exits."""
+    once.  A warp releases a stage only if its "full" wait saw the copy land;
+    thread 0 refills a stage only once all warps released it (its "empty"
+    wait gives up once the word is set, unless the release had already
+    completed, so a slice may be skipped and a later one still issued), and
+    finish_abort waits for the latest copy issued into each stage.  Checks
+    that no stage ever gets a second fill while its previous copy is in
+    flight, and that no copy is in flight when the CTA exits."""
     rng = random.Random(seed)
     full = [Barrier(1, f"full{s}") for s in range(stages)]
     empty = [Barrier(warps, f"empty{s}") for s in range(stages)]
     flying = [False] * stages
     in_flight = []
-    state = {"abort": False, "step": 0, "issued": 0}
+    state = {"abort": False, "step": 0}
+    last = [None] * stages            # slice last issued into each stage
 
     def wait(bar, k):
         # bounded wait: gives up once the abort word is set
@@ -242,12 +245,10 @@ def simt_tma_abort(pieces, stages, warps, seed, abort_step):
             ok = yield from wait(empty[s], g // stages - 1)
             if not ok:
                 return
-        if state["abort"]:
-            return
         assert not flying[s], "a stage got a second fill while its copy was in flight"
         flying[s] = True
         in_flight.append(g)
-        state["issued"] = g + 1
+        last[s] = g
 
     def tma():
         while True:
@@ -266,18 +267,19 @@ def simt_tma_abort(pieces, stages, warps, seed, abort_step):
                     yield from issue(g0 + j)
             for kt in range(n):
                 s = gk % stages
-                yield from wait(full[s], gk // stages)
+                landed = yield from wait(full[s], gk // stages)
                 gk += 1
                 yield
-                empty[s].arrive()
+                if landed:
+                    empty[s].arrive()
                 if w == 0 and kt + stages - 1 < n:
                     yield from issue(g0 + kt + stages - 1)
         if w == 0 and state["abort"]:
             # finish_abort: the latest fill of every stage lands before exit
-            n = state["issued"]
-            for g in range(max(0, n - stages), n):
-                while full[g % stages].completed < g // stages + 1:
-                    yield
+            for s in range(stages):
+                if last[s] is not None:
+                    while full[s].completed < last[s] // stages + 1:
+                        yield
 
     t = tma()
     alive = [warp(w) for w in range(warps)]
