@@ -278,10 +278,35 @@ def tc_kernel_name(K: int) -> str:
     return "tf32x3_persistent_kernel" if K <= 256 else "tf32x3_chunked_kernel"
 
 
+def graph_ms(torch, stream, fn, ms_one):
+    """Device time per call with the host's launch cost taken out: `reps`
+    back-to-back calls captured in one CUDA graph, replayed three times, the
+    median replay divided by `reps`."""
+    reps = 20 if ms_one < 0.5 else 3
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            fn()
+    ts = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+    return sorted(ts)[1] / reps
+
+
 def workload_table(torch, sg, dev, stream, sp, reps=5):
     """ms, TFLOP/s and compulsory-byte GB/s of sgemm_f32 and sgemm_f32_tf32x3 on
     every named workload (operands resident on the device, median of `reps`
-    after two warm-ups)."""
+    after two warm-ups), each call timed alone between CUDA events (the host's
+    launch cost included: it dominates the smallest problems), and `*_graph_ms`
+    the device time per call from back-to-back calls in a CUDA graph."""
     out = {}
     for name, w in workloads.WORKLOADS.items():
         case = workloads.make_case(w)
@@ -332,6 +357,9 @@ def workload_table(torch, sg, dev, stream, sp, reps=5):
             ms = sorted(ts)[len(ts) // 2]
             row[label + "_ms"] = ms
             row[label + "_tflops"] = workloads.flops(w.M, w.N, w.K, w.batch) / (ms * 1e-3) / 1e12
+            gms = graph_ms(torch, stream, fn, ms)
+            row[label + "_graph_ms"] = gms
+            row[label + "_graph_tflops"] = workloads.flops(w.M, w.N, w.K, w.batch) / (gms * 1e-3) / 1e12
             # compulsory bytes / time: the figure that matters where a path
             # is bandwidth-bound (the batched QK^T shape on the tensor cores)
             row[label + "_gbs"] = row["min_bytes"] / (ms * 1e-3) / 1e9

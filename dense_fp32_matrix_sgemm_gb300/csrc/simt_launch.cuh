@@ -7,6 +7,7 @@
 #include <utility>
 
 #include "simt_sgemm.cuh"
+#include "simt_small.cuh"
 
 namespace sgemm {
 namespace simt {
@@ -198,12 +199,113 @@ bool launch_cluster_split(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
     return true;
 }
 
+// 32-deep K slices per CTA when `tiles` tiles split K over clusters of the
+// largest power of two up to 16 with tiles * S <= sms (residency not checked):
+// the work on each CTA's critical path.
+inline long long split_slices_per_cta(long long tiles, long long slices, long long sms) {
+    long long best = slices;
+    for (long long c = 2; c <= kMaxClusterSplit; c *= 2) {
+        if (tiles * c > sms || c > slices) break;
+        best = (slices + c - 1) / c;
+    }
+    return best;
+}
+
+// A 64 x 64 slice (4 x 4 outputs per thread, two 16-byte shared loads per 8
+// packed FMAs) costs about 0.65 of a 128 x 128 one on its CTA's critical path
+// (measured: 128 x 128 x 32768 on 64 CTAs of 64 x 64 against 16 of 128 x 128,
+// 64 slices each, 114 against 180 us).  So the small tiles pay where they cut
+// the slices per CTA: 256^3 (1 slice each way, 8.2 -> 6.6 us), 384^3 (2 -> 3,
+// 11.1 -> 8.6 us), but not 512^3 (2 -> 8, 16.2 against 17.0 us) or
+// 256 x 256 x 4096 (8 -> 16, 28.6 against 43.6 us).
+constexpr double kSmallSliceCost = 0.65;
+
+// The 64 x 64 cluster split (simt_small.cuh) for problems whose 64 x 64
+// tiles cover at most half the SMs (256^3: 16 tiles) and whose slices per CTA
+// it cuts enough against the 128 x 128 split (kSmallSliceCost).  S CTAs per
+// cluster, S in {1, 2, 4, 8, 16}: the fewest 32-deep slices per CTA subject to
+// tiles * S <= SMs and every cluster being resident at once.  Returns false
+// (launching nothing) when the problem is not such a case; else launches and
+// stores the launch status in `err`.
+template <bool TA, bool TB, bool VEC>
+bool launch_small_split(const GemmArgs &a, cudaStream_t s, cudaError_t &err) {
+    auto kern = sgemm_simt_small_kernel<TA, TB, VEC>;
+    const long long sms = sm_count();
+    const long long tm = (a.M + kSmallTile - 1) / kSmallTile;
+    const long long tn = (a.N + kSmallTile - 1) / kSmallTile;
+    const long long tiles = (long long)a.batch * tm * tn;
+    if (a.kchunk != 0 || tiles * 2 > sms) return false;
+    const long long slices = (a.K + kSmallBK - 1) / kSmallBK;
+    {
+        const long long big_tiles = (long long)a.batch * ((a.M + BM - 1) / BM) * ((a.N + 127) / 128);
+        const double small = kSmallSliceCost * (double)split_slices_per_cta(tiles, slices, sms);
+        const double big = (double)split_slices_per_cta(big_tiles, (a.K + kBK - 1) / kBK, sms);
+        if (!(small < big)) return false;
+    }
+
+    int dev = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return true;
+    static PerContext<bool> nonportable;
+    bool opted = false;
+    if (!nonportable.get(current_context_id(), opted)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+            (void)cudaGetLastError();   // then clusters of 16 report no residency below
+        nonportable.put(current_context_id(), true);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static std::atomic<int> resident[64][4];
+    auto fits = [&](int c) {
+        std::atomic<int> &slot = resident[dev & 63][c == 2 ? 0 : (c == 4 ? 1 : (c == 8 ? 2 : 3))];
+        int n = slot.load();
+        if (n == 0) {
+            attr[0].val.clusterDim.x = (unsigned)c;
+            cfg.gridDim = dim3((unsigned)c);
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+                (void)cudaGetLastError();
+                n = -1;
+            }
+            slot.store(n);
+        }
+        return n >= tiles;
+    };
+    int S = 1;
+    long long best = slices;
+    for (int c = 2; c <= kMaxClusterSplit; c *= 2) {
+        if (tiles * c > sms || c > slices) break;
+        const long long per = (slices + c - 1) / c;
+        if (per < best && fits(c)) {
+            best = per;
+            S = c;
+        }
+    }
+    GemmArgs g = a;
+    g.tiles_m = (int)tm;
+    g.tiles_n = (int)tn;
+    g.kchunk = (int)(best * kSmallBK);
+    attr[0].val.clusterDim.x = (unsigned)S;
+    cfg.gridDim = dim3((unsigned)(tiles * S));
+    err = cudaLaunchKernelEx(&cfg, kern, g);
+    return true;
+}
+
 // The wide tile is used only where B arrives by cp.async (row-major B) and
 // with 16-byte access: corner-turning a 256-wide B slice needs 32 more
 // staging registers than the 255-register budget leaves.
 template <bool TA, bool TB, bool VEC>
 cudaError_t launch_variant(const GemmArgs &a, cudaStream_t s) {
     cudaError_t err = cudaSuccess;
+    if (launch_small_split<TA, TB, VEC>(a, s, err)) return err;
     if (launch_cluster_split<TA, TB, VEC>(a, s, err)) return err;
     // 16-byte access: the TMA-fed kernel (two CTAs per SM), unless the
     // operands cannot be described as tensor maps

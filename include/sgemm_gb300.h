@@ -89,7 +89,9 @@ typedef enum {
  * output tiles cover at most half the SMs (e.g. 256 x 256 x 256: four tiles)
  * split K over the 2, 4, 8 or 16 CTAs of a thread-block cluster and add the
  * partial tiles on chip through distributed shared memory, in chunk order:
- * the split-K of the ChetanC28/cuda-kernels page without a workspace.
+ * the split-K of the ChetanC28/cuda-kernels page without a workspace.  The
+ * smallest of them (256^3, 384^3, 128 x 128 x 32768, ...) take 64 x 64 tiles
+ * for this, which cuts the work on each CTA's critical path.
  */
 int sgemm_f32(int64_t M, int64_t N, int64_t K,
               const float *A, int64_t lda,

@@ -640,13 +640,16 @@ def test_matmul_convenience_epilogue_and_splitk():
         sg.matmul(A, B, beta=1.0)          # beta reads out, which was not given
 
 
-# sgemm_f32 on problems whose 128 x 128 tiles cover at most half the SMs:
-# K is split over the CTAs of a cluster (2, 4 or 8) and the partial tiles are
-# added through distributed shared memory.  Shapes pick each cluster size,
-# chunks of one slice, a last chunk holding a single k, and more ranks than
-# non-empty chunks.
+# sgemm_f32 on problems whose tiles cover at most half the SMs: K is split
+# over the CTAs of a cluster (2 to 16) and the partial tiles are added through
+# distributed shared memory, on 64 x 64 tiles where that cuts the slices per
+# CTA (256^3, 384^3, 128 x 128 x 32768, ...) and on 128 x 128 tiles otherwise
+# (512^3, 256 x 256 x 4096, 300 x 260 x 4096).  Shapes pick each cluster size,
+# chunks of one slice, a last chunk holding a single k, more ranks than
+# non-empty chunks, and a 64 x 64 problem with K <= 32 (no split).
 CLUSTER = [(256, 256, 256), (130, 129, 77), (200, 70, 33), (300, 260, 4096),
-           (128, 128, 32768), (1000, 1000, 300), (100, 100, 264), (64, 384, 96)]
+           (128, 128, 32768), (1000, 1000, 300), (100, 100, 264), (64, 384, 96),
+           (384, 384, 384), (512, 512, 512), (256, 256, 4096), (100, 100, 20), (64, 64, 64)]
 
 
 @pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
@@ -661,9 +664,13 @@ def test_cluster_split_shapes(M, N, K, tA, tB):
 
 
 @pytest.mark.parametrize("offset", [1, 3])
-def test_cluster_split_unaligned_batched_deterministic(offset):
-    case = workloads.make_operands(150, 90, 700, batch=3, transA=1, lda=153, ldb=91,
-                                   dist="normal", seed=52, key=500)
+@pytest.mark.parametrize("batch,tA,tB", [(3, 1, 0), (5, 0, 1)])
+def test_cluster_split_unaligned_batched_deterministic(offset, batch, tA, tB):
+    M, N, K = 150, 90, 700
+    lda = (M if tA else K) + 3
+    ldb = (K if tB else N) + 1
+    case = workloads.make_operands(M, N, K, batch=batch, transA=tA, transB=tB, lda=lda, ldb=ldb,
+                                   dist="normal", seed=52, key=500 + batch)
     first = run(case, entry="sgemm_f32_strided_batched", offset=offset)
     check_full(case, first, label=f"cluster batched offset={offset}")
     again = run(case, entry="sgemm_f32_strided_batched", offset=offset)
@@ -672,8 +679,8 @@ def test_cluster_split_unaligned_batched_deterministic(offset):
 
 @pytest.mark.parametrize("alpha,beta,with_bias", [(0.7, -1.3, True), (1.0, 0.0, True),
                                                   (-2.0, 0.5, False)])
-def test_cluster_split_epilogue(alpha, beta, with_bias):
-    M, N, K = 200, 190, 1500
+@pytest.mark.parametrize("M,N,K", [(200, 190, 1500), (130, 129, 300)])   # 128- and 64-wide tiles
+def test_cluster_split_epilogue(alpha, beta, with_bias, M, N, K):
     case = workloads.make_operands(M, N, K, transB=1, ldc=N + 2, dist="normal", seed=53, key=501)
     rng = np.random.default_rng(54)
     C_in = rng.standard_normal((M, N)).astype(np.float32)
