@@ -71,6 +71,15 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire;\n" ::: "memory");
 }
 
+// Cluster-wide barrier that orders nothing: a CTA passes it once every CTA
+// of the cluster has arrived.  For the barrier that keeps a CTA's shared
+// memory alive until its peers have read it: each reading thread has used
+// the values it loaded before it arrives, so no release is needed.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n"
+                 "barrier.cluster.wait;\n" ::: "memory");
+}
+
 // 16-byte load from the shared memory of CTA `rank` of this cluster, at the
 // offset that `local` (a shared::cta address) has in this CTA.
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t local, uint32_t rank) {
@@ -82,6 +91,27 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t local, uint32_t rank) {
     return v;
 }
 
+// Sum over ranks 0..n-1 (n <= 16) of the float4 at the offset `local` has in
+// each CTA of the cluster, added in rank order.  All n loads are issued before
+// the first add, so their latencies overlap instead of adding up.
+__device__ __forceinline__ float4 cluster_sum_f4(uint32_t local, uint32_t n) {
+    float4 v[16];
+#pragma unroll
+    for (uint32_t q = 0; q < 16; ++q)
+        if (q < n) v[q] = ld_cluster_f4(local, q);
+    float4 sum = v[0];
+#pragma unroll
+    for (uint32_t q = 1; q < 16; ++q) {
+        if (q < n) {
+            sum.x += v[q].x;
+            sum.y += v[q].y;
+            sum.z += v[q].z;
+            sum.w += v[q].w;
+        }
+    }
+    return sum;
+}
+
 // 4-byte load from the shared memory of CTA `rank` of this cluster.
 __device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
     uint32_t remote;
@@ -89,6 +119,19 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local, uint32_t rank) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
     return v;
+}
+
+// cluster_sum_f4 for one float.
+__device__ __forceinline__ float cluster_sum_f32(uint32_t local, uint32_t n) {
+    float v[16];
+#pragma unroll
+    for (uint32_t q = 0; q < 16; ++q)
+        if (q < n) v[q] = ld_cluster_f32(local, q);
+    float sum = v[0];
+#pragma unroll
+    for (uint32_t q = 1; q < 16; ++q)
+        if (q < n) sum += v[q];
+    return sum;
 }
 
 }  // namespace sgemm

@@ -192,22 +192,14 @@ gemv_colsum_kernel(const GemvArgs a) {
         if constexpr (VEC) {
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                float4 t = ld_cluster_f4(at + 16 * j, 0);
-                for (uint32_t c = 1; c < cs; ++c) {
-                    const float4 u = ld_cluster_f4(at + 16 * j, c);
-                    t.x += u.x;
-                    t.y += u.y;
-                    t.z += u.z;
-                    t.w += u.w;
-                }
+                const float4 t = cluster_sum_f4(at + 16 * j, cs);
                 sum[4 * j + 0] = t.x;
                 sum[4 * j + 1] = t.y;
                 sum[4 * j + 2] = t.z;
                 sum[4 * j + 3] = t.w;
             }
         } else {
-            sum[0] = ld_cluster_f32(at, 0);
-            for (uint32_t c = 1; c < cs; ++c) sum[0] += ld_cluster_f32(at, c);
+            sum[0] = cluster_sum_f32(at, cs);
         }
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
@@ -218,7 +210,7 @@ gemv_colsum_kernel(const GemvArgs a) {
         }
     }
     // no CTA leaves while CTA 0 still reads its shared memory
-    cluster_sync();
+    cluster_sync_relaxed();
 }
 
 bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }

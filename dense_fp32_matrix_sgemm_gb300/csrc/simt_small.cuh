@@ -157,19 +157,12 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_small_kernel(const GemmArg
     for (int g = tid; g < (r1 - r0) * G; g += THREADS) {
         const int r = r0 + g / G, c = 4 * (g % G);
         const uint32_t at = smem_u32(part + r * kSmallPartialLd + c);
-        float4 sum = ld_cluster_f4(at, 0);
-        for (uint32_t q = 1; q < csize; ++q) {
-            const float4 v = ld_cluster_f4(at, q);
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-        }
+        const float4 sum = cluster_sum_f4(at, csize);
         const int row = m0 + r;
         if (row < p.M) store_c4(p, Cz + (int64_t)row * p.ldc, n0 + c, sum, VEC, plain);
     }
     // no CTA may leave (releasing its shared memory) while a peer still reads it
-    cluster_sync();
+    cluster_sync_relaxed();
 }
 
 }  // namespace simt
