@@ -67,7 +67,7 @@ extern "C" int sgemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const f
         char msg[256];
         snprintf(msg, sizeof msg,
                  "M=%lld N=%lld K=%lld needs %llu bytes of scratch; the built-in scratch of "
-                 "sgemm_f32_tf32x3_noalloc holds %llu bytes (2*(M+N)*round_up(K,4)*4 must fit)",
+                 "sgemm_f32_tf32x3_noalloc holds %llu bytes (2*(M+N)*round_up(K,32)*4 must fit)",
                  (long long)M, (long long)N, (long long)K, (unsigned long long)need,
                  sgemm::kNoallocScratchBytes);
         return sgemm::record_error(SGEMM_EWORKSPACE, msg);

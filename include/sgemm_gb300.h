@@ -267,10 +267,10 @@ int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K,
                                      void *workspace, uint64_t workspace_bytes, void *stream);
 
 /* Workspace bytes the tf32x3 entry points need: the hi and lo TF32 planes of
- * op(A) and op(B), 2 * batch * (M + N) * round_up(K, 4) floats plus padding
- * (an operand stored K-contiguous with 16-byte aligned rows is read as its own
- * hi term and uses only its lo plane, but the size does not depend on the
- * pointers).  0 for empty problems or negative sizes. */
+ * op(A) and op(B), 2 * batch * (M + N) * round_up(K, 32) floats plus padding
+ * (an operand stored K-contiguous with aligned rows, 16 bytes for K <= 256
+ * and 128 bytes above, is read as its own hi term and uses only its lo plane,
+ * but the size does not depend on the pointers).  0 for empty problems or negative sizes. */
 uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
 
 /*
@@ -303,7 +303,7 @@ int sgemm_f32_tf32_strided_batched(int64_t M, int64_t N, int64_t K,
                                    void *workspace, uint64_t workspace_bytes, void *stream);
 
 /* Workspace bytes of the sgemm_f32_tf32 entry points: batch * (M + N) *
- * round_up(K, 4) floats plus padding.  0 for empty problems. */
+ * round_up(K, 32) floats plus padding.  0 for empty problems. */
 uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
 
 /*
@@ -318,7 +318,7 @@ uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
  * There is no counterpart on the source pages; it exists for these callers.
  *
  * Arguments, layout, precision and results as sgemm_f32_tf32x3 (no batch).
- * Limit: 2 * (M + N) * round_up(K, 4) * 4 bytes (plus 256-byte alignment
+ * Limit: 2 * (M + N) * round_up(K, 32) * 4 bytes (plus 256-byte alignment
  * padding) must fit in the scratch, e.g. M = N = K = 2048; larger problems
  * return SGEMM_EWORKSPACE with the sizes in sgemm_last_error().
  * The first call in each CUDA context (per device, and again after

@@ -337,6 +337,35 @@ def test_chunked_tensor_kernel(M, N, K, tA, tB, batch, offset, dist):
     check_full(case, got, exact=dist == "int", label=f"chunked {M}x{N}x{K}x{batch} {tA}{tB}")
 
 
+# K-contiguous operands whose rows start on 128-byte boundaries (leading
+# dimension a multiple of 32 floats) are read raw by the K-chunked kernel as
+# their own hi term, next to a lo-only plane; rows only 16-byte aligned go
+# through full planes, as does every operand of the same buffers shifted by
+# one float.  The MMAs see the same values on both routes, so the bits agree.
+# NN (A raw), NT (both), TT (B raw), a K tail, both tile widths, a batch.
+CHUNKED_RAW = [  # M, N, K, tA, tB, batch
+    (1000, 1100, 600, 0, 0, 1), (700, 900, 300, 0, 1, 1), (600, 700, 501, 1, 1, 1),
+    (2000, 2001, 1000, 0, 1, 1), (256, 384, 300, 0, 1, 3),
+]
+
+
+@pytest.mark.parametrize("M,N,K,tA,tB,batch", CHUNKED_RAW)
+def test_chunked_raw_rows(M, N, K, tA, tB, batch):
+    rup32 = lambda d: (d + 31) // 32 * 32 + 32   # 128-byte rows and a padding block
+    lda = M + 4 if tA else rup32(K)
+    ldb = rup32(K) if tB else N + 4
+    case = workloads.make_operands(M, N, K, batch=batch, transA=tA, transB=tB, lda=lda, ldb=ldb,
+                                   ldc=N + 4, dist="normal", poison=True, seed=93,
+                                   key=930 + M + N + K + tA + 2 * tB)
+    entry = "sgemm_f32_tf32x3_strided_batched" if batch > 1 else "sgemm_f32_tf32x3"
+    assert sg.device_status(reset=True) == 0
+    raw = run(case, entry=entry)
+    planes = run(case, entry=entry, offset=1)
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    assert np.array_equal(raw, planes), "raw rows differ from the split kernel's planes"
+    check_full(case, raw, label=f"chunked raw {M}x{N}x{K}x{batch} {tA}{tB}")
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 270, 700), (2000, 2048, 1000)])
 def test_chunked_tensor_epilogue(M, N, K):
     case = workloads.make_operands(M, N, K, transB=1, ldc=N + 2, dist="normal", seed=91,
