@@ -237,20 +237,47 @@ def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
     return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
 
 
-def tc_plan(M, N, K, batch, transA, transB, aligned=True):
-    """(kernels label, launches) of one 3xTF32 call, mirroring csrc/tf32x3.cu
-    for 16-byte aligned operands: a K-contiguous operand (row-major A, B
-    stored transposed) is read as its own hi term; its lo term is made by
-    converter warps inside the GEMM when K <= 64, or K <= 256 with at most 8
-    tiles reading each of its panels, else written by the split kernel as a
-    lo plane; other operands are split into hi and lo planes."""
+def tc_wide_tile(M, N, K, batch, sms):
+    """The K-chunked kernel's tile width (csrc/tf32x3.cu, tc_wide_tile): a
+    128 x 256 tile counts as 1.75 128 x 128 tiles; tiles per SM rounded up."""
+    if K <= 256:
+        return False
+    tm = -(-M // 128)
+    wide, narrow = batch * tm * -(-N // 256), batch * tm * -(-N // 128)
+    return 1.75 * -(-wide // sms) <= -(-narrow // sms)
+
+
+def tc_split_tail(M, N, K, batch, sms):
+    """K segments per tail tile of the K-chunked kernel (csrc/tf32x3.cu,
+    chunked_plan), 0 when the tiles run whole: the last wave's tiles are split
+    into SMs // tail segments of at least two K blocks when that is two or
+    more (the workspace has room for their partial tiles)."""
+    if K <= 256:
+        return 0
+    wide = tc_wide_tile(M, N, K, batch, sms)
+    bn, bk = (256, 16) if wide else (128, 32)
+    tail = batch * -(-M // 128) * -(-N // bn) % sms
+    split = min(sms // tail, -(-K // bk) // 2) if tail else 0
+    return split if split >= 2 else 0
+
+
+def tc_plan(M, N, K, batch, transA, transB, aligned=True, rows128=True, sms=152):
+    """(kernels label, launches) of one 3xTF32 call, mirroring csrc/tf32x3.cu:
+    a K-contiguous operand (row-major A, B stored transposed) with aligned
+    rows (16 bytes for K <= 256, 128 bytes beyond: `aligned`, `rows128`) is
+    read as its own hi term; its lo term is made by converter warps inside
+    the GEMM when K <= 64, or K <= 256 with at most 8 tiles reading each of
+    its panels, else written by the split kernel as a lo plane; other
+    operands are split into hi and lo planes.  Tail tiles split in K add the
+    fix-up kernel."""
     tiles_m, tiles_n = -(-M // 128), -(-N // 128)   # K <= 256 takes 128-wide tiles
 
     def conv(reuse):
         return K <= 64 or (K <= 256 and reuse <= 8)
+    ok = aligned if K <= 256 else aligned and rows128
     parts, split = [], []
     for name, kcontig, reuse in (("A", not transA, tiles_n), ("B", bool(transB), tiles_m)):
-        if kcontig and aligned:
+        if kcontig and ok:
             if conv(reuse):
                 parts.append(f"{name} raw, lo by converter warps")
             else:
@@ -263,13 +290,20 @@ def tc_plan(M, N, K, batch, transA, transB, aligned=True):
                 "kind::tf32, TMEM, TMA-store epilogue" +
                 ("; " + ", ".join(parts) if parts else "") + ")")
     else:
-        gemm = ("tf32x3_chunked_kernel (one CTA per SM; 128x256 or 128x128 tiles by wave count; "
+        width = "128x256" if tc_wide_tile(M, N, K, batch, sms) else "128x128"
+        gemm = (f"tf32x3_chunked_kernel (one CTA per SM; {width} tiles; "
                 "TMA ring, tcgen05 kind::tf32 into two TMEM chunk accumulators, each 128 of K "
                 "added into fp32 registers by 8 epilogue warps, TMA-store epilogue" +
                 ("; " + ", ".join(parts) if parts else "") + ")")
+    launches = 1
+    split = tc_split_tail(M, N, K, batch, sms)
     if split:
-        return f"split_kernel ({', '.join(split)}) + {gemm}", 2
-    return gemm, 1
+        gemm += (f", last wave's tiles split into {split} K segments + tf32x3_fixup_kernel "
+                 "(adds the segments' partial tiles)")
+        launches += 1
+    if split:
+        return f"split_kernel ({', '.join(split)}) + {gemm}", launches + 1
+    return gemm, launches
 
 
 def tc_kernel_name(K: int) -> str:
@@ -612,6 +646,7 @@ def main():
     sk_ws = torch.empty(max(sk_need, 1), dtype=torch.uint8, device=dev)
     sms_dev = torch.cuda.get_device_properties(dev).multi_processor_count
     aligned = lda % 4 == 0 and ldb % 4 == 0 and ldc % 4 == 0
+    rows128 = lda % 32 == 0 and ldb % 32 == 0   # (device buffers are 512-byte aligned)
     launches = (streamk_launches(M, N, K, w.transA, w.transB, sms_dev, aligned) if batch == 1
                 else 1)
 
@@ -844,8 +879,9 @@ def main():
         tf32_probe = tf32_probe_tflops(torch, sg, dev, stream)
         tc = {
             "value": world * tc_alg, "unit": "TFLOP/s", "ms_per_step": tc_ms,
-            "kernels": tc_plan(M, N, K, batch, w.transA, w.transB, aligned)[0],
-            "gpu_launches_per_step": tc_plan(M, N, K, batch, w.transA, w.transB, aligned)[1],
+            "kernels": tc_plan(M, N, K, batch, w.transA, w.transB, aligned, rows128, sms_dev)[0],
+            "gpu_launches_per_step": tc_plan(M, N, K, batch, w.transA, w.transB, aligned,
+                                             rows128, sms_dev)[1],
             "pct_of_fp32_peak_at_max_clock": None,
             "roofline": {"bound": "tensor", "achieved": 3 * tc_alg, "peak": tf32_probe,
                          "unit": "TFLOP/s", "frac": 3 * tc_alg / tf32_probe,

@@ -239,7 +239,7 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     a.bias = epi.bias;
     if (a.alpha == 0.f) K = 0;   // the product term vanishes: A and B are not read
     if (path != Path::Simt && K > 0) {
-        const uint64_t need = path == Path::Tf32x3 ? tf32x3_workspace_bytes(M, N, K, batch)
+        const uint64_t need = path == Path::Tf32x3 ? tf32x3_workspace_min_bytes(M, N, K, batch)
                                                    : tf32_workspace_bytes(M, N, K, batch);
         if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
             return fail(SGEMM_EWORKSPACE, "workspace %p of %llu bytes: need %llu bytes, 256-byte "
@@ -253,7 +253,7 @@ int run(Path path, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
     if (K == 0) {
         e = launch_epilogue_only(a, s);
     } else if (path == Path::Tf32x3) {
-        e = launch_tf32x3(a, transA != 0, transB != 0, workspace, s);
+        e = launch_tf32x3(a, transA != 0, transB != 0, workspace, workspace_bytes, s);
     } else if (path == Path::Tf32) {
         e = launch_tf32(a, transA != 0, transB != 0, workspace, s);
     } else if (gemv_shape(a)) {

@@ -83,9 +83,14 @@ __host__ __device__ inline bool plain_epilogue(const GemmArgs &a) {
 // dimension and batch stride allows 16-byte accesses.
 cudaError_t launch_simt(const GemmArgs &a, bool transA, bool transB, bool vec, cudaStream_t s);
 
-// Tensor-core 3xTF32 path: split kernels into `ws`, then the tcgen05 GEMM.
-cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s);
+// Tensor-core 3xTF32 path: split kernels into `ws` (ws_bytes long, at least
+// tf32x3_workspace_min_bytes: the planes), then the tcgen05 GEMM.  With
+// tf32x3_workspace_bytes, a problem whose last wave of tiles leaves at least
+// half the SMs idle also gets partial tiles for splitting those tiles in K.
+cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, size_t ws_bytes,
+                          cudaStream_t s);
 size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
+size_t tf32x3_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int64_t batch);
 cudaError_t tf32x3_read_error(unsigned int *flags, bool reset);
 cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t s);
 // TF32 tensor-pipe probe: `ctas` CTAs (one per SM), `iters` rounds each.

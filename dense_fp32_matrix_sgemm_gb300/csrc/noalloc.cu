@@ -62,7 +62,11 @@ extern "C" int sgemm_f32_tf32x3_noalloc(int64_t M, int64_t N, int64_t K, const f
                                         int64_t lda, const float *B, int64_t ldb, float *C,
                                         int64_t ldc, int transA, int transB, void *stream) {
     // Sizes beyond the built-in scratch are rejected before anything runs.
-    const uint64_t need = sgemm_f32_tf32x3_workspace_size(M, N, K, 1);
+    // The planes must fit; the stream-K schedule's partial tiles are used
+    // when they fit too, exactly as sgemm_f32_tf32x3 does with a workspace of
+    // this size.
+    const uint64_t need =
+        (M <= 0 || N <= 0 || K <= 0) ? 0 : sgemm::tf32x3_workspace_min_bytes(M, N, K, 1);
     if (need > sgemm::kNoallocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,

@@ -100,6 +100,13 @@ __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+// Until at most N of this thread's bulk groups are incomplete (their global
+// writes done).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
+}
+
 // Until at most N of this thread's bulk groups still read shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {

@@ -12,11 +12,11 @@
 //
 // Stage 1 (one split launch for both operands): op(A) and op(B) are
 //   rewritten into a caller-owned workspace as K-major planes
-//   [batch][TERMS == 3 ? hi|lo : hi][rows][Kp] (Kp = K rounded up to 4 so
-//   rows are 16-byte aligned for TMA).  M- or N-major operands are
+//   [batch][TERMS == 3 ? hi|lo : hi][rows][Kp] (Kp = K rounded up to 32 so
+//   rows start on 128-byte boundaries).  M- or N-major operands are
 //   corner-turned through a padded shared tile.  A K-contiguous operand with
-//   16-byte aligned rows needs no hi plane for three terms (the GEMM loads
-//   the caller's rows, which the MMA reads as hi), so only its lo plane is
+//   aligned rows needs no hi plane for three terms (the GEMM loads the
+//   caller's rows, which the MMA reads as hi), so only its lo plane is
 //   written; for short reductions it needs no split at all (converter warps
 //   make lo, or the rounded hi of one term, inside the GEMM).  The GEMM is
 //   launched as a programmatic dependent of it and waits for it before
@@ -239,6 +239,12 @@ struct Tf32x3Params {
     float alpha, beta;      // epilogue C = alpha * acc + beta * C + bias[col]
     const float *bias;
     int kcb;                // K-chunked kernel: K blocks per chunk (>= 1)
+    // K-chunked kernel schedule (see piece_of): the first tiles_dp tiles are
+    // computed whole; each of the other `tail` tiles is split into `split`
+    // K segments (tail = 0: every tile whole).  Segment j of tail tile t runs
+    // on CTA j * tail + t, and its sum is partial tile j * tail + t of `part`.
+    int tiles_dp, tail, split;
+    float *part;            // [split * tail][BM * BN] partial tiles, row-major
 };
 
 __device__ __forceinline__ void raster(const Tf32x3Params &p, int bid, int &z, int &tm, int &tn) {
@@ -692,31 +698,32 @@ struct Chunked {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// Stores 32 rows x COLS columns of a finished tile from the running sums of
-// the calling warp's threads (thread `lane` holds row m0 + 32q + lane, columns
-// n0 .. n0 + COLS - 1), 32 columns at a time through the warp's 4 KB staging
-// block (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7), so
-// the eight rows a quarter-warp writes, and the 32 columns of one row the warp
-// reads back, hit distinct banks).
-//   TMA path (p.tma_c): one lane stores the block with a TMA tensor store,
-//   after the previous block's store has read the staging block; `cc` counts
-//   the blocks staged so far.
-//   Otherwise the warp reads the block back a row at a time, lane j taking
-//   column j, and stores it with the epilogue: each store is one 128-byte row
-//   segment.
+// Stores 32 rows x COLS columns of running sums from the calling warp's
+// threads (thread `lane` holds row m0 + 32q + lane, columns n0 .. n0 + COLS
+// - 1 of a rows x cols matrix), 32 columns at a time through the warp's 4 KB
+// staging block (128-byte swizzle: 16-byte chunk j of row r at chunk
+// j ^ (r & 7), so the eight rows a quarter-warp writes, and the 32 columns of
+// one row the warp reads back, hit distinct banks).
+//   tma: one lane stores the block with a TMA tensor store through `map`
+//   (C, or the partial tiles as [slot][BM][BN]) at (n0 + 32c, row, z), after
+//   the previous block's store has read the staging block; `cc` counts the
+//   blocks stored this way so far.
+//   Otherwise (C only) the warp reads the block back a row at a time, lane j
+//   taking column j, and stores it with the epilogue: each store is one
+//   128-byte row segment.
 template <int COLS>
-__device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const CUtensorMap *tmC,
-                                                   const float (&run)[COLS], int q, int lane,
-                                                   int z, int m0, int n0, uint32_t stage,
-                                                   int &cc) {
+__device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const CUtensorMap *map,
+                                                   bool tma, const float (&run)[COLS], int q,
+                                                   int lane, int z, int m0, int n0, int rows,
+                                                   int cols, uint32_t stage, int &cc) {
     const int row0 = m0 + 32 * q;
-    if (row0 >= p.M) return;
+    if (row0 >= rows) return;
     const uint32_t rbase = stage + (uint32_t)lane * 128u;
 #pragma unroll
     for (int c = 0; c < COLS / 32; ++c) {
-        if (n0 + 32 * c >= p.N) break;
-        if (p.tma_c && cc > 0) {
-            if (lane == 0) tc::bulk_wait_group_read<0>();   // the previous block has been read
+        if (n0 + 32 * c >= cols) break;
+        if (cc > 0) {
+            if (lane == 0) tc::bulk_wait_group_read<0>();   // the previous store has read the block
         }
         __syncwarp();   // (and, without TMA, the warp's reads of the previous block are done)
 #pragma unroll
@@ -724,11 +731,11 @@ __device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const 
             tc::st_shared_v4(rbase + ((uint32_t)(j ^ (lane & 7)) << 4), run[32 * c + 4 * j],
                              run[32 * c + 4 * j + 1], run[32 * c + 4 * j + 2],
                              run[32 * c + 4 * j + 3]);
-        if (p.tma_c) {
+        if (tma) {
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tc::tma_store_3d(tmC, stage, n0 + 32 * c, row0, z);
+                tc::tma_store_3d(map, stage, n0 + 32 * c, row0, z);
                 tc::bulk_commit_group();
             }
             ++cc;
@@ -759,9 +766,116 @@ __device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const 
     }
 }
 
-// One CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... (as the
-// persistent kernel); tile i's chunk c is the CTA's chunk gc = i * nchunks + c,
-// in accumulator gc % 2.  Barriers: a ring stage's j-th fill is waited on with
+// The K-chunked kernel's schedule over its G CTAs.  The first tiles_dp tiles
+// (whole waves) are computed whole, tile c + i*G on CTA c.  The remaining
+// `tail` tiles, fewer than G, would leave G - tail SMs idle for a whole tile
+// time; instead each is split into `split` = G / tail segments of K blocks
+// [j * kblocks / split, (j+1) * kblocks / split), and segment j of tail tile
+// t runs on CTA j * tail + t, after its whole tiles.  The segments of one
+// index start together and walk K in step, so tiles sharing an operand
+// panel read the same K slices at about the same time and L2 serves the
+// repeats, as it does for the whole-tile waves.  (Dealing the tail's K
+// blocks out evenly over all CTAs, stream-K style, starts every CTA at a
+// different K offset: at 3072^3 that read 637 MB from DRAM against 251 MB
+// and ran 12 % slower.)  A segment's sum is a partial tile, which
+// tf32x3_fixup_kernel adds in K order.
+struct Piece {
+    int t;          // tile index (batch-major, as raster() takes it)
+    int kb0, kb1;   // K blocks [kb0, kb1)
+    int slot;       // -1: the whole tile, stored to C; else its partial tile
+};
+
+__device__ __forceinline__ int piece_count(const Tf32x3Params &p, int c, int G) {
+    const int ndp = c < p.tiles_dp ? (p.tiles_dp - 1 - c) / G + 1 : 0;
+    return ndp + (c < p.split * p.tail ? 1 : 0);
+}
+
+__device__ __forceinline__ Piece piece_of(const Tf32x3Params &p, int c, int G, int kblocks,
+                                          int i) {
+    Piece pc;
+    const int ndp = c < p.tiles_dp ? (p.tiles_dp - 1 - c) / G + 1 : 0;
+    if (i < ndp) {
+        pc.t = c + i * G;
+        pc.kb0 = 0;
+        pc.kb1 = kblocks;
+        pc.slot = -1;
+        return pc;
+    }
+    const int j = c / p.tail, tl = c - j * p.tail;
+    pc.t = p.tiles_dp + tl;
+    pc.kb0 = (int)((long long)j * kblocks / p.split);
+    pc.kb1 = (int)(((long long)j + 1) * kblocks / p.split);
+    pc.slot = c;
+    return pc;
+}
+
+// Adds the `split` partial tiles of every tail tile and stores the sums to C
+// with the epilogue: grid (BM * BN / (1024 * kFixupVecs), tail) x 256
+// threads, kFixupVecs float4 per thread 1024 floats apart (each load and
+// store instruction coalesced across the warp), every load of a segment
+// issued before its adds, segments added in K order starting from zero.
+// Launched as a programmatic dependent of the GEMM kernel.
+constexpr int kFixupVecs = 4;
+
+template <int BN>
+__global__ void __launch_bounds__(256) tf32x3_fixup_kernel(const Tf32x3Params p) {
+    constexpr int V = kFixupVecs;
+    static_assert((BM * BN) % (1024 * V) == 0, "whole float4 groups per CTA");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int tl = blockIdx.y;
+    const int e0 = (blockIdx.x * 256 * V + threadIdx.x) * 4;
+    float4 acc[V];
+#pragma unroll
+    for (int r = 0; r < V; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < p.split; ++j) {
+        const float *piece = p.part + ((long long)j * p.tail + tl) * (BM * BN) + e0;
+        float4 v[V];
+#pragma unroll
+        for (int r = 0; r < V; ++r) v[r] = *reinterpret_cast<const float4 *>(piece + 1024 * r);
+#pragma unroll
+        for (int r = 0; r < V; ++r) {
+            acc[r].x += v[r].x;
+            acc[r].y += v[r].y;
+            acc[r].z += v[r].z;
+            acc[r].w += v[r].w;
+        }
+    }
+    int z, tm, tn;
+    raster(p, p.tiles_dp + tl, z, tm, tn);
+    const bool plain = p.alpha == 1.f && p.beta == 0.f && p.bias == nullptr;
+#pragma unroll
+    for (int r = 0; r < V; ++r) {
+        const int e = e0 + 1024 * r;
+        const int row = tm * BM + e / BN, col = tn * BN + e % BN;
+        if (row >= p.M || col >= p.N) continue;
+        float *cp = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc + col;
+        float o[4] = {acc[r].x, acc[r].y, acc[r].z, acc[r].w};
+        if (!plain) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (col + j >= p.N) break;
+                const float old = p.beta != 0.f ? cp[j] : 0.f;
+                const float b = p.bias != nullptr ? p.bias[col + j] : 0.f;
+                o[j] = fmaf(p.beta, old, p.alpha * o[j]) + b;
+            }
+        }
+        if (p.vec_c && col + 3 < p.N) {
+            *reinterpret_cast<float4 *>(cp) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (col + j < p.N) cp[j] = o[j];
+        }
+    }
+}
+
+// One CTA per SM walks its pieces (piece_of: whole tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ..., then at most one K segment of a tail tile).  A piece's K
+// blocks split into chunks at the multiples of the chunk length (kcb blocks),
+// so a piece that starts or ends inside a chunk has a shorter first or last
+// chunk; the CTA's chunks are counted across pieces (gc) and chunk gc goes to
+// accumulator gc % 2, and its K blocks are counted across pieces (g) for the
+// ring.  Barriers: a ring stage's j-th fill is waited on with
 // parity j & 1 and its (j-1)-th release with parity (j-1) & 1 (as in the
 // persistent kernel); accumulator s's u-th chunk ("chunk full", one
 // tcgen05.commit) with parity u & 1 and its (u-1)-th drain ("chunk free", one
@@ -775,7 +889,8 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmAlo,
                       const __grid_constant__ CUtensorMap tmBlo,
-                      const __grid_constant__ CUtensorMap tmC, const Tf32x3Params p) {
+                      const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmP, const Tf32x3Params p) {
     using P = Chunked<CFG>;
     constexpr int BK = CFG::BK, STAGES = CFG::STAGES, PLANES = CFG::PLANES;
     constexpr int BN = CFG::BN;
@@ -799,10 +914,9 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int total = p.batch * p.tiles_m * p.tiles_n;
-    const int nlocal = ((int)blockIdx.x < total) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int kblocks = (p.K + BK - 1) / BK;
-    const int nchunks = (kblocks + KCB - 1) / KCB;
+    const int cta = (int)blockIdx.x, G = (int)gridDim.x;
+    const int npieces = piece_count(p, cta, G);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -834,13 +948,14 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
             // ---------------- TMA producer (the ring runs on across tiles)
             long long issued = 0;
+            long long g = 0;   // the CTA's K blocks so far
             bool stop = false;
-            for (int i = 0; i < nlocal && !stop; ++i) {
+            for (int i = 0; i < npieces && !stop; ++i) {
+                const Piece pc = piece_of(p, cta, G, kblocks, i);
                 int z, tm, tn;
-                raster(p, (int)blockIdx.x + i * (int)gridDim.x, z, tm, tn);
+                raster(p, pc.t, z, tm, tn);
                 const int m0 = tm * BM, n0 = tn * BN;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    const long long g = (long long)i * kblocks + kb;
+                for (int kb = pc.kb0; kb < pc.kb1; ++kb, ++g) {
                     const int s = (int)(g % STAGES);
                     const int j = (int)(g / STAGES);
                     if (g >= STAGES && !tc::mbar_wait(empty0 + 8 * s, (j & 1) ^ 1, abort_flag)) {
@@ -877,10 +992,10 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             if (*abort_flag) {
                 // the latest fill of every stage lands before the CTA exits
-                for (long long g = (issued > STAGES ? issued - STAGES : 0); g < issued; ++g) {
-                    const int s = (int)(g % STAGES);
+                for (long long f = (issued > STAGES ? issued - STAGES : 0); f < issued; ++f) {
+                    const int s = (int)(f % STAGES);
                     const long long t0 = clock64();
-                    while (!tc::mbar_try_wait(full0 + 8 * s, (int)((g / STAGES) & 1)) &&
+                    while (!tc::mbar_try_wait(full0 + 8 * s, (int)((f / STAGES) & 1)) &&
                            clock64() - t0 < tc::kWaitLimitCycles) {
                     }
                 }
@@ -892,8 +1007,10 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
             constexpr uint32_t idesc = tc::tf32_idesc<BM, BN>();
             bool stop = false;
             long long gc = 0;   // the CTA's chunk counter
-            for (int i = 0; i < nlocal && !stop; ++i) {
-                for (int c = 0; c < nchunks; ++c, ++gc) {
+            long long g = 0;    // the CTA's K blocks so far
+            for (int i = 0; i < npieces && !stop; ++i) {
+                const Piece pc = piece_of(p, cta, G, kblocks, i);
+                for (int c = pc.kb0 / KCB; c <= (pc.kb1 - 1) / KCB; ++c, ++gc) {
                     const int sl = (int)(gc % NSLOT);
                     const long long u = gc / NSLOT;
                     if (gc >= NSLOT && !tc::mbar_wait(che0 + 8 * sl, (int)((u - 1) & 1), abort_flag)) {
@@ -902,10 +1019,9 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                     tc::fence_after_sync();
                     const uint32_t acc = tmem + (uint32_t)(sl * P::SLOT_COLS);
-                    const int kb0 = c * KCB;
-                    const int kb1 = min(kblocks, kb0 + KCB);
-                    for (int kb = kb0; kb < kb1; ++kb) {
-                        const long long g = (long long)i * kblocks + kb;
+                    const int kb0 = max(pc.kb0, c * KCB);
+                    const int kb1 = min(pc.kb1, (c + 1) * KCB);
+                    for (int kb = kb0; kb < kb1; ++kb, ++g) {
                         const int s = (int)(g % STAGES);
                         if (!tc::mbar_wait(full0 + 8 * s, (int)((g / STAGES) & 1), abort_flag)) {
                             stop = true;
@@ -949,11 +1065,12 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
         int cc = 0;
         long long gc = 0;
         bool stop = false;
-        for (int i = 0; i < nlocal && !stop; ++i) {
+        for (int i = 0; i < npieces && !stop; ++i) {
+            const Piece pc = piece_of(p, cta, G, kblocks, i);
             float run[COLS];
 #pragma unroll
             for (int j = 0; j < COLS; ++j) run[j] = 0.f;
-            for (int c = 0; c < nchunks; ++c, ++gc) {
+            for (int c = pc.kb0 / KCB; c <= (pc.kb1 - 1) / KCB; ++c, ++gc) {
                 const int sl = (int)(gc % NSLOT);
                 const long long u = gc / NSLOT;
                 const bool ok = tc::mbar_wait(chf0 + 8 * sl, (int)(u & 1), abort_flag);
@@ -983,12 +1100,18 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (lane == 0) tc::mbar_arrive(che0 + 8 * sl);
             }
             if (stop) break;
+            // a whole tile to C, a segment's sum to its partial tile (whole)
             int z, tm, tn;
-            raster(p, (int)blockIdx.x + i * (int)gridDim.x, z, tm, tn);
-            store_running_rows<COLS>(p, &tmC, run, q, lane, z, tm * BM, tn * BN + h * COLS, stage,
-                                     cc);
+            raster(p, pc.t, z, tm, tn);
+            const bool part = pc.slot >= 0;
+            store_running_rows<COLS>(p, part ? &tmP : &tmC, part || p.tma_c, run, q, lane,
+                                     part ? pc.slot : z, part ? 0 : tm * BM,
+                                     (part ? 0 : tn * BN) + h * COLS, part ? BM : p.M,
+                                     part ? BN : p.N, stage, cc);
         }
-        if (lane == 0 && cc > 0) tc::bulk_wait_group_read<0>();
+        // the stores' global writes are done before the CTA ends (the fix-up
+        // kernel reads the partial tiles)
+        if (lane == 0 && cc > 0) tc::bulk_wait_group<0>();
     }
     __syncwarp();
 
@@ -1166,6 +1289,21 @@ bool make_c_map(CUtensorMap *map, float *C, int M, int N, int64_t ldc, int64_t s
     return r == CUDA_SUCCESS;
 }
 
+// The partial tiles as a [slots][BM][bn] tensor, box 32 x 32 x 1 with the
+// 128-byte swizzle the epilogue stages in.
+bool make_part_map(CUtensorMap *map, float *part, int slots, int bn) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)bn, (cuuint64_t)BM, (cuuint64_t)slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)bn * 4, (cuuint64_t)BM * bn * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Floats per row of a TF32 plane: K rounded up to 32, so every row starts on
@@ -1251,6 +1389,10 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int co
     p.beta = a.beta;
     p.bias = a.bias;
     p.kcb = 1;
+    p.tiles_dp = a.batch * p.tiles_m * p.tiles_n;
+    p.tail = 0;
+    p.split = 0;
+    p.part = nullptr;
     // The TMA store takes the plain product into a C whose base, rows and
     // batches are 16-byte aligned and whose width is a whole number of
     // 16-byte granules: with N not a multiple of 4 the store was seen to
@@ -1421,9 +1563,44 @@ cudaError_t launch_persistent(const GemmArgs &a, bool transA, bool transB, void 
 // An operand stored K-contiguous with 16-byte aligned rows is loaded raw as
 // its own hi term with a lo-only plane from the split kernel; other operands
 // get hi and lo planes.
+// The K-chunked kernel's schedule for `tiles` output tiles BN wide of
+// `kblocks` K blocks on `sms` SMs, one CTA per SM (see piece_of): whole waves
+// of tiles, then the tail split into G / tail K segments when that is at
+// least two, each segment at least two K blocks; the segments' partial
+// tiles take split * tail * BM * BN floats of workspace.
+struct ChunkedPlan {
+    int G, tiles_dp, tail, split;
+    size_t part_bytes;
+};
+
+ChunkedPlan chunked_plan(long long tiles, int kblocks, int bn, int sms) {
+    ChunkedPlan pl = {};
+    pl.G = (int)(tiles < sms ? tiles : sms);
+    pl.tiles_dp = (int)tiles;
+    const long long tail = tiles % sms;
+    if (sms < 2 || tail == 0) return pl;
+    int split = (int)(sms / tail);
+    if (split > kblocks / 2) split = kblocks / 2;
+    if (split < 2) return pl;
+    pl.G = sms;
+    pl.tiles_dp = (int)(tiles - tail);
+    pl.tail = (int)tail;
+    pl.split = split;
+    pl.part_bytes = (size_t)split * (size_t)tail * BM * (size_t)bn * sizeof(float);
+    return pl;
+}
+
+template <class CFG>
+ChunkedPlan chunked_plan_for(const GemmArgs &a, int sms) {
+    const long long tiles =
+        (long long)a.batch * ((a.M + BM - 1) / BM) * ((a.N + CFG::BN - 1) / CFG::BN);
+    return chunked_plan(tiles, (a.K + CFG::BK - 1) / CFG::BK, CFG::BN, sms);
+}
+
 template <class CFG, int RAW>
 cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void *ws,
-                               cudaStream_t s, CUtensorMap &tmA, CUtensorMap &tmB) {
+                               size_t ws_bytes, cudaStream_t s, CUtensorMap &tmA,
+                               CUtensorMap &tmB) {
     using P = Chunked<CFG>;
     static PerContext<bool> configured;
     cudaError_t e = ensure_smem(tf32x3_chunked_kernel<CFG, RAW>, P::SMEM_BYTES, configured);
@@ -1438,9 +1615,22 @@ cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void
     e = prepare<CFG>(a, transA, transB, RAW, 0, ws, s, tmA, tmB, tmAlo, tmBlo, tmC, p);
     if (e != cudaSuccess) return e;
     p.kcb = g_chunk_k.load(std::memory_order_relaxed) / CFG::BK;
-    const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
+    // the partial tiles follow the planes; a workspace without room for them
+    // keeps the whole-tile schedule
+    const size_t planes = plane_bytes(a.M, a.K, a.batch, 2) + plane_bytes(a.N, a.K, a.batch, 2);
+    ChunkedPlan pl = chunked_plan_for<CFG>(a, sms);
+    if (pl.split > 0 && ws_bytes >= planes + pl.part_bytes) {
+        p.tiles_dp = pl.tiles_dp;
+        p.tail = pl.tail;
+        p.split = pl.split;
+        p.part = reinterpret_cast<float *>(static_cast<char *>(ws) + planes);
+    } else {
+        const long long tiles = (long long)a.batch * p.tiles_m * p.tiles_n;
+        pl.G = (int)(tiles < sms ? tiles : sms);
+        pl.split = 0;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
+    cfg.gridDim = dim3((unsigned)pl.G);
     cfg.blockDim = dim3(P::THREADS);
     cfg.dynamicSmemBytes = P::SMEM_BYTES;
     cfg.stream = s;
@@ -1449,7 +1639,18 @@ cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tf32x3_chunked_kernel<CFG, RAW>, tmA, tmB, tmAlo, tmBlo, tmC, p);
+    CUtensorMap tmP = {};
+    if (pl.split > 0 && !make_part_map(&tmP, p.part, pl.split * pl.tail, CFG::BN))
+        return cudaErrorInvalidValue;
+    e = cudaLaunchKernelEx(&cfg, tf32x3_chunked_kernel<CFG, RAW>, tmA, tmB, tmAlo, tmBlo, tmC, tmP,
+                           p);
+    if (e != cudaSuccess) return e;
+    if (pl.split == 0) return cudaGetLastError();
+    // the tail tiles' sums, as a programmatic dependent of the GEMM
+    cfg.gridDim = dim3((unsigned)(BM * CFG::BN / (1024 * kFixupVecs)), (unsigned)pl.tail);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, tf32x3_fixup_kernel<CFG::BN>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1460,7 +1661,8 @@ cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void
 // each slice straddles sectors, and the split kernel's planes are the cheaper
 // route (3000 x 2000 x 1500 with row-major A of ld 1500).
 template <class CFG>
-cudaError_t launch_chunked(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+cudaError_t launch_chunked(const GemmArgs &a, bool transA, bool transB, void *ws, size_t ws_bytes,
+                           cudaStream_t s) {
     static_assert(CFG::PLANES == 2, "three terms");
     auto raw_ok = [&](const float *X, int64_t ld, int64_t sX, bool kcontig) {
         return kcontig && reinterpret_cast<uintptr_t>(X) % 128 == 0 && ld % 32 == 0 &&
@@ -1475,10 +1677,10 @@ cudaError_t launch_chunked(const GemmArgs &a, bool transA, bool transB, void *ws
         make_raw_map<CFG>(&tmB, a.B, a.N, a.K, a.ldb, a.strideB, a.batch, CFG::BN))
         raw |= 2;
     switch (raw) {
-        case 1: return launch_chunked_raw<CFG, 1>(a, transA, transB, ws, s, tmA, tmB);
-        case 2: return launch_chunked_raw<CFG, 2>(a, transA, transB, ws, s, tmA, tmB);
-        case 3: return launch_chunked_raw<CFG, 3>(a, transA, transB, ws, s, tmA, tmB);
-        default: return launch_chunked_raw<CFG, 0>(a, transA, transB, ws, s, tmA, tmB);
+        case 1: return launch_chunked_raw<CFG, 1>(a, transA, transB, ws, ws_bytes, s, tmA, tmB);
+        case 2: return launch_chunked_raw<CFG, 2>(a, transA, transB, ws, ws_bytes, s, tmA, tmB);
+        case 3: return launch_chunked_raw<CFG, 3>(a, transA, transB, ws, ws_bytes, s, tmA, tmB);
+        default: return launch_chunked_raw<CFG, 0>(a, transA, transB, ws, ws_bytes, s, tmA, tmB);
     }
 }
 
@@ -1517,8 +1719,27 @@ bool tc_wide_tile(const GemmArgs &a, int terms) {
 
 }  // namespace
 
-size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
+size_t tf32x3_workspace_min_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
     return tf32x3::plane_bytes(M, K, batch, 2) + tf32x3::plane_bytes(N, K, batch, 2);
+}
+
+// The planes, then (K-chunked kernel whose tail tiles are split in K on this
+// device) the segments' partial tiles.
+size_t tf32x3_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
+    const size_t planes = tf32x3_workspace_min_bytes(M, N, K, batch);
+    if (K <= tf32x3::kChunkMinK || M <= 0 || N <= 0 || batch <= 0) return planes;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return planes;
+    GemmArgs a = {};
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.batch = (int)batch;
+    const tf32x3::ChunkedPlan pl = tc_wide_tile(a, 3) ? tf32x3::chunked_plan_for<Tf32x3Wide>(a, sms)
+                                                      : tf32x3::chunked_plan_for<Tf32x3Narrow>(a, sms);
+    return planes + pl.part_bytes;
 }
 
 size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
@@ -1529,11 +1750,13 @@ size_t tf32_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t batch) {
 // kernel (128-wide tiles, converter warps where they pay); longer ones the
 // K-chunked kernel, whose sums are promoted to round-to-nearest fp32 adds
 // every 128 of K, on the tile width the wave count favours.
-cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {
+cudaError_t launch_tf32x3(const GemmArgs &a, bool transA, bool transB, void *ws, size_t ws_bytes,
+                          cudaStream_t s) {
     if (a.K <= tf32x3::kChunkMinK)
         return tf32x3::launch_persistent<Tf32x3Narrow, 2>(a, transA, transB, ws, s);
-    return tc_wide_tile(a, 3) ? tf32x3::launch_chunked<Tf32x3Wide>(a, transA, transB, ws, s)
-                              : tf32x3::launch_chunked<Tf32x3Narrow>(a, transA, transB, ws, s);
+    return tc_wide_tile(a, 3)
+               ? tf32x3::launch_chunked<Tf32x3Wide>(a, transA, transB, ws, ws_bytes, s)
+               : tf32x3::launch_chunked<Tf32x3Narrow>(a, transA, transB, ws, ws_bytes, s);
 }
 
 cudaError_t launch_tf32(const GemmArgs &a, bool transA, bool transB, void *ws, cudaStream_t s) {

@@ -231,16 +231,22 @@ uint64_t sgemm_f32_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int sp
  * rounding of lo are each below 2^-20 of |a||b| per product, so results meet
  * the same elementwise bound as
  * sgemm_f32; small-integer inputs are exact.  Not bit-identical to
- * sgemm_f32 (different summation order), deterministic across calls.
+ * sgemm_f32 (different summation order), deterministic across calls on the
+ * same device with the same workspace size.
  * Defined by: "CUDA GEMM operator performance optimization", section 1.1
  * (GEMM); the TF32 accuracy trade-off it removes is the FMA vs TF32 RRMSE
  * comparison (1.03e-6 vs 7.78e-4) on the ChetanC28/cuda-kernels page.
  *
- * Arguments as sgemm_f32, plus a caller-owned DEVICE workspace of at least
+ * Arguments as sgemm_f32, plus a caller-owned DEVICE workspace of
  * sgemm_f32_tf32x3_workspace_size(M, N, K, 1) bytes, 256-byte aligned, not
  * overlapping A, B or C, and not used by other work while this call's
- * kernels run on `stream` (it holds the split operands).
- * SGEMM_EWORKSPACE if it is NULL, misaligned or too small.
+ * kernels run on `stream` (it holds the split operands).  A workspace of only
+ * the planes' bytes (2 * (M + N) * round_up(K, 32) floats, each operand's
+ * part rounded up to 256 bytes) is accepted too: the call then computes
+ * every output tile whole, instead of splitting in K the tiles of a last
+ * wave that would leave at least half the SMs idle, and those tiles' sums
+ * may differ in the last bit.
+ * SGEMM_EWORKSPACE if it is NULL, misaligned or smaller than the planes.
  */
 int sgemm_f32_tf32x3(int64_t M, int64_t N, int64_t K,
                      const float *A, int64_t lda,
@@ -266,11 +272,15 @@ int sgemm_f32_tf32x3_strided_batched(int64_t M, int64_t N, int64_t K,
                                      int64_t batch, int transA, int transB,
                                      void *workspace, uint64_t workspace_bytes, void *stream);
 
-/* Workspace bytes the tf32x3 entry points need: the hi and lo TF32 planes of
- * op(A) and op(B), 2 * batch * (M + N) * round_up(K, 32) floats plus padding
- * (an operand stored K-contiguous with aligned rows, 16 bytes for K <= 256
- * and 128 bytes above, is read as its own hi term and uses only its lo plane,
- * but the size does not depend on the pointers).  0 for empty problems or negative sizes. */
+/* Workspace bytes for the tf32x3 entry points on the current device: the hi
+ * and lo TF32 planes of op(A) and op(B), 2 * batch * (M + N) * round_up(K, 32)
+ * floats plus padding (an operand stored K-contiguous with aligned rows, 16
+ * bytes for K <= 256 and 128 bytes above, is read as its own hi term and uses
+ * only its lo plane, but the size does not depend on the pointers), then, for
+ * K > 256 when the last wave of output tiles leaves at least half the SMs
+ * idle, the partial tiles of those tiles' K segments (at most one 128 x 256
+ * fp32 tile per SM, 19.9 MB on GB300).  0 for empty problems or negative
+ * sizes. */
 uint64_t sgemm_f32_tf32x3_workspace_size(int64_t M, int64_t N, int64_t K, int64_t batch);
 
 /*
@@ -317,10 +327,13 @@ uint64_t sgemm_f32_tf32_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
  * library reserves on every GPU that loads it, for the life of the process.
  * There is no counterpart on the source pages; it exists for these callers.
  *
- * Arguments, layout, precision and results as sgemm_f32_tf32x3 (no batch).
+ * Arguments, layout, precision and results as sgemm_f32_tf32x3 (no batch)
+ * with a workspace of the scratch's size.
  * Limit: 2 * (M + N) * round_up(K, 32) * 4 bytes (plus 256-byte alignment
  * padding) must fit in the scratch, e.g. M = N = K = 2048; larger problems
- * return SGEMM_EWORKSPACE with the sizes in sgemm_last_error().
+ * return SGEMM_EWORKSPACE with the sizes in sgemm_last_error().  Where the
+ * partial tiles of split tail tiles fit as well, the call splits them as
+ * sgemm_f32_tf32x3 does.
  * The first call in each CUDA context (per device, and again after
  * cudaDeviceReset or when another context is made current) looks up the
  * scratch's device address (cudaGetSymbolAddress); make that first call

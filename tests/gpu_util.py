@@ -19,13 +19,25 @@ def _upload(arr: np.ndarray, offset: int):
     return buf, buf.data_ptr() + 4 * (GUARD + offset)
 
 
+def tf32x3_planes_bytes(M: int, N: int, K: int, batch: int) -> int:
+    """The least workspace of the tf32x3 entry points: the hi and lo planes of
+    op(A) and op(B), rows of round_up(K, 32) floats, each operand's region
+    rounded up to 256 bytes (no room for the partial tiles of tail tiles
+    split in K)."""
+    Kp = (K + 31) // 32 * 32
+    region = lambda rows: (2 * batch * rows * Kp * 4 + 255) // 256 * 256
+    return region(M) + region(N)
+
+
 def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
-        stream=None, splits: int = 0) -> np.ndarray:
+        stream=None, splits: int = 0, planes_only: bool = False) -> np.ndarray:
     """Run the case on the GPU; returns C (batch, M, N).
 
     ``offset`` shifts every buffer by that many floats (4-byte aligned only when
-    offset % 4 != 0), exercising the scalar-access path.  Asserts that the guard
-    bands and the padding columns of C are still NaN afterwards.
+    offset % 4 != 0), exercising the scalar-access path.  ``planes_only`` gives
+    a tf32x3 entry only the planes' bytes of workspace (whole-tile schedule).
+    Asserts that the guard bands and the padding columns of C are still NaN
+    afterwards.
     """
     import torch
     batch, M, N, K = case["batch"], case["M"], case["N"], case["K"]
@@ -51,6 +63,8 @@ def run(case: dict, *, entry: str = "sgemm_f32", offset: int = 0, strideB=None,
     if "tf32" in entry:
         size = sg.tf32x3_workspace_size if "tf32x3" in entry else sg.tf32_workspace_size
         need = size(M, N, K, batch)
+        if planes_only:
+            need = tf32x3_planes_bytes(M, N, K, batch)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
         extra = (ws.data_ptr(), need)
     if entry.endswith("strided_batched"):

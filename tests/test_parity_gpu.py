@@ -13,7 +13,7 @@ import dense_fp32_matrix_sgemm_gb300 as sg
 import oracle
 import workloads
 
-from gpu_util import run
+from gpu_util import run, tf32x3_planes_bytes
 
 pytestmark = pytest.mark.gpu
 
@@ -337,6 +337,48 @@ def test_chunked_tensor_kernel(M, N, K, tA, tB, batch, offset, dist):
     check_full(case, got, exact=dist == "int", label=f"chunked {M}x{N}x{K}x{batch} {tA}{tB}")
 
 
+# Tail tiles split in K: when the last wave of tiles leaves at least half of
+# the 152 SMs idle (or there is less than one wave), each of those tiles is
+# split into SMs / tail K segments that run side by side, and a fix-up kernel
+# adds the segments' partial tiles in K order, then applies the epilogue.
+# Both tile widths, whole waves before the tail or none, segments that start
+# and end inside a chunk, a batch, C without 16-byte alignment (the fix-up's
+# scalar stores), N not a multiple of 4.  Against the oracle in full; exact on
+# small integers and then bit-identical to the whole-tile schedule (a
+# workspace of the planes' bytes alone); on normal data the result does not
+# change between calls.
+CHUNKED_SK = [  # M, N, K, tA, tB, batch, offset, dist
+    (2500, 1999, 513, 0, 0, 1, 0, "int"),      # 128 x 128 tiles: 2 waves, 16 tiles in 8
+    (1000, 1100, 1000, 1, 1, 1, 0, "int"),     # 72 tiles, 2 segments each
+    (1024, 1024, 300, 0, 1, 5, 0, "int"),      # 320 tiles over 5 problems: 2 waves + 16 in 5
+    (4000, 4000, 777, 1, 0, 1, 1, "normal"),   # 128 x 256: 3 waves + 56, misaligned C
+    (700, 900, 300, 0, 0, 1, 0, "normal"),     # 48 tiles, 3 segments of 10 K blocks
+    (512, 512, 4096, 0, 0, 1, 0, "normal"),    # 16 tiles, 9 segments
+]
+
+
+@pytest.mark.parametrize("M,N,K,tA,tB,batch,offset,dist", CHUNKED_SK)
+def test_chunked_split_tail(M, N, K, tA, tB, batch, offset, dist):
+    import torch
+    assert torch.cuda.get_device_properties(0).multi_processor_count == 152
+    pad = lambda d: (-d) % 4 + 4
+    lda = (M if tA else K) + pad(M if tA else K)
+    ldb = (K if tB else N) + pad(K if tB else N)
+    case = workloads.make_operands(M, N, K, batch=batch, transA=tA, transB=tB, lda=lda, ldb=ldb,
+                                   ldc=N + 3, dist=dist, poison=True, seed=94,
+                                   key=940 + M + N + K + tA + 2 * tB)
+    entry = "sgemm_f32_tf32x3_strided_batched" if batch > 1 else "sgemm_f32_tf32x3"
+    assert sg.tf32x3_workspace_size(M, N, K, batch) > tf32x3_planes_bytes(M, N, K, batch)
+    assert sg.device_status(reset=True) == 0
+    got = run(case, entry=entry, offset=offset)
+    assert sg.device_status(reset=True) == 0, "a pipeline wait ran out"
+    check_full(case, got, exact=dist == "int", label=f"split tail {M}x{N}x{K}x{batch} {tA}{tB}")
+    if dist == "int":
+        assert np.array_equal(got, run(case, entry=entry, offset=offset, planes_only=True))
+    else:
+        assert np.array_equal(got, run(case, entry=entry, offset=offset)), "not deterministic"
+
+
 # K-contiguous operands whose rows start on 128-byte boundaries (leading
 # dimension a multiple of 32 floats) are read raw by the K-chunked kernel as
 # their own hi term, next to a lo-only plane; rows only 16-byte aligned go
@@ -366,7 +408,7 @@ def test_chunked_raw_rows(M, N, K, tA, tB, batch):
     check_full(case, raw, label=f"chunked raw {M}x{N}x{K}x{batch} {tA}{tB}")
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 270, 700), (2000, 2048, 1000)])
+@pytest.mark.parametrize("M,N,K", [(300, 270, 700), (2000, 2048, 1000), (2500, 2048, 700)])
 def test_chunked_tensor_epilogue(M, N, K):
     case = workloads.make_operands(M, N, K, transB=1, ldc=N + 2, dist="normal", seed=91,
                                    key=910 + M)

@@ -447,18 +447,26 @@ def test_tensor_persistent_pipeline(stages, acc_bufs, conv, nlocal, kblocks):
 
 # ------------------------------------------------------------ K-chunked tensor kernel
 
-def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
-    """tf32x3_chunked_kernel: the ring as in the persistent kernel; tile i's
-    chunk c (K blocks [c * kcb, min(kblocks, (c + 1) * kcb))) is the CTA's
-    chunk gc = i * nchunks + c, accumulated in chunk accumulator gc % nslot.
+def piece_chunks(kb0, kb1, kcb):
+    """The chunks of a piece of K blocks [kb0, kb1): split at the multiples of
+    kcb (tf32x3_chunked_kernel)."""
+    return [(max(kb0, c * kcb), min(kb1, (c + 1) * kcb))
+            for c in range(kb0 // kcb, (kb1 - 1) // kcb + 1)]
+
+
+def tensor_chunked(pieces, stages, kcb, seed, nslot=2, epi_warps=8):
+    """tf32x3_chunked_kernel: the ring as in the persistent kernel, its fills
+    counted across the CTA's pieces (g); piece i = K blocks [kb0, kb1) of a
+    tile (a whole tile, or a stream-K piece) splits into chunks at the
+    multiples of kcb, and the CTA's chunks, counted across pieces (gc), go to
+    chunk accumulator gc % nslot.
     MMA: before chunk gc >= nslot waits "chunk free" of its accumulator
     (parity (gc / nslot - 1) & 1), then per K block the "full" barrier, and
     commits each stage to "empty" and the finished chunk to "chunk full".
     Epilogue warps (8) wait "chunk full" (parity (gc / nslot) & 1), add the
-    chunk into their running sums and arrive on "chunk free"; after a tile's
-    last chunk they hold the tile's whole sum."""
+    chunk into their running sums and arrive on "chunk free"; after a piece's
+    last chunk they hold the piece's whole sum."""
     rng = random.Random(seed)
-    nchunks = -(-kblocks // kcb)
     full = [Barrier(1, f"full{s}") for s in range(stages)]
     empty = [Barrier(1, f"empty{s}") for s in range(stages)]
     chf = [Barrier(1, f"chunk_full{s}") for s in range(nslot)]
@@ -466,12 +474,12 @@ def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
     ring = [None] * stages
     acc = [None] * nslot              # [chunk gc, K blocks accumulated]
     in_flight, commits = [], []
-    sums = {}                         # (warp, tile) -> K blocks summed
+    sums = {}                         # (warp, piece) -> K blocks summed
 
     def producer():
-        for i in range(nlocal):
-            for kb in range(kblocks):
-                g = i * kblocks + kb
+        g = 0
+        for kb0, kb1 in pieces:
+            for kb in range(kb0, kb1):
                 s = g % stages
                 if g >= stages:
                     while not empty[s].passed(g // stages - 1):
@@ -479,20 +487,20 @@ def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
                 assert ring[s] is None or ring[s]["consumed"], "stage refilled before its MMAs completed"
                 ring[s] = {"g": g, "landed": False, "consumed": False}
                 in_flight.append(g)
+                g += 1
                 yield
 
     def mma():
-        gc = 0
-        for i in range(nlocal):
-            for c in range(nchunks):
+        gc = g = 0
+        for kb0, kb1 in pieces:
+            for c0, c1 in piece_chunks(kb0, kb1, kcb):
                 sl, u = gc % nslot, gc // nslot
                 if gc >= nslot:
                     while not che[sl].passed(u - 1):
                         yield
                 assert acc[sl] is None, "MMAs into a chunk accumulator the epilogue has not drained"
                 acc[sl] = [gc, 0]
-                for kb in range(c * kcb, min(kblocks, (c + 1) * kcb)):
-                    g = i * kblocks + kb
+                for _ in range(c0, c1):
                     s = g % stages
                     while not full[s].passed(g // stages):
                         yield
@@ -500,19 +508,20 @@ def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
                     assert st["g"] == g and st["landed"]
                     acc[sl][1] += 1
                     commits.append(("empty", s, g))
+                    g += 1
                     yield
                 commits.append(("chf", sl, gc))
                 gc += 1
 
     def epilogue(w):
         gc = 0
-        for i in range(nlocal):
+        for i, (kb0, kb1) in enumerate(pieces):
             total = 0
-            for c in range(nchunks):
+            for c0, c1 in piece_chunks(kb0, kb1, kcb):
                 sl, u = gc % nslot, gc // nslot
                 while not chf[sl].passed(u):
                     yield
-                want = min(kblocks, (c + 1) * kcb) - c * kcb
+                want = c1 - c0
                 assert acc[sl] == [gc, want], f"epilogue read {acc[sl]} for chunk {gc}"
                 total += acc[sl][1]
                 if che[sl].pending == 1:
@@ -553,7 +562,8 @@ def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
             next(alive[i])
         except StopIteration:
             alive.pop(i)
-    assert sums == {(w, i): kblocks for w in range(epi_warps) for i in range(nlocal)}
+    assert sums == {(w, i): kb1 - kb0 for w in range(epi_warps)
+                    for i, (kb0, kb1) in enumerate(pieces)}
     assert not in_flight and not commits
 
 
@@ -561,4 +571,15 @@ def tensor_chunked(nlocal, kblocks, stages, kcb, seed, nslot=2, epi_warps=8):
 @pytest.mark.parametrize("nlocal,kblocks", [(2, 9), (3, 8), (1, 1), (4, 3), (2, 193)])
 def test_tensor_chunked_pipeline(stages, kcb, nlocal, kblocks):
     for seed in range(4):
-        tensor_chunked(nlocal, kblocks, stages, kcb, seed)
+        tensor_chunked([(0, kblocks)] * nlocal, stages, kcb, seed)
+
+
+# Pieces of other lengths: whole tiles followed by a K segment of a tail tile
+# that starts and ends inside a chunk, and sequences of segments (one-block
+# chunks at either end included).
+@pytest.mark.parametrize("stages,kcb", [(4, 4), (3, 2)])
+@pytest.mark.parametrize("pieces", [[(0, 9), (0, 9), (5, 9), (0, 2)], [(0, 8), (7, 8), (0, 1)],
+                                    [(3, 10)], [(0, 97), (33, 66)], [(1, 2), (0, 5)]])
+def test_tensor_chunked_pipeline_segments(stages, kcb, pieces):
+    for seed in range(4):
+        tensor_chunked(pieces, stages, kcb, seed)

@@ -73,10 +73,22 @@ def test_noalloc_at_the_scratch_limit():
     assert sg.device_status(reset=True) == 0
 
 
+def test_noalloc_when_only_the_planes_fit():
+    # 72 tiles of 128 x 128 on 152 SMs: with a full workspace each is split
+    # into two K segments, whose partial tiles (9.4 MB) do not fit beside
+    # these planes (63.75 MiB) in the scratch, so the call computes whole
+    # tiles; on small integers both schedules are exact, hence equal
+    cap = sg.tf32x3_noalloc_max_bytes()
+    M, N, K = 1024, 1152, 3840
+    assert sg.tf32x3_workspace_size(M, N, K, 1) > cap
+    _check(workloads.make_operands(M, N, K, dist="int", seed=14, key=403))
+    assert sg.device_status(reset=True) == 0
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     cap = sg.tf32x3_noalloc_max_bytes()
     assert cap == 64 << 20
-    # one 4-wide K group past the limit
+    # one 32-wide K group past the limit (plane rows are round_up(K, 32) floats)
     M, N, K = 2048, 2048, 2052
     assert sg.tf32x3_workspace_size(M, N, K, 1) > cap
     st = sg.sgemm_f32_tf32x3_noalloc(M, N, K, 16, K, 16, N, 16, N, 0, 0, 0, check=False)
