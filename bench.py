@@ -237,14 +237,31 @@ def simt_kernel_label(M, N, batch, transB, sms, K=3072, transA=0):
     return "sgemm_simt_kernel 128x128 tile, BK 32, 2 stages, 2 CTAs/SM, fma.rn.f32x2"
 
 
+def _chunked_split(tiles, kblocks, sms):
+    """K segments per tail tile (csrc/tf32x3.cu chunked_plan), 0 for whole tiles."""
+    tail = tiles % sms
+    split = min(sms // tail, kblocks // 2) if tail else 0
+    return split if split >= 2 else 0
+
+
+def _chunked_cost_us(tiles, K, kblocks, bn, sms):
+    split = _chunked_split(tiles, kblocks, sms)
+    tile_us = 0.019 * K * (1.5 if bn == 256 else 1.0)
+    if split:
+        part = split * (tiles % sms) * 128 * bn * 4
+        return (tiles // sms + 1.0 / split) * tile_us + 2.0 * part / 20e6
+    return (tiles // sms + (1 if tiles % sms else 0)) * tile_us
+
+
 def tc_wide_tile(M, N, K, batch, sms):
-    """The K-chunked kernel's tile width (csrc/tf32x3.cu, tc_wide_tile): a
-    128 x 256 tile counts as 1.75 128 x 128 tiles; tiles per SM rounded up."""
+    """The K-chunked kernel's tile width (csrc/tf32x3.cu, tc_wide_tile and
+    chunked_cost_us)."""
     if K <= 256:
         return False
     tm = -(-M // 128)
     wide, narrow = batch * tm * -(-N // 256), batch * tm * -(-N // 128)
-    return 1.75 * -(-wide // sms) <= -(-narrow // sms)
+    return (_chunked_cost_us(wide, K, -(-K // 16), 256, sms)
+            <= _chunked_cost_us(narrow, K, -(-K // 32), 128, sms))
 
 
 def tc_split_tail(M, N, K, batch, sms):
@@ -256,9 +273,7 @@ def tc_split_tail(M, N, K, batch, sms):
         return 0
     wide = tc_wide_tile(M, N, K, batch, sms)
     bn, bk = (256, 16) if wide else (128, 32)
-    tail = batch * -(-M // 128) * -(-N // bn) % sms
-    split = min(sms // tail, -(-K // bk) // 2) if tail else 0
-    return split if split >= 2 else 0
+    return _chunked_split(batch * -(-M // 128) * -(-N // bn), -(-K // bk), sms)
 
 
 def tc_plan(M, N, K, batch, transA, transB, aligned=True, rows128=True, sms=152):
@@ -296,9 +311,9 @@ def tc_plan(M, N, K, batch, transA, transB, aligned=True, rows128=True, sms=152)
                 "added into fp32 registers by 8 epilogue warps, TMA-store epilogue" +
                 ("; " + ", ".join(parts) if parts else "") + ")")
     launches = 1
-    split = tc_split_tail(M, N, K, batch, sms)
-    if split:
-        gemm += (f", last wave's tiles split into {split} K segments + tf32x3_fixup_kernel "
+    nseg = tc_split_tail(M, N, K, batch, sms)
+    if nseg:
+        gemm += (f", last wave's tiles split into {nseg} K segments + tf32x3_fixup_kernel "
                  "(adds the segments' partial tiles)")
         launches += 1
     if split:

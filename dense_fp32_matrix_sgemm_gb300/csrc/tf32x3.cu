@@ -810,34 +810,45 @@ __device__ __forceinline__ Piece piece_of(const Tf32x3Params &p, int c, int G, i
 }
 
 // Adds the `split` partial tiles of every tail tile and stores the sums to C
-// with the epilogue: grid (BM * BN / (1024 * kFixupVecs), tail) x 256
-// threads, kFixupVecs float4 per thread 1024 floats apart (each load and
-// store instruction coalesced across the warp), every load of a segment
-// issued before its adds, segments added in K order starting from zero.
+// with the epilogue: grid (BM * BN / (1024 * V), tail) x 256 threads, V
+// float4 per thread 1024 floats apart (each load and store instruction
+// coalesced across the warp).  A thread reads 8 / V segments at a time,
+// every load of such a batch issued before its adds, so a long split costs
+// split * V / 8 round trips; the adds go in K order starting from zero.  The
+// launcher takes V = 4 when that still gives a CTA per SM, else V = 1.
 // Launched as a programmatic dependent of the GEMM kernel.
-constexpr int kFixupVecs = 4;
-
-template <int BN>
+template <int BN, int V>
 __global__ void __launch_bounds__(256) tf32x3_fixup_kernel(const Tf32x3Params p) {
-    constexpr int V = kFixupVecs;
+    constexpr int NB = 8 / V;   // segments per batch
     static_assert((BM * BN) % (1024 * V) == 0, "whole float4 groups per CTA");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tl = blockIdx.y;
-    const int e0 = (blockIdx.x * 256 * V + threadIdx.x) * 4;
+    const int e0 = (blockIdx.x * 256 * V + threadIdx.x) * 4;   // element of the BM x BN tile
+    const long long seg = (long long)p.tail * (BM * BN);        // floats between segments
+    const float *base = p.part + (long long)tl * (BM * BN) + e0;
     float4 acc[V];
 #pragma unroll
     for (int r = 0; r < V; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < p.split; ++j) {
-        const float *piece = p.part + ((long long)j * p.tail + tl) * (BM * BN) + e0;
-        float4 v[V];
+    for (int j0 = 0; j0 < p.split; j0 += NB) {
+        float4 v[NB][V];
 #pragma unroll
-        for (int r = 0; r < V; ++r) v[r] = *reinterpret_cast<const float4 *>(piece + 1024 * r);
+        for (int b = 0; b < NB; ++b)
+            if (j0 + b < p.split) {
 #pragma unroll
-        for (int r = 0; r < V; ++r) {
-            acc[r].x += v[r].x;
-            acc[r].y += v[r].y;
-            acc[r].z += v[r].z;
-            acc[r].w += v[r].w;
+                for (int r = 0; r < V; ++r)
+                    v[b][r] = *reinterpret_cast<const float4 *>(base + (j0 + b) * seg + 1024 * r);
+            }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (j0 + b < p.split) {
+#pragma unroll
+                for (int r = 0; r < V; ++r) {
+                    acc[r].x += v[b][r].x;
+                    acc[r].y += v[b][r].y;
+                    acc[r].z += v[b][r].z;
+                    acc[r].w += v[b][r].w;
+                }
+            }
         }
     }
     int z, tm, tn;
@@ -1647,10 +1658,15 @@ cudaError_t launch_chunked_raw(const GemmArgs &a, bool transA, bool transB, void
     if (e != cudaSuccess) return e;
     if (pl.split == 0) return cudaGetLastError();
     // the tail tiles' sums, as a programmatic dependent of the GEMM
-    cfg.gridDim = dim3((unsigned)(BM * CFG::BN / (1024 * kFixupVecs)), (unsigned)pl.tail);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, tf32x3_fixup_kernel<CFG::BN>, p);
+    if ((long long)pl.tail * (BM * CFG::BN / 4096) >= sms) {
+        cfg.gridDim = dim3((unsigned)(BM * CFG::BN / 4096), (unsigned)pl.tail);
+        e = cudaLaunchKernelEx(&cfg, tf32x3_fixup_kernel<CFG::BN, 4>, p);
+    } else {
+        cfg.gridDim = dim3((unsigned)(BM * CFG::BN / 1024), (unsigned)pl.tail);
+        e = cudaLaunchKernelEx(&cfg, tf32x3_fixup_kernel<CFG::BN, 1>, p);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1697,12 +1713,30 @@ using Tf32Narrow = tf32x3::Config<32, 6, 1, 128>;     // two buffers of 128 colu
 
 namespace {
 
-// A 128 x 256 tile costs about 1.75 128 x 128 tiles (8192 x 8192 x 4096,
-// where the wave tail is negligible); count tiles per SM and take the cheaper
-// tiling, the wide one on ties.  For the three-term product a short K (at
-// most 256) takes the narrow tile whatever the count: only it has two
-// accumulator buffers, and with few K steps per tile the overlapped epilogue
-// matters most (96 x 512 x 512 x 64: 54.8 us narrow, 61.0 us wide).
+// Tile width.  Plain TF32 (the persistent kernel): a 128 x 256 tile costs
+// about 1.75 128 x 128 tiles (8192 x 8192 x 4096, where the wave tail is
+// negligible); count tiles per SM and take the cheaper tiling, the wide one
+// on ties.  Three terms: a short K (at most 256) takes the narrow tile
+// whatever the count: only it has two accumulator buffers, and with few K
+// steps per tile the overlapped epilogue matters most (96 x 512 x 512 x 64:
+// 54.8 us narrow, 61.0 us wide).  A longer K runs the K-chunked kernel,
+// costed in microseconds by chunked_cost_us: a 128 x 128 tile takes about
+// 0.019 us per unit of K on one SM and a 128 x 256 tile 1.5 times that
+// (8192 x 8192 x 4096: 287 TFLOP/s wide, 220 narrow); a tail split in K
+// costs 1 / split of a tile plus writing and reading back its partial tiles
+// at about 20 TB/s (they stay in L2).  Fitted to the whole call on GB300 with
+// each width forced: 2049 x 3071 x 1537 takes a wave of wide tiles and a
+// tail in halves (183 TFLOP/s; three waves of narrow ones, 151), 700 x 900 x
+// 300 takes 48 narrow tiles in 3 segments (21.3; 24 wide in 6, 19.5), and
+// 512 x 512 x 4096 8 wide tiles in 19 (72.6; 16 narrow in 9, 68.8).
+double chunked_cost_us(long long tiles, int K, int kblocks, int bn, int sms) {
+    const tf32x3::ChunkedPlan pl = tf32x3::chunked_plan(tiles, kblocks, bn, sms);
+    const double tile_us = 0.019 * K * (bn == 256 ? 1.5 : 1.0);
+    const double waves = (double)(tiles / sms);
+    if (pl.split > 0) return (waves + 1.0 / pl.split) * tile_us + 2.0 * pl.part_bytes / 20e6;
+    return (waves + (tiles % sms != 0 ? 1.0 : 0.0)) * tile_us;
+}
+
 bool tc_wide_tile(const GemmArgs &a, int terms) {
     if (terms == 3 && a.K <= 256) return false;
     int dev = 0, sms = 0;
@@ -1712,6 +1746,10 @@ bool tc_wide_tile(const GemmArgs &a, int terms) {
     const long long tm = (a.M + tf32x3::BM - 1) / tf32x3::BM;
     const long long wide = (long long)a.batch * tm * ((a.N + 255) / 256);
     const long long narrow = (long long)a.batch * tm * ((a.N + 127) / 128);
+    if (terms == 3)
+        return chunked_cost_us(wide, a.K, (a.K + Tf32x3Wide::BK - 1) / Tf32x3Wide::BK, 256, sms) <=
+               chunked_cost_us(narrow, a.K, (a.K + Tf32x3Narrow::BK - 1) / Tf32x3Narrow::BK, 128,
+                               sms);
     const double cost_wide = 1.75 * (double)((wide + sms - 1) / sms);
     const double cost_narrow = (double)((narrow + sms - 1) / sms);
     return cost_wide <= cost_narrow;

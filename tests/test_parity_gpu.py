@@ -310,10 +310,11 @@ def test_tf32x3_fma_class_accuracy_large(name):
 
 
 # The K-chunked three-term kernel (K > 256): partial last chunks, both tile
-# widths (the wave count picks 128 x 256 for 2000 x 2001 and 3001 x 2999,
-# 128 x 128 for the others), the TMA store and the threads' own stores (N not a
-# multiple of 4, a misaligned C), every layout, batches, and the epilogue;
-# exact on small integers, else within the FP32 bound.
+# widths (128 x 128 for 517 x 300 and the batched shapes, 128 x 256 for the
+# others), whole tiles (2000 x 2001, 3001 x 2999)
+# and tiles split in K (the rest), the TMA store and the threads' own stores
+# (N not a multiple of 4, a misaligned C), every layout, batches, and the
+# epilogue; exact on small integers, else within the FP32 bound.
 CHUNKED = [  # M, N, K, tA, tB, batch, offset, dist
     (300, 204, 257, 0, 0, 1, 0, "int"), (300, 204, 383, 1, 1, 1, 0, "int"),
     (1000, 1001, 515, 1, 0, 1, 0, "int"), (2000, 2001, 1000, 0, 1, 1, 0, "int"),
@@ -348,12 +349,13 @@ def test_chunked_tensor_kernel(M, N, K, tA, tB, batch, offset, dist):
 # workspace of the planes' bytes alone); on normal data the result does not
 # change between calls.
 CHUNKED_SK = [  # M, N, K, tA, tB, batch, offset, dist
-    (2500, 1999, 513, 0, 0, 1, 0, "int"),      # 128 x 128 tiles: 2 waves, 16 tiles in 8
-    (1000, 1100, 1000, 1, 1, 1, 0, "int"),     # 72 tiles, 2 segments each
-    (1024, 1024, 300, 0, 1, 5, 0, "int"),      # 320 tiles over 5 problems: 2 waves + 16 in 5
-    (4000, 4000, 777, 1, 0, 1, 1, "normal"),   # 128 x 256: 3 waves + 56, misaligned C
-    (700, 900, 300, 0, 0, 1, 0, "normal"),     # 48 tiles, 3 segments of 10 K blocks
-    (512, 512, 4096, 0, 0, 1, 0, "normal"),    # 16 tiles, 9 segments
+    (2500, 1999, 513, 0, 0, 1, 0, "int"),      # 128 x 256 tiles: 1 wave + 8 tiles in 16 segments
+    (1280, 2045, 700, 1, 0, 1, 0, "int"),      # 128 x 128 tiles: 1 wave + 8 tiles in 11
+    (1000, 1100, 1000, 1, 1, 1, 0, "int"),     # 72 tiles of 128 x 128, 2 segments each
+    (1024, 1024, 300, 0, 1, 5, 0, "int"),      # 160 tiles over 5 problems: 1 wave + 8 in 9
+    (4000, 4000, 777, 1, 0, 1, 1, "normal"),   # 128 x 256: 3 waves + 56 in 2, misaligned C
+    (700, 900, 300, 0, 0, 1, 0, "normal"),     # 48 tiles of 128 x 128, 3 segments of 3 or 4 K blocks
+    (512, 512, 4096, 0, 0, 1, 0, "normal"),    # 8 tiles, 19 segments
 ]
 
 
