@@ -395,25 +395,41 @@ struct Persist {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// Over one landed operand tile of `bytes` bytes holding raw fp32 x in the hi
-// slot.  Three terms: the same position of the lo slot (`bytes` further) gets
-// tf32_lo(x, tf32_hi(x)) and the hi slot stays as it is (the MMAs read x as
-// tf32_hi(x)).  One term: the hi slot becomes tf32_rn(x) in place.  These are
-// the values the split kernel writes, so the MMAs see the same operands.  The
-// swizzle moves whole 16-byte chunks, so position-wise work ignores it.
-template <int PLANES>
-__device__ __forceinline__ void convert_tile(uint8_t *tile, int bytes, int t, int nt) {
-    float4 *hi = reinterpret_cast<float4 *>(tile);
-    float4 *lo = reinterpret_cast<float4 *>(tile + bytes);
-    for (int v = t; v < bytes / 16; v += nt) {
-        const float4 x = hi[v];
+// The converted operand tiles of one landed stage, each holding raw fp32 x in
+// its hi slot.  Three terms: the same position of the lo slot (one tile
+// further) gets tf32_lo(x, tf32_hi(x)) and the hi slot stays as it is (the
+// MMAs read x as tf32_hi(x)).  One term: the hi slot becomes tf32_rn(x) in
+// place.  These are the values the split kernel writes, so the MMAs see the
+// same operands.  The swizzle moves whole 16-byte chunks, so position-wise
+// work ignores it.  Thread t of NT takes 16-byte chunks t, t + NT, ... of
+// each tile, and issues every load of the stage before its first store, so
+// one shared-memory round trip covers the stage.
+template <int PLANES, int CONV, int A_BYTES, int B_BYTES, int NT>
+__device__ __forceinline__ void convert_stage(uint8_t *st, int t) {
+    constexpr int NA = (CONV & 1) ? A_BYTES / (16 * NT) : 0;
+    constexpr int NB = (CONV & 2) ? B_BYTES / (16 * NT) : 0;
+    static_assert(A_BYTES % (16 * NT) == 0 && B_BYTES % (16 * NT) == 0, "whole chunks per thread");
+    float4 *ahi = reinterpret_cast<float4 *>(st);
+    float4 *bhi = reinterpret_cast<float4 *>(st + PLANES * A_BYTES);
+    float4 *alo = PLANES == 2 ? reinterpret_cast<float4 *>(st + A_BYTES) : ahi;
+    float4 *blo = PLANES == 2 ? reinterpret_cast<float4 *>(st + PLANES * A_BYTES + B_BYTES) : bhi;
+    float4 xa[NA > 0 ? NA : 1], xb[NB > 0 ? NB : 1];
+#pragma unroll
+    for (int i = 0; i < NA; ++i) xa[i] = ahi[t + i * NT];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) xb[i] = bhi[t + i * NT];
+    auto conv = [](float4 x) {
         if constexpr (PLANES == 2)
-            lo[v] = make_float4(tf32_lo(x.x, tf32_hi(x.x)), tf32_lo(x.y, tf32_hi(x.y)),
-                                tf32_lo(x.z, tf32_hi(x.z)), tf32_lo(x.w, tf32_hi(x.w)));
+            return make_float4(tf32_lo(x.x, tf32_hi(x.x)), tf32_lo(x.y, tf32_hi(x.y)),
+                               tf32_lo(x.z, tf32_hi(x.z)), tf32_lo(x.w, tf32_hi(x.w)));
         else
-            hi[v] = make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
-                                tc::to_tf32(x.w));
-    }
+            return make_float4(tc::to_tf32(x.x), tc::to_tf32(x.y), tc::to_tf32(x.z),
+                               tc::to_tf32(x.w));
+    };
+#pragma unroll
+    for (int i = 0; i < NA; ++i) alo[t + i * NT] = conv(xa[i]);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) blo[t + i * NT] = conv(xb[i]);
 }
 
 // tmA / tmB: the operand's planes, or (RAW) its raw rows; tmAlo / tmBlo: the
@@ -613,8 +629,7 @@ tf32x3_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                     break;
                 }
                 uint8_t *st = smem + s * STAGE_BYTES;
-                if constexpr (CONV & 1) convert_tile<PLANES>(st, A_TILE, t, NT);
-                if constexpr (CONV & 2) convert_tile<PLANES>(st + PLANES * A_TILE, B_TILE, t, NT);
+                convert_stage<PLANES, CONV, A_TILE, B_TILE, NT>(st, t);
                 // the planes are read by the tensor cores (async proxy)
                 tc::fence_proxy_async_smem();
                 __syncwarp();
