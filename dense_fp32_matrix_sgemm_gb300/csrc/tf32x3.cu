@@ -118,7 +118,7 @@ struct SplitJob {
     int64_t blocks;
     int R;
     int kcontig;
-    int vec;   // kcontig rows allow 16-byte loads
+    int vec;   // rows allow 16-byte loads (along K, or along r for M/N-major X)
     int lo_only;
 };
 
@@ -209,21 +209,97 @@ __device__ __forceinline__ void split_transpose(const SplitJob &j, int K, int Kp
     }
 }
 
+// M/N-major operand with 16-byte aligned rows: 32 (k) x 128 (r) blocks.  Each
+// thread loads four 16-byte row segments of X (4 consecutive r), the block
+// passes through a shared tile of row stride 129 floats, and each thread
+// writes 4 consecutive k of a plane row per 16-byte store: a quarter of the
+// load and store instructions of the 32 x 32 form and four times the bytes
+// per barrier.  Reads of the tile (tile[4q + e][r], q = thread % 8,
+// r = thread / 8 + 32 i) fall in 32 distinct banks.  Plane columns from K up
+// to the block's end get zeros (inside the row: Kp is a multiple of 32).
+template <int PLANES>
+__device__ __forceinline__ void split_transpose_wide(const SplitJob &j, int K, int Kp, int batch,
+                                                     int64_t b, float (*tile)[129]) {
+    const int64_t plane = (int64_t)j.R * Kp;
+    const int tid = threadIdx.x;
+    const int64_t rt_n = (j.R + 127) / 128, kt_n = (K + 31) / 32;
+    const int64_t total = (int64_t)batch * kt_n * rt_n;
+    const int lr = 4 * (tid & 31), lk = tid >> 5;   // load: r quad, k row (0..7)
+    const int kq = tid & 7, sr = tid >> 3;          // store: k quad, plane row (0..31)
+    for (int64_t t = b; t < total; t += j.blocks) {
+        const int64_t z = t / (kt_n * rt_n), rem = t - z * kt_n * rt_n;
+        const int k0 = (int)(rem / rt_n) * 32, r0 = (int)(rem % rt_n) * 128;
+        const float *src = j.X + z * j.sX;
+        float4 x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + lk + 8 * i, r = r0 + lr;
+            x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < K) {
+                const float *row = src + (int64_t)k * j.ld + r;
+                if (r + 3 < j.R) {
+                    x[i] = __ldg(reinterpret_cast<const float4 *>(row));
+                } else {
+                    if (r + 0 < j.R) x[i].x = __ldg(row + 0);
+                    if (r + 1 < j.R) x[i].y = __ldg(row + 1);
+                    if (r + 2 < j.R) x[i].z = __ldg(row + 2);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float *trow = tile[lk + 8 * i] + lr;
+            trow[0] = x[i].x;
+            trow[1] = x[i].y;
+            trow[2] = x[i].z;
+            trow[3] = x[i].w;
+        }
+        __syncthreads();
+        float *hi = j.out + (PLANES * z) * plane;
+        const int k = k0 + 4 * kq;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = sr + 32 * i, r = r0 + c;
+            if (r < j.R) {
+                const float4 v = make_float4(tile[4 * kq][c], tile[4 * kq + 1][c],
+                                             tile[4 * kq + 2][c], tile[4 * kq + 3][c]);
+                float *dst = hi + (int64_t)r * Kp + k;
+                if constexpr (PLANES == 2) {
+                    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z),
+                                                 tf32_hi(v.w));
+                    *reinterpret_cast<float4 *>(dst) = h;
+                    *reinterpret_cast<float4 *>(dst + plane) =
+                        make_float4(tf32_lo(v.x, h.x), tf32_lo(v.y, h.y), tf32_lo(v.z, h.z),
+                                    tf32_lo(v.w, h.w));
+                } else {
+                    *reinterpret_cast<float4 *>(dst) =
+                        make_float4(tc::to_tf32(v.x), tc::to_tf32(v.y), tc::to_tf32(v.z),
+                                    tc::to_tf32(v.w));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // Both operands in one launch: CTAs [0, job[0].blocks) split op(A), the rest
 // op(B).  The GEMM that follows is launched as a programmatic dependent, so
 // this grid lets it start its set-up early; the GEMM waits for this grid's
 // completion before it reads a plane.
 template <int PLANES>
 __global__ void __launch_bounds__(256) split_kernel(const SplitArgs a) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[32 * 129];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int w = (int64_t)blockIdx.x < a.job[0].blocks ? 0 : 1;
     const int64_t b = (int64_t)blockIdx.x - (w ? a.job[0].blocks : 0);
     const SplitJob j = w ? a.job[1] : a.job[0];   // no dynamic index into the parameters
     if (j.kcontig)
         split_kcontig<PLANES>(j, a.K, a.Kp, a.batch, b);
+    else if (j.vec)
+        split_transpose_wide<PLANES>(j, a.K, a.Kp, a.batch, b,
+                                     reinterpret_cast<float (*)[129]>(tile));
     else
-        split_transpose<PLANES>(j, a.K, a.Kp, a.batch, b, tile);
+        split_transpose<PLANES>(j, a.K, a.Kp, a.batch, b, reinterpret_cast<float (*)[33]>(tile));
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -1386,9 +1462,12 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int co
         j.R = R;
         j.kcontig = kcontig;
         j.lo_only = lo;
-        j.vec = kcontig && (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 && sX % 4 == 0;
-        const int64_t work = kcontig ? ((int64_t)a.batch * R * (Kp / 4) + 255) / 256
-                                     : (int64_t)a.batch * ((R + 31) / 32) * ((a.K + 31) / 32);
+        j.vec = (reinterpret_cast<uintptr_t>(X) % 16 == 0) && ld % 4 == 0 &&
+                (a.batch == 1 || sX % 4 == 0);
+        const int64_t work =
+            kcontig ? ((int64_t)a.batch * R * (Kp / 4) + 255) / 256
+                    : (int64_t)a.batch * ((R + (j.vec ? 127 : 31)) / (j.vec ? 128 : 32)) *
+                          ((a.K + 31) / 32);
         j.blocks = skip ? 0 : (work < 152 * 16 ? (work > 0 ? work : 1) : 152 * 16);
     };
     job(sa.job[0], a.A, a.lda, a.strideA, a.M, !transA, wsA, (conv & 1) != 0, (lo_only & 1) != 0);
