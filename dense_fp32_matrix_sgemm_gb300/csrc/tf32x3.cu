@@ -49,6 +49,7 @@
 // roles drain (copies in flight land, MMAs complete, TMEM is freed) and the
 // library's device error word is raised.
 #include <atomic>
+#include <climits>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -311,6 +312,9 @@ struct Tf32x3Params {
     int tiles_m, tiles_n, group_m;
     int vec_c;   // C rows allow 16-byte stores
     int tma_c;   // store C through the tmC tensor map (plain epilogue, aligned C)
+    int tma_n;   // with tma_c: 32-column blocks of C ending at or before column
+                 // tma_n go through the map, the block holding the last
+                 // columns of a width that is not a multiple of 4 does not
     int batch;
     float alpha, beta;      // epilogue C = alpha * acc + beta * C + bias[col]
     const float *bias;
@@ -354,7 +358,7 @@ __device__ __forceinline__ void store_tile_rows(const Tf32x3Params &p, const CUt
     const uint32_t lane_base = acc + ((uint32_t)(32 * q) << 16);
     if (p.tma_c) {
         const int row0 = m0 + 32 * q;
-        for (int c = 0; row0 < p.M && c < BN / 32 && n0 + 32 * c < p.N; ++c, ++cc) {
+        for (int c = 0; row0 < p.M && c < BN / 32 && n0 + 32 * c < p.N; ++c) {
             float v[32];
             const uint32_t ta = lane_base + (uint32_t)(32 * c);
             tc::tmem_ld_32(ta, v);
@@ -363,6 +367,18 @@ __device__ __forceinline__ void store_tile_rows(const Tf32x3Params &p, const CUt
                 tc::tmem_ld_32(ta + ACC_COLS, w);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] += w[j];
+            }
+            if (n0 + 32 * c + 32 > p.tma_n) {
+                // the last columns of a width that is not a multiple of 4:
+                // each thread stores its own row (plain product)
+                const int row = row0 + lane;
+                if (row < p.M) {
+                    float *crow = p.C + (int64_t)z * p.strideC + (int64_t)row * p.ldc;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (n0 + 32 * c + j < p.N) crow[n0 + 32 * c + j] = v[j];
+                }
+                continue;
             }
             const uint32_t buf = stage + (uint32_t)(cc & 1) * 4096u;
             if (cc >= 2) {
@@ -380,6 +396,7 @@ __device__ __forceinline__ void store_tile_rows(const Tf32x3Params &p, const CUt
                 tc::tma_store_3d(tmC, buf, n0 + 32 * c, row0, z);
                 tc::bulk_commit_group();
             }
+            ++cc;
         }
         return;
     }
@@ -797,16 +814,17 @@ struct Chunked {
 // one row the warp reads back, hit distinct banks).
 //   tma: one lane stores the block with a TMA tensor store through `map`
 //   (C, or the partial tiles as [slot][BM][BN]) at (n0 + 32c, row, z), after
-//   the previous block's store has read the staging block; `cc` counts the
-//   blocks stored this way so far.
+//   the previous block's store has read the staging block, for blocks that
+//   end at or before column tma_n; `cc` counts the blocks stored this way so
+//   far.
 //   Otherwise (C only) the warp reads the block back a row at a time, lane j
 //   taking column j, and stores it with the epilogue: each store is one
 //   128-byte row segment.
 template <int COLS>
 __device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const CUtensorMap *map,
-                                                   bool tma, const float (&run)[COLS], int q,
-                                                   int lane, int z, int m0, int n0, int rows,
-                                                   int cols, uint32_t stage, int &cc) {
+                                                   bool tma, int tma_n, const float (&run)[COLS],
+                                                   int q, int lane, int z, int m0, int n0,
+                                                   int rows, int cols, uint32_t stage, int &cc) {
     const int row0 = m0 + 32 * q;
     if (row0 >= rows) return;
     const uint32_t rbase = stage + (uint32_t)lane * 128u;
@@ -822,7 +840,7 @@ __device__ __forceinline__ void store_running_rows(const Tf32x3Params &p, const 
             tc::st_shared_v4(rbase + ((uint32_t)(j ^ (lane & 7)) << 4), run[32 * c + 4 * j],
                              run[32 * c + 4 * j + 1], run[32 * c + 4 * j + 2],
                              run[32 * c + 4 * j + 3]);
-        if (tma) {
+        if (tma && n0 + 32 * c + 32 <= tma_n) {
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -1206,7 +1224,8 @@ tf32x3_chunked_kernel(const __grid_constant__ CUtensorMap tmA,
             int z, tm, tn;
             raster(p, pc.t, z, tm, tn);
             const bool part = pc.slot >= 0;
-            store_running_rows<COLS>(p, part ? &tmP : &tmC, part || p.tma_c, run, q, lane,
+            store_running_rows<COLS>(p, part ? &tmP : &tmC, part || p.tma_c,
+                                     part ? INT_MAX : p.tma_n, run, q, lane,
                                      part ? pc.slot : z, part ? 0 : tm * BM,
                                      (part ? 0 : tn * BN) + h * COLS, part ? BM : p.M,
                                      part ? BN : p.N, stage, cc);
@@ -1499,13 +1518,17 @@ cudaError_t prepare(const GemmArgs &a, bool transA, bool transB, int raw, int co
     p.split = 0;
     p.part = nullptr;
     // The TMA store takes the plain product into a C whose base, rows and
-    // batches are 16-byte aligned and whose width is a whole number of
-    // 16-byte granules: with N not a multiple of 4 the store was seen to
-    // write the padding column next to column N-1, so such widths keep the
-    // threads' own guarded stores.  The map is only read when tma_c is set.
+    // batches are 16-byte aligned.  A store was seen to write whole 16-byte
+    // granules: with N not a multiple of 4 it wrote the padding column next
+    // to column N-1.  So the map is N rounded down to a multiple of 4 wide,
+    // and the 32-column block holding the last columns of such a width is
+    // stored by the threads themselves (tma_n).  The map is only read when
+    // tma_c is set.
     tmC = CUtensorMap{};
-    p.tma_c = p.vec_c && a.N % 4 == 0 && plain_epilogue(a) &&
-              make_c_map(&tmC, a.C, a.M, a.N, a.ldc, a.strideC, a.batch);
+    const int n4 = a.N / 4 * 4;
+    p.tma_c = p.vec_c && n4 > 0 && plain_epilogue(a) &&
+              make_c_map(&tmC, a.C, a.M, n4, a.ldc, a.strideC, a.batch);
+    p.tma_n = a.N % 4 == 0 ? INT_MAX : n4;
     return cudaSuccess;
 }
 
