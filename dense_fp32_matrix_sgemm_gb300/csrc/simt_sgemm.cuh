@@ -555,8 +555,9 @@ sgemm_simt_streamk_kernel(const GemmArgs p, const StreamK sk) {
 
 // Adds the pieces of the shared stream-K tiles: grid streamk_fixup_grid<BN_>,
 // kFixupVecs float4 per thread (256 float4 apart, so each load instruction is
-// coalesced across the CTA), all of a piece's loads issued before any add;
-// pieces added in K order (CTA order), then stored to C with the epilogue.
+// coalesced across the CTA), the loads of a tile's first three pieces issued
+// before any add; pieces added in K order (CTA order), then stored to C with
+// the epilogue.
 // Tiles that fell whole to one CTA are skipped.
 constexpr int kFixupVecs = 4;
 
@@ -579,11 +580,41 @@ __global__ void __launch_bounds__(256) streamk_fixup_kernel(const GemmArgs p, co
     float4 acc[V];
 #pragma unroll
     for (int r = 0; r < V; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c <= c1; ++c) {
+    // the piece of CTA c in this tile, or null when c has no units
+    auto piece_of = [&](int c) -> const float * {
         const int64_t start = (int64_t)c * U / sk.G;
-        if (((int64_t)c + 1) * U / sk.G == start) continue;   // a CTA with no units has no piece
+        if (((int64_t)c + 1) * U / sk.G == start) return nullptr;
         const int slot = start >= f ? 0 : 1;   // the tile is c's first piece or its last
-        const float *piece = sk.ws + ((int64_t)c * 2 + slot) * (BM * BN_) + e0;
+        return sk.ws + ((int64_t)c * 2 + slot) * (BM * BN_) + e0;
+    };
+    // the first three pieces (a shared tile mostly has two): every load
+    // issued before the first add, then added in K order
+    constexpr int kAhead = 3;
+    const float *first[kAhead];
+    int np = 0, c = c0;
+    for (; c <= c1 && np < kAhead; ++c) {
+        const float *pc = piece_of(c);
+        if (pc != nullptr) first[np++] = pc;
+    }
+    float4 w[kAhead][V];
+#pragma unroll
+    for (int q = 0; q < kAhead; ++q)
+        if (q < np)
+#pragma unroll
+            for (int r = 0; r < V; ++r) w[q][r] = *reinterpret_cast<const float4 *>(first[q] + 1024 * r);
+#pragma unroll
+    for (int q = 0; q < kAhead; ++q)
+        if (q < np)
+#pragma unroll
+            for (int r = 0; r < V; ++r) {
+                acc[r].x += w[q][r].x;
+                acc[r].y += w[q][r].y;
+                acc[r].z += w[q][r].z;
+                acc[r].w += w[q][r].w;
+            }
+    for (; c <= c1; ++c) {
+        const float *piece = piece_of(c);
+        if (piece == nullptr) continue;
         float4 v[V];
 #pragma unroll
         for (int r = 0; r < V; ++r) v[r] = *reinterpret_cast<const float4 *>(piece + 1024 * r);
