@@ -765,15 +765,18 @@ def test_cluster_split_epilogue(alpha, beta, with_bias, M, N, K):
     assert ok.all(), f"{int((~ok).sum())} outputs outside the bound"
 
 
-# The tensor path's TMA-store epilogue (plain product, 16-byte-aligned C, N a
-# multiple of 4): ragged rows inside a warp's 32-row box, ragged columns next
-# to aligned padding that must stay NaN, batches, and exact results on small
-# integers.  Widths that are not a multiple of 4 take the threads' own stores.
+# The tensor path's TMA-store epilogue (plain product, 16-byte-aligned C):
+# ragged rows inside a warp's 32-row box, ragged columns next to aligned
+# padding that must stay NaN, batches, and exact results on small integers.
+# A width that is not a multiple of 4 is stored through a map N rounded down
+# to 4 wide, and the 32-column block holding its last columns by the threads
+# themselves; K > 256 runs the K-chunked kernel's epilogue.
 @pytest.mark.parametrize("entry_name", ["sgemm_f32_tf32x3_strided_batched",
                                         "sgemm_f32_tf32_strided_batched"])
 @pytest.mark.parametrize("M,N,K", [(300, 204, 77), (33, 1000, 64), (1000, 36, 129),
                                    (128, 256, 16), (7, 8, 3), (300, 201, 77), (1000, 37, 129),
-                                   (7, 5, 3)])
+                                   (7, 5, 3), (300, 201, 300), (1000, 37, 700), (130, 2, 260),
+                                   (260, 290, 513)])
 def test_tensor_store_edges_exact(entry_name, M, N, K):
     ldc = (N + 3) // 4 * 4 + 4
     case = workloads.make_operands(M, N, K, batch=2, transB=1, ldc=ldc, dist="int", seed=60,
