@@ -263,3 +263,39 @@ def test_padded_transpose_tiles(rows_in_tile):
         for i, per_tid in table.items():
             for w in range(THREADS // 32):
                 assert banks_conflict_free_32bit([per_tid[t] for t in range(32 * w, 32 * w + 32)])
+
+
+def test_wide_transpose_tiles():
+    # split_transpose_wide (csrc/tf32x3.cu) and transpose_vec_kernel
+    # (csrc/turn.cu): a 32 x 128 block of X (32 source rows, 128 contiguous
+    # columns) through tile[32][129].  Load: thread t takes columns
+    # 4 (t % 32) .. +3 of rows t / 32 + 8 i (one 16-byte global load each) and
+    # writes them as four floats; store: thread t reads tile[4 (t % 8) + e]
+    # [t / 8 + 32 i] for e < 4 and writes them as one 16-byte row segment of
+    # the output (4 consecutive source rows of one column).
+    pitch = 129
+    cells_written, cells_read = [], []
+    for i in range(4):
+        for e in range(4):
+            w_addrs, r_addrs = [], []
+            for tid in range(THREADS):
+                lr, lk = 4 * (tid & 31), tid >> 5
+                row, col = lk + 8 * i, lr + e
+                w_addrs.append(row * pitch + col)
+                cells_written.append((row, col))
+                kq, sr = tid & 7, tid >> 3
+                rrow, rcol = 4 * kq + e, sr + 32 * i
+                r_addrs.append(rrow * pitch + rcol)
+                cells_read.append((rrow, rcol))
+            for w in range(THREADS // 32):
+                # the tile reads are conflict-free; the scalar writes of a
+                # 16-byte load meet at most 4-way conflicts (4 lanes 32 floats
+                # apart in the same bank), which the test bounds
+                assert banks_conflict_free_32bit(r_addrs[32 * w:32 * w + 32]), (i, e, w)
+                banks = {}
+                for a in w_addrs[32 * w:32 * w + 32]:
+                    banks.setdefault(a % 32, set()).add(a)
+                assert max(len(v) for v in banks.values()) <= 4
+    full = {(r, c) for r in range(32) for c in range(128)}
+    assert len(cells_written) == len(set(cells_written)) and set(cells_written) == full
+    assert len(cells_read) == len(set(cells_read)) and set(cells_read) == full
