@@ -1,10 +1,13 @@
 """GB300-native single-precision GEMM: C = op(A) op(B) in float32.
 
-This package is a thin ctypes binding over ``libsgemm_gb300.so``, whose C ABI
-is declared in ``include/sgemm_gb300.h``.  The binding only marshals
-arguments: every step of the product runs in the library's CUDA kernels.
-There is no CPU fallback; if the library has not been built, every call
-raises ``SgemmUnavailable``.
+This package is a thin binding over ``libsgemm_gb300.so``, whose C ABI is
+declared in ``include/sgemm_gb300.h``.  The binding only marshals arguments:
+every step of the product runs in the library's CUDA kernels.  The compute
+entry points go through ``_calls``, a small CPython extension bound to the
+loaded library's entry points (a fraction of a microsecond per call), when
+it was built, else through ctypes (about 0.2 us per argument); the library,
+and so every result, is the same either way.  There is no CPU fallback; if
+the library has not been built, every call raises ``SgemmUnavailable``.
 
 Low-level names mirror the C ABI (raw device pointers as Python ints, stream
 as a ``cudaStream_t`` int or 0).  ``matmul`` is a convenience for torch CUDA
@@ -27,7 +30,7 @@ __all__ = ["SgemmError", "SgemmUnavailable", "load_library", "library_path",
            "splitk_auto_splits", "splitk_workspace_size", "sgemm_f32_ex", "selftest_wait_timeout",
            "sgemm_f32_streamk", "streamk_workspace_size",
            "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex", "set_raster_group",
-           "set_tf32x3_chunk_k"]
+           "set_tf32x3_chunk_k", "marshalling"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libsgemm_gb300.so")
@@ -106,6 +109,14 @@ class SgemmError(RuntimeError):
 
 _lock = threading.Lock()
 _lib = None
+_api = None   # what the compute wrappers call: the _calls module, else the ctypes library
+
+# Compute entry points that the _calls extension marshals (same names, same
+# argument order as the C ABI); everything else goes through ctypes.
+FAST_ENTRIES = ("sgemm_f32", "sgemm_f32_strided_batched", "sgemm_f32_ex",
+                "sgemm_f32_ex_strided_batched", "sgemm_f32_tf32x3_ex", "sgemm_f32_splitk",
+                "sgemm_f32_streamk", "sgemm_f32_tf32x3", "sgemm_f32_tf32x3_strided_batched",
+                "sgemm_f32_tf32", "sgemm_f32_tf32_strided_batched", "sgemm_f32_tf32x3_noalloc")
 
 
 def library_path() -> str:
@@ -132,8 +143,35 @@ def load_library():
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
+        global _api
+        _api = _bind_calls(lib)
         _lib = lib
         return lib
+
+
+def _bind_calls(lib):
+    """The _calls extension bound to this library's entry points, or the
+    ctypes library itself when the extension was not built."""
+    try:
+        from . import _calls
+    except ImportError:
+        return lib
+    _calls.bind({name: ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+                 for name in FAST_ENTRIES})
+    return _calls
+
+
+def marshalling() -> str:
+    """'extension' when the compute calls go through the _calls module, else 'ctypes'."""
+    load_library()
+    return "ctypes" if _api is _lib else "extension"
+
+
+def _entry():
+    """The compute calls' route, loading the library first if needed."""
+    if _lib is None:
+        load_library()
+    return _api
 
 
 def status_string(status: int) -> str:
@@ -156,51 +194,51 @@ def _check(status: int) -> int:
 
 def sgemm_f32(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, stream=0, *, check=True):
     """C = op(A) op(B); A, B, C are device pointers (ints).  Returns the status."""
-    st = load_library().sgemm_f32(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
-                                  transA, transB, stream or None)
+    st = _entry().sgemm_f32(M, N, K, A or 0, lda, B or 0, ldb, C or 0, ldc,
+                            transA, transB, stream or 0)
     return _check(st) if check else st
 
 
 def sgemm_f32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
                               batch, transA=0, transB=0, stream=0, *, check=True):
     """Strided-batched C_z = op(A_z) op(B_z).  Returns the status."""
-    st = load_library().sgemm_f32_strided_batched(
-        M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
-        batch, transA, transB, stream or None)
+    st = _entry().sgemm_f32_strided_batched(
+        M, N, K, A or 0, lda, strideA, B or 0, ldb, strideB, C or 0, ldc, strideC,
+        batch, transA, transB, stream or 0)
     return _check(st) if check else st
 
 
 def sgemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=0, transA=0, transB=0,
                  stream=0, *, check=True):
     """C = alpha op(A) op(B) + beta C + bias (bias: device pointer to N floats or 0)."""
-    st = load_library().sgemm_f32_ex(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
-                                     C or None, ldc, bias or None, transA, transB, stream or None)
+    st = _entry().sgemm_f32_ex(M, N, K, alpha, A or 0, lda, B or 0, ldb, beta,
+                               C or 0, ldc, bias or 0, transA, transB, stream or 0)
     return _check(st) if check else st
 
 
 def sgemm_f32_ex_strided_batched(M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
                                  strideC, bias, batch, transA=0, transB=0, stream=0, *,
                                  check=True):
-    st = load_library().sgemm_f32_ex_strided_batched(
-        M, N, K, alpha, A or None, lda, strideA, B or None, ldb, strideB, beta, C or None, ldc,
-        strideC, bias or None, batch, transA, transB, stream or None)
+    st = _entry().sgemm_f32_ex_strided_batched(
+        M, N, K, alpha, A or 0, lda, strideA, B or 0, ldb, strideB, beta, C or 0, ldc,
+        strideC, bias or 0, batch, transA, transB, stream or 0)
     return _check(st) if check else st
 
 
 def sgemm_f32_tf32x3_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=0, transA=0, transB=0,
                         workspace=0, workspace_bytes=0, stream=0, *, check=True):
-    st = load_library().sgemm_f32_tf32x3_ex(M, N, K, alpha, A or None, lda, B or None, ldb, beta,
-                                            C or None, ldc, bias or None, transA, transB,
-                                            workspace or None, workspace_bytes, stream or None)
+    st = _entry().sgemm_f32_tf32x3_ex(M, N, K, alpha, A or 0, lda, B or 0, ldb, beta,
+                                      C or 0, ldc, bias or 0, transA, transB,
+                                      workspace or 0, workspace_bytes, stream or 0)
     return _check(st) if check else st
 
 
 def sgemm_f32_streamk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,
                       workspace_bytes=0, stream=0, *, check=True):
     """sgemm_f32 with turned operands and the stream-K tile schedule (see include/sgemm_gb300.h)."""
-    st = load_library().sgemm_f32_streamk(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
-                                          transA, transB, workspace or None, workspace_bytes,
-                                          stream or None)
+    st = _entry().sgemm_f32_streamk(M, N, K, A or 0, lda, B or 0, ldb, C or 0, ldc,
+                                    transA, transB, workspace or 0, workspace_bytes,
+                                    stream or 0)
     return _check(st) if check else st
 
 
@@ -211,9 +249,9 @@ def streamk_workspace_size(M: int, N: int, K: int, transA: int = 0, transB: int 
 def sgemm_f32_splitk(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, splits=0, workspace=0,
                      workspace_bytes=0, stream=0, *, check=True):
     """sgemm_f32 with K split into chunks summed in a fixed order (deterministic)."""
-    st = load_library().sgemm_f32_splitk(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
-                                         transA, transB, splits, workspace or None,
-                                         workspace_bytes, stream or None)
+    st = _entry().sgemm_f32_splitk(M, N, K, A or 0, lda, B or 0, ldb, C or 0, ldc,
+                                   transA, transB, splits, workspace or 0,
+                                   workspace_bytes, stream or 0)
     return _check(st) if check else st
 
 
@@ -229,9 +267,9 @@ def sgemm_f32_tf32x3(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, worksp
                      workspace_bytes=0, stream=0, *, check=True):
     """C = op(A) op(B) on the tensor cores (3xTF32); ``workspace`` is a device
     pointer of at least tf32x3_workspace_size(M, N, K, 1) bytes."""
-    st = load_library().sgemm_f32_tf32x3(M, N, K, A or None, lda, B or None, ldb, C or None,
-                                         ldc, transA, transB, workspace or None, workspace_bytes,
-                                         stream or None)
+    st = _entry().sgemm_f32_tf32x3(M, N, K, A or 0, lda, B or 0, ldb, C or 0,
+                                   ldc, transA, transB, workspace or 0, workspace_bytes,
+                                   stream or 0)
     return _check(st) if check else st
 
 
@@ -239,9 +277,9 @@ def sgemm_f32_tf32x3_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, 
                                      batch, transA=0, transB=0, workspace=0, workspace_bytes=0,
                                      stream=0, *, check=True):
     """Strided-batched 3xTF32 product."""
-    st = load_library().sgemm_f32_tf32x3_strided_batched(
-        M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
-        batch, transA, transB, workspace or None, workspace_bytes, stream or None)
+    st = _entry().sgemm_f32_tf32x3_strided_batched(
+        M, N, K, A or 0, lda, strideA, B or 0, ldb, strideB, C or 0, ldc, strideC,
+        batch, transA, transB, workspace or 0, workspace_bytes, stream or 0)
     return _check(st) if check else st
 
 
@@ -250,8 +288,8 @@ def sgemm_f32_tf32x3_noalloc(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0
     """3xTF32 product that allocates nothing: its scratch is the library's
     built-in device array (see include/sgemm_gb300.h for the size limit and
     the rule that overlapping calls race)."""
-    st = load_library().sgemm_f32_tf32x3_noalloc(M, N, K, A or None, lda, B or None, ldb,
-                                                 C or None, ldc, transA, transB, stream or None)
+    st = _entry().sgemm_f32_tf32x3_noalloc(M, N, K, A or 0, lda, B or 0, ldb,
+                                           C or 0, ldc, transA, transB, stream or 0)
     return _check(st) if check else st
 
 
@@ -262,18 +300,18 @@ def tf32x3_noalloc_max_bytes() -> int:
 def sgemm_f32_tf32(M, N, K, A, lda, B, ldb, C, ldc, transA=0, transB=0, workspace=0,
                    workspace_bytes=0, stream=0, *, check=True):
     """Plain single-TF32 tensor-core product (reduced precision, see the header)."""
-    st = load_library().sgemm_f32_tf32(M, N, K, A or None, lda, B or None, ldb, C or None, ldc,
-                                       transA, transB, workspace or None, workspace_bytes,
-                                       stream or None)
+    st = _entry().sgemm_f32_tf32(M, N, K, A or 0, lda, B or 0, ldb, C or 0, ldc,
+                                 transA, transB, workspace or 0, workspace_bytes,
+                                 stream or 0)
     return _check(st) if check else st
 
 
 def sgemm_f32_tf32_strided_batched(M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
                                    batch, transA=0, transB=0, workspace=0, workspace_bytes=0,
                                    stream=0, *, check=True):
-    st = load_library().sgemm_f32_tf32_strided_batched(
-        M, N, K, A or None, lda, strideA, B or None, ldb, strideB, C or None, ldc, strideC,
-        batch, transA, transB, workspace or None, workspace_bytes, stream or None)
+    st = _entry().sgemm_f32_tf32_strided_batched(
+        M, N, K, A or 0, lda, strideA, B or 0, ldb, strideB, C or 0, ldc, strideC,
+        batch, transA, transB, workspace or 0, workspace_bytes, stream or 0)
     return _check(st) if check else st
 
 

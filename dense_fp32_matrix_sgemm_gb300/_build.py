@@ -81,7 +81,38 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, jobs: int | None =
         os.replace(LIB + ".tmp", LIB)
     if verbose:
         sys.stderr.write(f"built {LIB}\n")
+    _build_calls(verbose)
     return LIB
+
+
+def _build_calls(verbose: bool = False):
+    """Compile _calls.c, the CPython argument-marshalling module for the
+    compute entry points (see that file), next to the library.  Without a C
+    compiler or the Python headers nothing is built and the package marshals
+    through ctypes instead; the library is the same either way."""
+    import sysconfig
+    src = os.path.join(PKG, "_calls.c")
+    out = os.path.join(PKG, "_calls" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+    inc = sysconfig.get_paths().get("include", "")
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if not cc or not os.path.exists(os.path.join(inc, "Python.h")):
+        if verbose:
+            sys.stderr.write("note: no C compiler or Python headers; the binding uses ctypes\n")
+        return None
+    newest = max(os.path.getmtime(src), os.path.getmtime(os.path.join(INCLUDE, "sgemm_gb300.h")))
+    if os.path.exists(out) and os.path.getmtime(out) >= newest:
+        return out
+    cmd = [cc, "-O2", "-std=gnu11", "-shared", "-fPIC", "-Wall", "-I", inc, "-I", INCLUDE, src,
+           "-o", out + ".tmp"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        if verbose:
+            sys.stderr.write(f"note: _calls.c did not build, the binding uses ctypes:\n{r.stderr}\n")
+        return None
+    os.replace(out + ".tmp", out)
+    if verbose:
+        sys.stderr.write(f"built {out}\n")
+    return out
 
 
 if __name__ == "__main__":

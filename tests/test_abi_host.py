@@ -158,3 +158,41 @@ def test_tf32x3_chunk_knob(lib):
     for bad in (-32, 16, 48, 100, (1 << 30) + 32):
         assert lib.sgemm_set_tf32x3_chunk_k(bad) == -1
     assert sg.set_tf32x3_chunk_k(0) == 128
+
+
+def test_extension_marshalling_matches_ctypes(lib):
+    """The _calls extension (built next to the library when a C compiler and
+    the Python headers are present) is bound to the same library instance as
+    ctypes: host-side argument errors give the same status and detail through
+    both routes, and the extension rejects malformed argument lists itself."""
+    if sg.marshalling() != "extension":
+        pytest.skip("the _calls extension was not built here")
+    from dense_fp32_matrix_sgemm_gb300 import _calls
+    cases = [
+        ("sgemm_f32", (-1, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, 0, 0)),
+        ("sgemm_f32_strided_batched", (4, 4, 4, FAKE, 4, 16, FAKE, 4, 16, FAKE, 4, 16, -2, 0, 0, 0)),
+        ("sgemm_f32_ex", (4, 4, 4, 1.0, FAKE, 2, FAKE, 4, 0.0, FAKE, 4, 0, 0, 0, 0)),
+        ("sgemm_f32_ex_strided_batched", (4, 4, 4, 1.0, FAKE, 4, 16, FAKE, 4, 16, 0.0, FAKE, 4,
+                                          16, 0, 2, 3, 0, 0)),
+        ("sgemm_f32_tf32x3_ex", (4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4, 0, 0, 0, 0, 0, 0)),
+        ("sgemm_f32_splitk", (4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, 0, -3, 0, 0, 0)),
+        ("sgemm_f32_streamk", (4, 4, 4, FAKE, 4, FAKE, 4, FAKE, 2, 0, 0, 0, 0, 0)),
+        ("sgemm_f32_tf32x3", (4, 4, 4, FAKE, 4, FAKE, 4, 0, 4, 0, 0, 0, 0, 0)),
+        ("sgemm_f32_tf32x3_strided_batched", (4, 4, 4, FAKE, 4, 16, FAKE, 4, 16, FAKE, 4, 16, 1,
+                                              2, 0, 0, 0, 0)),
+        ("sgemm_f32_tf32", (4, -4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, 0, 0, 0, 0)),
+        ("sgemm_f32_tf32_strided_batched", (4, 4, 4, FAKE, 4, 16, FAKE, 4, 16, FAKE, 4, 0, 2, 0,
+                                            0, 0, 0, 0)),
+        ("sgemm_f32_tf32x3_noalloc", (4, 4, 4, FAKE, 1, FAKE, 4, FAKE, 4, 0, 0, 0)),
+    ]
+    assert sorted(name for name, _ in cases) == sorted(sg.FAST_ENTRIES)
+    for name, args in cases:
+        via_ctypes = getattr(lib, name)(*args)
+        detail = sg.last_error()
+        via_ext = getattr(_calls, name)(*args)
+        assert via_ctypes != 0 and via_ext == via_ctypes, name
+        assert sg.last_error() == detail, name
+    with pytest.raises(TypeError):
+        _calls.sgemm_f32(4, 4, 4)
+    with pytest.raises(OverflowError):
+        _calls.sgemm_f32(1 << 70, 4, 4, FAKE, 4, FAKE, 4, FAKE, 4, 0, 0, 0)
