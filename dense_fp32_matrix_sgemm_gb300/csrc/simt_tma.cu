@@ -139,13 +139,19 @@ __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int 
                 }
             }
         } else {              // pairs along n, a[i] twice
+            // column pair outer, rows inner: the pair operand stays the same
+            // for 8 consecutive FMAs and the broadcast one changes (measured:
+            // 3072^3 A^T by B 65.5 -> 68.8 TFLOP/s one tile per CTA, the
+            // stream-K step 66.5 -> 68.9, 96 x 512^2 x 64 persistent 48.7 ->
+            // 51.9; the rows-outer order of the cp.async kernels stays, it
+            // lost 14 % there).  Every output still takes its k in order.
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 ai = make_float2(a[i], a[i]);
+            for (int j = 0; j < TN; j += 2) {
+                const float2 bj = make_float2(b[j], b[j + 1]);
 #pragma unroll
-                for (int j = 0; j < TN; j += 2) {
+                for (int i = 0; i < 8; ++i) {
                     float2 c = make_float2(acc[i][j], acc[i][j + 1]);
-                    c = __ffma2_rn(ai, make_float2(b[j], b[j + 1]), c);
+                    c = __ffma2_rn(make_float2(a[i], a[i]), bj, c);
                     acc[i][j] = c.x;
                     acc[i][j + 1] = c.y;
                 }
@@ -232,12 +238,12 @@ __device__ __forceinline__ void slice_fma(const float *at, const float *bt, int 
 // hence a record per stage.  The records live in shared memory, not in
 // registers held across the loop.
 // GUARD_FLAG picks how a warp decides to skip its release after an abort:
-// by reading the abort word at the release (true) or by keeping its own wait's
-// result (false).  Both are exact; they differ only in the registers the
-// compiler gives the loop, and each kernel takes the one it runs faster with
-// (3072^3, CUDA events: stream-K kernel 66.7 TFLOP/s by the word, 66.1 by the
-// flag; row-major A 60.3 by the flag, 59.1 by the word; A^T by B 65.5 by the
-// word, 64.2 by the flag).
+// by reading the abort word at the release (false) or by keeping its own
+// wait's result (true).  Both are exact; they differ only in the registers
+// the compiler gives the loop, and every kernel now runs fastest with its own
+// wait's result (3072^3, CUDA events, against the word: stream-K step 68.9 ->
+// 69.2 TFLOP/s, A^T by B 68.7 -> 69.0, both transposed 59.5 -> 60.5, row-major
+// A 60.2 against 58.9).
 template <int BK, int STAGES, int BN_, bool KA, bool KB, bool GUARD_FLAG>
 __device__ __forceinline__ void tma_mainloop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              float *As, float *Bs, uint32_t full0, uint32_t &gk,
@@ -401,7 +407,7 @@ sgemm_simt_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     thread_coords(a_col, b_col);
     float acc[8][BN_ / 16];
     uint32_t gk = 0;
-    tma_mainloop<BK, STAGES, BN_, KA, KB, KA>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z,
+    tma_mainloop<BK, STAGES, BN_, KA, KB, true>(&tmA, &tmB, As, Bs, full0, gk, tm * BM, tn * BN_, z,
                                               0, (p.K + BK - 1) / BK, a_col, b_col, acc, abort);
     finish_abort<STAGES>(full0, abort, status);
     store_tile<BN_, KA, KB>(p, z, tm * BM, tn * BN_, a_col, b_col, acc);
@@ -520,7 +526,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, b, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM,
+        tma_mainloop<BK, STAGES, BN_, KA, false, true>(&tmA, &tmB, As, Bs, full0, gk, tm * BM,
                                                         tn * BN_, z, 0, sk.kslices, a_col, b_col,
                                                         acc, abort);
         finish_abort<STAGES>(full0, abort, status);
@@ -543,7 +549,7 @@ sgemm_simt_streamk_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int z, tm, tn;
         raster(p, sk.tiles_dp + tl, z, tm, tn);
         float acc[8][BN_ / 16];
-        tma_mainloop<BK, STAGES, BN_, KA, false, false>(&tmA, &tmB, As, Bs, full0, gk, tm * BM,
+        tma_mainloop<BK, STAGES, BN_, KA, false, true>(&tmA, &tmB, As, Bs, full0, gk, tm * BM,
                                                         tn * BN_, z, s0 * BK, s1 - s0, a_col,
                                                         b_col, acc, abort);
         if (!(s0 == 0 && s1 == sk.kslices)) {
