@@ -299,3 +299,29 @@ def test_wide_transpose_tiles():
     full = {(r, c) for r in range(32) for c in range(128)}
     assert len(cells_written) == len(set(cells_written)) and set(cells_written) == full
     assert len(cells_read) == len(set(cells_read)) and set(cells_read) == full
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_tensor_c_store_column_rule(bn):
+    # csrc/tf32x3.cu, store_tile_rows / store_running_rows with tma_n: the C
+    # map is N rounded down to a multiple of 4 wide (n4); a 32-column block
+    # ending at or before tma_n (n4, or no limit when N % 4 == 0) goes through
+    # the map, which clips it at n4; the block holding the last columns of a
+    # width that is not a multiple of 4 is stored by the threads, up to N.
+    # Every column once, no TMA granule past n4 (16 bytes = 4 floats).
+    for N in list(range(1, 300)) + [3071, 3072, 2049, 4097]:
+        n4 = N // 4 * 4
+        tma_n = 1 << 30 if N % 4 == 0 else n4
+        seen = []
+        for n0 in range(0, N, bn):
+            for c in range(bn // 32):
+                b0 = n0 + 32 * c
+                if b0 >= N:
+                    break
+                if b0 + 32 <= tma_n:
+                    cols = range(b0, min(b0 + 32, n4))
+                    assert n4 % 4 == 0 and all(col < n4 for col in cols)
+                else:
+                    cols = range(b0, min(b0 + 32, N))
+                seen.extend(cols)
+        assert sorted(seen) == list(range(N)), N
